@@ -1,0 +1,25 @@
+"""Test configuration: markers and import path.
+
+``-m gpu`` tests need a CUDA device and the compiled library; everything else
+runs on the CPU (oracle pins, host-side validation, ABI exports, gloo ranks).
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the compiled library")
+    config.addinivalue_line("markers", "slow: larger CPU cases")
+
+
+@pytest.fixture(scope="session")
+def oracle_mod():
+    import oracle
+    oracle.build()
+    return oracle
