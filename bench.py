@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Throughput of tree/chain verification + accepted-path commit, per GDN layer.
+
+Metric: draft nodes verified per second per GDN layer = B * N / t_layer, where
+t_layer is the device time of one decode step of one layer: the pending
+commit of the previous step's accepted path fused into the verification of
+the new draft (the delayed state update of the SpecLA review, "Core claim").
+
+Protocol (layer-major decode, inputs larger than L2): R distinct layer
+instances, each with its own fp32 state, inputs and ping-pong factor buffers,
+R chosen so their footprint is at least 4x the L2 size; one step runs the R
+layers back to back, captured once as a CUDA graph and replayed.  Between two
+visits of a layer every other layer's data has streamed through L2, so each
+visit reads its state from HBM.  Steps are timed with CUDA events on the
+launching stream; W untimed warm-up steps come first.
+
+Also reported in the same JSON line:
+  roofline      algorithmic bytes of one layer call / measured t_layer, against
+                the measured HBM copy bandwidth
+  e2e           the same metric through the public API with pinned host inputs
+                copied in and outputs copied out inside every timed step
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
+  clocks        SM clocks and throttle reasons sampled while timing
+
+``--impl reference`` times the oracle itself as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica (weak scaling, no
+data-path collective); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft nodes verified/sec per GDN layer"
+UNIT = "nodes/s"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic traffic of one layer call (bytes that must cross HBM)
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(B, N, H, dk, dv, esz, L_total, Lmax, chain):
+    """Bytes one fused commit+verify layer call must move: L_total = accepted nodes summed over B."""
+    state = 2 * B * H * dv * dk * 4                       # read S, write committed S
+    inputs = B * N * H * (2 * dk + dv) * esz + 2 * B * N * H * 4 + (0 if chain else B * N * 4)
+    outputs = B * N * H * dv * 4                           # o_t
+    factors_out = B * H * N * (dv * 4 + dk * esz + 4) + B * N * 4
+    commit_in = L_total * H * (dv * 4 + dk * esz + 4) + B * Lmax * 4   # accepted rows of prev factors + path
+    return state + inputs + outputs + factors_out + commit_in
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                         if r[3].replace(".", "").isdigit())}
+
+
+# ---------------------------------------------------------------------------
+# the workload: R layer instances on one GPU
+# ---------------------------------------------------------------------------
+class Layer:
+    """One GDN layer instance: its state, this step's draft inputs, ping-pong factors."""
+
+    def __init__(self, w, device, torch, gdnspec):
+        def qkv(x):
+            if x.dtype == np.uint16:
+                return torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).to(device)
+            return torch.from_numpy(x.copy()).to(device)
+        self.w = w
+        self.q, self.k, self.v = qkv(w.q), qkv(w.k), qkv(w.v)
+        self.alpha = torch.from_numpy(w.alpha).to(device)
+        self.beta = torch.from_numpy(w.beta).to(device)
+        self.parent = torch.from_numpy(w.parent).to(device)
+        self.path = torch.from_numpy(w.path).to(device)
+        self.S = torch.from_numpy(w.S0).to(device)
+        self.out = torch.empty((w.B, w.N, w.H, w.dv), dtype=torch.float32, device=device)
+        self.fac = [gdnspec.empty_factors(w.B, w.N, w.H, w.dk, w.dv, w.dtype, device) for _ in range(2)]
+        self.ws = gdnspec.empty_workspace(w.B, w.N, w.H, w.dk, w.dv, device)
+
+    def nbytes(self):
+        ts = [self.q, self.k, self.v, self.alpha, self.beta, self.parent, self.path, self.S, self.out,
+              self.ws] + self.fac
+        return sum(t.numel() * t.element_size() for t in ts)
+
+
+def make_layers(cfg, R, seed0, device, torch, gdnspec, wl):
+    return [Layer(wl.make_workload(cfg, seed=seed0 + 7919 * r), device, torch, gdnspec) for r in range(R)]
+
+
+def layer_call(gdnspec, ly, parity, chain):
+    """One decode step of one layer: commit the previous accepted path inside the new verify."""
+    prev, nxt = ly.fac[parity], ly.fac[1 - parity]
+    w = ly.w
+    if chain:
+        gdnspec.gdn_commit_chain_verify(ly.S, prev, w.N, ly.path, ly.q, ly.k, ly.v, ly.alpha, ly.beta,
+                                        ly.out, nxt)
+    else:
+        gdnspec.gdn_commit_tree_verify(ly.S, prev, w.N, ly.path, ly.q, ly.k, ly.v, ly.alpha, ly.beta,
+                                       ly.parent, ly.out, nxt, ly.ws)
+
+
+def first_verify(gdnspec, ly, chain):
+    w = ly.w
+    if chain:
+        gdnspec.gdn_chain_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.S, ly.out, ly.fac[0])
+    else:
+        gdnspec.gdn_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out, ly.fac[0],
+                                ly.ws)
+
+
+def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist):
+    from speculative_decoding_linear_gb300 import gdnspec
+    from speculative_decoding_linear_gb300 import workloads as wl
+
+    torch.cuda.set_device(device_index)
+    device = torch.device("cuda", device_index)
+    spec = wl.SPECS[cfg]
+    chain = spec.tree == "chain"
+    props = torch.cuda.get_device_properties(device_index)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
+
+    probe = Layer(wl.make_workload(cfg), device, torch, gdnspec)
+    per_layer = probe.nbytes()
+    del probe
+    R = max(2, -(-4 * l2 // per_layer))
+    layers = make_layers(cfg, R, 1000 * (rank + 1) + cfg, device, torch, gdnspec, wl)
+    footprint = sum(ly.nbytes() for ly in layers)
+
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for ly in layers:
+            first_verify(gdnspec, ly, chain)
+        assert gdnspec.gdn_last_error(stream) == 0
+        for parity in (0, 1):                    # eager warm-up of both parities before capture
+            for ly in layers:
+                layer_call(gdnspec, ly, parity, chain)
+        assert gdnspec.gdn_last_error(stream) == 0
+        graphs = []
+        for parity in (0, 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for ly in layers:
+                    layer_call(gdnspec, ly, parity, chain)
+            graphs.append(g)
+        for i in range(max(warmup, 3)):
+            graphs[i % 2].replay()
+        stream.synchronize()
+        assert gdnspec.gdn_last_error(stream) == 0
+
+        # soak ~1 s so the clock sampler sees the GPU under this load, then time exactly K steps
+        sampler = ClockSampler(device_index)
+        sampler.start()
+        t_soak = time.time()
+        i = 0
+        while time.time() - t_soak < 1.0:
+            graphs[i % 2].replay()
+            i += 1
+            if i % 16 == 0:
+                stream.synchronize()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(steps):
+            graphs[s % 2].replay()
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        clocks = sampler.stop()
+        ms_local = e0.elapsed_time(e1)
+        assert gdnspec.gdn_last_error(stream) == 0
+
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API: pinned host inputs in, outputs out, every step
+    e2e = run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device)
+
+    w0 = layers[0].w
+    B, N, H, dk, dv = w0.B, w0.N, w0.H, w0.dk, w0.dv
+    esz = 2 if w0.dtype == wl.BF16 else 4
+    per_call = float(np.mean([algorithmic_bytes(B, N, H, dk, dv, esz, int(np.sum(ly.w.path >= 0)),
+                                                ly.w.path.shape[1], chain) for ly in layers]))
+    t_layer_s = ms / 1e3 / (steps * R)
+    peak, peak_kind = measured_peaks()
+    achieved = per_call / t_layer_s / 1e9
+    nodes = B * N * R * steps * world
+    value = nodes / (ms / 1e3)
+    launches_per_call = 1 if chain else 2
+    return dict(
+        value=value, ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
+        spec=spec, B=B, N=N, H=H, dk=dk, dv=dv, chain=chain,
+        roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                  "frac": round(achieved / peak, 4), "traffic": None,
+                  "peak_kind": peak_kind + " hbm_gbs (copy)",
+                  "kernel": "gdn_commit_chain_verify (chain_kernel)" if chain else
+                            "gdn_commit_tree_verify (tree_prep_kernel + tree_contract_kernel)",
+                  "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_layer_s * 1e6, 3)},
+        gpu_launches=launches_per_call * R * steps,
+    )
+
+
+def run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device):
+    """Same metric through the public API; H2D of each step's inputs and D2H of its outputs timed."""
+    names = ["q", "k", "v", "alpha", "beta", "path"] + ([] if chain else ["parent"])
+    host = [{n: getattr(ly, n).cpu().pin_memory() for n in names} for ly in layers]
+    outs = [torch.empty(ly.out.shape, dtype=ly.out.dtype).pin_memory() for ly in layers]
+    h2d = sum(t.numel() * t.element_size() for hd in host for t in hd.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    k = max(1, min(steps, 10))
+    with torch.cuda.stream(stream):
+        def one(parity):
+            for ly, hd in zip(layers, host):
+                for n in names:
+                    getattr(ly, n).copy_(hd[n], non_blocking=True)
+            for ly in layers:
+                layer_call(gdnspec, ly, parity, chain)
+            for ly, o in zip(layers, outs):
+                o.copy_(ly.out, non_blocking=True)
+        one(0)
+        one(1)
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for s in range(k):
+            one(s % 2)
+        stream.synchronize()
+        t1 = time.perf_counter()
+    sec = t1 - t0
+    if world > 1:
+        t = torch.tensor([sec], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    w = layers[0].w
+    nodes = w.B * w.N * len(layers) * k * world
+    return {"value": nodes / sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": k, "ms_per_step": 1e3 * sec / k}
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host cores
+# ---------------------------------------------------------------------------
+def oracle_layer_seconds(w, nthreads):
+    """Verify every node of one layer instance and commit its accepted path with the fp64 oracle."""
+    import oracle
+    x = dict(q=w.widened("q"), k=w.widened("k"), v=w.widened("v"), alpha=w.alpha.astype(np.float64),
+             beta=w.beta.astype(np.float64), parent=w.parent, S0=w.S0.astype(np.float64))
+    t0 = time.perf_counter()
+    oracle.tree_verify(**x, nthreads=nthreads)
+    oracle.commit(x["k"], x["v"], x["alpha"], x["beta"], w.parent, x["S0"], w.path, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, budget_s=10.0):
+    import oracle
+    from speculative_decoding_linear_gb300 import workloads as wl
+    oracle.build()
+    cores = os.cpu_count() or 1
+    w = wl.make_workload(cfg)
+    n, sec = 0, 0.0
+    while sec < budget_s:
+        sec += oracle_layer_seconds(w, cores)
+        n += 1
+    return {"value": w.B * w.N * n / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d repetitions of one layer instance of %s (verify all %d nodes x %d heads "
+                      "by path walks + commit), fp64, %d threads" % (n, w.spec.name, w.B * w.N, w.H, cores)}
+
+
+def run_reference(args):
+    """Reference arm: the oracle as it stands, timed on the host cores (rank 0 only)."""
+    from speculative_decoding_linear_gb300 import workloads as wl
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle.build()
+    cores = os.cpu_count() or 1
+    w = wl.make_workload(args.config)
+    for _ in range(max(args.warmup, 1)):
+        oracle_layer_seconds(w, cores)
+    sec = sum(oracle_layer_seconds(w, cores) for _ in range(args.steps))
+    value = w.B * w.N * args.steps / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.spec.name, "B": w.B, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one layer instance of %s per step (verify all nodes by path "
+                                       "walks + commit), fp64, %d threads" % (w.spec.name, cores)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    r = run_gpu(args.config, args.steps, args.warmup, rank, world, local, torch, dist)
+
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(args.config)
+        spec = r["spec"]
+        line = {
+            "metric": METRIC, "value": round(r["value"], 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": spec.name, "B": r["B"], "N": r["N"], "H": r["H"], "dk": r["dk"],
+                       "dv": r["dv"], "qkv": spec.dtype, "state": "f32",
+                       "step": "per layer: pending commit fused into the next %s verify"
+                               % ("chain" if r["chain"] else "tree"),
+                       "layers_rotated": r["R"], "footprint_bytes": r["footprint"], "l2_bytes": r["l2"],
+                       "l2_policy": "inputs larger than L2: %d-layer rotation, footprint >= 4x L2" % r["R"],
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+            "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * gdnspec.h -- C ABI of the GB300 (sm_103a) library for speculative
+ * verification and accepted-path commit of Gated DeltaNet (GDN) layers.
+ *
+ * Source of the method: "Pith review of SpecLA: Efficient Speculative
+ * Decoding for Linear-Attention Models" (pith.science 7ERME3HB) -- "Core
+ * claim" and "What carries the argument" (tree-masked factorized verifier,
+ * factor buffering, delayed state update fused into the next verification,
+ * V-dimension tiling for chains) and the Referee Report's summary.  The
+ * recurrence is the gated delta rule of "Gated Delta Networks: Improving
+ * Mamba2 with Delta Rule", which that review cites:
+ *
+ *     S_t = alpha_t S_parent(t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = S_t q_t,
+ *
+ * applied along each draft node's own root-to-node path, starting from the
+ * committed state S0.  S is d_v x d_k per (sequence, head), stored row-major
+ * (row = value index).
+ *
+ * Conventions for every entry point
+ *   - Every array argument is a DEVICE pointer owned by the caller, 16-byte
+ *     aligned, densely packed in the layout stated.  The library never
+ *     allocates device memory: factor buffers and workspaces are sized by
+ *     gdn_factors_bytes / gdn_workspace_bytes and passed in.
+ *   - Work is enqueued asynchronously on `stream` (0 = legacy default stream)
+ *     of the current device, which must be an sm_103 GPU.
+ *   - Shapes: 1 <= B, 1 <= H, 1 <= N <= 64 draft nodes per tree,
+ *     d_k and d_v in {16, 32, ..., 256}.  B * H * N must fit in int32.
+ *   - q/k/v element type: GDN_DTYPE_BF16 or GDN_DTYPE_F32.  alpha, beta, S,
+ *     outputs and the buffered innovations are fp32.
+ *   - Return value: GDN_OK, or a negative status for errors found on the host
+ *     (bad shape, null or misaligned pointer, unsupported device, failed
+ *     launch).  Errors found on the device (invalid parent_idx, invalid
+ *     accepted path, a bounded wait that ran out) are recorded in a per-device
+ *     error word and read back by gdn_last_error; kernels never trap.  After a
+ *     device-side error the outputs of that call are unspecified.
+ *   - Draft trees: parent_idx[b][t] is -1 (node hangs directly under the
+ *     committed state) or an earlier node index (topological order).  Several
+ *     -1 entries (a forest) are allowed; the arithmetic is the same.
+ */
+#ifndef GDNSPEC_H
+#define GDNSPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define GDN_OK 0
+#define GDN_ERR_ARG (-1)      /* bad shape, null or misaligned pointer, aliasing */
+#define GDN_ERR_TREE (-2)     /* parent_idx[t] >= t or < -1 (device-detected) */
+#define GDN_ERR_PATH (-3)     /* accepted path not root-first parent-chained (device-detected) */
+#define GDN_ERR_TIMEOUT (-4)  /* a bounded device wait ran out (device-detected) */
+#define GDN_ERR_CUDA (-5)     /* a CUDA runtime call or launch failed */
+#define GDN_ERR_DEVICE (-6)   /* current device is not sm_103 */
+
+/* ---- q/k/v element types ------------------------------------------------ */
+#define GDN_DTYPE_BF16 0
+#define GDN_DTYPE_F32 1
+
+/*
+ * Factor buffer.  Verification writes, for every draft node, the compact
+ * record the commit needs (review: "buffering the small per-token factors
+ * produced during verification and applying only the accepted path"):
+ *
+ *   delta  fp32  [B][H][N][d_v]   innovation delta_t = beta_t (v_t - alpha_t S_parent k_t)
+ *   key    dtype [B][H][N][d_k]   k_t (same element type as the q/k/v inputs)
+ *   g      fp32  [B][H][N]        cumulative log gate g_t = sum_{j on path(t)} log alpha_j
+ *   parent int32 [B][N]           copy of parent_idx
+ *
+ * Sections are placed in this order, each starting on a 256-byte boundary.
+ * With these, the state after accepting node a is
+ *   S_a = e^{g_a} S0 + sum_{j on path(a)} e^{g_a - g_j} delta_j k_j^T.
+ * gdn_factors_bytes writes the buffer size for a tree of N nodes.
+ */
+int gdn_factors_bytes(int B, int N, int H, int dk, int dv, int dtype, size_t* bytes);
+
+/*
+ * Workspace of the tree verifier: per-(sequence, head) coefficient tables of
+ * the masked solve (review, "Core claim": A_tree = M_tree (.) (K_b K_a^T),
+ * T_tree = solve_tril(I - A_tree)).  gdn_workspace_bytes writes its size;
+ * contents are scratch, valid only during one call.
+ */
+int gdn_workspace_bytes(int B, int N, int H, int dk, int dv, size_t* bytes);
+
+/*
+ * Ancestor mask of each draft tree (review, "Core claim": the tree mask
+ * M_tree that lets updates propagate only along ancestor paths).
+ *   parent_idx int32 [B][N]
+ *   mask       uint64 [B][N]: bit j of mask[b][t] set iff node j is a strict
+ *              ancestor of node t (N <= 64)
+ *   depth      int32 [B][N]: number of strict ancestors (roots have depth 0)
+ * Invalid parent_idx -> GDN_ERR_TREE in the error word.
+ */
+int gdn_tree_mask(const int32_t* parent_idx, int B, int N, uint64_t* mask, int32_t* depth,
+                  cudaStream_t stream);
+
+/*
+ * Tree-masked factorized verification (review, "Core claim" / "What carries
+ * the argument": O = Qhat S0^T - Attn (W S0^T) + Attn U from the masked UT
+ * solve).  Scores every draft node from the same committed state in one pass.
+ *   q, k       dtype [B][N][H][d_k]
+ *   v          dtype [B][N][H][d_v]
+ *   alpha,beta fp32  [B][N][H]      gate in (0, 1], write strength
+ *   parent_idx int32 [B][N]
+ *   S0         fp32  [B][H][d_v][d_k]   committed state (read only)
+ *   out        fp32  [B][N][H][d_v]     o_t for every node
+ *   factors    gdn_factors_bytes(B,N,H,dk,dv,dtype) bytes, written
+ *   workspace  gdn_workspace_bytes(B,N,H,dk,dv) bytes, scratch
+ * out, factors and workspace must not overlap each other or the inputs.
+ */
+int gdn_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                    const float* beta, const int32_t* parent_idx, const float* S0, float* out,
+                    void* factors, void* workspace, int B, int N, int H, int dk, int dv,
+                    cudaStream_t stream);
+
+/*
+ * Chain verification with the state kept on chip and tiled along d_v
+ * (review, "What carries the argument": "V-dimension tiling for the serial
+ * chain path").  The draft is a linear chain: node t hangs under t-1 and
+ * node 0 under S0.  Same tensors and factor record as gdn_tree_verify
+ * (the factor buffer's parent section receives -1, 0, 1, ..., N-2).
+ */
+int gdn_chain_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                     const float* beta, const float* S0, float* out, void* factors, int B, int N,
+                     int H, int dk, int dv, cudaStream_t stream);
+
+/*
+ * Accepted-path commit from buffered factors, without snapshots or replay
+ * (review, Referee Report summary: "accepted-state recovery via buffered
+ * per-token factors").
+ *   S0            fp32 [B][H][d_v][d_k]   state the factors were verified from
+ *   factors       written by a verify call with the same B, N, H, d_k, d_v, dtype
+ *   accepted_path int32 [B][Lmax]: root-first accepted nodes, padded with -1;
+ *                 path[b][0] must be a root, path[b][i] a child of path[b][i-1].
+ *                 An all -1 row accepts nothing (S_new = S0, bit-identical).
+ *   S_new         fp32 [B][H][d_v][d_k]; may equal S0 (in place)
+ * 1 <= Lmax <= 64.  Invalid path -> GDN_ERR_PATH in the error word.
+ */
+int gdn_commit(const float* S0, const void* factors, const int32_t* accepted_path, int Lmax,
+               float* S_new, int B, int N, int H, int dk, int dv, int dtype, cudaStream_t stream);
+
+/*
+ * Delayed state update fused into the next verification (review, "Core
+ * claim": "applying only the accepted path inside the next verification
+ * kernel").  In one pass over the state tiles:
+ *   S <- commit(S, prev_factors, prev_path)   (written back once, in place)
+ *   then the new tree is verified from the committed S, as gdn_tree_verify.
+ *   S            fp32 [B][H][d_v][d_k], in: state before the commit, out: committed
+ *   prev_factors factor buffer of the previous verify (tree size N_prev)
+ *   prev_path    int32 [B][Lmax] accepted path into the previous tree
+ *   factors      factor buffer for the new tree (must not overlap prev_factors)
+ * Other arguments as gdn_tree_verify.
+ */
+int gdn_commit_tree_verify(float* S, const void* prev_factors, int N_prev, const int32_t* prev_path,
+                           int Lmax, const void* q, const void* k, const void* v, int dtype,
+                           const float* alpha, const float* beta, const int32_t* parent_idx,
+                           float* out, void* factors, void* workspace, int B, int N, int H,
+                           int dk, int dv, cudaStream_t stream);
+
+/* As gdn_commit_tree_verify, with the new draft a linear chain (gdn_chain_verify). */
+int gdn_commit_chain_verify(float* S, const void* prev_factors, int N_prev,
+                            const int32_t* prev_path, int Lmax, const void* q, const void* k,
+                            const void* v, int dtype, const float* alpha, const float* beta,
+                            float* out, void* factors, int B, int N, int H, int dk, int dv,
+                            cudaStream_t stream);
+
+/*
+ * Waits for `stream`, returns the first device-side error recorded on the
+ * current device since the last call (GDN_OK if none) and clears it.
+ */
+int gdn_last_error(cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* gdn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDNSPEC_H */

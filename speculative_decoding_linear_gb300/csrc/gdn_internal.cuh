@@ -1,0 +1,250 @@
+// gdn_internal.cuh -- layouts, argument blocks and device helpers shared by
+// the kernels of libgdnspec.so.  Not part of the public ABI (include/gdnspec.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdnspec.h"
+
+namespace gdn {
+
+constexpr int kMaxNodes = 64;     // draft nodes per tree (one uint64 ancestor mask per node)
+constexpr int kMaxDim = 256;      // d_k, d_v upper bound
+constexpr int kMaxPath = 64;      // accepted path capacity (Lmax)
+constexpr size_t kSectionAlign = 256;
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int elem_bytes(int dtype) { return dtype == GDN_DTYPE_F32 ? 4 : 2; }
+
+// ---------------------------------------------------------------------------
+// factor buffer: delta fp32 [B][H][N][dv] | key dtype [B][H][N][dk] |
+//                g fp32 [B][H][N] | parent int32 [B][N]
+// ---------------------------------------------------------------------------
+struct FactorLayout {
+    size_t delta, key, g, parent, total;
+};
+
+inline FactorLayout factor_layout(int B, int N, int H, int dk, int dv, int dtype) {
+    FactorLayout L;
+    const size_t BHN = (size_t)B * H * N;
+    L.delta = 0;
+    L.key = align_up(L.delta + BHN * dv * 4, kSectionAlign);
+    L.g = align_up(L.key + BHN * dk * elem_bytes(dtype), kSectionAlign);
+    L.parent = align_up(L.g + BHN * 4, kSectionAlign);
+    L.total = align_up(L.parent + (size_t)B * N * 4, kSectionAlign);
+    return L;
+}
+
+// Device view of one factor buffer.
+struct Factors {
+    float* delta;       // [B][H][N][dv]
+    void* key;          // [B][H][N][dk], q/k/v element type
+    float* g;           // [B][H][N]
+    int32_t* parent;    // [B][N]
+    int N;
+};
+
+inline Factors factors_view(void* base, int B, int N, int H, int dk, int dv, int dtype) {
+    FactorLayout L = factor_layout(B, N, H, dk, dv, dtype);
+    char* p = static_cast<char*>(base);
+    return Factors{reinterpret_cast<float*>(p + L.delta), p + L.key,
+                   reinterpret_cast<float*>(p + L.g), reinterpret_cast<int32_t*>(p + L.parent), N};
+}
+
+// ---------------------------------------------------------------------------
+// tree workspace, one record per (b, h):
+//   T  fp32 [N][N]  (I + A)^-1, A = strict-ancestor masked beta_t e^{g_t-g_j} k_t.k_j
+//   P  fp32 [N][N]  Attn T, Attn = inclusive masked e^{g_t-g_j} q_t.k_j
+//   eg fp32 [N]     e^{g_t}
+//   bt fp32 [N]     beta_t
+//   anc u64 [N]     inclusive ancestor mask (path(t) as bits)
+// ---------------------------------------------------------------------------
+struct WsLayout {
+    size_t T, P, eg, bt, anc, record;
+};
+
+__host__ __device__ inline WsLayout ws_layout(int N) {
+    WsLayout L;
+    L.T = 0;
+    L.P = L.T + (size_t)N * N * 4;
+    L.eg = L.P + (size_t)N * N * 4;
+    L.bt = L.eg + (size_t)N * 4;
+    L.anc = align_up(L.bt + (size_t)N * 4, 8);
+    L.record = align_up(L.anc + (size_t)N * 8, kSectionAlign);
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// argument blocks
+// ---------------------------------------------------------------------------
+struct CommitSrc {             // accepted path into a previous tree (fused or standalone commit)
+    const float* delta;        // prev factors
+    const void* key;
+    const float* g;
+    const int32_t* parent;
+    int N;                     // previous tree size
+    const int32_t* path;       // [B][Lmax]
+    int Lmax;
+};
+
+struct VerifyArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* beta;
+    const int32_t* parent;     // nullptr for the chain path
+    float* S;                  // state (read; read-modify-write when commit.path != nullptr)
+    float* out;
+    Factors f;                 // new factors
+    char* ws;                  // tree workspace
+    int B, N, H, dk, dv;
+    CommitSrc commit;          // commit.path == nullptr: no fused commit
+    int* err;
+};
+
+struct CommitArgs {
+    const float* S0;
+    float* S_new;
+    CommitSrc src;
+    int B, H, dk, dv;
+    int* err;
+};
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const T* p, size_t i);
+template <>
+__device__ __forceinline__ float ld_elem<float>(const float* p, size_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void st_elem(T* p, size_t i, float x);
+template <>
+__device__ __forceinline__ void st_elem<float>(float* p, size_t i, float x) { p[i] = x; }
+template <>
+__device__ __forceinline__ void st_elem<__nv_bfloat16>(__nv_bfloat16* p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Accepted-path setup, executed by ONE full warp.  Validates the -1 padded,
+// root-first path row against the previous tree's parents and fills
+//   s_nodes[i]  accepted node i (root first), i < L
+//   s_coef[i]   e^{g_a - g_{node i}}, a = last accepted node
+//   *s_ega      e^{g_a} (1 when L == 0)
+// Returns L (0..Lmax) or -1 if the path is invalid.
+__device__ inline int commit_path_setup(const CommitSrc& c, int b, int h, int H, int* s_nodes,
+                                        float* s_coef, float* s_ega) {
+    const int lane = threadIdx.x & 31;
+    const int32_t* row = c.path + (size_t)b * c.Lmax;
+    int n[2], prev[2];
+    n[0] = lane < c.Lmax ? row[lane] : -1;
+    n[1] = lane + 32 < c.Lmax ? row[lane + 32] : -1;
+    const unsigned nn0 = __ballot_sync(0xffffffffu, n[0] >= 0);
+    const unsigned nn1 = __ballot_sync(0xffffffffu, n[1] >= 0);
+    const unsigned long long nn = (unsigned long long)nn0 | ((unsigned long long)nn1 << 32);
+    const int L = (~nn == 0ull) ? 64 : __ffsll((long long)~nn) - 1;
+    bool bad = (n[0] < -1) || (n[1] < -1) || (n[0] >= c.N) || (n[1] >= c.N);
+    bad = bad || (nn != (L == 64 ? ~0ull : ((1ull << L) - 1ull)));
+    prev[0] = __shfl_up_sync(0xffffffffu, n[0], 1);
+    prev[1] = __shfl_up_sync(0xffffffffu, n[1], 1);
+    const int carry = __shfl_sync(0xffffffffu, n[0], 31);
+    if (lane == 0) {
+        prev[0] = -1;
+        prev[1] = carry;
+    }
+    const int32_t* par = c.parent + (size_t)b * c.N;
+    for (int s = 0; s < 2; ++s) {
+        const int i = lane + 32 * s;
+        if (i < L && !bad && n[s] >= 0 && n[s] < c.N && par[n[s]] != prev[s]) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad)) return -1;
+    const float* g = c.g + (size_t)(b * H + h) * c.N;
+    float ga = 0.f;
+    if (L > 0) {
+        const int a_node = __shfl_sync(0xffffffffu, L - 1 < 32 ? n[0] : n[1], (L - 1) & 31);
+        ga = g[a_node];
+    }
+    for (int s = 0; s < 2; ++s) {
+        const int i = lane + 32 * s;
+        if (i < L) {
+            s_nodes[i] = n[s];
+            s_coef[i] = expf(ga - g[n[s]]);
+        }
+    }
+    if (lane == 0) *s_ega = L > 0 ? expf(ga) : 1.f;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// launchers (one per kernel family); each returns the launch status
+// ---------------------------------------------------------------------------
+cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint64_t* mask, int32_t* depth,
+                             int* err, cudaStream_t s);
+cudaError_t launch_tree_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_chain_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_commit(const CommitArgs& a, int dtype, cudaStream_t s);
+
+}  // namespace gdn
+
+namespace gdn {
+
+// Four consecutive elements starting at p[i] (i a multiple of 4) widened to fp32.
+template <typename T>
+__device__ __forceinline__ float4 ld4(const T* p, size_t i);
+template <>
+__device__ __forceinline__ float4 ld4<float>(const float* p, size_t i) {
+    return *reinterpret_cast<const float4*>(p + i);
+}
+template <>
+__device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+    float4 r;
+    r.x = __uint_as_float(u.x << 16);
+    r.y = __uint_as_float(u.x & 0xffff0000u);
+    r.z = __uint_as_float(u.y << 16);
+    r.w = __uint_as_float(u.y & 0xffff0000u);
+    return r;
+}
+
+// One committed quad of a state row:
+//   s' = e^{g_a} s + sum_i cd[i] k_{node i}[c..c+3],  cd[i] = e^{g_a - g_i} delta_i[row]
+// The same routine serves the standalone and the fused commit, so both give
+// identical bits.
+template <typename KT>
+__device__ __forceinline__ float4 commit_quad(float4 s, float ega, int L, const int* nodes,
+                                              const float* cd, int cd_stride, const KT* key_bh,
+                                              int dk, int c) {
+    float4 a;
+    a.x = ega * s.x;
+    a.y = ega * s.y;
+    a.z = ega * s.z;
+    a.w = ega * s.w;
+    for (int i = 0; i < L; ++i) {
+        const float w = cd[i * cd_stride];
+        const float4 kq = ld4<KT>(key_bh, (size_t)nodes[i] * dk + c);
+        a.x = fmaf(w, kq.x, a.x);
+        a.y = fmaf(w, kq.y, a.y);
+        a.z = fmaf(w, kq.z, a.z);
+        a.w = fmaf(w, kq.w, a.w);
+    }
+    return a;
+}
+
+}  // namespace gdn

@@ -1,0 +1,219 @@
+"""Thin Python binding of libgdnspec.so (the C ABI in include/gdnspec.h).
+
+Argument marshalling only: every function here forwards device pointers,
+sizes and the current CUDA stream to the entry point of the same name and
+turns a negative status into :class:`GdnError`.  All arithmetic runs in the
+library's CUDA kernels; there is no CPU fallback -- if the compiled library is
+missing, importing it raises.
+
+Tensors are PyTorch CUDA tensors (PyTorch is used for device memory and
+streams only); plain integer device addresses are accepted as well.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lib = None
+_lock = threading.Lock()
+
+OK, ERR_ARG, ERR_TREE, ERR_PATH, ERR_TIMEOUT, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
+DTYPE_BF16, DTYPE_F32 = 0, 1
+
+# (name, restype, argtypes) for every extern "C" symbol of include/gdnspec.h
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "gdn_factors_bytes": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
+    "gdn_workspace_bytes": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
+    "gdn_tree_mask": (_I, [_P, _I, _I, _P, _P, _P]),
+    "gdn_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_chain_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_commit": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_commit_tree_verify": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P,
+                                    _I, _I, _I, _I, _I, _P]),
+    "gdn_commit_chain_verify": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P,
+                                     _I, _I, _I, _I, _I, _P]),
+    "gdn_last_error": (_I, [_P]),
+    "gdn_strerror": (ctypes.c_char_p, [_I]),
+}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (status %d)" % (where, strerror(code), code))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """The loaded libgdnspec.so.  Builds it when absent (nvcc required); raises if it cannot."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if build_if_missing and not _build.up_to_date():
+                _build.build()
+            if not os.path.exists(path):
+                raise ImportError("libgdnspec.so not found at %s: the CUDA library is required "
+                                  "(there is no CPU fallback)" % path)
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().gdn_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise GdnError(rc, where)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, torch.Tensor):
+        if not x.is_cuda:
+            raise ValueError("expected a CUDA tensor")
+        if not x.is_contiguous():
+            raise ValueError("expected a contiguous tensor")
+        return x.data_ptr()
+    raise TypeError(type(x))
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def dtype_code(t) -> int:
+    if t in (torch.bfloat16, "bf16"):
+        return DTYPE_BF16
+    if t in (torch.float32, "f32"):
+        return DTYPE_F32
+    raise ValueError("q/k/v must be bf16 or fp32, got %s" % (t,))
+
+
+# ---------------------------------------------------------------------------
+# sizes
+# ---------------------------------------------------------------------------
+def gdn_factors_bytes(B, N, H, dk, dv, dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_factors_bytes(B, N, H, dk, dv, dtype_code(dtype) if not isinstance(dtype, int)
+                                   else dtype, ctypes.byref(out)), "gdn_factors_bytes")
+    return out.value
+
+
+def gdn_workspace_bytes(B, N, H, dk, dv) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_workspace_bytes(B, N, H, dk, dv, ctypes.byref(out)), "gdn_workspace_bytes")
+    return out.value
+
+
+def empty_factors(B, N, H, dk, dv, dtype, device="cuda"):
+    """Caller-owned factor buffer (uint8 tensor) of the size the library asks for."""
+    return torch.empty(gdn_factors_bytes(B, N, H, dk, dv, dtype), dtype=torch.uint8, device=device)
+
+
+def empty_workspace(B, N, H, dk, dv, device="cuda"):
+    return torch.empty(gdn_workspace_bytes(B, N, H, dk, dv), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+def _dims(q, v):
+    B, N, H, dk = q.shape
+    return B, N, H, dk, v.shape[-1]
+
+
+def gdn_tree_mask(parent_idx, mask, depth, stream=None):
+    B, N = parent_idx.shape
+    _check(lib().gdn_tree_mask(_ptr(parent_idx), B, N, _ptr(mask), _ptr(depth), _stream(stream)),
+           "gdn_tree_mask")
+
+
+def gdn_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, workspace, stream=None):
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_tree_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha),
+                                 _ptr(beta), _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(factors),
+                                 _ptr(workspace), B, N, H, dk, dv, _stream(stream)),
+           "gdn_tree_verify")
+
+
+def gdn_chain_verify(q, k, v, alpha, beta, S0, out, factors, stream=None):
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_chain_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha),
+                                  _ptr(beta), _ptr(S0), _ptr(out), _ptr(factors), B, N, H, dk, dv,
+                                  _stream(stream)), "gdn_chain_verify")
+
+
+def gdn_commit(S0, factors, accepted_path, S_new, N, dtype, stream=None):
+    B, H, dv, dk = S0.shape
+    _check(lib().gdn_commit(_ptr(S0), _ptr(factors), _ptr(accepted_path), accepted_path.shape[1],
+                            _ptr(S_new), B, N, H, dk, dv, dtype_code(dtype), _stream(stream)),
+           "gdn_commit")
+
+
+def gdn_commit_tree_verify(S, prev_factors, N_prev, prev_path, q, k, v, alpha, beta, parent_idx,
+                           out, factors, workspace, stream=None):
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_commit_tree_verify(_ptr(S), _ptr(prev_factors), N_prev, _ptr(prev_path),
+                                        prev_path.shape[1], _ptr(q), _ptr(k), _ptr(v),
+                                        dtype_code(q.dtype), _ptr(alpha), _ptr(beta),
+                                        _ptr(parent_idx), _ptr(out), _ptr(factors), _ptr(workspace),
+                                        B, N, H, dk, dv, _stream(stream)), "gdn_commit_tree_verify")
+
+
+def gdn_commit_chain_verify(S, prev_factors, N_prev, prev_path, q, k, v, alpha, beta, out, factors,
+                            stream=None):
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_commit_chain_verify(_ptr(S), _ptr(prev_factors), N_prev, _ptr(prev_path),
+                                         prev_path.shape[1], _ptr(q), _ptr(k), _ptr(v),
+                                         dtype_code(q.dtype), _ptr(alpha), _ptr(beta), _ptr(out),
+                                         _ptr(factors), B, N, H, dk, dv, _stream(stream)),
+           "gdn_commit_chain_verify")
+
+
+def gdn_last_error(stream=None) -> int:
+    return lib().gdn_last_error(_stream(stream))
+
+
+# ---------------------------------------------------------------------------
+# factor-buffer views (host-side reinterpretation of the documented layout)
+# ---------------------------------------------------------------------------
+def _align(x, a=256):
+    return (x + a - 1) // a * a
+
+
+def factor_views(buf, B, N, H, dk, dv, dtype):
+    """(delta [B,H,N,dv] f32, key [B,H,N,dk], g [B,H,N] f32, parent [B,N] i32) views of a factor buffer."""
+    esz = 4 if dtype_code(dtype) == DTYPE_F32 else 2
+    BHN = B * H * N
+    o_key = _align(BHN * dv * 4)
+    o_g = _align(o_key + BHN * dk * esz)
+    o_par = _align(o_g + BHN * 4)
+    kt = torch.float32 if esz == 4 else torch.bfloat16
+    delta = buf[: BHN * dv * 4].view(torch.float32).view(B, H, N, dv)
+    key = buf[o_key: o_key + BHN * dk * esz].view(kt).view(B, H, N, dk)
+    g = buf[o_g: o_g + BHN * 4].view(torch.float32).view(B, H, N)
+    par = buf[o_par: o_par + B * N * 4].view(torch.int32).view(B, N)
+    return delta, key, g, par

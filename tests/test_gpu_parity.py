@@ -1,0 +1,261 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Indices and masks are compared bit for bit; floating-point outputs, buffered
+innovations and committed states within max|err| <= 2e-3 x RMS of the oracle
+(fp32 state, bf16 inputs).
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import (TOL, alloc_outputs, assert_close, check_verify, dev_inputs, oracle_inputs,
+                     run_chain_verify, run_tree_verify)
+from speculative_decoding_linear_gb300 import gdnspec
+from speculative_decoding_linear_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_error_word():
+    gdnspec.gdn_last_error()
+    yield
+    assert gdnspec.gdn_last_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# ancestor mask (bit-exact)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, "chain64", "forest"])
+def test_tree_mask_bit_exact(oracle_mod, cfg):
+    if cfg == "chain64":
+        parent = wl.chain_tree(64)[None]
+    elif cfg == "forest":
+        parent = np.array([[-1, -1, 0, 1, 3, -1, 5, 2]], np.int32)
+    else:
+        parent = wl.make_workload(cfg).parent
+    B, N = parent.shape
+    p = torch.from_numpy(parent).cuda()
+    mask = torch.empty((B, N), dtype=torch.int64, device="cuda")
+    depth = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    gdnspec.gdn_tree_mask(p, mask, depth)
+    m_ref, d_ref = oracle_mod.tree_meta(parent)
+    assert np.array_equal(mask.cpu().numpy().view(np.uint64), m_ref)
+    assert np.array_equal(depth.cpu().numpy(), d_ref)
+
+
+# ---------------------------------------------------------------------------
+# tree verify
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_tree_verify_configs(oracle_mod, cfg):
+    w = wl.make_workload(cfg)
+    _, out, fac = run_tree_verify(w)
+    check_verify(w, out, fac, oracle_mod)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_tree_verify_fuzz(oracle_mod, seed):
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.choice([1, 2, 5, 17, 33, 64]))
+    dk = int(rng.choice([16, 32, 64, 128, 256]))
+    dv = int(rng.choice([16, 48, 96, 256]))
+    B, H = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+    maxdepth = int(rng.integers(0, N))
+    parent = np.stack([wl.random_tree(rng, N, maxdepth) for _ in range(B)])
+    if seed % 3 == 0 and N > 2:      # forests: extra roots
+        parent[:, N // 2] = -1
+    dtype = wl.F32 if seed % 4 == 1 else wl.BF16
+    w = wl.custom_workload(B, N, H, dk, dv, parent, seed=seed, dtype=dtype)
+    _, out, fac = run_tree_verify(w)
+    check_verify(w, out, fac, oracle_mod)
+
+
+def test_tree_verify_chain_topology_deep(oracle_mod):
+    """A 64-node chain through the tree path: 64 depth levels."""
+    w = wl.custom_workload(2, 64, 2, 256, 256, wl.chain_tree(64), seed=5)
+    _, out, fac = run_tree_verify(w)
+    check_verify(w, out, fac, oracle_mod)
+
+
+def test_sibling_isolation_on_gpu():
+    """Perturbing one node leaves every non-descendant's GPU output bit-identical."""
+    w = wl.make_workload(2)
+    d = dev_inputs(w)
+    _, out0, _ = run_tree_verify(w, d)
+    victim = 5
+    desc = {victim}
+    for t in range(victim + 1, w.N):
+        if w.parent[0, t] in desc:
+            desc.add(t)
+    d2 = {k: v.clone() for k, v in d.items()}
+    d2["k"][0, victim] = torch.flip(d2["k"][0, victim], dims=[-1])
+    d2["v"][0, victim] = -d2["v"][0, victim]
+    d2["beta"][0, victim] = 0.95
+    _, out1, _ = run_tree_verify(w, d2)
+    o0, o1 = out0.cpu().numpy(), out1.cpu().numpy()
+    for t in range(w.N):
+        if t in desc:
+            assert not np.array_equal(o0[0, t], o1[0, t])
+        else:
+            assert np.array_equal(o0[0, t], o1[0, t]), t
+
+
+# ---------------------------------------------------------------------------
+# chain verify (state-resident serial path)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", ["cfg1", "n1", "n64", "d16_f32", "b3_h5"])
+def test_chain_verify(oracle_mod, case):
+    if case == "cfg1":
+        w = wl.make_workload(1)
+    elif case == "n1":
+        w = wl.custom_workload(1, 1, 8, 256, 256, wl.chain_tree(1), seed=3)
+    elif case == "n64":
+        w = wl.custom_workload(1, 64, 4, 256, 256, wl.chain_tree(64), seed=4)
+    elif case == "d16_f32":
+        w = wl.custom_workload(2, 9, 3, 16, 16, wl.chain_tree(9), seed=6, dtype=wl.F32)
+    else:
+        w = wl.custom_workload(3, 13, 5, 128, 64, wl.chain_tree(13), seed=7)
+    _, out, fac = run_chain_verify(w)
+    check_verify(w, out, fac, oracle_mod)
+
+
+# ---------------------------------------------------------------------------
+# commit
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_commit(oracle_mod, cfg, inplace):
+    w = wl.make_workload(cfg)
+    d, out, fac = run_tree_verify(w)
+    S = d["S0"].clone() if inplace else d["S0"]
+    S_new = S if inplace else torch.empty_like(S)
+    gdnspec.gdn_commit(S, fac, d["path"], S_new, w.N, w.dtype)
+    assert gdnspec.gdn_last_error() == 0
+    x = oracle_inputs(w)
+    ref = oracle_mod.commit(x["k"], x["v"], x["alpha"], x["beta"], w.parent, x["S0"], w.path)
+    assert_close(S_new.cpu().numpy(), ref, "S_new")
+    # rows whose path is empty keep S0 bit for bit
+    for b in range(w.B):
+        if w.path[b, 0] < 0:
+            assert torch.equal(S_new[b], d["S0"][b])
+
+
+def test_commit_empty_path_bit_identical():
+    w = wl.make_workload(3)
+    d, _, fac = run_tree_verify(w)
+    path = torch.full_like(d["path"], -1)
+    S_new = torch.empty_like(d["S0"])
+    gdnspec.gdn_commit(d["S0"], fac, path, S_new, w.N, w.dtype)
+    assert torch.equal(S_new, d["S0"])
+
+
+def test_commit_full_chain_64(oracle_mod):
+    w = wl.custom_workload(1, 64, 2, 256, 256, wl.chain_tree(64), seed=9,
+                           path=np.arange(64, dtype=np.int32)[None], lmax=64)
+    d, _, fac = run_chain_verify(w)
+    S_new = torch.empty_like(d["S0"])
+    gdnspec.gdn_commit(d["S0"], fac, d["path"], S_new, w.N, w.dtype)
+    x = oracle_inputs(w)
+    ref = oracle_mod.commit(x["k"], x["v"], x["alpha"], x["beta"], w.parent, x["S0"], w.path)
+    assert_close(S_new.cpu().numpy(), ref, "S_new")
+
+
+# ---------------------------------------------------------------------------
+# fused commit + verify (delayed state update)
+# ---------------------------------------------------------------------------
+def _second_tree(w, seed, chain=False):
+    N2 = w.N if chain else max(1, w.N - 3)
+    parent = wl.chain_tree(N2) if chain else None
+    if parent is None:
+        rng = np.random.default_rng(seed)
+        parent = np.stack([wl.random_tree(rng, N2, 5) for _ in range(w.B)])
+    return wl.custom_workload(w.B, N2, w.H, w.dk, w.dv, parent, seed=seed, dtype=w.dtype)
+
+
+@pytest.mark.parametrize("cfg", [0, 2, 3])
+def test_fused_commit_tree_verify(oracle_mod, cfg):
+    w1 = wl.make_workload(cfg)
+    d1, _, fac1 = run_tree_verify(w1)
+    w2 = _second_tree(w1, seed=77 + cfg)
+    d2 = dev_inputs(w2)
+    S = d1["S0"].clone()
+    out2, fac2, ws2 = alloc_outputs(w2)
+    gdnspec.gdn_commit_tree_verify(S, fac1, w1.N, d1["path"], d2["q"], d2["k"], d2["v"], d2["alpha"],
+                                   d2["beta"], d2["parent"], out2, fac2, ws2)
+    assert gdnspec.gdn_last_error() == 0
+    # committed state == oracle commit of tree 1's accepted path
+    x1 = oracle_inputs(w1)
+    S_ref = oracle_mod.commit(x1["k"], x1["v"], x1["alpha"], x1["beta"], w1.parent, x1["S0"], w1.path)
+    assert_close(S.cpu().numpy(), S_ref, "committed S")
+    # fused == unfused commit, bit for bit
+    S_unf = torch.empty_like(S)
+    gdnspec.gdn_commit(d1["S0"], fac1, d1["path"], S_unf, w1.N, w1.dtype)
+    assert torch.equal(S, S_unf)
+    # tree 2 verified from the committed state
+    w2.S0 = S.cpu().numpy()
+    check_verify(w2, out2, fac2, oracle_mod)
+
+
+@pytest.mark.parametrize("cfg", [1, "b2"])
+def test_fused_commit_chain_verify(oracle_mod, cfg):
+    w1 = wl.make_workload(1) if cfg == 1 else wl.custom_workload(2, 8, 3, 64, 128, wl.chain_tree(8), seed=8)
+    d1, _, fac1 = run_chain_verify(w1)
+    w2 = _second_tree(w1, seed=91, chain=True)
+    d2 = dev_inputs(w2)
+    S = d1["S0"].clone()
+    out2, fac2, _ = alloc_outputs(w2)
+    gdnspec.gdn_commit_chain_verify(S, fac1, w1.N, d1["path"], d2["q"], d2["k"], d2["v"], d2["alpha"],
+                                    d2["beta"], out2, fac2)
+    assert gdnspec.gdn_last_error() == 0
+    S_unf = torch.empty_like(S)
+    gdnspec.gdn_commit(d1["S0"], fac1, d1["path"], S_unf, w1.N, w1.dtype)
+    assert torch.equal(S, S_unf)
+    x1 = oracle_inputs(w1)
+    S_ref = oracle_mod.commit(x1["k"], x1["v"], x1["alpha"], x1["beta"], w1.parent, x1["S0"], w1.path)
+    assert_close(S.cpu().numpy(), S_ref, "committed S")
+    w2.S0 = S.cpu().numpy()
+    check_verify(w2, out2, fac2, oracle_mod)
+
+
+def test_chain_and_tree_paths_agree():
+    """The chain kernel and the tree kernel on a chain topology give close results."""
+    w = wl.make_workload(1)
+    d = dev_inputs(w)
+    _, o_c, f_c = run_chain_verify(w, d)
+    _, o_t, f_t = run_tree_verify(w, d)
+    assert_close(o_c.cpu().numpy(), o_t.cpu().numpy(), "chain vs tree", tol=1e-3)
+
+
+# ---------------------------------------------------------------------------
+# device-detected errors
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("bad", [[-1, 0, 2, 1], [-1, 0, 1, 7], [-1, -3, 0, 1]])
+def test_invalid_parent_reported(bad):
+    w = wl.custom_workload(1, 4, 2, 32, 32, [-1, 0, 1, 2], seed=1)
+    d = dev_inputs(w)
+    d["parent"] = torch.tensor([bad], dtype=torch.int32, device="cuda")
+    out, fac, ws = alloc_outputs(w)
+    gdnspec.gdn_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"],
+                            out, fac, ws)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_TREE
+    assert gdnspec.gdn_last_error() == 0          # cleared by the read
+    mask = torch.empty((1, 4), dtype=torch.int64, device="cuda")
+    depth = torch.empty((1, 4), dtype=torch.int32, device="cuda")
+    gdnspec.gdn_tree_mask(d["parent"], mask, depth)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_TREE
+
+
+@pytest.mark.parametrize("bad", [[1, -1, -1], [0, 3, -1], [0, -1, 1], [0, 1, 5], [-2, -1, -1]])
+def test_invalid_path_reported(bad):
+    w = wl.custom_workload(1, 4, 2, 32, 32, [-1, 0, 0, 1], seed=2)
+    d, _, fac = run_tree_verify(w)
+    path = torch.tensor([bad], dtype=torch.int32, device="cuda")
+    S_new = torch.empty_like(d["S0"])
+    gdnspec.gdn_commit(d["S0"], fac, path, S_new, w.N, w.dtype)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_PATH
+    out, fac2, ws = alloc_outputs(w)
+    S = d["S0"].clone()
+    gdnspec.gdn_commit_tree_verify(S, fac, w.N, path, d["q"], d["k"], d["v"], d["alpha"], d["beta"],
+                                   d["parent"], out, fac2, ws)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_PATH
