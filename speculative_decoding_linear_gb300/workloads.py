@@ -64,11 +64,14 @@ def binary_tree_depth2() -> np.ndarray:
 
 
 def random_tree(rng: np.random.Generator, n: int, maxdepth: int) -> np.ndarray:
-    """Node 0 is the root; node i picks its parent uniformly among earlier nodes of depth < maxdepth."""
+    """Node 0 is the root; node i picks its parent uniformly among earlier nodes of depth < maxdepth
+    (with maxdepth 0 every node is a root)."""
     parent = np.full(n, -1, dtype=np.int32)
     depth = np.zeros(n, dtype=np.int64)
     for i in range(1, n):
         eligible = np.nonzero(depth[:i] < maxdepth)[0]
+        if len(eligible) == 0:          # maxdepth 0: every node is a root (a forest)
+            continue
         p = int(eligible[rng.integers(len(eligible))])
         parent[i] = p
         depth[i] = depth[p] + 1
