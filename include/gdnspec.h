@@ -170,6 +170,21 @@ int gdn_commit_chain_verify(float* S, const void* prev_factors, int N_prev,
                             cudaStream_t stream);
 
 /*
+ * Launch overlap between consecutive calls (process-wide switch, default off;
+ * returns the previous setting).  When on, the first kernel of every call is
+ * launched as a programmatic dependent of the kernel before it on the stream:
+ * it starts streaming its state tiles and pending-commit factors while that
+ * kernel finishes, and waits for it before reading q/k/v/alpha/beta/parent_idx
+ * and before writing anything.  This hides launch and prologue latency in a
+ * layer-major sweep ("Pith review of SpecLA", "What carries the argument":
+ * layer-major verification keeps per-layer state streaming back to back).
+ * Contract while on: the state S, S0 and factor buffers of a call must not be
+ * written by the kernel immediately before it on the stream -- e.g. the calls
+ * of a sweep visit different layers, each with its own state and factors.
+ */
+int gdn_set_launch_overlap(int enable);
+
+/*
  * Waits for `stream`, returns the first device-side error recorded on the
  * current device since the last call (GDN_OK if none) and clears it.
  */

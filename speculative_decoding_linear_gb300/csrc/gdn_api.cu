@@ -1,6 +1,7 @@
 // gdn_api.cu -- extern "C" entry points of libgdnspec.so (declared in
 // include/gdnspec.h): argument validation, buffer views, dispatch, and the
 // per-device error word that kernels write instead of trapping.
+#include <atomic>
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -15,6 +16,7 @@ constexpr int kMaxDevices = 64;
 int* g_err_ptr[kMaxDevices];
 int g_dev_ok[kMaxDevices];       // 0 unknown, 1 sm_103, -1 other
 std::mutex g_mu;
+std::atomic<int> g_overlap{0};   // gdn_set_launch_overlap
 
 // Address of this device's error word (host-side handle), or nullptr.
 int dev_setup(int* status) {
@@ -117,6 +119,7 @@ int verify_common(const void* q, const void* k, const void* v, int dtype, const 
     a.commit = fused ? commit_src(prev_factors, prev_path, Lmax, B, N_prev, H, dk, dv, dtype)
                      : CommitSrc{nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0};
     a.err = g_err_ptr[dev];
+    a.overlap = g_overlap.load() != 0;
     return from_cuda(chain ? launch_chain_verify(a, dtype, stream) : launch_tree_verify(a, dtype, stream));
 }
 
@@ -184,6 +187,7 @@ int gdn_commit(const float* S0, const void* factors, const int32_t* accepted_pat
     a.dk = dk;
     a.dv = dv;
     a.err = g_err_ptr[dev];
+    a.overlap = g_overlap.load() != 0;
     return from_cuda(launch_commit(a, dtype, stream));
 }
 
@@ -205,6 +209,10 @@ int gdn_commit_chain_verify(float* S, const void* prev_factors, int N_prev,
     if (prev_factors == nullptr || prev_path == nullptr) return GDN_ERR_ARG;
     return verify_common(q, k, v, dtype, alpha, beta, nullptr, true, S, out, factors, nullptr, B, N,
                          H, dk, dv, prev_factors, N_prev, prev_path, Lmax, stream);
+}
+
+int gdn_set_launch_overlap(int enable) {
+    return g_overlap.exchange(enable != 0 ? 1 : 0);
 }
 
 int gdn_last_error(cudaStream_t stream) {

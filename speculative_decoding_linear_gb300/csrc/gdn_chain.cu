@@ -9,120 +9,186 @@
 //     o_t[row] = S_t,row . q_t = alpha_t u + delta_t (k_t . q_t)
 //     S_row <- alpha_t S_row + delta_t k_t^T
 //
-// so the state is tiled along d_v: one CTA holds kRowsPerCta rows of one
-// (sequence, head) state in registers (one warp per kRowsPerWarp rows, each
-// lane holding d_k/32 columns) and runs the N tokens serially without ever
-// writing intermediate states.  When fused with a pending commit, the rows are
-// first committed (same arithmetic as the standalone commit) and written back
-// once.  The kernel emits the same factor record as the tree verifier.
+// so the state is tiled along d_v: one CTA holds kRows rows of one (sequence,
+// head) state in registers (each warp owns RPW rows, each lane d_k/32
+// interleaved columns) and runs the N tokens serially without ever writing an
+// intermediate state.
+//
+// Order of work inside a CTA:
+//   1. state rows -> registers and the pending commit's factor rows -> smem;
+//   2. the commit, applied in registers (1 and 2 only read memory, so with
+//      launch overlap enabled they may run while the previous kernel on the
+//      stream finishes);
+//   3. griddep_wait; committed rows written back once; this layer's
+//      q/k/v/alpha/beta staged with cp.async;
+//   4. the serial chain; outputs and the factor record.
 #include "gdn_internal.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kRowsPerWarp = 4;
-constexpr int kRowsPerCta = kWarps * kRowsPerWarp;   // 16
-constexpr int kEPL = kMaxDim / 32;                   // columns per lane
+constexpr int kEPL = kMaxDim / 32;   // state columns per lane
 
-struct ChainSmem {
-    float o[kMaxNodes * kRowsPerCta];
-    float d[kMaxNodes * kRowsPerCta];
-    float v[kMaxNodes * kRowsPerCta];
-    float alpha[kMaxNodes];
-    float beta[kMaxNodes];
-    float cd[kMaxPath * kRowsPerCta];
-    float coef[kMaxPath];
-    int nodes[kMaxPath];
-    float ega;
-    int L;
+template <int RPW>
+struct ChainGeom {
+    static constexpr int kRows = kWarps * RPW;
 };
 
-template <typename T>
+// dynamic smem layout (byte offsets), all 16-byte aligned
+struct ChainSmem {
+    int qk, key, v, alpha, beta, o, d, cd, coef, nodes, misc, total;
+    __host__ __device__ ChainSmem(int N, int dk, int Lcap, int rows, int esz) {
+        int off = 0;
+        auto take = [&](int bytes) { int o = off; off += (bytes + 15) / 16 * 16; return o; };
+        qk = take(N * 2 * dk * esz);     // [t][k | q][dk], input element type
+        key = take(Lcap * dk * esz);     // commit path keys
+        v = take(N * rows * esz);        // [t][row]
+        alpha = take(N * 4);
+        beta = take(N * 4);
+        o = take(N * rows * 4);
+        d = take(N * rows * 4);
+        cd = take(Lcap * rows * 4);      // e^{g_a - g_j} delta_j[row]
+        coef = take(kMaxPath * 4);
+        nodes = take(kMaxPath * 4);
+        misc = take(16);                 // ega, L
+        total = off;
+    }
+};
+
+template <typename T, int RPW>
 __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
-    __shared__ ChainSmem s;
+    constexpr int kRows = ChainGeom<RPW>::kRows;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int Lcap = a.commit.path ? a.commit.Lmax : 0;
+    const ChainSmem L(a.N, a.dk, Lcap, kRows, (int)sizeof(T));
+    T* s_qk = reinterpret_cast<T*>(smem + L.qk);
+    T* s_key = reinterpret_cast<T*>(smem + L.key);
+    T* s_v = reinterpret_cast<T*>(smem + L.v);
+    float* s_alpha = reinterpret_cast<float*>(smem + L.alpha);
+    float* s_beta = reinterpret_cast<float*>(smem + L.beta);
+    float* s_o = reinterpret_cast<float*>(smem + L.o);
+    float* s_d = reinterpret_cast<float*>(smem + L.d);
+    float* s_cd = reinterpret_cast<float*>(smem + L.cd);
+    float* s_coef = reinterpret_cast<float*>(smem + L.coef);
+    int* s_nodes = reinterpret_cast<int*>(smem + L.nodes);
+    float* s_ega = reinterpret_cast<float*>(smem + L.misc);
+    int* s_L = reinterpret_cast<int*>(smem + L.misc + 4);
+
     const int bh = blockIdx.x;
     const int b = bh / a.H, h = bh % a.H;
     const int N = a.N, dk = a.dk, dv = a.dv, tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int v0 = blockIdx.y * kRowsPerCta;
-    const int rows = min(kRowsPerCta, dv - v0);
-    const T* q = static_cast<const T*>(a.q);
-    const T* k = static_cast<const T*>(a.k);
-    const T* vv = static_cast<const T*>(a.v);
-
-    // gates and values of this CTA's rows
-    for (int t = tid; t < N; t += kWarps * 32) {
-        const size_t gi = ((size_t)b * N + t) * a.H + h;
-        s.alpha[t] = a.alpha[gi];
-        s.beta[t] = a.beta[gi];
-    }
-    for (int i = tid; i < N * kRowsPerCta; i += kWarps * 32) {
-        const int t = i / kRowsPerCta, r = i % kRowsPerCta;
-        s.v[i] = r < rows ? ld_elem<T>(vv, (((size_t)b * N + t) * a.H + h) * dv + v0 + r) : 0.f;
-    }
+    const int v0 = blockIdx.y * kRows;
+    const int rows = min(kRows, dv - v0);
     const bool fused = a.commit.path != nullptr;
-    if (fused) {
-        if (warp == 0) {
-            const int L = commit_path_setup(a.commit, b, h, a.H, s.nodes, s.coef, &s.ega);
-            if (lane == 0) {
-                s.L = L;
-                if (L < 0) set_error(a.err, GDN_ERR_PATH);
-            }
-        }
-        __syncthreads();
-        if (s.L < 0) return;
-        const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
-        for (int i = tid; i < s.L * kRowsPerCta; i += kWarps * 32) {
-            const int j = i / kRowsPerCta, r = i % kRowsPerCta;
-            s.cd[i] = r < rows ? s.coef[j] * dl[(size_t)s.nodes[j] * dv + v0 + r] : 0.f;
-        }
-    }
-    __syncthreads();
 
-    // state rows -> registers (committed and written back once when fused)
-    float S[kRowsPerWarp][kEPL];
-    const T* ckey = fused ? static_cast<const T*>(a.commit.key) + (size_t)bh * a.commit.N * dk : nullptr;
+    // 1. state rows -> registers (loads in flight while the commit is set up)
+    float S[RPW][kEPL];
 #pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        const int r = warp * kRowsPerWarp + rr;
-        const size_t row = ((size_t)bh * dv + v0 + r) * dk;
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int r = warp * RPW + rr;
+        const float* row = a.S + ((size_t)bh * dv + v0 + r) * dk;
 #pragma unroll
         for (int e = 0; e < kEPL; ++e) {
             const int c = lane + 32 * e;
-            float x = 0.f;
-            if (r < rows && c < dk) {
-                x = a.S[row + c];
-                if (fused) {
-                    float acc = s.ega * x;
-                    for (int i = 0; i < s.L; ++i)
-                        acc = fmaf(s.cd[i * kRowsPerCta + r],
-                                   ld_elem<T>(ckey, (size_t)s.nodes[i] * dk + c), acc);
-                    x = acc;
-                    a.S[row + c] = x;
+            S[rr][e] = (r < rows && c < dk) ? row[c] : 0.f;
+        }
+    }
+    int nL = 0;
+    if (fused) {
+        if (warp == 0) {
+            const int Lp = commit_path_setup(a.commit, b, h, a.H, s_nodes, s_coef, s_ega);
+            if (lane == 0) {
+                *s_L = Lp;
+                if (Lp < 0) set_error(a.err, GDN_ERR_PATH);
+            }
+        }
+        __syncthreads();
+        nL = *s_L;
+        if (nL < 0) return;
+        const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
+        const T* key_bh = static_cast<const T*>(a.commit.key) + (size_t)bh * a.commit.N * dk;
+        for (int i = 0; i < nL; ++i)
+            cp_async_block(s_key + (size_t)i * dk, key_bh + (size_t)s_nodes[i] * dk, dk * (int)sizeof(T),
+                           tid, kWarps * 32);
+        for (int i = tid; i < nL * kRows; i += kWarps * 32) {
+            const int j = i / kRows, r = i % kRows;
+            s_cd[i] = r < rows ? s_coef[j] * dl[(size_t)s_nodes[j] * dv + v0 + r] : 0.f;
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // 2. commit in registers (same arithmetic order as gdn_commit)
+        const float ega = *s_ega;
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = warp * RPW + rr;
+#pragma unroll
+            for (int e = 0; e < kEPL; ++e) {
+                const int c = lane + 32 * e;
+                if (r < rows && c < dk) {
+                    float acc = ega * S[rr][e];
+                    for (int i = 0; i < nL; ++i)
+                        acc = fmaf(s_cd[i * kRows + r], ld_elem<T>(s_key, (size_t)i * dk + c), acc);
+                    S[rr][e] = acc;
                 }
             }
-            S[rr][e] = x;
         }
     }
 
-    // serial chain
+    // Everything above only read memory.  Writes and this layer's inputs come
+    // after the programmatic wait.
+    griddep_wait();
+    griddep_launch();
+    if (fused) {    // committed rows written back once
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = warp * RPW + rr;
+            float* row = a.S + ((size_t)bh * dv + v0 + r) * dk;
+#pragma unroll
+            for (int e = 0; e < kEPL; ++e) {
+                const int c = lane + 32 * e;
+                if (r < rows && c < dk) row[c] = S[rr][e];
+            }
+        }
+    }
+
+    // 3. this layer's draft inputs
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    const T* vv = static_cast<const T*>(a.v);
+    const int rowb = dk * (int)sizeof(T);
     for (int t = 0; t < N; ++t) {
         const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
+        cp_async_block(s_qk + (size_t)(2 * t) * dk, k + rt, rowb, tid, kWarps * 32);
+        cp_async_block(s_qk + (size_t)(2 * t + 1) * dk, q + rt, rowb, tid, kWarps * 32);
+    }
+    for (int i = tid; i < N * kRows; i += kWarps * 32) {
+        const int t = i / kRows, r = i % kRows;
+        if (r < rows) s_v[i] = vv[(((size_t)b * N + t) * a.H + h) * dv + v0 + r];
+    }
+    for (int t = tid; t < N; t += kWarps * 32) {
+        const size_t gi = ((size_t)b * N + t) * a.H + h;
+        s_alpha[t] = a.alpha[gi];
+        s_beta[t] = a.beta[gi];
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // 4. serial chain
+    for (int t = 0; t < N; ++t) {
         float kt[kEPL], qt[kEPL];
         float kq = 0.f;
 #pragma unroll
         for (int e = 0; e < kEPL; ++e) {
             const int c = lane + 32 * e;
-            kt[e] = c < dk ? ld_elem<T>(k, rt + c) : 0.f;
-            qt[e] = c < dk ? ld_elem<T>(q, rt + c) : 0.f;
+            kt[e] = c < dk ? ld_elem<T>(s_qk, (size_t)(2 * t) * dk + c) : 0.f;
+            qt[e] = c < dk ? ld_elem<T>(s_qk, (size_t)(2 * t + 1) * dk + c) : 0.f;
             kq = fmaf(kt[e], qt[e], kq);
         }
-        kq = warp_sum(kq);
-        const float al = s.alpha[t], be = s.beta[t];
-        float sk[kRowsPerWarp], sq[kRowsPerWarp];
+        float sk[RPW], sq[RPW];
 #pragma unroll
-        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        for (int rr = 0; rr < RPW; ++rr) {
             float x = 0.f, y = 0.f;
 #pragma unroll
             for (int e = 0; e < kEPL; ++e) {
@@ -134,47 +200,51 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
+            kq += __shfl_xor_sync(0xffffffffu, kq, o);
 #pragma unroll
-            for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+            for (int rr = 0; rr < RPW; ++rr) {
                 sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
                 sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
             }
         }
+        const float al = s_alpha[t], be = s_beta[t];
 #pragma unroll
-        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-            const int r = warp * kRowsPerWarp + rr;
-            const float dlt = be * (s.v[t * kRowsPerCta + r] - al * sk[rr]);
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = warp * RPW + rr;
+            const float vt = r < rows ? ld_elem<T>(s_v, (size_t)t * kRows + r) : 0.f;
+            const float dlt = be * (vt - al * sk[rr]);
             const float o = fmaf(al, sq[rr], dlt * kq);
 #pragma unroll
             for (int e = 0; e < kEPL; ++e) S[rr][e] = fmaf(al, S[rr][e], dlt * kt[e]);
             if (lane == 0) {
-                s.o[t * kRowsPerCta + r] = o;
-                s.d[t * kRowsPerCta + r] = dlt;
+                s_o[t * kRows + r] = o;
+                s_d[t * kRows + r] = dlt;
             }
         }
     }
     __syncthreads();
 
     // outputs and factors (coalesced along d_v)
-    for (int i = tid; i < N * kRowsPerCta; i += kWarps * 32) {
-        const int t = i / kRowsPerCta, r = i % kRowsPerCta;
+    for (int i = tid; i < N * kRows; i += kWarps * 32) {
+        const int t = i / kRows, r = i % kRows;
         if (r >= rows) continue;
-        a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + r] = s.o[i];
-        a.f.delta[((size_t)bh * N + t) * dv + v0 + r] = s.d[i];
+        a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + r] = s_o[i];
+        a.f.delta[((size_t)bh * N + t) * dv + v0 + r] = s_d[i];
     }
-    // key copy, gates and parents: spread over the CTAs of this (b, h)
+    // key copy (from smem), gates and parents: spread over the CTAs of this (b, h)
     T* key_out = static_cast<T*>(a.f.key);
+    const int vecs = rowb / 16;
     for (int t = blockIdx.y; t < N; t += gridDim.y) {
-        const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
-        for (int c = tid; c < dk; c += kWarps * 32)
-            key_out[((size_t)bh * N + t) * dk + c] = k[rt + c];
+        const uint4* src = reinterpret_cast<const uint4*>(s_qk + (size_t)(2 * t) * dk);
+        uint4* dst = reinterpret_cast<uint4*>(key_out + ((size_t)bh * N + t) * dk);
+        for (int i = tid; i < vecs; i += kWarps * 32) dst[i] = src[i];
     }
     if (blockIdx.y == 0 && warp == 0) {
         // g_t = sum_{i <= t} log alpha_i : warp scan over chunks of 32 nodes
         float carry = 0.f;
         for (int t0 = 0; t0 < N; t0 += 32) {
             const int t = t0 + lane;
-            float x = t < N ? logf(s.alpha[t]) : 0.f;
+            float x = t < N ? logf(s_alpha[t]) : 0.f;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -190,15 +260,28 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     }
 }
 
+template <typename T, int RPW>
+cudaError_t launch_chain_t(const VerifyArgs& a, cudaStream_t s) {
+    static bool attr[64];
+    constexpr int kRows = ChainGeom<RPW>::kRows;
+    const ChainSmem L(a.N, a.dk, a.commit.path ? a.commit.Lmax : 0, kRows, (int)sizeof(T));
+    cudaError_t e = ensure_smem(chain_kernel<T, RPW>, L.total, attr);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.B * a.H, (a.dv + kRows - 1) / kRows);
+    return launch_kernel(chain_kernel<T, RPW>, grid, dim3(kWarps * 32), L.total, s, a.overlap, a);
+}
+
+template <typename T>
+cudaError_t launch_chain_dt(const VerifyArgs& a, cudaStream_t s) {
+    // Small problems: 8-row CTAs so that more SMs stream the state.
+    const long long ctas16 = (long long)a.B * a.H * ((a.dv + 15) / 16);
+    return ctas16 < 2 * 148 ? launch_chain_t<T, 2>(a, s) : launch_chain_t<T, 4>(a, s);
+}
+
 }  // namespace
 
 cudaError_t launch_chain_verify(const VerifyArgs& a, int dtype, cudaStream_t s) {
-    dim3 grid(a.B * a.H, (a.dv + kRowsPerCta - 1) / kRowsPerCta);
-    if (dtype == GDN_DTYPE_F32)
-        chain_kernel<float><<<grid, kWarps * 32, 0, s>>>(a);
-    else
-        chain_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return dtype == GDN_DTYPE_F32 ? launch_chain_dt<float>(a, s) : launch_chain_dt<__nv_bfloat16>(a, s);
 }
 
 }  // namespace gdn

@@ -104,6 +104,7 @@ struct VerifyArgs {
     int B, N, H, dk, dv;
     CommitSrc commit;          // commit.path == nullptr: no fused commit
     int* err;
+    bool overlap;              // launch the call's first kernel as a programmatic dependent
 };
 
 struct CommitArgs {
@@ -112,6 +113,7 @@ struct CommitArgs {
     CommitSrc src;
     int B, H, dk, dv;
     int* err;
+    bool overlap;
 };
 
 // ---------------------------------------------------------------------------
@@ -200,6 +202,9 @@ cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint64_t* mask
 cudaError_t launch_tree_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_chain_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, int dtype, cudaStream_t s);
+// tensor-core contraction of the tree verifier (gdn_tree_tc.cu)
+bool tc_contract_eligible(const VerifyArgs& a);
+cudaError_t launch_tree_contract_tc(const VerifyArgs& a, cudaStream_t s);
 
 }  // namespace gdn
 
@@ -224,13 +229,13 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p, siz
 }
 
 // One committed quad of a state row:
-//   s' = e^{g_a} s + sum_i cd[i] k_{node i}[c..c+3],  cd[i] = e^{g_a - g_i} delta_i[row]
-// The same routine serves the standalone and the fused commit, so both give
-// identical bits.
+//   s' = e^{g_a} s + sum_i cd[i] k_i[c..c+3],  cd[i] = e^{g_a - g_i} delta_i[row]
+// with the accepted path's keys staged as rows keys[i][0..dk).  Every commit
+// (standalone or fused into a verify) uses this order of operations, so they
+// all give identical bits.
 template <typename KT>
-__device__ __forceinline__ float4 commit_quad(float4 s, float ega, int L, const int* nodes,
-                                              const float* cd, int cd_stride, const KT* key_bh,
-                                              int dk, int c) {
+__device__ __forceinline__ float4 commit_quad(float4 s, float ega, int L, const float* cd,
+                                              int cd_stride, const KT* keys, int dk, int c) {
     float4 a;
     a.x = ega * s.x;
     a.y = ega * s.y;
@@ -238,13 +243,81 @@ __device__ __forceinline__ float4 commit_quad(float4 s, float ega, int L, const 
     a.w = ega * s.w;
     for (int i = 0; i < L; ++i) {
         const float w = cd[i * cd_stride];
-        const float4 kq = ld4<KT>(key_bh, (size_t)nodes[i] * dk + c);
+        const float4 kq = ld4<KT>(keys, (size_t)i * dk + c);
         a.x = fmaf(w, kq.x, a.x);
         a.y = fmaf(w, kq.y, a.y);
         a.z = fmaf(w, kq.z, a.z);
         a.w = fmaf(w, kq.w, a.w);
     }
     return a;
+}
+
+}  // namespace gdn
+
+namespace gdn {
+
+// ---------------------------------------------------------------------------
+// async staging, programmatic dependent launch, launch helper
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global -> shared copy that bypasses registers (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Cooperative copy of `bytes` (a multiple of 16) with cp.async.
+__device__ __forceinline__ void cp_async_block(void* smem, const void* gmem, int bytes, int tid, int nthr) {
+    char* d = static_cast<char*>(smem);
+    const char* s = static_cast<const char*>(gmem);
+    for (int o = tid * 16; o < bytes; o += nthr * 16) cp_async16(d + o, s + o);
+}
+
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// serialization attribute may start before its predecessor on the stream has
+// finished; griddep_wait() blocks until the predecessor has completed and its
+// writes are visible (a no-op for normally launched kernels).  Every kernel of
+// this library calls griddep_launch() only after its own griddep_wait(), so a
+// kernel's pre-wait section always sees the writes of every kernel launched
+// two or more positions earlier on the stream.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool programmatic, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+template <typename K>
+inline cudaError_t ensure_smem(K kernel, size_t bytes, bool* done_per_device) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (bytes > 48 * 1024 && !done_per_device[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        done_per_device[dev] = true;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace gdn

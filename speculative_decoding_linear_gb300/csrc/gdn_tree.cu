@@ -1,4 +1,4 @@
-// gdn_tree.cu -- tree-masked factorized verification (SIMT path).
+// gdn_tree.cu -- tree-masked factorized verification: mask, prologue, SIMT contraction.
 //
 // Review of SpecLA (pith.science 7ERME3HB), "Core claim": A_tree = M_tree (.)
 // (K_b K_a^T), T_tree = solve_tril(I - A_tree), O = Qhat S0^T - Attn (W S0^T)
@@ -18,18 +18,46 @@
 // only the <= depth(t)+1 rows of R on path(t): the "N x N" products are short
 // gathers along each node's path.
 //
-// Two kernels:
-//   tree_prep_kernel      one CTA per (b, h): ancestor masks, gates, the masked
-//                         Gram entries, T by depth levels, P = Attn T; writes
-//                         the workspace record and the factor record's g,
-//                         parent and key sections.
-//   tree_contract_kernel  one CTA per (b, h, 32 rows of d_v): streams the S0
-//                         tile (applying a pending commit first when fused),
-//                         forms Y = [Q; K] S0_tile^T, then R, Delta and O.
+// Kernels here:
+//   tree_mask_kernel      ancestor bitmask + depth (gdn_tree_mask).
+//   tree_prep_kernel      one CTA per (b, h): stages Q and K with cp.async,
+//                         ancestor masks, gates, masked Gram entries, T by
+//                         depth levels, P = Attn T; writes the workspace
+//                         record and the factor record's g, parent and keys.
+//   tree_contract_kernel  SIMT contraction for any d_k/d_v/dtype: one CTA per
+//                         (b, h, 32 state rows); streams the state tile
+//                         (committing a pending path first when fused), forms
+//                         Y = [Q; K] S_tile^T, then R, Delta and O.
+//                         (gdn_tree_tc.cu holds the tensor-core version.)
 #include "gdn_internal.cuh"
 
 namespace gdn {
 namespace {
+
+template <typename T>
+struct Chunk;   // 16-byte chunk of q/k elements
+template <>
+struct Chunk<__nv_bfloat16> {
+    __device__ static float dot(uint4 a, uint4 b) {
+        const uint32_t x[4] = {a.x, a.y, a.z, a.w}, y[4] = {b.x, b.y, b.z, b.w};
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            s = fmaf(__uint_as_float(x[i] << 16), __uint_as_float(y[i] << 16), s);
+            s = fmaf(__uint_as_float(x[i] & 0xffff0000u), __uint_as_float(y[i] & 0xffff0000u), s);
+        }
+        return s;
+    }
+};
+template <>
+struct Chunk<float> {
+    __device__ static float dot(uint4 a, uint4 b) {
+        float s = __uint_as_float(a.x) * __uint_as_float(b.x);
+        s = fmaf(__uint_as_float(a.y), __uint_as_float(b.y), s);
+        s = fmaf(__uint_as_float(a.z), __uint_as_float(b.z), s);
+        return fmaf(__uint_as_float(a.w), __uint_as_float(b.w), s);
+    }
+};
 
 // ---------------------------------------------------------------------------
 // ancestor mask + depth (gdn_tree_mask)
@@ -65,43 +93,82 @@ __global__ void tree_mask_kernel(const int32_t* parent, int N, uint64_t* mask, i
 // per-(b, h) prologue
 // ---------------------------------------------------------------------------
 constexpr int kPrepThreads = 256;
-constexpr int kLd = kMaxNodes + 1;   // padded row stride of the N x N tables in smem
 
-struct PrepSmem {
-    float A[kMaxNodes * kLd];
-    float At[kMaxNodes * kLd];       // Attn
-    float T[kMaxNodes * kLd];
-    uint64_t anc[kMaxNodes];         // strict ancestors
-    float la[kMaxNodes];             // log alpha_t
-    float g[kMaxNodes];
-    float beta[kMaxNodes];
-    int par[kMaxNodes];
-    int depth[kMaxNodes];
-    int maxdepth;
+struct PrepLayout {
+    int qs, ks, A, At, T, pairs, par, anc, la, g, beta, depth, off, misc, total, ld;
+    __host__ __device__ PrepLayout(int N, int dk, int esz) {
+        int o = 0;
+        auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
+        ld = N + 1;
+        qs = take(N * dk * esz);
+        ks = take(N * dk * esz);
+        A = take(N * ld * 4);
+        At = take(N * ld * 4);
+        T = take(N * ld * 4);
+        pairs = take(N * (N + 1) / 2 * 2);
+        par = take(N * 4);
+        anc = take(N * 8);
+        la = take(N * 4);
+        g = take(N * 4);
+        beta = take(N * 4);
+        depth = take(N * 4);
+        off = take((N + 1) * 4);
+        misc = take(16);
+        total = o;
+    }
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    PrepSmem& s = *reinterpret_cast<PrepSmem*>(smem_raw);
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int N = a.N, dk = a.dk, tid = threadIdx.x;
+    const PrepLayout Ly(N, dk, (int)sizeof(T));
+    T* Qs = reinterpret_cast<T*>(smem + Ly.qs);
+    T* Ks = reinterpret_cast<T*>(smem + Ly.ks);
+    float* sA = reinterpret_cast<float*>(smem + Ly.A);
+    float* sAt = reinterpret_cast<float*>(smem + Ly.At);
+    float* sT = reinterpret_cast<float*>(smem + Ly.T);
+    uint16_t* pairs = reinterpret_cast<uint16_t*>(smem + Ly.pairs);
+    int* par = reinterpret_cast<int*>(smem + Ly.par);
+    uint64_t* anc = reinterpret_cast<uint64_t*>(smem + Ly.anc);
+    float* la = reinterpret_cast<float*>(smem + Ly.la);
+    float* sg = reinterpret_cast<float*>(smem + Ly.g);
+    float* sbeta = reinterpret_cast<float*>(smem + Ly.beta);
+    int* sdepth = reinterpret_cast<int*>(smem + Ly.depth);
+    int* off = reinterpret_cast<int*>(smem + Ly.off);
+    int* maxdepth = reinterpret_cast<int*>(smem + Ly.misc);
+    const int ld = Ly.ld;
+
     const int bh = blockIdx.x;
     const int b = bh / a.H, h = bh % a.H;
-    const int N = a.N, tid = threadIdx.x;
     const WsLayout wl = ws_layout(N);
     char* rec = a.ws + (size_t)bh * wl.record;
 
-    // 1. parents, validated
+    // This layer's inputs may come from the previous kernel on the stream.
+    griddep_wait();
+    griddep_launch();
+
+    // 1. stage Q, K rows (cp.async) and the per-node scalars
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    const int rowb = dk * (int)sizeof(T);
+    for (int t = 0; t < N; ++t) {
+        const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
+        cp_async_block(Qs + (size_t)t * dk, q + rt, rowb, tid, kPrepThreads);
+        cp_async_block(Ks + (size_t)t * dk, k + rt, rowb, tid, kPrepThreads);
+    }
     bool bad = false;
     if (tid < N) {
         const int p = a.parent[(size_t)b * N + tid];
         bad = p < -1 || p >= tid;
-        s.par[tid] = p;
+        par[tid] = p;
         const size_t gi = ((size_t)b * N + tid) * a.H + h;
-        s.la[tid] = logf(a.alpha[gi]);
-        s.beta[tid] = a.beta[gi];
+        la[tid] = logf(a.alpha[gi]);
+        sbeta[tid] = a.beta[gi];
     }
-    if (tid == 0) s.maxdepth = 0;
-    for (int i = tid; i < kMaxNodes * kLd; i += kPrepThreads) s.A[i] = s.At[i] = s.T[i] = 0.f;
+    if (tid == 0) *maxdepth = 0;
+    for (int i = tid; i < N * ld; i += kPrepThreads) sA[i] = sAt[i] = sT[i] = 0.f;
+    cp_async_wait_all();
     if (__syncthreads_or(bad)) {
         if (tid == 0) {
             set_error(a.err, GDN_ERR_TREE);
@@ -114,99 +181,122 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
     if (tid < N) {
         uint64_t m = 0;
         int d = 0;
-        for (int j = s.par[tid]; j >= 0; j = s.par[j]) {
+        for (int j = par[tid]; j >= 0; j = par[j]) {
             m |= 1ull << j;
             ++d;
         }
-        s.anc[tid] = m;
-        s.depth[tid] = d;
-        atomicMax(&s.maxdepth, d);
+        anc[tid] = m;
+        sdepth[tid] = d;
+        atomicMax(maxdepth, d);
         float gs = 0.f;
-        for (uint64_t r = m; r; r &= r - 1) gs += s.la[__ffsll((long long)r) - 1];
-        s.g[tid] = gs + s.la[tid];
+        for (uint64_t r = m; r; r &= r - 1) gs += la[__ffsll((long long)r) - 1];
+        sg[tid] = gs + la[tid];
     }
     __syncthreads();
 
-    // 3. masked Gram entries; one warp per row t, lanes split d_k
+    // 3. enumerate (t, j in path(t)) pairs: exclusive scan of path lengths
     const int warp = tid >> 5, lane = tid & 31;
-    const T* q = static_cast<const T*>(a.q);
-    const T* k = static_cast<const T*>(a.k);
-    T* key_out = static_cast<T*>(a.f.key);
-    for (int t = warp; t < N; t += kPrepThreads / 32) {
-        const size_t rt = ((size_t)b * N + t) * a.H + h;
-        float kt[kMaxDim / 32], qt[kMaxDim / 32];
+    if (warp == 0) {
+        int carry = 0;
+        for (int t0 = 0; t0 < N; t0 += 32) {
+            const int t = t0 + lane;
+            int x = t < N ? sdepth[t] + 1 : 0;
 #pragma unroll
-        for (int e = 0; e < kMaxDim / 32; ++e) {
-            const int c = lane + 32 * e;
-            const bool in = c < a.dk;
-            kt[e] = in ? ld_elem<T>(k, rt * a.dk + c) : 0.f;
-            qt[e] = in ? ld_elem<T>(q, rt * a.dk + c) : 0.f;
-            if (in) st_elem<T>(key_out, ((size_t)bh * N + t) * a.dk + c, kt[e]);
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (t < N) off[t + 1] = carry + x;
+            carry += __shfl_sync(0xffffffffu, x, 31);
         }
-        const float gt = s.g[t], bt = s.beta[t];
-        uint64_t path = s.anc[t] | (1ull << t);
-        for (; path; path &= path - 1) {
-            const int j = __ffsll((long long)path) - 1;
-            const size_t rj = ((size_t)b * N + j) * a.H + h;
-            float pkk = 0.f, pqk = 0.f;
+        if (lane == 0) off[0] = 0;
+    }
+    __syncthreads();
+    if (tid < N) {
+        int o = off[tid];
+        for (uint64_t r = anc[tid]; r; r &= r - 1)
+            pairs[o++] = (uint16_t)((tid << 8) | (__ffsll((long long)r) - 1));
+        pairs[o] = (uint16_t)((tid << 8) | tid);
+    }
+    __syncthreads();
+
+    // 4. masked Gram entries: 8 lanes per pair, 16-byte chunks interleaved across the group
+    const int npairs = off[N];
+    const int grp = lane >> 3, gl = lane & 7;
+    const int nchunk = rowb / 16;
+    for (int base = warp * 4; base < npairs; base += (kPrepThreads / 32) * 4) {
+        const int p = base + grp;
+        const bool valid = p < npairs;
+        const int pr = valid ? pairs[p] : 0;
+        const int t = pr >> 8, j = pr & 255;
+        float pkk = 0.f, pqk = 0.f;
+        if (valid) {
+            const uint4* kt = reinterpret_cast<const uint4*>(Ks + (size_t)t * dk);
+            const uint4* qt = reinterpret_cast<const uint4*>(Qs + (size_t)t * dk);
+            const uint4* kj = reinterpret_cast<const uint4*>(Ks + (size_t)j * dk);
+            for (int c = gl; c < nchunk; c += 8) {
+                const uint4 x = kj[c];
+                pkk += Chunk<T>::dot(kt[c], x);
+                pqk += Chunk<T>::dot(qt[c], x);
+            }
+        }
 #pragma unroll
-            for (int e = 0; e < kMaxDim / 32; ++e) {
-                const int c = lane + 32 * e;
-                const float kj = c < a.dk ? ld_elem<T>(k, rj * a.dk + c) : 0.f;
-                pkk = fmaf(kt[e], kj, pkk);
-                pqk = fmaf(qt[e], kj, pqk);
-            }
-            pkk = warp_sum(pkk);
-            pqk = warp_sum(pqk);
-            if (lane == 0) {
-                const float gam = expf(gt - s.g[j]);
-                s.At[t * kLd + j] = gam * pqk;
-                if (j != t) s.A[t * kLd + j] = bt * gam * pkk;
-            }
+        for (int o = 4; o > 0; o >>= 1) {
+            pkk += __shfl_xor_sync(0xffffffffu, pkk, o);
+            pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
+        }
+        if (valid && gl == 0) {
+            const float gam = expf(sg[t] - sg[j]);
+            sAt[t * ld + j] = gam * pqk;
+            if (j != t) sA[t * ld + j] = sbeta[t] * gam * pkk;
         }
     }
     __syncthreads();
 
-    // 4. T = (I + A)^-1 by depth levels: row t needs only rows of its ancestors
-    for (int d = 0; d <= s.maxdepth; ++d) {
+    // 5. T = (I + A)^-1 by depth levels: row t needs only rows of its ancestors
+    const int md = *maxdepth;
+    for (int d = 0; d <= md; ++d) {
         for (int i = tid; i < N * N; i += kPrepThreads) {
             const int t = i / N, c = i % N;
-            if (s.depth[t] != d) continue;
-            const uint64_t an = s.anc[t];
+            if (sdepth[t] != d) continue;
+            const uint64_t an = anc[t];
             if (c != t && !((an >> c) & 1ull)) continue;
             float x = c == t ? 1.f : 0.f;
             for (uint64_t r = an; r; r &= r - 1) {
                 const int j = __ffsll((long long)r) - 1;
-                x = fmaf(-s.A[t * kLd + j], s.T[j * kLd + c], x);
+                x = fmaf(-sA[t * ld + j], sT[j * ld + c], x);
             }
-            s.T[t * kLd + c] = x;
+            sT[t * ld + c] = x;
         }
         __syncthreads();
     }
 
-    // 5. P = Attn T (support on path(t)); write the workspace record
+    // 6. P = Attn T (support on path(t)); workspace record and factor record
     float* wT = reinterpret_cast<float*>(rec + wl.T);
     float* wP = reinterpret_cast<float*>(rec + wl.P);
     for (int i = tid; i < N * N; i += kPrepThreads) {
         const int t = i / N, c = i % N;
-        const uint64_t path = s.anc[t] | (1ull << t);
+        const uint64_t path = anc[t] | (1ull << t);
         float x = 0.f;
         if ((path >> c) & 1ull) {
             for (uint64_t r = path; r; r &= r - 1) {
                 const int j = __ffsll((long long)r) - 1;
-                x = fmaf(s.At[t * kLd + j], s.T[j * kLd + c], x);
+                x = fmaf(sAt[t * ld + j], sT[j * ld + c], x);
             }
         }
         wP[i] = x;
-        wT[i] = s.T[t * kLd + c];
+        wT[i] = sT[t * ld + c];
     }
     if (tid < N) {
-        reinterpret_cast<float*>(rec + wl.eg)[tid] = expf(s.g[tid]);
-        reinterpret_cast<float*>(rec + wl.bt)[tid] = s.beta[tid];
-        reinterpret_cast<uint64_t*>(rec + wl.anc)[tid] = s.anc[tid] | (1ull << tid);
-        a.f.g[(size_t)bh * N + tid] = s.g[tid];
-        if (h == 0) a.f.parent[(size_t)b * N + tid] = s.par[tid];
+        reinterpret_cast<float*>(rec + wl.eg)[tid] = expf(sg[tid]);
+        reinterpret_cast<float*>(rec + wl.bt)[tid] = sbeta[tid];
+        reinterpret_cast<uint64_t*>(rec + wl.anc)[tid] = anc[tid] | (1ull << tid);
+        a.f.g[(size_t)bh * N + tid] = sg[tid];
+        if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
     }
+    uint4* key_out = reinterpret_cast<uint4*>(static_cast<T*>(a.f.key) + (size_t)bh * N * dk);
+    const uint4* ksrc = reinterpret_cast<const uint4*>(Ks);
+    for (int i = tid; i < N * nchunk; i += kPrepThreads) key_out[i] = ksrc[i];
 }
 
 // ---------------------------------------------------------------------------
@@ -218,71 +308,124 @@ constexpr int kCThreads = 256;
 constexpr int kRowGroups = kCThreads / 32;
 constexpr int kMaxRowsPerThread = 2 * kMaxNodes / kRowGroups;   // 16
 
-struct ContractSmem {
-    float S[kVT * (kMaxDim + 1)];            // state tile, padded rows
-    float qk[kKC * (2 * kMaxNodes + 1)];     // [c][r] (row stride 2N+1): r < N -> q_r, else k_{r-N}
-    float YQ[kMaxNodes * (kVT + 1)];
-    float R[kMaxNodes * (kVT + 1)];
-    float cd[kMaxPath * kVT];                // fused commit: e^{g_a-g_j} delta_j[row]
-    float coef[kMaxPath];
-    int nodes[kMaxPath];
-    float ega;
-    int L;
+struct ContractLayout {
+    int S, qk, YQ, R, T, P, eg, bt, anc, cd, key, coef, nodes, misc, total;
+    __host__ __device__ ContractLayout(int N, int dk, int Lcap, int esz) {
+        int o = 0;
+        auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
+        S = take(kVT * (dk + 1) * 4);
+        qk = take(kKC * (2 * N + 1) * 4);
+        YQ = take(N * (kVT + 1) * 4);
+        R = take(N * (kVT + 1) * 4);
+        T = take(N * N * 4);
+        P = take(N * N * 4);
+        eg = take(N * 4);
+        bt = take(N * 4);
+        anc = take(N * 8);
+        cd = take(Lcap * kVT * 4);
+        key = take(Lcap * dk * esz);
+        coef = take(kMaxPath * 4);
+        nodes = take(kMaxPath * 4);
+        misc = take(16);
+        total = o;
+    }
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ContractSmem& s = *reinterpret_cast<ContractSmem*>(smem_raw);
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int N = a.N, dk = a.dk, dv = a.dv, tid = threadIdx.x;
+    const bool fused = a.commit.path != nullptr;
+    const ContractLayout Ly(N, dk, fused ? a.commit.Lmax : 0, (int)sizeof(T));
+    float* sS = reinterpret_cast<float*>(smem + Ly.S);
+    float* sqk = reinterpret_cast<float*>(smem + Ly.qk);
+    float* sYQ = reinterpret_cast<float*>(smem + Ly.YQ);
+    float* sR = reinterpret_cast<float*>(smem + Ly.R);
+    float* sT = reinterpret_cast<float*>(smem + Ly.T);
+    float* sP = reinterpret_cast<float*>(smem + Ly.P);
+    float* seg = reinterpret_cast<float*>(smem + Ly.eg);
+    float* sbt = reinterpret_cast<float*>(smem + Ly.bt);
+    uint64_t* sanc = reinterpret_cast<uint64_t*>(smem + Ly.anc);
+    float* scd = reinterpret_cast<float*>(smem + Ly.cd);
+    T* skey = reinterpret_cast<T*>(smem + Ly.key);
+    float* scoef = reinterpret_cast<float*>(smem + Ly.coef);
+    int* snodes = reinterpret_cast<int*>(smem + Ly.nodes);
+    float* sega = reinterpret_cast<float*>(smem + Ly.misc);
+    int* sL = reinterpret_cast<int*>(smem + Ly.misc + 4);
+
     const int bh = blockIdx.x;
     const int b = bh / a.H, h = bh % a.H;
-    const int N = a.N, dk = a.dk, dv = a.dv, tid = threadIdx.x;
     const int v0 = blockIdx.y * kVT;
     const int rows = min(kVT, dv - v0);
+    const int ldS = dk + 1;
     const WsLayout wl = ws_layout(N);
     const char* rec = a.ws + (size_t)bh * wl.record;
-    const uint64_t* anc = reinterpret_cast<const uint64_t*>(rec + wl.anc);
-    const int ldS = dk + 1;
 
-    if (anc[0] == ~0ull) return;    // prologue rejected this tree (error already recorded)
-
-    // 1. pending commit (fused path)
-    const bool fused = a.commit.path != nullptr;
-    if (fused) {
-        if (tid < 32) {
-            const int L = commit_path_setup(a.commit, b, h, a.H, s.nodes, s.coef, &s.ega);
-            if (tid == 0) {
-                s.L = L;
-                if (L < 0) set_error(a.err, GDN_ERR_PATH);
-            }
-        }
-        __syncthreads();
-        if (s.L < 0) return;
-        const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
-        for (int i = tid; i < s.L * kVT; i += kCThreads) {
-            const int j = i / kVT, r = i % kVT;
-            s.cd[i] = r < rows ? s.coef[j] * dl[(size_t)s.nodes[j] * dv + v0 + r] : 0.f;
-        }
-        __syncthreads();
-    }
-
-    // 2. state tile -> smem (committed and written back once when fused)
+    // 1. state tile -> smem and the pending commit (reads only: overlaps the prologue kernel)
     const int quads = dk / 4;
     const size_t sbase = ((size_t)bh * dv + v0) * dk;
-    const T* ckey = fused ? static_cast<const T*>(a.commit.key) + (size_t)bh * a.commit.N * dk : nullptr;
     for (int i = tid; i < rows * quads; i += kCThreads) {
         const int r = i / quads, c = (i % quads) * 4;
-        const size_t off = sbase + (size_t)r * dk + c;
-        float4 x = *reinterpret_cast<const float4*>(a.S + off);
-        if (fused) {
-            x = commit_quad<T>(x, s.ega, s.L, s.nodes, s.cd + r, kVT, ckey, dk, c);
-            *reinterpret_cast<float4*>(a.S + off) = x;
-        }
-        float* d = s.S + r * ldS + c;
+        const float4 x = *reinterpret_cast<const float4*>(a.S + sbase + (size_t)r * dk + c);
+        float* d = sS + r * ldS + c;
         d[0] = x.x;
         d[1] = x.y;
         d[2] = x.z;
         d[3] = x.w;
+    }
+    if (fused) {
+        if (tid < 32) {
+            const int L = commit_path_setup(a.commit, b, h, a.H, snodes, scoef, sega);
+            if (tid == 0) {
+                *sL = L;
+                if (L < 0) set_error(a.err, GDN_ERR_PATH);
+            }
+        }
+        __syncthreads();
+        const int L = *sL;
+        if (L < 0) return;
+        const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
+        const T* key_bh = static_cast<const T*>(a.commit.key) + (size_t)bh * a.commit.N * dk;
+        for (int i = 0; i < L; ++i)
+            cp_async_block(skey + (size_t)i * dk, key_bh + (size_t)snodes[i] * dk, dk * (int)sizeof(T),
+                           tid, kCThreads);
+        for (int i = tid; i < L * kVT; i += kCThreads) {
+            const int j = i / kVT, r = i % kVT;
+            scd[i] = r < rows ? scoef[j] * dl[(size_t)snodes[j] * dv + v0 + r] : 0.f;
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        const float ega = *sega;
+        for (int i = tid; i < rows * quads; i += kCThreads) {
+            const int r = i / quads, c = (i % quads) * 4;
+            float* d = sS + r * ldS + c;
+            const float4 x = commit_quad<T>(make_float4(d[0], d[1], d[2], d[3]), ega, L, scd + r, kVT,
+                                            skey, dk, c);
+            d[0] = x.x;
+            d[1] = x.y;
+            d[2] = x.z;
+            d[3] = x.w;
+        }
+    }
+
+    // 2. wait for the prologue kernel; stage its tables; write the committed tile
+    griddep_wait();
+    griddep_launch();
+    if (*reinterpret_cast<const uint64_t*>(rec + wl.anc) == ~0ull) return;   // tree rejected
+    cp_async_block(sT, rec + wl.T, N * N * 4, tid, kCThreads);
+    cp_async_block(sP, rec + wl.P, N * N * 4, tid, kCThreads);
+    for (int t = tid; t < N; t += kCThreads) {
+        seg[t] = reinterpret_cast<const float*>(rec + wl.eg)[t];
+        sbt[t] = reinterpret_cast<const float*>(rec + wl.bt)[t];
+        sanc[t] = reinterpret_cast<const uint64_t*>(rec + wl.anc)[t];
+    }
+    __syncthreads();
+    if (fused) {
+        for (int i = tid; i < rows * quads; i += kCThreads) {
+            const int r = i / quads, c = (i % quads) * 4;
+            const float* d = sS + r * ldS + c;
+            *reinterpret_cast<float4*>(a.S + sbase + (size_t)r * dk + c) = make_float4(d[0], d[1], d[2], d[3]);
+        }
     }
 
     // 3. Y = [Q; K] S_tile^T : thread (row group rg, lane = tile row v)
@@ -300,15 +443,14 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
             const int r = i / kKC, c = i % kKC;
             const int t = r < N ? r : r - N;
             const size_t row = ((size_t)b * N + t) * a.H + h;
-            const float x = c0 + c < dk ? ld_elem<T>(r < N ? q : k, row * dk + c0 + c) : 0.f;
-            s.qk[c * ldq + r] = x;
+            sqk[c * ldq + r] = c0 + c < dk ? ld_elem<T>(r < N ? q : k, row * dk + c0 + c) : 0.f;
         }
         __syncthreads();
         if (lane < rows) {
             const int cn = min(kKC, dk - c0);
             for (int c = 0; c < cn; ++c) {
-                const float sv = s.S[lane * ldS + c0 + c];
-                const float* col = s.qk + c * ldq;
+                const float sv = sS[lane * ldS + c0 + c];
+                const float* col = sqk + c * ldq;
 #pragma unroll
                 for (int i = 0; i < kMaxRowsPerThread; ++i) {
                     const int r = rg + kRowGroups * i;
@@ -317,40 +459,37 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
             }
         }
     }
+    cp_async_wait_all();
     __syncthreads();
 
     // 4. Y_Q -> smem; R = beta (v - e^g Y_K) -> smem
-    const float* eg = reinterpret_cast<const float*>(rec + wl.eg);
-    const float* bt = reinterpret_cast<const float*>(rec + wl.bt);
     const T* vv = static_cast<const T*>(a.v);
     if (lane < rows) {
 #pragma unroll
         for (int i = 0; i < kMaxRowsPerThread; ++i) {
             const int r = rg + kRowGroups * i;
             if (r < N) {
-                s.YQ[r * (kVT + 1) + lane] = acc[i];
+                sYQ[r * (kVT + 1) + lane] = acc[i];
             } else if (r < nr) {
                 const int t = r - N;
                 const float vt = ld_elem<T>(vv, (((size_t)b * N + t) * a.H + h) * dv + v0 + lane);
-                s.R[t * (kVT + 1) + lane] = bt[t] * (vt - eg[t] * acc[i]);
+                sR[t * (kVT + 1) + lane] = sbt[t] * (vt - seg[t] * acc[i]);
             }
         }
     }
     __syncthreads();
 
     // 5. Delta_t = sum_{j in path(t)} T[t,j] R_j ; O_t = e^{g_t} YQ_t + sum_j P[t,j] R_j
-    const float* wT = reinterpret_cast<const float*>(rec + wl.T);
-    const float* wP = reinterpret_cast<const float*>(rec + wl.P);
     for (int t = rg; t < N; t += kRowGroups) {
         if (lane >= rows) continue;
         float d = 0.f, o = 0.f;
-        for (uint64_t m = anc[t]; m; m &= m - 1) {
+        for (uint64_t m = sanc[t]; m; m &= m - 1) {
             const int j = __ffsll((long long)m) - 1;
-            const float rj = s.R[j * (kVT + 1) + lane];
-            d = fmaf(wT[t * N + j], rj, d);
-            o = fmaf(wP[t * N + j], rj, o);
+            const float rj = sR[j * (kVT + 1) + lane];
+            d = fmaf(sT[t * N + j], rj, d);
+            o = fmaf(sP[t * N + j], rj, o);
         }
-        o = fmaf(eg[t], s.YQ[t * (kVT + 1) + lane], o);
+        o = fmaf(seg[t], sYQ[t * (kVT + 1) + lane], o);
         a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + lane] = o;
         a.f.delta[((size_t)bh * N + t) * dv + v0 + lane] = d;
     }
@@ -365,31 +504,37 @@ cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint64_t* mask
 }
 
 template <typename T>
-static cudaError_t launch_tree_t(const VerifyArgs& a, cudaStream_t s) {
-    const int prep_smem = (int)sizeof(PrepSmem);
-    const int con_smem = (int)sizeof(ContractSmem);
-    static bool attr_set[64];   // per device: opt in to > 48 KiB dynamic smem once
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+cudaError_t launch_tree_prep(const VerifyArgs& a, cudaStream_t s) {
+    static bool attr[64];
+    const PrepLayout Ly(a.N, a.dk, (int)sizeof(T));
+    cudaError_t e = ensure_smem(tree_prep_kernel<T>, Ly.total, attr);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(tree_prep_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(tree_contract_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, con_smem);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
-    tree_prep_kernel<T><<<a.B * a.H, kPrepThreads, prep_smem, s>>>(a);
-    e = cudaGetLastError();
+    return launch_kernel(tree_prep_kernel<T>, dim3(a.B * a.H), dim3(kPrepThreads), Ly.total, s,
+                         a.overlap, a);
+}
+
+template <typename T>
+cudaError_t launch_tree_contract_simt(const VerifyArgs& a, cudaStream_t s) {
+    static bool attr[64];
+    const ContractLayout Ly(a.N, a.dk, a.commit.path ? a.commit.Lmax : 0, (int)sizeof(T));
+    cudaError_t e = ensure_smem(tree_contract_kernel<T>, Ly.total, attr);
     if (e != cudaSuccess) return e;
     dim3 grid(a.B * a.H, (a.dv + kVT - 1) / kVT);
-    tree_contract_kernel<T><<<grid, kCThreads, con_smem, s>>>(a);
-    return cudaGetLastError();
+    // always a programmatic dependent of the prologue kernel launched just before it
+    return launch_kernel(tree_contract_kernel<T>, grid, dim3(kCThreads), Ly.total, s, true, a);
 }
 
 cudaError_t launch_tree_verify(const VerifyArgs& a, int dtype, cudaStream_t s) {
-    return dtype == GDN_DTYPE_F32 ? launch_tree_t<float>(a, s) : launch_tree_t<__nv_bfloat16>(a, s);
+    cudaError_t e;
+    if (dtype == GDN_DTYPE_F32) {
+        e = launch_tree_prep<float>(a, s);
+        if (e != cudaSuccess) return e;
+        return launch_tree_contract_simt<float>(a, s);
+    }
+    e = launch_tree_prep<__nv_bfloat16>(a, s);
+    if (e != cudaSuccess) return e;
+    if (tc_contract_eligible(a)) return launch_tree_contract_tc(a, s);
+    return launch_tree_contract_simt<__nv_bfloat16>(a, s);
 }
 
 }  // namespace gdn

@@ -38,6 +38,7 @@ SIGNATURES = {
                                     _I, _I, _I, _I, _I, _P]),
     "gdn_commit_chain_verify": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P,
                                      _I, _I, _I, _I, _I, _P]),
+    "gdn_set_launch_overlap": (_I, [_I]),
     "gdn_last_error": (_I, [_P]),
     "gdn_strerror": (ctypes.c_char_p, [_I]),
 }
@@ -191,6 +192,11 @@ def gdn_commit_chain_verify(S, prev_factors, N_prev, prev_path, q, k, v, alpha, 
                                          dtype_code(q.dtype), _ptr(alpha), _ptr(beta), _ptr(out),
                                          _ptr(factors), B, N, H, dk, dv, _stream(stream)),
            "gdn_commit_chain_verify")
+
+
+def gdn_set_launch_overlap(enable: bool) -> bool:
+    """Process-wide switch; returns the previous setting (see include/gdnspec.h)."""
+    return bool(lib().gdn_set_launch_overlap(1 if enable else 0))
 
 
 def gdn_last_error(stream=None) -> int:

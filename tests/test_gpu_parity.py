@@ -259,3 +259,46 @@ def test_invalid_path_reported(bad):
     gdnspec.gdn_commit_tree_verify(S, fac, w.N, path, d["q"], d["k"], d["v"], d["alpha"], d["beta"],
                                    d["parent"], out, fac2, ws)
     assert gdnspec.gdn_last_error() == gdnspec.ERR_PATH
+
+
+# ---------------------------------------------------------------------------
+# layer-major sweep with launch overlap (programmatic dependent launch)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [1, 2, 3])
+def test_overlapped_layer_sweep_matches_serial(cfg):
+    """Several layers back to back with launch overlap on give the same bits as with it off."""
+    chain = cfg == 1
+    results = []
+    for overlap in (False, True):
+        prev = gdnspec.gdn_set_launch_overlap(overlap)
+        try:
+            layers = []
+            for r in range(4):
+                w = wl.make_workload(cfg, seed=100 + r)
+                d = dev_inputs(w)
+                out, fac0, ws = alloc_outputs(w)
+                fac1 = gdnspec.empty_factors(w.B, w.N, w.H, w.dk, w.dv, w.dtype)
+                layers.append((w, d, out, fac0, fac1, ws))
+            for step in range(3):
+                for (w, d, out, fac0, fac1, ws) in layers:
+                    prevf, nextf = (fac0, fac1) if step % 2 == 0 else (fac1, fac0)
+                    if step == 0:
+                        if chain:
+                            gdnspec.gdn_chain_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["S0"],
+                                                     out, fac1)
+                        else:
+                            gdnspec.gdn_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"],
+                                                    d["S0"], out, fac1, ws)
+                    elif chain:
+                        gdnspec.gdn_commit_chain_verify(d["S0"], prevf, w.N, d["path"], d["q"], d["k"], d["v"],
+                                                        d["alpha"], d["beta"], out, nextf)
+                    else:
+                        gdnspec.gdn_commit_tree_verify(d["S0"], prevf, w.N, d["path"], d["q"], d["k"], d["v"],
+                                                       d["alpha"], d["beta"], d["parent"], out, nextf, ws)
+            torch.cuda.synchronize()
+            assert gdnspec.gdn_last_error() == 0
+            results.append([(l[1]["S0"].clone(), l[2].clone()) for l in layers])
+        finally:
+            gdnspec.gdn_set_launch_overlap(prev)
+    for (s0, o0), (s1, o1) in zip(*results):
+        assert torch.equal(s0, s1) and torch.equal(o0, o1)
