@@ -140,8 +140,9 @@ class Layer:
         return sum(t.numel() * t.element_size() for t in ts)
 
 
-def make_layers(cfg, R, seed0, device, torch, gdnspec, wl):
-    return [Layer(wl.make_workload(cfg, seed=seed0 + 7919 * r), device, torch, gdnspec) for r in range(R)]
+def make_layers(cfg, R, seed0, device, torch, gdnspec, wl, batch=None):
+    return [Layer(wl.make_workload(cfg, seed=seed0 + 7919 * r, B=batch), device, torch, gdnspec)
+            for r in range(R)]
 
 
 def layer_call(gdnspec, ly, parity, chain):
@@ -165,7 +166,7 @@ def first_verify(gdnspec, ly, chain):
                                 ly.ws)
 
 
-def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=False):
+def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=False, batch=None):
     from speculative_decoding_linear_gb300 import gdnspec
     from speculative_decoding_linear_gb300 import workloads as wl
 
@@ -176,11 +177,11 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
     props = torch.cuda.get_device_properties(device_index)
     l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
 
-    probe = Layer(wl.make_workload(cfg), device, torch, gdnspec)
+    probe = Layer(wl.make_workload(cfg, B=batch), device, torch, gdnspec)
     per_layer = probe.nbytes()
     del probe
     R = max(2, -(-4 * l2 // per_layer))
-    layers = make_layers(cfg, R, 1000 * (rank + 1) + cfg, device, torch, gdnspec, wl)
+    layers = make_layers(cfg, R, 1000 * (rank + 1) + cfg, device, torch, gdnspec, wl, batch)
     footprint = sum(ly.nbytes() for ly in layers)
 
     stream = torch.cuda.Stream(device=device)
@@ -368,6 +369,7 @@ def main():
     ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
     ap.add_argument("--profile", action="store_true",
                     help="for profiler runs: no clock soak, no e2e leg, no CPU baseline")
     args = ap.parse_args()
@@ -393,7 +395,8 @@ def main():
         __graft_entry__.build()
     if world > 1:
         dist.barrier()
-    r = run_gpu(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile)
+    r = run_gpu(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
+                args.batch)
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or args.profile or world > 1 else cpu_baseline(args.config)

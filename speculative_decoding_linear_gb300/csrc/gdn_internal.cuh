@@ -66,13 +66,17 @@ struct WsLayout {
     size_t T, P, eg, bt, anc, record;
 };
 
+// Every section starts on a 16-byte boundary and is padded to a multiple of
+// 16 bytes, so kernels may stage whole sections with 16-byte async copies.
+__host__ __device__ inline size_t ws_table_bytes(int N) { return align_up((size_t)N * N * 4, 16); }
+
 __host__ __device__ inline WsLayout ws_layout(int N) {
     WsLayout L;
     L.T = 0;
-    L.P = L.T + (size_t)N * N * 4;
-    L.eg = L.P + (size_t)N * N * 4;
-    L.bt = L.eg + (size_t)N * 4;
-    L.anc = align_up(L.bt + (size_t)N * 4, 8);
+    L.P = L.T + ws_table_bytes(N);
+    L.eg = L.P + ws_table_bytes(N);
+    L.bt = L.eg + align_up((size_t)N * 4, 16);
+    L.anc = L.bt + align_up((size_t)N * 4, 16);
     L.record = align_up(L.anc + (size_t)N * 8, kSectionAlign);
     return L;
 }

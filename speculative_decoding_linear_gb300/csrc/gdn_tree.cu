@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
     griddep_wait();
     griddep_launch();
     if (*reinterpret_cast<const uint64_t*>(rec + wl.anc) == ~0ull) return;   // tree rejected
-    cp_async_block(sT, rec + wl.T, N * N * 4, tid, kCThreads);
-    cp_async_block(sP, rec + wl.P, N * N * 4, tid, kCThreads);
+    cp_async_block(sT, rec + wl.T, (int)ws_table_bytes(N), tid, kCThreads);
+    cp_async_block(sP, rec + wl.P, (int)ws_table_bytes(N), tid, kCThreads);
     for (int t = tid; t < N; t += kCThreads) {
         seg[t] = reinterpret_cast<const float*>(rec + wl.eg)[t];
         sbt[t] = reinterpret_cast<const float*>(rec + wl.bt)[t];

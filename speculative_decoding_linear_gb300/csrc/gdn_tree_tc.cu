@@ -1,10 +1,497 @@
 // gdn_tree_tc.cu -- tensor-core (tcgen05) contraction of the tree verifier.
+//
+// Same mathematics as the SIMT contraction in gdn_tree.cu (review of SpecLA,
+// pith.science 7ERME3HB, "Core claim": O = Qhat S0^T - Attn (W S0^T) + Attn U):
+//
+//   Y = S_tile [Q; K]^T          (the dense part: 4 N d_k d_v FLOP per (b, h))
+//   R_t   = beta_t (v_t - e^{g_t} Y_K[:, t])
+//   Delta_t = sum_{j in path(t)} T[t,j] R_j
+//   O_t     = e^{g_t} Y_Q[:, t] + sum_{j in path(t)} P[t,j] R_j
+//
+// One CTA owns 128 state rows of one (sequence b, head h) -- the MMA's M --
+// and all draft nodes: rows 0..63 of the B operand are the queries of nodes
+// 0..63, rows 64..127 their keys (MMA N = 128), so TMEM lane v holds, for state
+// row v, every node's Y_Q and Y_K.  d_k is walked in four 64-wide slabs (one
+// 128-byte swizzle atom of bf16):
+//
+//   * the fp32 state slab is loaded to registers (one slab ahead), the
+//     pending commit is applied there (fused path), the committed slab is
+//     written back, and each value is split into bf16 hi + lo (hi = bf16(x),
+//     lo = bf16(x - hi), |x - hi - lo| <= 2^-16 |x|) and stored to shared
+//     memory in the 128-byte-swizzled K-major layout;
+//   * the query/key slab arrives by TMA (3-D tensor map, 128-byte swizzle);
+//   * one thread issues 8 MMAs (4 K-steps x {hi, lo}) of kind::f16 with
+//     bf16 operands into one fp32 accumulator in TMEM and commits them to an
+//     mbarrier that frees the stage; two stages alternate.
+//
+// bf16 q/k times the two-term state is exact to ~2^-16 relative per product,
+// with fp32 accumulation: far inside the 2e-3 x RMS budget.
+//
+// Epilogue: warps 0-3 read Y_K (TMEM columns 64..127), form R into shared
+// memory; after a barrier warps 0-3 gather Delta and warps 4-7 read Y_Q
+// (columns 0..63) and gather O.  T and P come from the prologue kernel's
+// workspace, staged into the first stage's buffers once its MMAs are done.
+//
+// Every mbarrier wait is bounded (about one second, then GDN_ERR_TIMEOUT is
+// recorded and the CTA skips ahead to its teardown); TMEM is always freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
+namespace {
 
-bool tc_contract_eligible(const VerifyArgs&) { return false; }
+constexpr int kThreads = 256;
+constexpr int kTileV = 128;        // state rows per CTA (MMA M)
+constexpr int kSlab = 64;          // d_k per slab
+constexpr int kDk = 256;           // d_k handled by this kernel
+constexpr int kSlabs = kDk / kSlab;
+constexpr int kNodeRows = 64;      // B operand: Q rows 0..63, K rows 64..127 (MMA N = 128)
+constexpr int kBufBytes = kTileV * 128;        // one 128-row x 128-byte operand buffer (16 KiB)
+constexpr int kStageBytes = 3 * kBufBytes;     // A_hi, A_lo, B
+constexpr uint32_t kTmemCols = 128;
+constexpr int kMaxTcPath = 16;
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N = 128, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
+                            ((uint32_t)(128 >> 4) << 24);
 
-cudaError_t launch_tree_contract_tc(const VerifyArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Bounded wait for the completion of the mbarrier phase with this parity.
+// Returns false (and records GDN_ERR_TIMEOUT) after about one second.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > 1000000000ull) {
+            set_error(err, GDN_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t holder, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(holder),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+                 : "memory");
+}
+// 32 consecutive TMEM columns of this warp's 32 lanes (one fp32 per column per lane).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 8-row (1024-byte) groups.  The leading-byte offset is unused
+// for this layout; the stride-byte offset is the 1024-byte group pitch.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Byte offset of bf16 quad (4 elements, 8 bytes) `c4` (0..15) of row `r` in a
+// 128-byte-swizzled K-major buffer.
+__device__ __forceinline__ uint32_t sw128_quad(int r, int c4) {
+    return (uint32_t)(r * 128 + (((c4 >> 1) ^ (r & 7)) << 4) + ((c4 & 1) << 3));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo_elem, hi_elem);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+struct TcLayout {
+    // offsets from the 1024-aligned base
+    int cd, key, coef, nodes, bars, misc, total;
+    __host__ __device__ TcLayout(int Lcap) {
+        int o = 2 * kStageBytes;
+        auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
+        cd = take(Lcap * kTileV * 4);
+        key = take(Lcap * kDk * 2);
+        coef = take(kMaxPath * 4);
+        nodes = take(kMaxPath * 4);
+        bars = take(64);
+        misc = take(16);
+        total = o + 1024;   // slack for aligning the base to 1024 bytes
+    }
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+    tree_contract_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                            VerifyArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    unsigned char* base = smem_raw + (base_s - raw_s);
+    const bool fused = a.commit.path != nullptr;
+    const TcLayout Ly(fused ? a.commit.Lmax : 0);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H;
+    const int N = a.N, dv = a.dv;
+    const int v0 = blockIdx.y * kTileV;
+
+    float* s_cd = reinterpret_cast<float*>(base + Ly.cd);
+    __nv_bfloat16* s_key = reinterpret_cast<__nv_bfloat16*>(base + Ly.key);
+    float* s_coef = reinterpret_cast<float*>(base + Ly.coef);
+    int* s_nodes = reinterpret_cast<int*>(base + Ly.nodes);
+    const uint32_t bar_tma0 = base_s + Ly.bars, bar_mma0 = base_s + Ly.bars + 16;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
+    float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 4);
+    int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 8);   // path length, or -1: skip the CTA
+
+    if (tid == 0) {
+        mbar_init(bar_tma0, 1);
+        mbar_init(bar_tma0 + 8, 1);
+        mbar_init(bar_mma0, 1);
+        mbar_init(bar_mma0 + 8, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        fence_proxy_async_smem();
+        *s_flag = 0;
+        *s_ega = 1.f;
+    }
+    if (warp == 1) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    // ---- 1. reads only: pending commit's factor rows, first state slab ----
+    const size_t srow0 = ((size_t)bh * dv + v0) * kDk;
+    const int c4 = tid & 15;         // column quad within a slab
+    const int rbase = tid >> 4;      // rows rbase + 16 j, j = 0..7
+    float4 xa[8], xb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        xa[j] = *reinterpret_cast<const float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk + 4 * c4);
+    if (fused) {
+        if (warp == 2) {
+            const int L = commit_path_setup(a.commit, b, h, a.H, s_nodes, s_coef, s_ega);
+            if (lane == 0) {
+                *s_flag = L;
+                if (L < 0) set_error(a.err, GDN_ERR_PATH);
+            }
+        }
+        __syncthreads();
+        const int L = *s_flag;
+        if (L > 0) {
+            const __nv_bfloat16* key_bh =
+                static_cast<const __nv_bfloat16*>(a.commit.key) + (size_t)bh * a.commit.N * kDk;
+            for (int i = 0; i < L; ++i)
+                cp_async_block(s_key + (size_t)i * kDk, key_bh + (size_t)s_nodes[i] * kDk, kDk * 2, tid,
+                               kThreads);
+            const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
+            for (int i = tid; i < L * kTileV; i += kThreads) {
+                const int j = i / kTileV, r = i % kTileV;
+                s_cd[i] = s_coef[j] * dl[(size_t)s_nodes[j] * dv + v0 + r];
+            }
+            cp_async_wait_all();
+        }
+    }
+    __syncthreads();
+    const int L = fused ? *s_flag : 0;
+    const float ega = *s_ega;
+
+    // ---- 2. wait for the prologue kernel (and this layer's q/k) ----
+    griddep_wait();
+    griddep_launch();
+    const WsLayout wl = ws_layout(N);
+    const char* rec = a.ws + (size_t)bh * wl.record;
+    const bool run = L >= 0 && *reinterpret_cast<const uint64_t*>(rec + wl.anc) != ~0ull;
+    bool ok = run;
+
+    if (run) {
+        if (tid == 0) {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const uint32_t bsm = base_s + s * kStageBytes + 2 * kBufBytes;
+                mbar_expect_tx(bar_tma0 + 8 * s, 2 * kNodeRows * 128);
+                tma_load_3d(bsm, &tmQ, s * kSlab, h, b * N, bar_tma0 + 8 * s);
+                tma_load_3d(bsm + kNodeRows * 128, &tmK, s * kSlab, h, b * N, bar_tma0 + 8 * s);
+            }
+        }
+#pragma unroll
+        for (int ks = 0; ks < kSlabs; ++ks) {
+            const int s = ks & 1;
+            float4(&x)[8] = (ks & 1) ? xb : xa;
+            float4(&xn)[8] = (ks & 1) ? xa : xb;
+            if (ks + 1 < kSlabs) {      // next slab in flight while this one is processed
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    xn[j] = *reinterpret_cast<const float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk +
+                                                            (ks + 1) * kSlab + 4 * c4);
+            }
+            if (ks >= 2) {              // stage s is free once slab ks-2's MMAs are done
+                ok = mbar_wait(bar_mma0 + 8 * s, 0, a.err) && ok;
+                if (tid == 0 && ok) {
+                    const uint32_t bsm = base_s + s * kStageBytes + 2 * kBufBytes;
+                    mbar_expect_tx(bar_tma0 + 8 * s, 2 * kNodeRows * 128);
+                    tma_load_3d(bsm, &tmQ, ks * kSlab, h, b * N, bar_tma0 + 8 * s);
+                    tma_load_3d(bsm + kNodeRows * 128, &tmK, ks * kSlab, h, b * N, bar_tma0 + 8 * s);
+                }
+            }
+            unsigned char* ahi = base + s * kStageBytes;
+            unsigned char* alo = ahi + kBufBytes;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int r = rbase + 16 * j;
+                float4 v = x[j];
+                if (fused) {
+                    v = commit_quad<__nv_bfloat16>(v, ega, L, s_cd + r, kTileV, s_key, kDk,
+                                                   ks * kSlab + 4 * c4);
+                    *reinterpret_cast<float4*>(a.S + srow0 + (size_t)r * kDk + ks * kSlab + 4 * c4) = v;
+                }
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+                const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                uint2 hi, lo;
+                hi.x = *reinterpret_cast<const uint32_t*>(&h01);
+                hi.y = *reinterpret_cast<const uint32_t*>(&h23);
+                lo.x = pack_bf16(v.x - f01.x, v.y - f01.y);
+                lo.y = pack_bf16(v.z - f23.x, v.w - f23.y);
+                const uint32_t off = sw128_quad(r, c4);
+                *reinterpret_cast<uint2*>(ahi + off) = hi;
+                *reinterpret_cast<uint2*>(alo + off) = lo;
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0 && ok) {
+                ok = mbar_wait(bar_tma0 + 8 * s, (ks >> 1) & 1, a.err);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t a_hi = base_s + s * kStageBytes;
+                    const uint32_t a_lo = a_hi + kBufBytes;
+                    const uint32_t bsm = a_hi + 2 * kBufBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kSlab / 16; ++kk) {
+                        const uint64_t bd = sw128_desc(bsm + kk * 32);
+                        mma_bf16(tmem, sw128_desc(a_hi + kk * 32), bd, (ks > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16(tmem, sw128_desc(a_lo + kk * 32), bd, 1u);
+                    }
+                    mma_commit(bar_mma0 + 8 * s);
+                }
+            }
+        }
+        // stage 0 is free once slab kSlabs-2 is done: stage T, P, e^g, beta, masks there
+        ok = __syncthreads_and(ok);
+        if (ok) ok = mbar_wait(bar_mma0, 1, a.err);
+        float* sT = reinterpret_cast<float*>(base);
+        float* sP = reinterpret_cast<float*>(base + kBufBytes);
+        float* seg = reinterpret_cast<float*>(base + 2 * kBufBytes);
+        float* sbt = seg + kMaxNodes;
+        uint64_t* sanc = reinterpret_cast<uint64_t*>(sbt + kMaxNodes);
+        float* sR = reinterpret_cast<float*>(base + kStageBytes);   // stage 1 A buffers, after the last MMA
+        if (ok) {
+            cp_async_block(sT, rec + wl.T, (int)ws_table_bytes(N), tid, kThreads);
+            cp_async_block(sP, rec + wl.P, (int)ws_table_bytes(N), tid, kThreads);
+            for (int t = tid; t < N; t += kThreads) {
+                seg[t] = reinterpret_cast<const float*>(rec + wl.eg)[t];
+                sbt[t] = reinterpret_cast<const float*>(rec + wl.bt)[t];
+                sanc[t] = reinterpret_cast<const uint64_t*>(rec + wl.anc)[t];
+            }
+            ok = mbar_wait(bar_mma0 + 8, 1, a.err);
+        }
+        cp_async_wait_all();
+        ok = __syncthreads_and(ok);
+        tc_fence_after();
+
+        const int v = 32 * (warp & 3) + lane;            // state row of this thread (TMEM lane)
+        const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(a.v);
+        if (ok && warp < 4) {
+            // R_t = beta_t (v_t - e^{g_t} Y_K[v, t])
+#pragma unroll
+            for (int c = 0; c < kNodeRows / 32; ++c) {
+                if (32 * c >= N) break;
+                float vin[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = 32 * c + i;
+                    vin[i] = t < N ? __bfloat162float(vv[(((size_t)b * N + t) * a.H + h) * dv + v0 + v]) : 0.f;
+                }
+                float yk[32];
+                tmem_ld32(t_lane + kNodeRows + 32 * c, yk);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = 32 * c + i;
+                    if (t < N) sR[t * kTileV + v] = sbt[t] * (vin[i] - seg[t] * yk[i]);
+                }
+            }
+        }
+        __syncthreads();
+        if (ok && warp < 4) {
+            // Delta_t = sum_{j in path(t)} T[t, j] R_j
+            for (int t = 0; t < N; ++t) {
+                float d = 0.f;
+                for (uint64_t m = sanc[t]; m; m &= m - 1) {
+                    const int j = __ffsll((long long)m) - 1;
+                    d = fmaf(sT[t * N + j], sR[j * kTileV + v], d);
+                }
+                a.f.delta[((size_t)bh * N + t) * dv + v0 + v] = d;
+            }
+        } else if (ok) {
+            // O_t = e^{g_t} Y_Q[v, t] + sum_{j in path(t)} P[t, j] R_j
+#pragma unroll
+            for (int c = 0; c < kNodeRows / 32; ++c) {
+                if (32 * c >= N) break;
+                float yq[32];
+                tmem_ld32(t_lane + 32 * c, yq);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = 32 * c + i;
+                    if (t < N) {
+                        float o = seg[t] * yq[i];
+                        for (uint64_t m = sanc[t]; m; m &= m - 1) {
+                            const int j = __ffsll((long long)m) - 1;
+                            o = fmaf(sP[t * N + j], sR[j * kTileV + v], o);
+                        }
+                        a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + v] = o;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: TMEM is always released ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// q or k [B][N][H][256] bf16 viewed as 3-D (d_k, H, B*N); box = one 64-wide
+// slab of 64 consecutive nodes of one head.
+bool make_qk_map(CUtensorMap* m, const void* ptr, int B, int N, int H) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kDk, (cuuint64_t)H, (cuuint64_t)B * N};
+    const cuuint64_t strides[2] = {(cuuint64_t)kDk * 2, (cuuint64_t)H * kDk * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kSlab, 1u, (cuuint32_t)kNodeRows};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// bf16 inputs, d_k = 256, d_v a multiple of 128, short accepted paths, and
+// enough (b, h, 128-row) tiles to fill the GPU; otherwise the SIMT kernel.
+bool tc_contract_eligible(const VerifyArgs& a) {
+    if (a.dk != kDk || a.dv % kTileV != 0) return false;
+    if (a.commit.path != nullptr && a.commit.Lmax > kMaxTcPath) return false;
+    const long long tiles = (long long)a.B * a.H * (a.dv / kTileV);
+    if (tiles < 120) return false;
+    return encode_fn() != nullptr;
+}
+
+cudaError_t launch_tree_contract_tc(const VerifyArgs& a, cudaStream_t s) {
+    static bool attr[64];
+    CUtensorMap tq, tk;
+    if (!make_qk_map(&tq, a.q, a.B, a.N, a.H) || !make_qk_map(&tk, a.k, a.B, a.N, a.H))
+        return cudaErrorInvalidValue;
+    const TcLayout Ly(a.commit.path ? a.commit.Lmax : 0);
+    cudaError_t e = ensure_smem(tree_contract_tc_kernel, Ly.total, attr);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.B * a.H, a.dv / kTileV);
+    // always a programmatic dependent of the prologue kernel launched just before it
+    return launch_kernel(tree_contract_tc_kernel, grid, dim3(kThreads), Ly.total, s, true, tq, tk, a);
+}
 
 }  // namespace gdn

@@ -302,3 +302,52 @@ def test_overlapped_layer_sweep_matches_serial(cfg):
             gdnspec.gdn_set_launch_overlap(prev)
     for (s0, o0), (s1, o1) in zip(*results):
         assert torch.equal(s0, s1) and torch.equal(o0, o1)
+
+
+# ---------------------------------------------------------------------------
+# tensor-core contraction (bf16, d_k = 256, >= 120 (b, h, 128-row) tiles)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", ["b8_n37", "b15_n64_lastrows_oob", "b60_n1", "forest_b8", "deep_chain"])
+def test_tensor_core_contraction(oracle_mod, case):
+    rng = np.random.default_rng(hash(case) % 2 ** 32)
+    if case == "b8_n37":
+        B, N, md = 8, 37, 6
+    elif case == "b15_n64_lastrows_oob":
+        B, N, md = 15, 64, 8
+    elif case == "b60_n1":
+        B, N, md = 60, 1, 0
+    elif case == "forest_b8":
+        B, N, md = 8, 20, 0
+    else:
+        B, N, md = 8, 64, 63
+    parent = np.stack([wl.chain_tree(N) if case == "deep_chain" else wl.random_tree(rng, N, md)
+                       for _ in range(B)])
+    w = wl.custom_workload(B, N, 8, 256, 256, parent, seed=len(case))
+    _, out, fac = run_tree_verify(w)
+    check_verify(w, out, fac, oracle_mod)
+
+
+@pytest.mark.parametrize("L", [0, 1, 9, 16])
+def test_tensor_core_fused_commit(oracle_mod, L):
+    """Fused commit on the tensor-core path: paths of length 0..16 into a 16-deep chain tree."""
+    B, N = 8, 16
+    w1 = wl.custom_workload(B, N, 8, 256, 256, wl.chain_tree(N), seed=40 + L,
+                            path=np.tile(np.r_[np.arange(L), -np.ones(16 - L)].astype(np.int32), (B, 1)), lmax=16)
+    d1, _, fac1 = run_tree_verify(w1)
+    rng = np.random.default_rng(L)
+    w2 = wl.custom_workload(B, 48, 8, 256, 256, np.stack([wl.random_tree(rng, 48, 7) for _ in range(B)]),
+                            seed=60 + L)
+    d2 = dev_inputs(w2)
+    S = d1["S0"].clone()
+    out2, fac2, ws2 = alloc_outputs(w2)
+    gdnspec.gdn_commit_tree_verify(S, fac1, N, d1["path"], d2["q"], d2["k"], d2["v"], d2["alpha"],
+                                   d2["beta"], d2["parent"], out2, fac2, ws2)
+    assert gdnspec.gdn_last_error() == 0
+    S_unf = torch.empty_like(S)
+    gdnspec.gdn_commit(d1["S0"], fac1, d1["path"], S_unf, N, w1.dtype)
+    assert torch.equal(S, S_unf)
+    x1 = oracle_inputs(w1)
+    S_ref = oracle_mod.commit(x1["k"], x1["v"], x1["alpha"], x1["beta"], w1.parent, x1["S0"], w1.path)
+    assert_close(S.cpu().numpy(), S_ref, "committed S")
+    w2.S0 = S.cpu().numpy()
+    check_verify(w2, out2, fac2, oracle_mod)
