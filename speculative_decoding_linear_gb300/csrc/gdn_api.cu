@@ -124,6 +124,15 @@ int verify_common(const void* q, const void* k, const void* v, int dtype, const 
 }
 
 }  // namespace
+
+// Accessors for the library's other translation units.
+int* current_error_word(int* status) {
+    const int dev = dev_setup(status);
+    return dev < 0 ? nullptr : g_err_ptr[dev];
+}
+
+bool launch_overlap_enabled() { return g_overlap.load() != 0; }
+
 }  // namespace gdn
 
 using namespace gdn;

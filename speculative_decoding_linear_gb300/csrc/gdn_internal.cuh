@@ -206,6 +206,10 @@ cudaError_t launch_tree_mask(const int32_t* parent, int B, int N, uint64_t* mask
 cudaError_t launch_tree_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_chain_verify(const VerifyArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, int dtype, cudaStream_t s);
+// error word of the current device (nullptr and a status on failure) and the
+// launch-overlap switch (gdn_api.cu)
+int* current_error_word(int* status);
+bool launch_overlap_enabled();
 // tensor-core contraction of the tree verifier (gdn_tree_tc.cu)
 bool tc_contract_eligible(const VerifyArgs& a);
 cudaError_t launch_tree_contract_tc(const VerifyArgs& a, cudaStream_t s);
@@ -230,6 +234,27 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p, siz
     r.z = __uint_as_float(u.y << 16);
     r.w = __uint_as_float(u.y & 0xffff0000u);
     return r;
+}
+
+// Eight consecutive elements starting at p[i] (16-byte aligned) widened to fp32.
+template <typename T>
+__device__ __forceinline__ void ld8(const T* p, float (&x)[8]);
+template <>
+__device__ __forceinline__ void ld8<float>(const float* p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void ld8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
 }
 
 // One committed quad of a state row:

@@ -303,7 +303,6 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
 // contraction + epilogue (SIMT)
 // ---------------------------------------------------------------------------
 constexpr int kVT = 32;          // state rows per CTA
-constexpr int kKC = 32;          // d_k chunk staged in smem
 constexpr int kCThreads = 256;
 constexpr int kRowGroups = kCThreads / 32;
 constexpr int kMaxRowsPerThread = 2 * kMaxNodes / kRowGroups;   // 16
@@ -313,8 +312,8 @@ struct ContractLayout {
     __host__ __device__ ContractLayout(int N, int dk, int Lcap, int esz) {
         int o = 0;
         auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
-        S = take(kVT * (dk + 1) * 4);
-        qk = take(kKC * (2 * N + 1) * 4);
+        S = take(kVT * (dk + 4) * 4);    // rows padded by 16 bytes: float4 reads spread over banks
+        qk = take(2 * N * dk * esz);     // [Q rows; K rows] in the input element type
         YQ = take(N * (kVT + 1) * 4);
         R = take(N * (kVT + 1) * 4);
         T = take(N * N * 4);
@@ -357,7 +356,7 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
     const int b = bh / a.H, h = bh % a.H;
     const int v0 = blockIdx.y * kVT;
     const int rows = min(kVT, dv - v0);
-    const int ldS = dk + 1;
+    const int ldS = dk + 4;
     const WsLayout wl = ws_layout(N);
     const char* rec = a.ws + (size_t)bh * wl.record;
 
@@ -366,12 +365,7 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
     const size_t sbase = ((size_t)bh * dv + v0) * dk;
     for (int i = tid; i < rows * quads; i += kCThreads) {
         const int r = i / quads, c = (i % quads) * 4;
-        const float4 x = *reinterpret_cast<const float4*>(a.S + sbase + (size_t)r * dk + c);
-        float* d = sS + r * ldS + c;
-        d[0] = x.x;
-        d[1] = x.y;
-        d[2] = x.z;
-        d[3] = x.w;
+        cp_async16(sS + r * ldS + c, a.S + sbase + (size_t)r * dk + c);
     }
     if (fused) {
         if (tid < 32) {
@@ -398,13 +392,8 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
         const float ega = *sega;
         for (int i = tid; i < rows * quads; i += kCThreads) {
             const int r = i / quads, c = (i % quads) * 4;
-            float* d = sS + r * ldS + c;
-            const float4 x = commit_quad<T>(make_float4(d[0], d[1], d[2], d[3]), ega, L, scd + r, kVT,
-                                            skey, dk, c);
-            d[0] = x.x;
-            d[1] = x.y;
-            d[2] = x.z;
-            d[3] = x.w;
+            float4* d = reinterpret_cast<float4*>(sS + r * ldS + c);
+            *d = commit_quad<T>(*d, ega, L, scd + r, kVT, skey, dk, c);
         }
     }
 
@@ -423,43 +412,53 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
     if (fused) {
         for (int i = tid; i < rows * quads; i += kCThreads) {
             const int r = i / quads, c = (i % quads) * 4;
-            const float* d = sS + r * ldS + c;
-            *reinterpret_cast<float4*>(a.S + sbase + (size_t)r * dk + c) = make_float4(d[0], d[1], d[2], d[3]);
+            *reinterpret_cast<float4*>(a.S + sbase + (size_t)r * dk + c) =
+                *reinterpret_cast<const float4*>(sS + r * ldS + c);
         }
     }
 
-    // 3. Y = [Q; K] S_tile^T : thread (row group rg, lane = tile row v)
+    // 3. Y = [Q; K] S_tile^T : thread (row group rg, lane = tile row v); [Q; K] rows
+    //    staged once with cp.async, consumed 8 columns at a time
     const int rg = tid >> 5, lane = tid & 31;
     const int nr = 2 * N;
-    const int ldq = nr + 1;
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    T* sQK = reinterpret_cast<T*>(smem + Ly.qk);
+    const int rowb = dk * (int)sizeof(T);
+    for (int r = 0; r < nr; ++r) {
+        const int t = r < N ? r : r - N;
+        const size_t row = ((size_t)b * N + t) * a.H + h;
+        cp_async_block(sQK + (size_t)r * dk, (r < N ? q : k) + row * dk, rowb, tid, kCThreads);
+    }
+    cp_async_wait_all();
+    __syncthreads();
     float acc[kMaxRowsPerThread];
 #pragma unroll
     for (int i = 0; i < kMaxRowsPerThread; ++i) acc[i] = 0.f;
-    const T* q = static_cast<const T*>(a.q);
-    const T* k = static_cast<const T*>(a.k);
-    for (int c0 = 0; c0 < dk; c0 += kKC) {
-        __syncthreads();
-        for (int i = tid; i < nr * kKC; i += kCThreads) {
-            const int r = i / kKC, c = i % kKC;
-            const int t = r < N ? r : r - N;
-            const size_t row = ((size_t)b * N + t) * a.H + h;
-            sqk[c * ldq + r] = c0 + c < dk ? ld_elem<T>(r < N ? q : k, row * dk + c0 + c) : 0.f;
-        }
-        __syncthreads();
-        if (lane < rows) {
-            const int cn = min(kKC, dk - c0);
-            for (int c = 0; c < cn; ++c) {
-                const float sv = sS[lane * ldS + c0 + c];
-                const float* col = sqk + c * ldq;
+    if (lane < rows) {
+        const float* srow = sS + lane * ldS;
+        for (int c = 0; c < dk; c += 8) {
+            const float4 s0 = *reinterpret_cast<const float4*>(srow + c);
+            const float4 s1 = *reinterpret_cast<const float4*>(srow + c + 4);
 #pragma unroll
-                for (int i = 0; i < kMaxRowsPerThread; ++i) {
-                    const int r = rg + kRowGroups * i;
-                    if (r < nr) acc[i] = fmaf(col[r], sv, acc[i]);
+            for (int i = 0; i < kMaxRowsPerThread; ++i) {
+                const int r = rg + kRowGroups * i;
+                if (r < nr) {
+                    float x[8];
+                    ld8<T>(sQK + (size_t)r * dk + c, x);
+                    float a0 = acc[i];
+                    a0 = fmaf(x[0], s0.x, a0);
+                    a0 = fmaf(x[1], s0.y, a0);
+                    a0 = fmaf(x[2], s0.z, a0);
+                    a0 = fmaf(x[3], s0.w, a0);
+                    a0 = fmaf(x[4], s1.x, a0);
+                    a0 = fmaf(x[5], s1.y, a0);
+                    a0 = fmaf(x[6], s1.z, a0);
+                    acc[i] = fmaf(x[7], s1.w, a0);
                 }
             }
         }
     }
-    cp_async_wait_all();
     __syncthreads();
 
     // 4. Y_Q -> smem; R = beta (v - e^g Y_K) -> smem
