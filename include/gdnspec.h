@@ -57,6 +57,7 @@ extern "C" {
 #define GDN_ERR_TIMEOUT (-4)  /* a bounded device wait ran out (device-detected) */
 #define GDN_ERR_CUDA (-5)     /* a CUDA runtime call or launch failed */
 #define GDN_ERR_DEVICE (-6)   /* current device is not sm_103 */
+#define GDN_ERR_CAPACITY (-7) /* request larger than gdn_tree_verify_noalloc's fixed scratch */
 
 /* ---- q/k/v element types ------------------------------------------------ */
 #define GDN_DTYPE_BF16 0
@@ -117,6 +118,32 @@ int gdn_tree_verify(const void* q, const void* k, const void* v, int dtype, cons
                     const float* beta, const int32_t* parent_idx, const float* S0, float* out,
                     void* factors, void* workspace, int B, int N, int H, int dk, int dv,
                     cudaStream_t stream);
+
+/*
+ * gdn_tree_verify without the workspace argument, for callers that cannot
+ * allocate device memory: code running inside a host framework that owns all
+ * device memory through its own pool and forbids raw cudaMalloc, and
+ * latency-critical decode loops where an allocation and the device
+ * synchronization it may imply are not acceptable.  (The paper has no
+ * counterpart; this is a property of this library's interface.)
+ *   Same arguments, layouts and results as gdn_tree_verify.  The workspace
+ *   lives in a fixed 32 MiB scratch array inside the library, held by every
+ *   GPU that loads the library until the process exits.  B * H * (workspace
+ *   record of one (sequence, head)) must fit in it -- at N = 64 that is up to
+ *   992 (sequence, head) pairs, e.g. B = 124 with H = 8; larger requests
+ *   return GDN_ERR_CAPACITY without launching anything.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.  The call allocates nothing.
+ *   All calls on a device share the array, which keeps the last call's
+ *   contents (every entry is rewritten before it is read, so nothing needs
+ *   clearing); calls whose kernels overlap on the GPU -- e.g. on two streams
+ *   at once -- race on it.
+ */
+int gdn_tree_verify_noalloc(const void* q, const void* k, const void* v, int dtype,
+                            const float* alpha, const float* beta, const int32_t* parent_idx,
+                            const float* S0, float* out, void* factors, int B, int N, int H, int dk,
+                            int dv, cudaStream_t stream);
 
 /*
  * Chain verification with the state kept on chip and tiled along d_v

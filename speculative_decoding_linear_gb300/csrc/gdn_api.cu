@@ -247,6 +247,7 @@ const char* gdn_strerror(int code) {
         case GDN_ERR_TIMEOUT: return "a bounded device wait ran out";
         case GDN_ERR_CUDA: return "CUDA runtime error";
         case GDN_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        case GDN_ERR_CAPACITY: return "request exceeds the fixed scratch capacity of gdn_tree_verify_noalloc";
         default: return "unknown status";
     }
 }

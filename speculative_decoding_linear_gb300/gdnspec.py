@@ -22,7 +22,7 @@ from . import build as _build
 _lib = None
 _lock = threading.Lock()
 
-OK, ERR_ARG, ERR_TREE, ERR_PATH, ERR_TIMEOUT, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
+OK, ERR_ARG, ERR_TREE, ERR_PATH, ERR_TIMEOUT, ERR_CUDA, ERR_DEVICE, ERR_CAPACITY = 0, -1, -2, -3, -4, -5, -6, -7
 DTYPE_BF16, DTYPE_F32 = 0, 1
 
 # (name, restype, argtypes) for every extern "C" symbol of include/gdnspec.h
@@ -32,6 +32,7 @@ SIGNATURES = {
     "gdn_workspace_bytes": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
     "gdn_tree_mask": (_I, [_P, _I, _I, _P, _P, _P]),
     "gdn_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_tree_verify_noalloc": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_chain_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_commit": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gdn_commit_tree_verify": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P,
@@ -158,6 +159,18 @@ def gdn_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, workspac
                                  _ptr(beta), _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(factors),
                                  _ptr(workspace), B, N, H, dk, dv, _stream(stream)),
            "gdn_tree_verify")
+
+
+def gdn_tree_verify_noalloc(q, k, v, alpha, beta, parent_idx, S0, out, factors, stream=None):
+    """gdn_tree_verify without a workspace argument: for callers that cannot allocate device
+    memory (a framework that owns all device memory, or a decode loop that must not allocate).
+    The workspace is a fixed 32 MiB scratch array inside the library, shared by all calls on a
+    device; calls overlapping on the GPU race on it.  See include/gdnspec.h."""
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_tree_verify_noalloc(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha),
+                                         _ptr(beta), _ptr(parent_idx), _ptr(S0), _ptr(out),
+                                         _ptr(factors), B, N, H, dk, dv, _stream(stream)),
+           "gdn_tree_verify_noalloc")
 
 
 def gdn_chain_verify(q, k, v, alpha, beta, S0, out, factors, stream=None):
