@@ -63,18 +63,26 @@ inline Factors factors_view(void* base, int B, int N, int H, int dk, int dv, int
 //   anc u64 [N]     inclusive ancestor mask (path(t) as bits)
 // ---------------------------------------------------------------------------
 struct WsLayout {
-    size_t T, P, eg, bt, anc, record;
+    size_t T, P, op, eg, bt, anc, record;
 };
 
 // Every section starts on a 16-byte boundary and is padded to a multiple of
 // 16 bytes, so kernels may stage whole sections with 16-byte async copies.
 __host__ __device__ inline size_t ws_table_bytes(int N) { return align_up((size_t)N * N * 4, 16); }
 
+// The tensor-core contraction's second MMA operand [T; P]: 128 rows (T rows
+// 0..63, P rows 64..127) x 64 columns, bf16 hi then lo, each 16 KiB in the
+// 128-byte-swizzled K-major shared-memory layout.  It shares storage with the
+// fp32 T and P tables (a call uses one form or the other).
+constexpr size_t kTcOperandBytes = 2 * 128 * 128;
+
 __host__ __device__ inline WsLayout ws_layout(int N) {
     WsLayout L;
     L.T = 0;
     L.P = L.T + ws_table_bytes(N);
-    L.eg = L.P + ws_table_bytes(N);
+    L.op = 0;
+    const size_t tab = 2 * ws_table_bytes(N) > kTcOperandBytes ? 2 * ws_table_bytes(N) : kTcOperandBytes;
+    L.eg = tab;
     L.bt = L.eg + align_up((size_t)N * 4, 16);
     L.anc = L.bt + align_up((size_t)N * 4, 16);
     L.record = align_up(L.anc + (size_t)N * 8, kSectionAlign);
@@ -109,6 +117,7 @@ struct VerifyArgs {
     CommitSrc commit;          // commit.path == nullptr: no fused commit
     int* err;
     bool overlap;              // launch the call's first kernel as a programmatic dependent
+    bool tc;                   // the tensor-core contraction runs: prologue writes its operand form
 };
 
 struct CommitArgs {

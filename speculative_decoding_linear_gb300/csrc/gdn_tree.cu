@@ -21,9 +21,11 @@
 // Kernels here:
 //   tree_mask_kernel      ancestor bitmask + depth (gdn_tree_mask).
 //   tree_prep_kernel      one CTA per (b, h): stages Q and K with cp.async,
-//                         ancestor masks, gates, masked Gram entries, T by
-//                         depth levels, P = Attn T; writes the workspace
-//                         record and the factor record's g, parent and keys.
+//                         ancestor masks, gates, masked Gram entries, each
+//                         node's row of T by back-substitution along its own
+//                         path, P = Attn T; writes the workspace record (fp32
+//                         T and P, or the tensor-core operand form of [T; P])
+//                         and the factor record's g, parent and keys.
 //   tree_contract_kernel  SIMT contraction for any d_k/d_v/dtype: one CTA per
 //                         (b, h, 32 state rows); streams the state tile
 //                         (committing a pending path first when fused), forms
@@ -136,7 +138,6 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
     float* sbeta = reinterpret_cast<float*>(smem + Ly.beta);
     int* sdepth = reinterpret_cast<int*>(smem + Ly.depth);
     int* off = reinterpret_cast<int*>(smem + Ly.off);
-    int* maxdepth = reinterpret_cast<int*>(smem + Ly.misc);
     const int ld = Ly.ld;
 
     const int bh = blockIdx.x;
@@ -166,8 +167,6 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
         la[tid] = logf(a.alpha[gi]);
         sbeta[tid] = a.beta[gi];
     }
-    if (tid == 0) *maxdepth = 0;
-    for (int i = tid; i < N * ld; i += kPrepThreads) sA[i] = sAt[i] = sT[i] = 0.f;
     cp_async_wait_all();
     if (__syncthreads_or(bad)) {
         if (tid == 0) {
@@ -187,7 +186,6 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
         }
         anc[tid] = m;
         sdepth[tid] = d;
-        atomicMax(maxdepth, d);
         float gs = 0.f;
         for (uint64_t r = m; r; r &= r - 1) gs += la[__ffsll((long long)r) - 1];
         sg[tid] = gs + la[tid];
@@ -253,39 +251,79 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
     }
     __syncthreads();
 
-    // 5. T = (I + A)^-1 by depth levels: row t needs only rows of its ancestors
-    const int md = *maxdepth;
-    for (int d = 0; d <= md; ++d) {
-        for (int i = tid; i < N * N; i += kPrepThreads) {
-            const int t = i / N, c = i % N;
-            if (sdepth[t] != d) continue;
-            const uint64_t an = anc[t];
-            if (c != t && !((an >> c) & 1ull)) continue;
-            float x = c == t ? 1.f : 0.f;
-            for (uint64_t r = an; r; r &= r - 1) {
-                const int j = __ffsll((long long)r) - 1;
-                x = fmaf(-sA[t * ld + j], sT[j * ld + c], x);
-            }
-            sT[t * ld + c] = x;
-        }
-        __syncthreads();
-    }
-
-    // 6. P = Attn T (support on path(t)); workspace record and factor record
-    float* wT = reinterpret_cast<float*>(rec + wl.T);
-    float* wP = reinterpret_cast<float*>(rec + wl.P);
-    for (int i = tid; i < N * N; i += kPrepThreads) {
-        const int t = i / N, c = i % N;
+    // 5. Row t of T = (I + A)^-1.  The principal block of I + A on path(t) is
+    //    closed (ancestors of path nodes are on the path), so row t of T is the
+    //    last row of that block's inverse: x_t = 1 and, walking up the path,
+    //    x_k = -sum_{i on path(t), i below k} x_i A[i, k].  One thread per node,
+    //    no level barriers; only path entries of the row are written.
+    if (tid < N) {
+        const int t = tid;
         const uint64_t path = anc[t] | (1ull << t);
-        float x = 0.f;
-        if ((path >> c) & 1ull) {
-            for (uint64_t r = path; r; r &= r - 1) {
-                const int j = __ffsll((long long)r) - 1;
+        float* row = sT + t * ld;
+        row[t] = 1.f;
+        for (uint64_t up = anc[t]; up;) {
+            const int kk = 63 - __clzll((long long)up);          // deepest remaining ancestor
+            up &= ~(1ull << kk);
+            float x = 0.f;
+            for (uint64_t below = path & ~((2ull << kk) - 1ull); below; below &= below - 1) {
+                const int i = __ffsll((long long)below) - 1;
+                x = fmaf(row[i], sA[i * ld + kk], x);
+            }
+            row[kk] = -x;
+        }
+    }
+    __syncthreads();
+
+    // 6. P = Attn T: P[t, c] = sum_{j on path(t), j at or below c} Attn[t, j] T[j, c],
+    //    into sA (A is no longer needed); then the workspace record and factor record
+    if (tid < N) {
+        const int t = tid;
+        const uint64_t path = anc[t] | (1ull << t);
+        for (uint64_t cs = path; cs; cs &= cs - 1) {
+            const int c = __ffsll((long long)cs) - 1;
+            float x = 0.f;
+            for (uint64_t js = path & ~((1ull << c) - 1ull); js; js &= js - 1) {
+                const int j = __ffsll((long long)js) - 1;
                 x = fmaf(sAt[t * ld + j], sT[j * ld + c], x);
             }
+            sA[t * ld + c] = x;   // row t of A is only read by thread t's descendants in step 5: done
         }
-        wP[i] = x;
-        wT[i] = sT[t * ld + c];
+    }
+    __syncthreads();
+    if (a.tc) {
+        // [T; P] as the tensor-core contraction's second MMA operand: bf16 hi and lo,
+        // 128-byte-swizzled K-major rows (zeros off the ancestor mask and beyond N)
+        unsigned char* op = reinterpret_cast<unsigned char*>(rec + wl.op);
+        for (int item = tid; item < 128 * 8; item += kPrepThreads) {
+            const int r = item >> 3, cc = item & 7;
+            const int t = r & 63;
+            const float* src = r >= 64 ? sA : sT;
+            const uint64_t path = t < N ? (anc[t] | (1ull << t)) : 0ull;
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j0 = 8 * cc + 2 * e, j1 = j0 + 1;
+                const float x0 = ((path >> j0) & 1ull) ? src[t * ld + j0] : 0.f;
+                const float x1 = ((path >> j1) & 1ull) ? src[t * ld + j1] : 0.f;
+                const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+                const float2 hf = __bfloat1622float2(hh);
+                const __nv_bfloat162 ll = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+                hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
+            }
+            const uint32_t off = (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
+            *reinterpret_cast<uint4*>(op + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(op + kTcOperandBytes / 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+    } else {
+        float* wT = reinterpret_cast<float*>(rec + wl.T);
+        float* wP = reinterpret_cast<float*>(rec + wl.P);
+        for (int i = tid; i < N * N; i += kPrepThreads) {
+            const int t = i / N, c = i % N;
+            const bool on = ((anc[t] | (1ull << t)) >> c) & 1ull;
+            wT[i] = on ? sT[t * ld + c] : 0.f;
+            wP[i] = on ? sA[t * ld + c] : 0.f;
+        }
     }
     if (tid < N) {
         reinterpret_cast<float*>(rec + wl.eg)[tid] = expf(sg[tid]);
@@ -337,7 +375,6 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
     const bool fused = a.commit.path != nullptr;
     const ContractLayout Ly(N, dk, fused ? a.commit.Lmax : 0, (int)sizeof(T));
     float* sS = reinterpret_cast<float*>(smem + Ly.S);
-    float* sqk = reinterpret_cast<float*>(smem + Ly.qk);
     float* sYQ = reinterpret_cast<float*>(smem + Ly.YQ);
     float* sR = reinterpret_cast<float*>(smem + Ly.R);
     float* sT = reinterpret_cast<float*>(smem + Ly.T);
@@ -523,16 +560,19 @@ cudaError_t launch_tree_contract_simt(const VerifyArgs& a, cudaStream_t s) {
     return launch_kernel(tree_contract_kernel<T>, grid, dim3(kCThreads), Ly.total, s, true, a);
 }
 
-cudaError_t launch_tree_verify(const VerifyArgs& a, int dtype, cudaStream_t s) {
+cudaError_t launch_tree_verify(const VerifyArgs& args, int dtype, cudaStream_t s) {
+    VerifyArgs a = args;
     cudaError_t e;
     if (dtype == GDN_DTYPE_F32) {
+        a.tc = false;
         e = launch_tree_prep<float>(a, s);
         if (e != cudaSuccess) return e;
         return launch_tree_contract_simt<float>(a, s);
     }
+    a.tc = tc_contract_eligible(a);
     e = launch_tree_prep<__nv_bfloat16>(a, s);
     if (e != cudaSuccess) return e;
-    if (tc_contract_eligible(a)) return launch_tree_contract_tc(a, s);
+    if (a.tc) return launch_tree_contract_tc(a, s);
     return launch_tree_contract_simt<__nv_bfloat16>(a, s);
 }
 

@@ -27,10 +27,12 @@
 // bf16 q/k times the two-term state is exact to ~2^-16 relative per product,
 // with fp32 accumulation: far inside the 2e-3 x RMS budget.
 //
-// Epilogue: warps 0-3 read Y_K (TMEM columns 64..127), form R into shared
-// memory; after a barrier warps 0-3 gather Delta and warps 4-7 read Y_Q
-// (columns 0..63) and gather O.  T and P come from the prologue kernel's
-// workspace, staged into the first stage's buffers once its MMAs are done.
+// Epilogue, also on the tensor core: warps 0-3 read Y_K (TMEM columns 64..127)
+// and write R as bf16 hi + lo rows of a second A operand; the prologue kernel
+// has already written [T; P] (bf16 hi + lo, swizzled) into the workspace, and
+// one bulk copy brings it in.  Twelve MMAs (4 K-steps x {hi.hi, hi.lo, lo.hi})
+// give [T R | P R] in TMEM columns 128..255; warps 0-3 store Delta = T R and
+// warps 4-7 store O = e^g Y_Q + P R.
 //
 // Every mbarrier wait is bounded (about one second, then GDN_ERR_TIMEOUT is
 // recorded and the CTA skips ahead to its teardown); TMEM is always freed.
@@ -50,7 +52,7 @@ constexpr int kSlabs = kDk / kSlab;
 constexpr int kNodeRows = 64;      // B operand: Q rows 0..63, K rows 64..127 (MMA N = 128)
 constexpr int kBufBytes = kTileV * 128;        // one 128-row x 128-byte operand buffer (16 KiB)
 constexpr int kStageBytes = 3 * kBufBytes;     // A_hi, A_lo, B
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemCols = 256;     // Y in columns 0..127, [Delta | P R] in 128..255
 constexpr int kMaxTcPath = 16;
 // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N = 128, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
@@ -102,6 +104,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -214,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float* s_coef = reinterpret_cast<float*>(base + Ly.coef);
     int* s_nodes = reinterpret_cast<int*>(base + Ly.nodes);
     const uint32_t bar_tma0 = base_s + Ly.bars, bar_mma0 = base_s + Ly.bars + 16;
+    const uint32_t bar_op = base_s + Ly.bars + 32, bar_e = base_s + Ly.bars + 40;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
     float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 4);
     int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 8);   // path length, or -1: skip the CTA
@@ -223,6 +231,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(bar_tma0 + 8, 1);
         mbar_init(bar_mma0, 1);
         mbar_init(bar_mma0 + 8, 1);
+        mbar_init(bar_op, 1);
+        mbar_init(bar_e, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         fence_proxy_async_smem();
         *s_flag = 0;
@@ -350,26 +360,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-        // stage 0 is free once slab kSlabs-2 is done: stage T, P, e^g, beta, masks there
+        // Stage 0 is free once slab kSlabs-2 is done: bring the [T; P] operand (bf16 hi, lo)
+        // into its A buffers with one bulk copy, e^g and beta into its B buffer.
         ok = __syncthreads_and(ok);
         if (ok) ok = mbar_wait(bar_mma0, 1, a.err);
-        float* sT = reinterpret_cast<float*>(base);
-        float* sP = reinterpret_cast<float*>(base + kBufBytes);
+        const uint32_t op_s = base_s;                                  // B2: hi, then lo (16 KiB each)
+        const uint32_t r_s = base_s + kStageBytes;                     // A2: R hi, then lo (stage 1)
         float* seg = reinterpret_cast<float*>(base + 2 * kBufBytes);
-        float* sbt = seg + kMaxNodes;
-        uint64_t* sanc = reinterpret_cast<uint64_t*>(sbt + kMaxNodes);
-        float* sR = reinterpret_cast<float*>(base + kStageBytes);   // stage 1 A buffers, after the last MMA
-        if (ok) {
-            cp_async_block(sT, rec + wl.T, (int)ws_table_bytes(N), tid, kThreads);
-            cp_async_block(sP, rec + wl.P, (int)ws_table_bytes(N), tid, kThreads);
-            for (int t = tid; t < N; t += kThreads) {
-                seg[t] = reinterpret_cast<const float*>(rec + wl.eg)[t];
-                sbt[t] = reinterpret_cast<const float*>(rec + wl.bt)[t];
-                sanc[t] = reinterpret_cast<const uint64_t*>(rec + wl.anc)[t];
-            }
-            ok = mbar_wait(bar_mma0 + 8, 1, a.err);
+        float* sbt = seg + kNodeRows;
+        if (ok && tid == 0) {
+            mbar_expect_tx(bar_op, (uint32_t)kTcOperandBytes);
+            bulk_copy_g2s(op_s, rec + wl.op, (uint32_t)kTcOperandBytes, bar_op);
         }
-        cp_async_wait_all();
+        if (ok && tid < kNodeRows) {
+            seg[tid] = tid < N ? reinterpret_cast<const float*>(rec + wl.eg)[tid] : 0.f;
+            sbt[tid] = tid < N ? reinterpret_cast<const float*>(rec + wl.bt)[tid] : 0.f;
+        }
+        if (ok) ok = mbar_wait(bar_mma0 + 8, 1, a.err);                // Y complete
         ok = __syncthreads_and(ok);
         tc_fence_after();
 
@@ -377,10 +384,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(a.v);
         if (ok && warp < 4) {
-            // R_t = beta_t (v_t - e^{g_t} Y_K[v, t])
+            // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N), stored as bf16 hi + lo
+            // rows of the second MMA's A operand (row v, 64 columns t)
+            unsigned char* rhi = base + kStageBytes;
+            unsigned char* rlo = rhi + kBufBytes;
 #pragma unroll
             for (int c = 0; c < kNodeRows / 32; ++c) {
-                if (32 * c >= N) break;
                 float vin[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -390,41 +399,72 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float yk[32];
                 tmem_ld32(t_lane + kNodeRows + 32 * c, yk);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * c + i;
-                    if (t < N) sR[t * kTileV + v] = sbt[t] * (vin[i] - seg[t] * yk[i]);
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = 8 * q8 + 2 * e, i1 = i0 + 1;
+                        const int t0 = 32 * c + i0, t1 = t0 + 1;
+                        const float r0 = t0 < N ? sbt[t0] * (vin[i0] - seg[t0] * yk[i0]) : 0.f;
+                        const float r1 = t1 < N ? sbt[t1] * (vin[i1] - seg[t1] * yk[i1]) : 0.f;
+                        const __nv_bfloat162 hh = __floats2bfloat162_rn(r0, r1);
+                        const float2 hf = __bfloat1622float2(hh);
+                        const __nv_bfloat162 ll = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
+                        hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                        lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
+                    }
+                    const int cc = 4 * c + q8;                           // 16-byte chunk = 8 nodes
+                    const uint32_t off = (uint32_t)(v * 128 + ((cc ^ (v & 7)) << 4));
+                    *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(rlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
         __syncthreads();
-        if (ok && warp < 4) {
-            // Delta_t = sum_{j in path(t)} T[t, j] R_j
-            for (int t = 0; t < N; ++t) {
-                float d = 0.f;
-                for (uint64_t m = sanc[t]; m; m &= m - 1) {
-                    const int j = __ffsll((long long)m) - 1;
-                    d = fmaf(sT[t * N + j], sR[j * kTileV + v], d);
+        if (tid == 0 && ok) {
+            // [Delta | P R] (v, t) = sum_j R[v, j] [T; P](t, j): three bf16 terms (hi.hi, hi.lo, lo.hi)
+            if (mbar_wait(bar_op, 0, a.err)) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kNodeRows / 16; ++kk) {
+                    const uint64_t ahi = sw128_desc(r_s + kk * 32), alo = sw128_desc(r_s + kBufBytes + kk * 32);
+                    const uint64_t bhi = sw128_desc(op_s + kk * 32), blo = sw128_desc(op_s + kBufBytes + kk * 32);
+                    mma_bf16(tmem + 128, ahi, bhi, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + 128, ahi, blo, 1u);
+                    mma_bf16(tmem + 128, alo, bhi, 1u);
                 }
-                a.f.delta[((size_t)bh * N + t) * dv + v0 + v] = d;
+                mma_commit(bar_e);
             }
-        } else if (ok) {
-            // O_t = e^{g_t} Y_Q[v, t] + sum_{j in path(t)} P[t, j] R_j
+        }
+        if (ok) ok = mbar_wait(bar_e, 0, a.err);
+        tc_fence_after();
+        if (ok && warp < 4) {
+            // Delta_t[v] = (T R)[v, t]
 #pragma unroll
             for (int c = 0; c < kNodeRows / 32; ++c) {
                 if (32 * c >= N) break;
-                float yq[32];
-                tmem_ld32(t_lane + 32 * c, yq);
+                float d[32];
+                tmem_ld32(t_lane + 128 + 32 * c, d);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int t = 32 * c + i;
-                    if (t < N) {
-                        float o = seg[t] * yq[i];
-                        for (uint64_t m = sanc[t]; m; m &= m - 1) {
-                            const int j = __ffsll((long long)m) - 1;
-                            o = fmaf(sP[t * N + j], sR[j * kTileV + v], o);
-                        }
-                        a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + v] = o;
-                    }
+                    if (t < N) a.f.delta[((size_t)bh * N + t) * dv + v0 + v] = d[i];
+                }
+            }
+        } else if (ok) {
+            // O_t[v] = e^{g_t} Y_Q[v, t] + (P R)[v, t]
+#pragma unroll
+            for (int c = 0; c < kNodeRows / 32; ++c) {
+                if (32 * c >= N) break;
+                float yq[32], pr[32];
+                tmem_ld32(t_lane + 32 * c, yq);
+                tmem_ld32(t_lane + 192 + 32 * c, pr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int t = 32 * c + i;
+                    if (t < N) a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + v] = fmaf(seg[t], yq[i], pr[i]);
                 }
             }
         }
@@ -471,13 +511,11 @@ bool make_qk_map(CUtensorMap* m, const void* ptr, int B, int N, int H) {
 
 }  // namespace
 
-// bf16 inputs, d_k = 256, d_v a multiple of 128, short accepted paths, and
-// enough (b, h, 128-row) tiles to fill the GPU; otherwise the SIMT kernel.
+// bf16 inputs, d_k = 256, d_v a multiple of 128 and accepted paths of at most
+// 16 nodes; otherwise the SIMT kernel.
 bool tc_contract_eligible(const VerifyArgs& a) {
     if (a.dk != kDk || a.dv % kTileV != 0) return false;
     if (a.commit.path != nullptr && a.commit.Lmax > kMaxTcPath) return false;
-    const long long tiles = (long long)a.B * a.H * (a.dv / kTileV);
-    if (tiles < 120) return false;
     return encode_fn() != nullptr;
 }
 
