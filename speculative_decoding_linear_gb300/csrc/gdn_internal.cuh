@@ -219,9 +219,9 @@ cudaError_t launch_commit(const CommitArgs& a, int dtype, cudaStream_t s);
 // launch-overlap switch (gdn_api.cu)
 int* current_error_word(int* status);
 bool launch_overlap_enabled();
-// tensor-core contraction of the tree verifier (gdn_tree_tc.cu)
+// tensor-core prologue + contraction of the tree verifier (gdn_tree_tc.cu)
 bool tc_contract_eligible(const VerifyArgs& a);
-cudaError_t launch_tree_contract_tc(const VerifyArgs& a, cudaStream_t s);
+cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s);
 
 }  // namespace gdn
 

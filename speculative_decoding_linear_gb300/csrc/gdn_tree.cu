@@ -21,17 +21,19 @@
 // Kernels here:
 //   tree_mask_kernel      ancestor bitmask + depth (gdn_tree_mask).
 //   tree_prep_kernel      one CTA per (b, h): stages Q and K with cp.async,
-//                         ancestor masks, gates, masked Gram entries, each
-//                         node's row of T by back-substitution along its own
-//                         path, P = Attn T; writes the workspace record (fp32
-//                         T and P, or the tensor-core operand form of [T; P])
-//                         and the factor record's g, parent and keys.
+//                         ancestor masks, gates, masked Gram entries (8 lanes
+//                         per (node, ancestor) pair), each node's row of T by
+//                         back-substitution along its own path, P = Attn T;
+//                         writes dense fp32 T and P to the workspace and the
+//                         factor record's g, parent and keys.
 //   tree_contract_kernel  SIMT contraction for any d_k/d_v/dtype: one CTA per
 //                         (b, h, 32 state rows); streams the state tile
 //                         (committing a pending path first when fused), forms
 //                         Y = [Q; K] S_tile^T, then R, Delta and O.
-//                         (gdn_tree_tc.cu holds the tensor-core version.)
+//                         (gdn_tree_tc.cu holds the tensor-core versions of
+//                         both kernels, used for bf16 inputs with d_k = 256.)
 #include "gdn_internal.cuh"
+#include "gdn_prep_common.cuh"
 
 namespace gdn {
 namespace {
@@ -176,49 +178,13 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
         return;
     }
 
-    // 2. strict ancestor masks, depths, cumulative log gates (ascending = root first)
-    if (tid < N) {
-        uint64_t m = 0;
-        int d = 0;
-        for (int j = par[tid]; j >= 0; j = par[j]) {
-            m |= 1ull << j;
-            ++d;
-        }
-        anc[tid] = m;
-        sdepth[tid] = d;
-        float gs = 0.f;
-        for (uint64_t r = m; r; r &= r - 1) gs += la[__ffsll((long long)r) - 1];
-        sg[tid] = gs + la[tid];
-    }
+    // 2. masks, depths, gates; 3. (t, j on path(t)) pairs
+    prep::node_meta(tid, N, par, la, anc, sdepth, sg);
     __syncthreads();
-
-    // 3. enumerate (t, j in path(t)) pairs: exclusive scan of path lengths
-    const int warp = tid >> 5, lane = tid & 31;
-    if (warp == 0) {
-        int carry = 0;
-        for (int t0 = 0; t0 < N; t0 += 32) {
-            const int t = t0 + lane;
-            int x = t < N ? sdepth[t] + 1 : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (t < N) off[t + 1] = carry + x;
-            carry += __shfl_sync(0xffffffffu, x, 31);
-        }
-        if (lane == 0) off[0] = 0;
-    }
-    __syncthreads();
-    if (tid < N) {
-        int o = off[tid];
-        for (uint64_t r = anc[tid]; r; r &= r - 1)
-            pairs[o++] = (uint16_t)((tid << 8) | (__ffsll((long long)r) - 1));
-        pairs[o] = (uint16_t)((tid << 8) | tid);
-    }
-    __syncthreads();
+    prep::pair_list(tid, N, sdepth, anc, off, pairs);
 
     // 4. masked Gram entries: 8 lanes per pair, 16-byte chunks interleaved across the group
+    const int warp = tid >> 5, lane = tid & 31;
     const int npairs = off[N];
     const int grp = lane >> 3, gl = lane & 7;
     const int nchunk = rowb / 16;
@@ -243,95 +209,15 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
             pkk += __shfl_xor_sync(0xffffffffu, pkk, o);
             pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
         }
-        if (valid && gl == 0) {
-            const float gam = expf(sg[t] - sg[j]);
-            sAt[t * ld + j] = gam * pqk;
-            if (j != t) sA[t * ld + j] = sbeta[t] * gam * pkk;
-        }
+        if (valid && gl == 0) prep::gram_entry(t, j, pkk, pqk, ld, sg, sbeta, sA, sAt);
     }
     __syncthreads();
 
-    // 5. Row t of T = (I + A)^-1.  The principal block of I + A on path(t) is
-    //    closed (ancestors of path nodes are on the path), so row t of T is the
-    //    last row of that block's inverse: x_t = 1 and, walking up the path,
-    //    x_k = -sum_{i on path(t), i below k} x_i A[i, k].  One thread per node,
-    //    no level barriers; only path entries of the row are written.
-    if (tid < N) {
-        const int t = tid;
-        const uint64_t path = anc[t] | (1ull << t);
-        float* row = sT + t * ld;
-        row[t] = 1.f;
-        for (uint64_t up = anc[t]; up;) {
-            const int kk = 63 - __clzll((long long)up);          // deepest remaining ancestor
-            up &= ~(1ull << kk);
-            float x = 0.f;
-            for (uint64_t below = path & ~((2ull << kk) - 1ull); below; below &= below - 1) {
-                const int i = __ffsll((long long)below) - 1;
-                x = fmaf(row[i], sA[i * ld + kk], x);
-            }
-            row[kk] = -x;
-        }
-    }
-    __syncthreads();
-
-    // 6. P = Attn T: P[t, c] = sum_{j on path(t), j at or below c} Attn[t, j] T[j, c],
-    //    into sA (A is no longer needed); then the workspace record and factor record
-    if (tid < N) {
-        const int t = tid;
-        const uint64_t path = anc[t] | (1ull << t);
-        for (uint64_t cs = path; cs; cs &= cs - 1) {
-            const int c = __ffsll((long long)cs) - 1;
-            float x = 0.f;
-            for (uint64_t js = path & ~((1ull << c) - 1ull); js; js &= js - 1) {
-                const int j = __ffsll((long long)js) - 1;
-                x = fmaf(sAt[t * ld + j], sT[j * ld + c], x);
-            }
-            sA[t * ld + c] = x;   // row t of A is only read by thread t's descendants in step 5: done
-        }
-    }
-    __syncthreads();
-    if (a.tc) {
-        // [T; P] as the tensor-core contraction's second MMA operand: bf16 hi and lo,
-        // 128-byte-swizzled K-major rows (zeros off the ancestor mask and beyond N)
-        unsigned char* op = reinterpret_cast<unsigned char*>(rec + wl.op);
-        for (int item = tid; item < 128 * 8; item += kPrepThreads) {
-            const int r = item >> 3, cc = item & 7;
-            const int t = r & 63;
-            const float* src = r >= 64 ? sA : sT;
-            const uint64_t path = t < N ? (anc[t] | (1ull << t)) : 0ull;
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int j0 = 8 * cc + 2 * e, j1 = j0 + 1;
-                const float x0 = ((path >> j0) & 1ull) ? src[t * ld + j0] : 0.f;
-                const float x1 = ((path >> j1) & 1ull) ? src[t * ld + j1] : 0.f;
-                const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
-                const float2 hf = __bfloat1622float2(hh);
-                const __nv_bfloat162 ll = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-                hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
-                lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
-            }
-            const uint32_t off = (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
-            *reinterpret_cast<uint4*>(op + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(op + kTcOperandBytes / 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-    } else {
-        float* wT = reinterpret_cast<float*>(rec + wl.T);
-        float* wP = reinterpret_cast<float*>(rec + wl.P);
-        for (int i = tid; i < N * N; i += kPrepThreads) {
-            const int t = i / N, c = i % N;
-            const bool on = ((anc[t] | (1ull << t)) >> c) & 1ull;
-            wT[i] = on ? sT[t * ld + c] : 0.f;
-            wP[i] = on ? sA[t * ld + c] : 0.f;
-        }
-    }
-    if (tid < N) {
-        reinterpret_cast<float*>(rec + wl.eg)[tid] = expf(sg[tid]);
-        reinterpret_cast<float*>(rec + wl.bt)[tid] = sbeta[tid];
-        reinterpret_cast<uint64_t*>(rec + wl.anc)[tid] = anc[tid] | (1ull << tid);
-        a.f.g[(size_t)bh * N + tid] = sg[tid];
-        if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
-    }
+    // 5-6. rows of T, then P over A; workspace and factor records
+    prep::solve_rows(tid, N, ld, anc, sA, sAt, sT);
+    prep::write_dense(tid, kPrepThreads, N, ld, anc, sA, sT, reinterpret_cast<float*>(rec + wl.T),
+                      reinterpret_cast<float*>(rec + wl.P));
+    prep::write_meta(tid, N, b, h, bh, rec, wl, sg, sbeta, anc, par, a.f);
     uint4* key_out = reinterpret_cast<uint4*>(static_cast<T*>(a.f.key) + (size_t)bh * N * dk);
     const uint4* ksrc = reinterpret_cast<const uint4*>(Ks);
     for (int i = tid; i < N * nchunk; i += kPrepThreads) key_out[i] = ksrc[i];
@@ -570,9 +456,9 @@ cudaError_t launch_tree_verify(const VerifyArgs& args, int dtype, cudaStream_t s
         return launch_tree_contract_simt<float>(a, s);
     }
     a.tc = tc_contract_eligible(a);
+    if (a.tc) return launch_tree_tc(a, s);
     e = launch_tree_prep<__nv_bfloat16>(a, s);
     if (e != cudaSuccess) return e;
-    if (a.tc) return launch_tree_contract_tc(a, s);
     return launch_tree_contract_simt<__nv_bfloat16>(a, s);
 }
 

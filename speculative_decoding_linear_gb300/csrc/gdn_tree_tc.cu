@@ -1,4 +1,4 @@
-// gdn_tree_tc.cu -- tensor-core (tcgen05) contraction of the tree verifier.
+// gdn_tree_tc.cu -- tensor-core (tcgen05) prologue and contraction of the tree verifier.
 //
 // Same mathematics as the SIMT contraction in gdn_tree.cu (review of SpecLA,
 // pith.science 7ERME3HB, "Core claim": O = Qhat S0^T - Attn (W S0^T) + Attn U):
@@ -40,9 +40,12 @@
 #include <cudaTypedefs.h>
 
 #include "gdn_internal.cuh"
+#include "gdn_prep_common.cuh"
+#include "gdn_tc_ptx.cuh"
 
 namespace gdn {
 namespace {
+using namespace tc;
 
 constexpr int kThreads = 256;
 constexpr int kTileV = 128;        // state rows per CTA (MMA M)
@@ -54,135 +57,7 @@ constexpr int kBufBytes = kTileV * 128;        // one 128-row x 128-byte operand
 constexpr int kStageBytes = 3 * kBufBytes;     // A_hi, A_lo, B
 constexpr uint32_t kTmemCols = 256;     // Y in columns 0..127, [Delta | P R] in 128..255
 constexpr int kMaxTcPath = 16;
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N = 128, M = 128
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
-                            ((uint32_t)(128 >> 4) << 24);
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-    return t;
-}
-// Bounded wait for the completion of the mbarrier phase with this parity.
-// Returns false (and records GDN_ERR_TIMEOUT) after about one second.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
-            set_error(err, GDN_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t holder, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(holder),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-                 : "memory");
-}
-// 32 consecutive TMEM columns of this warp's 32 lanes (one fp32 per column per lane).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes in 8-row (1024-byte) groups.  The leading-byte offset is unused
-// for this layout; the stride-byte offset is the 1024-byte group pitch.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// Byte offset of bf16 quad (4 elements, 8 bytes) `c4` (0..15) of row `r` in a
-// 128-byte-swizzled K-major buffer.
-__device__ __forceinline__ uint32_t sw128_quad(int r, int c4) {
-    return (uint32_t)(r * 128 + (((c4 >> 1) ^ (r & 7)) << 4) + ((c4 & 1) << 3));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
-    const __nv_bfloat162 p = __floats2bfloat162_rn(lo_elem, hi_elem);
-    return *reinterpret_cast<const uint32_t*>(&p);
-}
+constexpr uint32_t kIdesc = idesc_bf16(128, 128);   // D fp32, A/B bf16 K-major, M = N = 128
 
 struct TcLayout {
     // offsets from the 1024-aligned base
@@ -248,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const size_t srow0 = ((size_t)bh * dv + v0) * kDk;
     const int c4 = tid & 15;         // column quad within a slab
     const int rbase = tid >> 4;      // rows rbase + 16 j, j = 0..7
-    float4 xa[8], xb[8];
+    float4 xa[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         xa[j] = *reinterpret_cast<const float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk + 4 * c4);
@@ -298,15 +173,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tma_load_3d(bsm + kNodeRows * 128, &tmK, s * kSlab, h, b * N, bar_tma0 + 8 * s);
             }
         }
-#pragma unroll
+#pragma unroll 1
         for (int ks = 0; ks < kSlabs; ++ks) {
             const int s = ks & 1;
-            float4(&x)[8] = (ks & 1) ? xb : xa;
-            float4(&xn)[8] = (ks & 1) ? xa : xb;
+            float4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = xa[j];
             if (ks + 1 < kSlabs) {      // next slab in flight while this one is processed
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    xn[j] = *reinterpret_cast<const float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk +
+                    xa[j] = *reinterpret_cast<const float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk +
                                                             (ks + 1) * kSlab + 4 * c4);
             }
             if (ks >= 2) {              // stage s is free once slab ks-2's MMAs are done
@@ -318,17 +194,40 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tma_load_3d(bsm + kNodeRows * 128, &tmK, ks * kSlab, h, b * N, bar_tma0 + 8 * s);
                 }
             }
+            const int col = ks * kSlab + 4 * c4;
+            if (fused) {
+                // S <- e^{g_a} S + sum_i cd_i[row] k_i[col..col+3], path node outermost: one
+                // key quad per node serves this thread's 8 rows (same order of operations
+                // per element as commit_quad, so the result is bit-identical to gdn_commit)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    x[j].x *= ega;
+                    x[j].y *= ega;
+                    x[j].z *= ega;
+                    x[j].w *= ega;
+                }
+                for (int i = 0; i < L; ++i) {
+                    const float4 kq = ld4<__nv_bfloat16>(s_key, (size_t)i * kDk + col);
+                    const float* cdi = s_cd + i * kTileV + rbase;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float w = cdi[16 * j];
+                        x[j].x = fmaf(w, kq.x, x[j].x);
+                        x[j].y = fmaf(w, kq.y, x[j].y);
+                        x[j].z = fmaf(w, kq.z, x[j].z);
+                        x[j].w = fmaf(w, kq.w, x[j].w);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk + col) = x[j];
+            }
             unsigned char* ahi = base + s * kStageBytes;
             unsigned char* alo = ahi + kBufBytes;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int r = rbase + 16 * j;
-                float4 v = x[j];
-                if (fused) {
-                    v = commit_quad<__nv_bfloat16>(v, ega, L, s_cd + r, kTileV, s_key, kDk,
-                                                   ks * kSlab + 4 * c4);
-                    *reinterpret_cast<float4*>(a.S + srow0 + (size_t)r * kDk + ks * kSlab + 4 * c4) = v;
-                }
+                const float4 v = x[j];
                 const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
                 const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
                 const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
@@ -353,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int kk = 0; kk < kSlab / 16; ++kk) {
                         const uint64_t bd = sw128_desc(bsm + kk * 32);
-                        mma_bf16(tmem, sw128_desc(a_hi + kk * 32), bd, (ks > 0 || kk > 0) ? 1u : 0u);
-                        mma_bf16(tmem, sw128_desc(a_lo + kk * 32), bd, 1u);
+                        mma_bf16(tmem, sw128_desc(a_hi + kk * 32), bd, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16(tmem, sw128_desc(a_lo + kk * 32), bd, kIdesc, 1u);
                     }
                     mma_commit(bar_mma0 + 8 * s);
                 }
@@ -431,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int kk = 0; kk < kNodeRows / 16; ++kk) {
                     const uint64_t ahi = sw128_desc(r_s + kk * 32), alo = sw128_desc(r_s + kBufBytes + kk * 32);
                     const uint64_t bhi = sw128_desc(op_s + kk * 32), blo = sw128_desc(op_s + kBufBytes + kk * 32);
-                    mma_bf16(tmem + 128, ahi, bhi, kk > 0 ? 1u : 0u);
-                    mma_bf16(tmem + 128, ahi, blo, 1u);
-                    mma_bf16(tmem + 128, alo, bhi, 1u);
+                    mma_bf16(tmem + 128, ahi, bhi, kIdesc, kk > 0 ? 1u : 0u);
+                    mma_bf16(tmem + 128, ahi, blo, kIdesc, 1u);
+                    mma_bf16(tmem + 128, alo, bhi, kIdesc, 1u);
                 }
                 mma_commit(bar_e);
             }
@@ -480,6 +379,171 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
+// prologue on the tensor core: masked Gram from one MMA
+// ---------------------------------------------------------------------------
+constexpr int kPrepThreads = 256;
+constexpr uint32_t kPrepTmemCols = 64;
+constexpr uint32_t kGramIdesc = idesc_bf16(128, 64);   // [Q; K] (128 rows) x K^T (64 keys)
+
+struct PrepTcLayout {
+    // offsets from the 1024-aligned base; the first 64 KiB hold [Q; K] as four
+    // 64-column slabs (rows 0..63 queries, 64..127 keys), 128-byte swizzled
+    int G, A, At, T, pairs, par, anc, la, g, beta, depth, off, bars, misc, total, ld;
+    __host__ __device__ PrepTcLayout(int N) {
+        int o = kSlabs * kBufBytes;
+        auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
+        ld = N + 1;
+        G = take(128 * 65 * 4);          // Gram rows: q_t.k_j (rows 0..63), k_t.k_j (rows 64..127)
+        A = take(N * ld * 4);
+        At = take(N * ld * 4);
+        T = take(N * ld * 4);
+        pairs = take(N * (N + 1) / 2 * 2);
+        par = take(N * 4);
+        anc = take(N * 8);
+        la = take(N * 4);
+        g = take(N * 4);
+        beta = take(N * 4);
+        depth = take(N * 4);
+        off = take((N + 1) * 4);
+        bars = take(16);
+        misc = take(16);
+        total = o + 1024;
+    }
+};
+
+// One CTA per (sequence b, head h).  Q and K of the tree arrive by TMA in the
+// MMA's swizzled layout; one tcgen05 MMA (M = 128 [Q; K] rows, N = 64 keys,
+// K = 256) gives every q_t.k_j and k_t.k_j in TMEM (bf16 products are exact in
+// fp32, accumulation in fp32); the masked entries, the per-node solves and
+// the outputs follow as in the SIMT prologue.  Writes the tensor-core operand
+// form of [T; P].
+__global__ void __launch_bounds__(kPrepThreads, 1)
+    tree_prep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        VerifyArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    unsigned char* base = smem_raw + (base_s - raw_s);
+    const int N = a.N, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const PrepTcLayout Ly(N);
+    const int ld = Ly.ld;
+    float* sG = reinterpret_cast<float*>(base + Ly.G);
+    float* sA = reinterpret_cast<float*>(base + Ly.A);
+    float* sAt = reinterpret_cast<float*>(base + Ly.At);
+    float* sT = reinterpret_cast<float*>(base + Ly.T);
+    uint16_t* pairs = reinterpret_cast<uint16_t*>(base + Ly.pairs);
+    int* par = reinterpret_cast<int*>(base + Ly.par);
+    uint64_t* anc = reinterpret_cast<uint64_t*>(base + Ly.anc);
+    float* la = reinterpret_cast<float*>(base + Ly.la);
+    float* sg = reinterpret_cast<float*>(base + Ly.g);
+    float* sbeta = reinterpret_cast<float*>(base + Ly.beta);
+    int* sdepth = reinterpret_cast<int*>(base + Ly.depth);
+    int* off = reinterpret_cast<int*>(base + Ly.off);
+    const uint32_t bar_tma = base_s + Ly.bars, bar_mma = base_s + Ly.bars + 8;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
+
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H;
+    const WsLayout wl = ws_layout(N);
+    char* rec = a.ws + (size_t)bh * wl.record;
+
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(s_tmem), kPrepTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    // This layer's inputs may come from the previous kernel on the stream.
+    griddep_wait();
+    griddep_launch();
+
+    if (tid == 0) {
+        mbar_expect_tx(bar_tma, (uint32_t)(kSlabs * 2 * kNodeRows * 128));
+#pragma unroll
+        for (int sl = 0; sl < kSlabs; ++sl) {
+            tma_load_3d(base_s + sl * kBufBytes, &tmQ, sl * kSlab, h, b * N, bar_tma);
+            tma_load_3d(base_s + sl * kBufBytes + kNodeRows * 128, &tmK, sl * kSlab, h, b * N, bar_tma);
+        }
+    }
+    bool bad = false;
+    if (tid < N) {
+        const int p = a.parent[(size_t)b * N + tid];
+        bad = p < -1 || p >= tid;
+        par[tid] = p;
+        const size_t gi = ((size_t)b * N + tid) * a.H + h;
+        la[tid] = logf(a.alpha[gi]);
+        sbeta[tid] = a.beta[gi];
+    }
+    bad = __syncthreads_or(bad);
+    bool ok = mbar_wait(bar_tma, 0, a.err);       // the copies land even if the tree is rejected
+    if (bad && tid == 0) {
+        set_error(a.err, GDN_ERR_TREE);
+        *reinterpret_cast<uint64_t*>(rec + wl.anc) = ~0ull;   // record marked invalid
+    }
+    if (!bad) {
+        if (tid == 0 && ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int sl = 0; sl < kSlabs; ++sl)
+#pragma unroll
+                for (int kk = 0; kk < kSlab / 16; ++kk) {
+                    const uint32_t q_s = base_s + sl * kBufBytes + kk * 32;
+                    mma_bf16(tmem, sw128_desc(q_s), sw128_desc(q_s + kNodeRows * 128), kGramIdesc,
+                             (sl > 0 || kk > 0) ? 1u : 0u);
+                }
+            mma_commit(bar_mma);
+        }
+        prep::node_meta(tid, N, par, la, anc, sdepth, sg);
+        __syncthreads();
+        prep::pair_list(tid, N, sdepth, anc, off, pairs);
+        // keys into the factor record, unswizzled from the K half of the operand
+        __nv_bfloat16* key_out = static_cast<__nv_bfloat16*>(a.f.key) + (size_t)bh * N * kDk;
+        for (int item = tid; item < N * kSlabs * 8; item += kPrepThreads) {
+            const int t = item / (kSlabs * 8), sl = (item / 8) % kSlabs, cc = item % 8;
+            const uint4 x = *reinterpret_cast<const uint4*>(base + sl * kBufBytes + (kNodeRows + t) * 128 +
+                                                            ((cc ^ (t & 7)) << 4));
+            *reinterpret_cast<uint4*>(key_out + (size_t)t * kDk + sl * kSlab + cc * 8) = x;
+        }
+        ok = mbar_wait(bar_mma, 0, a.err) && ok;
+        tc_fence_after();
+        if (ok && warp < 4) {                     // TMEM lane = operand row
+            const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16);
+            const int r = 32 * warp + lane;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float gr[32];
+                tmem_ld32(t_lane + 32 * c, gr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sG[r * 65 + 32 * c + i] = gr[i];
+            }
+        }
+        __syncthreads();
+        for (int p = tid; p < off[N]; p += kPrepThreads) {
+            const int pr = pairs[p];
+            const int t = pr >> 8, j = pr & 255;
+            prep::gram_entry(t, j, sG[(kNodeRows + t) * 65 + j], sG[t * 65 + j], ld, sg, sbeta, sA, sAt);
+        }
+        __syncthreads();
+        prep::solve_rows(tid, N, ld, anc, sA, sAt, sT);
+        prep::write_operand(tid, kPrepThreads, N, ld, anc, sA, sT, reinterpret_cast<unsigned char*>(rec + wl.op));
+        prep::write_meta(tid, N, b, h, bh, rec, wl, sg, sbeta, anc, par, a.f);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kPrepTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -519,13 +583,18 @@ bool tc_contract_eligible(const VerifyArgs& a) {
     return encode_fn() != nullptr;
 }
 
-cudaError_t launch_tree_contract_tc(const VerifyArgs& a, cudaStream_t s) {
-    static bool attr[64];
+cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s) {
+    static bool attr_p[64], attr_c[64];
     CUtensorMap tq, tk;
     if (!make_qk_map(&tq, a.q, a.B, a.N, a.H) || !make_qk_map(&tk, a.k, a.B, a.N, a.H))
         return cudaErrorInvalidValue;
+    const PrepTcLayout Lp(a.N);
+    cudaError_t e = ensure_smem(tree_prep_tc_kernel, Lp.total, attr_p);
+    if (e != cudaSuccess) return e;
+    e = launch_kernel(tree_prep_tc_kernel, dim3(a.B * a.H), dim3(kPrepThreads), Lp.total, s, a.overlap, tq, tk, a);
+    if (e != cudaSuccess) return e;
     const TcLayout Ly(a.commit.path ? a.commit.Lmax : 0);
-    cudaError_t e = ensure_smem(tree_contract_tc_kernel, Ly.total, attr);
+    e = ensure_smem(tree_contract_tc_kernel, Ly.total, attr_c);
     if (e != cudaSuccess) return e;
     dim3 grid(a.B * a.H, a.dv / kTileV);
     // always a programmatic dependent of the prologue kernel launched just before it
