@@ -16,11 +16,12 @@
 namespace gdn {
 namespace prep {
 
-// Strict-ancestor masks, depths and cumulative log gates; threads t < N.
-// par, la (log alpha) must be in shared memory.  Ascending bit order walks the
-// path from the root, so g_t sums log alpha root first.
+// Strict-ancestor masks, depths, cumulative log gates and root-first path
+// lists (plist[t * 64 + i] = i-th node of path(t), i = 0..depth(t)); threads
+// t < N.  par, la (log alpha) must be in shared memory.  Ascending bit order
+// walks the path from the root, so g_t sums log alpha root first.
 __device__ __forceinline__ void node_meta(int tid, int N, const int* par, const float* la, uint64_t* anc,
-                                          int* depth, float* g) {
+                                          int* depth, float* g, uint8_t* plist) {
     if (tid < N) {
         uint64_t m = 0;
         int d = 0;
@@ -30,8 +31,15 @@ __device__ __forceinline__ void node_meta(int tid, int N, const int* par, const 
         }
         anc[tid] = m;
         depth[tid] = d;
+        uint8_t* pl = plist + tid * 64;
         float gs = 0.f;
-        for (uint64_t r = m; r; r &= r - 1) gs += la[__ffsll((long long)r) - 1];
+        int i = 0;
+        for (uint64_t r = m; r; r &= r - 1) {
+            const int j = __ffsll((long long)r) - 1;
+            gs += la[j];
+            pl[i++] = (uint8_t)j;
+        }
+        pl[i] = (uint8_t)tid;
         g[tid] = gs + la[tid];
     }
 }
@@ -76,40 +84,130 @@ __device__ __forceinline__ void gram_entry(int t, int j, float kk, float qk, int
 
 // Rows of T = (I + A)^-1, then P = Attn T over A.  The principal block of
 // I + A on path(t) is closed (ancestors of path nodes are on the path), so
-// row t of T is the last row of that block's inverse: x_t = 1 and, walking up
-// the path, x_k = -sum_{i on path(t) below k} x_i A[i, k].  Then
-// P[t, c] = sum_{j on path(t) at or below c} Attn[t, j] T[j, c].  One thread
-// per node, no level barriers.  Call with every thread; contains barriers.
-__device__ __forceinline__ void solve_rows(int tid, int N, int ld, const uint64_t* anc, float* sA,
-                                           const float* sAt, float* sT) {
+// row t of T is the last row of that block's inverse: with the path
+// p_0 (root) .. p_m = t, x_m = 1 and x_k = -sum_{i > k} x_i A[p_i, p_k]
+// (k = m-1 .. 0).  Then P[t, p_k] = sum_{i >= k} Attn[t, p_i] T[p_i, p_k].
+// One thread per node, counted loops over the path list (independent loads),
+// no level barriers.  Call with every thread; contains barriers.
+__device__ __forceinline__ void solve_rows(int tid, int N, int ld, const int* depth, const uint8_t* plist,
+                                           float* sA, const float* sAt, float* sT) {
     if (tid < N) {
-        const int t = tid;
-        const uint64_t path = anc[t] | (1ull << t);
+        const int t = tid, m = depth[t];
+        const uint8_t* p = plist + t * 64;
         float* row = sT + t * ld;
         row[t] = 1.f;
-        for (uint64_t up = anc[t]; up;) {
-            const int kk = 63 - __clzll((long long)up);          // deepest remaining ancestor
-            up &= ~(1ull << kk);
-            float x = 0.f;
-            for (uint64_t below = path & ~((2ull << kk) - 1ull); below; below &= below - 1) {
-                const int i = __ffsll((long long)below) - 1;
-                x = fmaf(row[i], sA[i * ld + kk], x);
+        for (int k = m - 1; k >= 0; --k) {
+            const int pk = p[k];
+            float x0 = 0.f, x1 = 0.f;
+            int i = k + 1;
+            for (; i + 1 <= m; i += 2) {
+                const int a0 = p[i], a1 = p[i + 1];
+                x0 = fmaf(row[a0], sA[a0 * ld + pk], x0);
+                x1 = fmaf(row[a1], sA[a1 * ld + pk], x1);
             }
-            row[kk] = -x;
+            if (i <= m) x0 = fmaf(row[p[i]], sA[p[i] * ld + pk], x0);
+            row[pk] = -(x0 + x1);
         }
     }
     __syncthreads();
     if (tid < N) {
-        const int t = tid;
-        const uint64_t path = anc[t] | (1ull << t);
-        for (uint64_t cs = path; cs; cs &= cs - 1) {
-            const int c = __ffsll((long long)cs) - 1;
-            float x = 0.f;
-            for (uint64_t js = path & ~((1ull << c) - 1ull); js; js &= js - 1) {
-                const int j = __ffsll((long long)js) - 1;
-                x = fmaf(sAt[t * ld + j], sT[j * ld + c], x);
+        const int t = tid, m = depth[t];
+        const uint8_t* p = plist + t * 64;
+        for (int k = 0; k <= m; ++k) {
+            const int pk = p[k];
+            float x0 = 0.f, x1 = 0.f;
+            int i = k;
+            for (; i + 1 <= m; i += 2) {
+                const int a0 = p[i], a1 = p[i + 1];
+                x0 = fmaf(sAt[t * ld + a0], sT[a0 * ld + pk], x0);
+                x1 = fmaf(sAt[t * ld + a1], sT[a1 * ld + pk], x1);
             }
-            sA[t * ld + c] = x;   // A is no longer read: step one finished behind the barrier
+            if (i <= m) x0 = fmaf(sAt[t * ld + p[i]], sT[p[i] * ld + pk], x0);
+            sA[t * ld + pk] = x0 + x1;   // A is no longer read: step one finished behind the barrier
+        }
+    }
+    __syncthreads();
+}
+
+// Row t's A and Attn entries from its Gram rows: qk[j] = q_t.k_j, kk[j] = k_t.k_j
+// (row pointers into a Gram table), for j on path(t).  One thread per node.
+__device__ __forceinline__ void gram_row(int t, int m, const uint8_t* plist, const float* qk, const float* kk,
+                                         int ld, const float* g, const float* beta, float* sA, float* sAt) {
+    const uint8_t* p = plist + t * 64;
+    const float gt = g[t], bt = beta[t];
+    for (int i = 0; i <= m; ++i) {
+        const int j = p[i];
+        const float gam = expf(gt - g[j]);
+        sAt[t * ld + j] = gam * qk[j];
+        if (j != t) sA[t * ld + j] = bt * gam * kk[j];
+    }
+}
+
+// solve_rows with the path held in registers: q_0 = t, q_1 = parent, ..., q_m
+// = root.  Row t of T: x_0 = 1, x_i = -sum_{j < i} x_j A[q_j, q_i]; row t of
+// P: P[t, q_i] = sum_{j <= i} Attn[t, q_j] T[q_j, q_i].  Fully unrolled for
+// depth < kRegDepth (independent shared-memory loads), the generic loops of
+// solve_rows otherwise.  Call with every thread; contains barriers.
+constexpr int kRegDepth = 12;
+
+__device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const int* depth, const uint8_t* plist,
+                                                float* sA, const float* sAt, float* sT) {
+    const int t = tid;
+    const int m = tid < N ? depth[t] : 0;
+    const bool fast = tid < N && m < kRegDepth;
+    int q[kRegDepth];
+    float x[kRegDepth];
+    if (fast) {
+        const uint8_t* p = plist + t * 64;
+#pragma unroll
+        for (int i = 0; i < kRegDepth; ++i) q[i] = i <= m ? p[m - i] : t;
+        x[0] = 1.f;
+#pragma unroll
+        for (int i = 1; i < kRegDepth; ++i) {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < i; j += 2) {
+                s0 = fmaf(x[j], sA[q[j] * ld + q[i]], s0);
+                if (j + 1 < i) s1 = fmaf(x[j + 1], sA[q[j + 1] * ld + q[i]], s1);
+            }
+            x[i] = i <= m ? -(s0 + s1) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kRegDepth; ++i)
+            if (i <= m) sT[t * ld + q[i]] = x[i];
+    } else if (tid < N) {
+        const uint8_t* p = plist + t * 64;
+        float* row = sT + t * ld;
+        row[t] = 1.f;
+        for (int k = m - 1; k >= 0; --k) {
+            const int pk = p[k];
+            float x0 = 0.f;
+            for (int i = k + 1; i <= m; ++i) x0 = fmaf(row[p[i]], sA[p[i] * ld + pk], x0);
+            row[pk] = -x0;
+        }
+    }
+    __syncthreads();
+    if (fast) {
+        float at[kRegDepth];
+#pragma unroll
+        for (int j = 0; j < kRegDepth; ++j) at[j] = j <= m ? sAt[t * ld + q[j]] : 0.f;
+#pragma unroll
+        for (int i = 0; i < kRegDepth; ++i) {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int j = 0; j <= i; j += 2) {
+                s0 = fmaf(at[j], sT[q[j] * ld + q[i]], s0);
+                if (j + 1 <= i) s1 = fmaf(at[j + 1], sT[q[j + 1] * ld + q[i]], s1);
+            }
+            if (i <= m) sA[t * ld + q[i]] = s0 + s1;
+        }
+    } else if (tid < N) {
+        const uint8_t* p = plist + t * 64;
+        for (int k = 0; k <= m; ++k) {
+            const int pk = p[k];
+            float x0 = 0.f;
+            for (int i = k; i <= m; ++i) x0 = fmaf(sAt[t * ld + p[i]], sT[p[i] * ld + pk], x0);
+            sA[t * ld + pk] = x0;
         }
     }
     __syncthreads();

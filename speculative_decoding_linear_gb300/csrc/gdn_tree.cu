@@ -99,7 +99,7 @@ __global__ void tree_mask_kernel(const int32_t* parent, int N, uint64_t* mask, i
 constexpr int kPrepThreads = 256;
 
 struct PrepLayout {
-    int qs, ks, A, At, T, pairs, par, anc, la, g, beta, depth, off, misc, total, ld;
+    int qs, ks, A, At, T, pairs, plist, par, anc, la, g, beta, depth, off, misc, total, ld;
     __host__ __device__ PrepLayout(int N, int dk, int esz) {
         int o = 0;
         auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
@@ -110,6 +110,7 @@ struct PrepLayout {
         At = take(N * ld * 4);
         T = take(N * ld * 4);
         pairs = take(N * (N + 1) / 2 * 2);
+        plist = take(N * 64);
         par = take(N * 4);
         anc = take(N * 8);
         la = take(N * 4);
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
     float* sAt = reinterpret_cast<float*>(smem + Ly.At);
     float* sT = reinterpret_cast<float*>(smem + Ly.T);
     uint16_t* pairs = reinterpret_cast<uint16_t*>(smem + Ly.pairs);
+    uint8_t* plist = reinterpret_cast<uint8_t*>(smem + Ly.plist);
     int* par = reinterpret_cast<int*>(smem + Ly.par);
     uint64_t* anc = reinterpret_cast<uint64_t*>(smem + Ly.anc);
     float* la = reinterpret_cast<float*>(smem + Ly.la);
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
     }
 
     // 2. masks, depths, gates; 3. (t, j on path(t)) pairs
-    prep::node_meta(tid, N, par, la, anc, sdepth, sg);
+    prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
     __syncthreads();
     prep::pair_list(tid, N, sdepth, anc, off, pairs);
 
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
     __syncthreads();
 
     // 5-6. rows of T, then P over A; workspace and factor records
-    prep::solve_rows(tid, N, ld, anc, sA, sAt, sT);
+    prep::solve_rows(tid, N, ld, sdepth, plist, sA, sAt, sT);
     prep::write_dense(tid, kPrepThreads, N, ld, anc, sA, sT, reinterpret_cast<float*>(rec + wl.T),
                       reinterpret_cast<float*>(rec + wl.P));
     prep::write_meta(tid, N, b, h, bh, rec, wl, sg, sbeta, anc, par, a.f);

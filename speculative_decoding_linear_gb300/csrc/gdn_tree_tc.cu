@@ -61,7 +61,7 @@ constexpr uint32_t kIdesc = idesc_bf16(128, 128);   // D fp32, A/B bf16 K-major,
 
 struct TcLayout {
     // offsets from the 1024-aligned base
-    int cd, key, coef, nodes, bars, misc, total;
+    int cd, key, coef, nodes, bars, misc, egbt, total;
     __host__ __device__ TcLayout(int Lcap) {
         int o = 2 * kStageBytes;
         auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
@@ -71,9 +71,90 @@ struct TcLayout {
         nodes = take(kMaxPath * 4);
         bars = take(64);
         misc = take(16);
+        egbt = take(2 * kNodeRows * 4);
         total = o + 1024;   // slack for aligning the base to 1024 bytes
     }
 };
+
+// One state slab (this thread's 8 float4 of a 128 x 64 fp32 block) and its
+// conversion to the bf16 hi/lo A-operand buffers of one stage.
+__device__ __forceinline__ void load_slab(float4 (&x)[8], const float* S, size_t srow0, int rbase, int col) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        x[j] = *reinterpret_cast<const float4*>(S + srow0 + (size_t)(rbase + 16 * j) * kDk + col);
+}
+
+// S <- e^{g_a} S + sum_i cd_i[row] k_i[col..col+3], path node outermost (one key
+// quad per node serves the thread's 8 rows); per element the same order of
+// operations as commit_quad, so the result is bit-identical to gdn_commit.
+__device__ __forceinline__ void commit_slab(float4 (&x)[8], float ega, int L, const float* s_cd,
+                                            const __nv_bfloat16* s_key, int rbase, int col) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        x[j].x *= ega;
+        x[j].y *= ega;
+        x[j].z *= ega;
+        x[j].w *= ega;
+    }
+    for (int i = 0; i < L; ++i) {
+        const float4 kq = ld4<__nv_bfloat16>(s_key, (size_t)i * kDk + col);
+        const float* cdi = s_cd + i * kTileV + rbase;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float w = cdi[16 * j];
+            x[j].x = fmaf(w, kq.x, x[j].x);
+            x[j].y = fmaf(w, kq.y, x[j].y);
+            x[j].z = fmaf(w, kq.z, x[j].z);
+            x[j].w = fmaf(w, kq.w, x[j].w);
+        }
+    }
+}
+
+__device__ __forceinline__ void store_slab(const float4 (&x)[8], float* S, size_t srow0, int rbase, int col) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(S + srow0 + (size_t)(rbase + 16 * j) * kDk + col) = x[j];
+}
+
+// hi = bf16(x), lo = bf16(x - hi), stored to the stage's swizzled K-major buffers.
+__device__ __forceinline__ void convert_slab(const float4 (&x)[8], unsigned char* ahi, int rbase, int c4) {
+    unsigned char* alo = ahi + kBufBytes;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int r = rbase + 16 * j;
+        const float4 v = x[j];
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        uint2 hi, lo;
+        hi.x = *reinterpret_cast<const uint32_t*>(&h01);
+        hi.y = *reinterpret_cast<const uint32_t*>(&h23);
+        lo.x = pack_bf16(v.x - f01.x, v.y - f01.y);
+        lo.y = pack_bf16(v.z - f23.x, v.w - f23.y);
+        const uint32_t off = sw128_quad(r, c4);
+        *reinterpret_cast<uint2*>(ahi + off) = hi;
+        *reinterpret_cast<uint2*>(alo + off) = lo;
+    }
+}
+
+// Four K-steps of one slab, hi and lo terms, into the Y accumulator.
+__device__ __forceinline__ void issue_slab_mma(uint32_t tmem, uint32_t stage_s, bool first) {
+    const uint32_t a_hi = stage_s, a_lo = stage_s + kBufBytes, bsm = stage_s + 2 * kBufBytes;
+#pragma unroll
+    for (int kk = 0; kk < kSlab / 16; ++kk) {
+        const uint64_t bd = sw128_desc(bsm + kk * 32);
+        mma_bf16(tmem, sw128_desc(a_hi + kk * 32), bd, kIdesc, (!first || kk > 0) ? 1u : 0u);
+        mma_bf16(tmem, sw128_desc(a_lo + kk * 32), bd, kIdesc, 1u);
+    }
+}
+
+__device__ __forceinline__ void issue_qk_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint32_t stage_s,
+                                             int ks, int h, int row0, uint32_t bar) {
+    const uint32_t bsm = stage_s + 2 * kBufBytes;
+    mbar_expect_tx(bar, 2 * kNodeRows * 128);
+    tma_load_3d(bsm, tmQ, ks * kSlab, h, row0, bar);
+    tma_load_3d(bsm + kNodeRows * 128, tmK, ks * kSlab, h, row0, bar);
+}
 
 __global__ void __launch_bounds__(kThreads, 2)
     tree_contract_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -96,10 +177,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     float* s_coef = reinterpret_cast<float*>(base + Ly.coef);
     int* s_nodes = reinterpret_cast<int*>(base + Ly.nodes);
     const uint32_t bar_tma0 = base_s + Ly.bars, bar_mma0 = base_s + Ly.bars + 16;
-    const uint32_t bar_op = base_s + Ly.bars + 32, bar_e = base_s + Ly.bars + 40;
+    const uint32_t bar_op = base_s + Ly.bars + 32, bar_e = base_s + Ly.bars + 40, bar_eg = base_s + Ly.bars + 48;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
     float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 4);
     int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 8);   // path length, or -1: skip the CTA
+    float* seg = reinterpret_cast<float*>(base + Ly.egbt);
+    float* sbt = seg + kNodeRows;
+    const uint32_t stage0 = base_s, stage1 = base_s + kStageBytes;
 
     if (tid == 0) {
         mbar_init(bar_tma0, 1);
@@ -108,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_init(bar_mma0 + 8, 1);
         mbar_init(bar_op, 1);
         mbar_init(bar_e, 1);
+        mbar_init(bar_eg, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         fence_proxy_async_smem();
         *s_flag = 0;
@@ -119,14 +204,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    // ---- 1. reads only: pending commit's factor rows, first state slab ----
+    // ---- 1. the state tile, before the wait: the whole HBM stream of this CTA ----
+    // (Only this call's prologue kernel runs before the wait releases, and it
+    // touches neither S nor the previous factors; every kernel before it has
+    // completed.  So the committed state may be written here.)
     const size_t srow0 = ((size_t)bh * dv + v0) * kDk;
     const int c4 = tid & 15;         // column quad within a slab
     const int rbase = tid >> 4;      // rows rbase + 16 j, j = 0..7
-    float4 xa[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        xa[j] = *reinterpret_cast<const float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk + 4 * c4);
+    if (tid < 8) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * 16 * kDk, 16 * kDk * 4);
+    float4 x0[8], x1[8];
+    load_slab(x0, a.S, srow0, rbase, 4 * c4);
     if (fused) {
         if (warp == 2) {
             const int L = commit_path_setup(a.commit, b, h, a.H, s_nodes, s_coef, s_ega);
@@ -153,170 +240,142 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();
     const int L = fused ? *s_flag : 0;
+    const bool commit_ok = L >= 0;
     const float ega = *s_ega;
+    // slabs 0 and 1 -> stage buffers; committed slabs 2 and 3 stay in registers
+    float4 x2[8], x3[8];
+    load_slab(x1, a.S, srow0, rbase, kSlab + 4 * c4);
+    if (fused && commit_ok) {
+        commit_slab(x0, ega, L, s_cd, s_key, rbase, 4 * c4);
+        store_slab(x0, a.S, srow0, rbase, 4 * c4);
+    }
+    convert_slab(x0, base, rbase, c4);
+    load_slab(x2, a.S, srow0, rbase, 2 * kSlab + 4 * c4);
+    if (fused && commit_ok) {
+        commit_slab(x1, ega, L, s_cd, s_key, rbase, kSlab + 4 * c4);
+        store_slab(x1, a.S, srow0, rbase, kSlab + 4 * c4);
+    }
+    convert_slab(x1, base + kStageBytes, rbase, c4);
+    load_slab(x3, a.S, srow0, rbase, 3 * kSlab + 4 * c4);
+    if (fused && commit_ok) {
+        commit_slab(x2, ega, L, s_cd, s_key, rbase, 2 * kSlab + 4 * c4);
+        store_slab(x2, a.S, srow0, rbase, 2 * kSlab + 4 * c4);
+        commit_slab(x3, ega, L, s_cd, s_key, rbase, 3 * kSlab + 4 * c4);
+        store_slab(x3, a.S, srow0, rbase, 3 * kSlab + 4 * c4);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
 
-    // ---- 2. wait for the prologue kernel (and this layer's q/k) ----
+    // ---- 2. wait for the prologue kernel (and this layer's q/k/v) ----
     griddep_wait();
     griddep_launch();
     const WsLayout wl = ws_layout(N);
     const char* rec = a.ws + (size_t)bh * wl.record;
-    const bool run = L >= 0 && *reinterpret_cast<const uint64_t*>(rec + wl.anc) != ~0ull;
+    const bool run = commit_ok && *reinterpret_cast<const uint64_t*>(rec + wl.anc) != ~0ull;
     bool ok = run;
 
     if (run) {
         if (tid == 0) {
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                const uint32_t bsm = base_s + s * kStageBytes + 2 * kBufBytes;
-                mbar_expect_tx(bar_tma0 + 8 * s, 2 * kNodeRows * 128);
-                tma_load_3d(bsm, &tmQ, s * kSlab, h, b * N, bar_tma0 + 8 * s);
-                tma_load_3d(bsm + kNodeRows * 128, &tmK, s * kSlab, h, b * N, bar_tma0 + 8 * s);
+            issue_qk_tma(&tmQ, &tmK, stage0, 0, h, b * N, bar_tma0);
+            issue_qk_tma(&tmQ, &tmK, stage1, 1, h, b * N, bar_tma0 + 8);
+            mbar_expect_tx(bar_eg, 2 * kNodeRows * 4);
+            bulk_copy_g2s(smem_u32(seg), rec + wl.eg, kNodeRows * 4, bar_eg);
+            bulk_copy_g2s(smem_u32(sbt), rec + wl.bt, kNodeRows * 4, bar_eg);
+            ok = mbar_wait(bar_tma0, 0, a.err);
+            if (ok) {
+                tc_fence_after();
+                issue_slab_mma(tmem, stage0, true);
+                mma_commit(bar_mma0);
+                ok = mbar_wait(bar_tma0 + 8, 0, a.err);
+            }
+            if (ok) {
+                tc_fence_after();
+                issue_slab_mma(tmem, stage1, false);
+                mma_commit(bar_mma0 + 8);
             }
         }
-#pragma unroll 1
-        for (int ks = 0; ks < kSlabs; ++ks) {
-            const int s = ks & 1;
-            float4 x[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) x[j] = xa[j];
-            if (ks + 1 < kSlabs) {      // next slab in flight while this one is processed
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    xa[j] = *reinterpret_cast<const float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk +
-                                                            (ks + 1) * kSlab + 4 * c4);
-            }
-            if (ks >= 2) {              // stage s is free once slab ks-2's MMAs are done
-                ok = mbar_wait(bar_mma0 + 8 * s, 0, a.err) && ok;
-                if (tid == 0 && ok) {
-                    const uint32_t bsm = base_s + s * kStageBytes + 2 * kBufBytes;
-                    mbar_expect_tx(bar_tma0 + 8 * s, 2 * kNodeRows * 128);
-                    tma_load_3d(bsm, &tmQ, ks * kSlab, h, b * N, bar_tma0 + 8 * s);
-                    tma_load_3d(bsm + kNodeRows * 128, &tmK, ks * kSlab, h, b * N, bar_tma0 + 8 * s);
-                }
-            }
-            const int col = ks * kSlab + 4 * c4;
-            if (fused) {
-                // S <- e^{g_a} S + sum_i cd_i[row] k_i[col..col+3], path node outermost: one
-                // key quad per node serves this thread's 8 rows (same order of operations
-                // per element as commit_quad, so the result is bit-identical to gdn_commit)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    x[j].x *= ega;
-                    x[j].y *= ega;
-                    x[j].z *= ega;
-                    x[j].w *= ega;
-                }
-                for (int i = 0; i < L; ++i) {
-                    const float4 kq = ld4<__nv_bfloat16>(s_key, (size_t)i * kDk + col);
-                    const float* cdi = s_cd + i * kTileV + rbase;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float w = cdi[16 * j];
-                        x[j].x = fmaf(w, kq.x, x[j].x);
-                        x[j].y = fmaf(w, kq.y, x[j].y);
-                        x[j].z = fmaf(w, kq.z, x[j].z);
-                        x[j].w = fmaf(w, kq.w, x[j].w);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<float4*>(a.S + srow0 + (size_t)(rbase + 16 * j) * kDk + col) = x[j];
-            }
-            unsigned char* ahi = base + s * kStageBytes;
-            unsigned char* alo = ahi + kBufBytes;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int r = rbase + 16 * j;
-                const float4 v = x[j];
-                const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
-                const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
-                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-                uint2 hi, lo;
-                hi.x = *reinterpret_cast<const uint32_t*>(&h01);
-                hi.y = *reinterpret_cast<const uint32_t*>(&h23);
-                lo.x = pack_bf16(v.x - f01.x, v.y - f01.y);
-                lo.y = pack_bf16(v.z - f23.x, v.w - f23.y);
-                const uint32_t off = sw128_quad(r, c4);
-                *reinterpret_cast<uint2*>(ahi + off) = hi;
-                *reinterpret_cast<uint2*>(alo + off) = lo;
-            }
-            fence_proxy_async_smem();
-            __syncthreads();
-            if (tid == 0 && ok) {
-                ok = mbar_wait(bar_tma0 + 8 * s, (ks >> 1) & 1, a.err);
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t a_hi = base_s + s * kStageBytes;
-                    const uint32_t a_lo = a_hi + kBufBytes;
-                    const uint32_t bsm = a_hi + 2 * kBufBytes;
-#pragma unroll
-                    for (int kk = 0; kk < kSlab / 16; ++kk) {
-                        const uint64_t bd = sw128_desc(bsm + kk * 32);
-                        mma_bf16(tmem, sw128_desc(a_hi + kk * 32), bd, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
-                        mma_bf16(tmem, sw128_desc(a_lo + kk * 32), bd, kIdesc, 1u);
-                    }
-                    mma_commit(bar_mma0 + 8 * s);
-                }
+        // slabs 2 and 3 reuse the stages once the MMAs of slabs 0 and 1 are done
+        ok = mbar_wait(bar_mma0, 0, a.err) && ok;
+        if (tid == 0 && ok) issue_qk_tma(&tmQ, &tmK, stage0, 2, h, b * N, bar_tma0);
+        convert_slab(x2, base, rbase, c4);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            ok = mbar_wait(bar_tma0, 1, a.err);
+            if (ok) {
+                tc_fence_after();
+                issue_slab_mma(tmem, stage0, false);
+                mma_commit(bar_mma0);
             }
         }
-        // Stage 0 is free once slab kSlabs-2 is done: bring the [T; P] operand (bf16 hi, lo)
-        // into its A buffers with one bulk copy, e^g and beta into its B buffer.
+        ok = mbar_wait(bar_mma0 + 8, 0, a.err) && ok;
+        if (tid == 0 && ok) issue_qk_tma(&tmQ, &tmK, stage1, 3, h, b * N, bar_tma0 + 8);
+        convert_slab(x3, base + kStageBytes, rbase, c4);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0 && ok) {
+            ok = mbar_wait(bar_tma0 + 8, 1, a.err);
+            if (ok) {
+                tc_fence_after();
+                issue_slab_mma(tmem, stage1, false);
+                mma_commit(bar_mma0 + 8);
+            }
+        }
+
+        // Stage 0 is free once slab 2 is done: the [T; P] operand (bf16 hi, lo) into its
+        // A buffers and this tile's v rows into its B buffer, by bulk copies.
         ok = __syncthreads_and(ok);
         if (ok) ok = mbar_wait(bar_mma0, 1, a.err);
-        const uint32_t op_s = base_s;                                  // B2: hi, then lo (16 KiB each)
-        const uint32_t r_s = base_s + kStageBytes;                     // A2: R hi, then lo (stage 1)
-        float* seg = reinterpret_cast<float*>(base + 2 * kBufBytes);
-        float* sbt = seg + kNodeRows;
-        if (ok && tid == 0) {
-            mbar_expect_tx(bar_op, (uint32_t)kTcOperandBytes);
-            bulk_copy_g2s(op_s, rec + wl.op, (uint32_t)kTcOperandBytes, bar_op);
-        }
-        if (ok && tid < kNodeRows) {
-            seg[tid] = tid < N ? reinterpret_cast<const float*>(rec + wl.eg)[tid] : 0.f;
-            sbt[tid] = tid < N ? reinterpret_cast<const float*>(rec + wl.bt)[tid] : 0.f;
+        const uint32_t op_s = stage0;                                  // B2: hi, then lo (16 KiB each)
+        const uint32_t r_s = stage1;                                   // A2: R hi, then lo (stage 1)
+        const uint32_t v_s = stage0 + 2 * kBufBytes;                   // v rows: [t][128] bf16
+        if (ok && warp == 0) {
+            if (lane == 0) {
+                mbar_expect_tx(bar_op, (uint32_t)(kTcOperandBytes + N * kTileV * 2));
+                bulk_copy_g2s(op_s, rec + wl.op, (uint32_t)kTcOperandBytes, bar_op);
+            }
+            __syncwarp();
+            const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(a.v);
+            for (int t = lane; t < N; t += 32)
+                bulk_copy_g2s(v_s + t * kTileV * 2, vv + (((size_t)b * N + t) * a.H + h) * dv + v0,
+                              kTileV * 2, bar_op);
         }
         if (ok) ok = mbar_wait(bar_mma0 + 8, 1, a.err);                // Y complete
+        if (ok) ok = mbar_wait(bar_op, 0, a.err);                      // operand and v rows landed
+        if (ok) ok = mbar_wait(bar_eg, 0, a.err);                      // e^g and beta landed
         ok = __syncthreads_and(ok);
         tc_fence_after();
 
         const int v = 32 * (warp & 3) + lane;            // state row of this thread (TMEM lane)
         const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(a.v);
-        if (ok && warp < 4) {
-            // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N), stored as bf16 hi + lo
-            // rows of the second MMA's A operand (row v, 64 columns t)
+        const __nv_bfloat16* vsm = reinterpret_cast<const __nv_bfloat16*>(base + 2 * kBufBytes);
+        if (ok) {
+            // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) as bf16 hi + lo rows of
+            // the second MMA's A operand (row v, 64 columns t); warps 0-3 take t < 32, warps 4-7 the rest
             unsigned char* rhi = base + kStageBytes;
             unsigned char* rlo = rhi + kBufBytes;
+            const int c = warp >> 2;
+            float yk[32];
+            tmem_ld32(t_lane + kNodeRows + 32 * c, yk);
 #pragma unroll
-            for (int c = 0; c < kNodeRows / 32; ++c) {
-                float vin[32];
+            for (int q8 = 0; q8 < 4; ++q8) {
+                uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * c + i;
-                    vin[i] = t < N ? __bfloat162float(vv[(((size_t)b * N + t) * a.H + h) * dv + v0 + v]) : 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    const int i0 = 8 * q8 + 2 * e, i1 = i0 + 1;
+                    const int t0 = 32 * c + i0, t1 = t0 + 1;
+                    const float r0 = t0 < N ? sbt[t0] * (__bfloat162float(vsm[t0 * kTileV + v]) - seg[t0] * yk[i0]) : 0.f;
+                    const float r1 = t1 < N ? sbt[t1] * (__bfloat162float(vsm[t1 * kTileV + v]) - seg[t1] * yk[i1]) : 0.f;
+                    const __nv_bfloat162 hh = __floats2bfloat162_rn(r0, r1);
+                    const float2 hf = __bfloat1622float2(hh);
+                    const __nv_bfloat162 ll = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
+                    hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                    lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
                 }
-                float yk[32];
-                tmem_ld32(t_lane + kNodeRows + 32 * c, yk);
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i0 = 8 * q8 + 2 * e, i1 = i0 + 1;
-                        const int t0 = 32 * c + i0, t1 = t0 + 1;
-                        const float r0 = t0 < N ? sbt[t0] * (vin[i0] - seg[t0] * yk[i0]) : 0.f;
-                        const float r1 = t1 < N ? sbt[t1] * (vin[i1] - seg[t1] * yk[i1]) : 0.f;
-                        const __nv_bfloat162 hh = __floats2bfloat162_rn(r0, r1);
-                        const float2 hf = __bfloat1622float2(hh);
-                        const __nv_bfloat162 ll = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
-                        hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
-                        lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
-                    }
-                    const int cc = 4 * c + q8;                           // 16-byte chunk = 8 nodes
-                    const uint32_t off = (uint32_t)(v * 128 + ((cc ^ (v & 7)) << 4));
-                    *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(rlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
+                const int cc = 4 * c + q8;                           // 16-byte chunk = 8 nodes
+                const uint32_t off = (uint32_t)(v * 128 + ((cc ^ (v & 7)) << 4));
+                *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(rlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
         fence_proxy_async_smem();
@@ -324,18 +383,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         if (tid == 0 && ok) {
             // [Delta | P R] (v, t) = sum_j R[v, j] [T; P](t, j): three bf16 terms (hi.hi, hi.lo, lo.hi)
-            if (mbar_wait(bar_op, 0, a.err)) {
-                tc_fence_after();
+            tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kNodeRows / 16; ++kk) {
-                    const uint64_t ahi = sw128_desc(r_s + kk * 32), alo = sw128_desc(r_s + kBufBytes + kk * 32);
-                    const uint64_t bhi = sw128_desc(op_s + kk * 32), blo = sw128_desc(op_s + kBufBytes + kk * 32);
-                    mma_bf16(tmem + 128, ahi, bhi, kIdesc, kk > 0 ? 1u : 0u);
-                    mma_bf16(tmem + 128, ahi, blo, kIdesc, 1u);
-                    mma_bf16(tmem + 128, alo, bhi, kIdesc, 1u);
-                }
-                mma_commit(bar_e);
+            for (int kk = 0; kk < kNodeRows / 16; ++kk) {
+                const uint64_t ahi = sw128_desc(r_s + kk * 32), alo = sw128_desc(r_s + kBufBytes + kk * 32);
+                const uint64_t bhi = sw128_desc(op_s + kk * 32), blo = sw128_desc(op_s + kBufBytes + kk * 32);
+                mma_bf16(tmem + 128, ahi, bhi, kIdesc, kk > 0 ? 1u : 0u);
+                mma_bf16(tmem + 128, ahi, blo, kIdesc, 1u);
+                mma_bf16(tmem + 128, alo, bhi, kIdesc, 1u);
             }
+            mma_commit(bar_e);
         }
         if (ok) ok = mbar_wait(bar_e, 0, a.err);
         tc_fence_after();
@@ -387,24 +444,26 @@ constexpr uint32_t kGramIdesc = idesc_bf16(128, 64);   // [Q; K] (128 rows) x K^
 
 struct PrepTcLayout {
     // offsets from the 1024-aligned base; the first 64 KiB hold [Q; K] as four
-    // 64-column slabs (rows 0..63 queries, 64..127 keys), 128-byte swizzled
-    int G, A, At, T, pairs, par, anc, la, g, beta, depth, off, bars, misc, total, ld;
+    // 64-column slabs (rows 0..63 queries, 64..127 keys), 128-byte swizzled.
+    // Once the Gram MMA has consumed them and the keys are copied out, the
+    // A, Attn and T tables reuse that space.
+    int G, A, At, T, plist, par, anc, la, g, beta, depth, bars, misc, total, ld;
     __host__ __device__ PrepTcLayout(int N) {
-        int o = kSlabs * kBufBytes;
-        auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
         ld = N + 1;
-        G = take(128 * 65 * 4);          // Gram rows: q_t.k_j (rows 0..63), k_t.k_j (rows 64..127)
+        int o = 0;
+        auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
         A = take(N * ld * 4);
         At = take(N * ld * 4);
         T = take(N * ld * 4);
-        pairs = take(N * (N + 1) / 2 * 2);
+        o = kSlabs * kBufBytes;
+        G = take(128 * 65 * 4);          // Gram rows: q_t.k_j (rows 0..63), k_t.k_j (rows 64..127)
+        plist = take(N * 64);
         par = take(N * 4);
         anc = take(N * 8);
         la = take(N * 4);
         g = take(N * 4);
         beta = take(N * 4);
         depth = take(N * 4);
-        off = take((N + 1) * 4);
         bars = take(16);
         misc = take(16);
         total = o + 1024;
@@ -417,7 +476,9 @@ struct PrepTcLayout {
 // fp32, accumulation in fp32); the masked entries, the per-node solves and
 // the outputs follow as in the SIMT prologue.  Writes the tensor-core operand
 // form of [T; P].
-__global__ void __launch_bounds__(kPrepThreads, 1)
+// At most 128 registers per thread, so that a prologue CTA and a contraction
+// CTA (of the previous or the same call) fit on one SM together.
+__global__ void __launch_bounds__(kPrepThreads, 2)
     tree_prep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         VerifyArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -431,14 +492,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     float* sA = reinterpret_cast<float*>(base + Ly.A);
     float* sAt = reinterpret_cast<float*>(base + Ly.At);
     float* sT = reinterpret_cast<float*>(base + Ly.T);
-    uint16_t* pairs = reinterpret_cast<uint16_t*>(base + Ly.pairs);
+    uint8_t* plist = reinterpret_cast<uint8_t*>(base + Ly.plist);
     int* par = reinterpret_cast<int*>(base + Ly.par);
     uint64_t* anc = reinterpret_cast<uint64_t*>(base + Ly.anc);
     float* la = reinterpret_cast<float*>(base + Ly.la);
     float* sg = reinterpret_cast<float*>(base + Ly.g);
     float* sbeta = reinterpret_cast<float*>(base + Ly.beta);
     int* sdepth = reinterpret_cast<int*>(base + Ly.depth);
-    int* off = reinterpret_cast<int*>(base + Ly.off);
     const uint32_t bar_tma = base_s + Ly.bars, bar_mma = base_s + Ly.bars + 8;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
 
@@ -487,7 +547,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         *reinterpret_cast<uint64_t*>(rec + wl.anc) = ~0ull;   // record marked invalid
     }
     if (!bad) {
-        if (tid == 0 && ok) {
+        if (tid == 128 && ok) {                  // a warp with no per-node work issues the Gram MMA
             tc_fence_after();
 #pragma unroll
             for (int sl = 0; sl < kSlabs; ++sl)
@@ -499,16 +559,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 }
             mma_commit(bar_mma);
         }
-        prep::node_meta(tid, N, par, la, anc, sdepth, sg);
-        __syncthreads();
-        prep::pair_list(tid, N, sdepth, anc, off, pairs);
-        // keys into the factor record, unswizzled from the K half of the operand
-        __nv_bfloat16* key_out = static_cast<__nv_bfloat16*>(a.f.key) + (size_t)bh * N * kDk;
-        for (int item = tid; item < N * kSlabs * 8; item += kPrepThreads) {
-            const int t = item / (kSlabs * 8), sl = (item / 8) % kSlabs, cc = item % 8;
-            const uint4 x = *reinterpret_cast<const uint4*>(base + sl * kBufBytes + (kNodeRows + t) * 128 +
-                                                            ((cc ^ (t & 7)) << 4));
-            *reinterpret_cast<uint4*>(key_out + (size_t)t * kDk + sl * kSlab + cc * 8) = x;
+        if (tid < N) {
+            prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
+        } else {
+            // keys into the factor record, unswizzled from the K half of the operand
+            __nv_bfloat16* key_out = static_cast<__nv_bfloat16*>(a.f.key) + (size_t)bh * N * kDk;
+            for (int item = tid - N; item < N * kSlabs * 8; item += kPrepThreads - N) {
+                const int t = item / (kSlabs * 8), sl = (item / 8) % kSlabs, cc = item % 8;
+                const uint4 x = *reinterpret_cast<const uint4*>(base + sl * kBufBytes + (kNodeRows + t) * 128 +
+                                                                ((cc ^ (t & 7)) << 4));
+                *reinterpret_cast<uint4*>(key_out + (size_t)t * kDk + sl * kSlab + cc * 8) = x;
+            }
         }
         ok = mbar_wait(bar_mma, 0, a.err) && ok;
         tc_fence_after();
@@ -523,14 +584,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 for (int i = 0; i < 32; ++i) sG[r * 65 + 32 * c + i] = gr[i];
             }
         }
+        __syncthreads();                          // [Q; K] consumed: A, Attn, T reuse its space
+        if (tid < N)
+            prep::gram_row(tid, sdepth[tid], plist, sG + tid * 65, sG + (kNodeRows + tid) * 65, ld, sg, sbeta,
+                           sA, sAt);
         __syncthreads();
-        for (int p = tid; p < off[N]; p += kPrepThreads) {
-            const int pr = pairs[p];
-            const int t = pr >> 8, j = pr & 255;
-            prep::gram_entry(t, j, sG[(kNodeRows + t) * 65 + j], sG[t * 65 + j], ld, sg, sbeta, sA, sAt);
-        }
-        __syncthreads();
-        prep::solve_rows(tid, N, ld, anc, sA, sAt, sT);
+        prep::solve_rows_fast(tid, N, ld, sdepth, plist, sA, sAt, sT);
         prep::write_operand(tid, kPrepThreads, N, ld, anc, sA, sT, reinterpret_cast<unsigned char*>(rec + wl.op));
         prep::write_meta(tid, N, b, h, bh, rec, wl, sg, sbeta, anc, par, a.f);
     }
