@@ -166,7 +166,7 @@ def first_verify(gdnspec, ly, chain):
                                 ly.ws)
 
 
-def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=False, batch=None):
+def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=False, batch=None, layers=None):
     from speculative_decoding_linear_gb300 import gdnspec
     from speculative_decoding_linear_gb300 import workloads as wl
 
@@ -180,7 +180,7 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
     probe = Layer(wl.make_workload(cfg, B=batch), device, torch, gdnspec)
     per_layer = probe.nbytes()
     del probe
-    R = max(2, -(-4 * l2 // per_layer))
+    R = max(2, -(-4 * l2 // per_layer)) if layers is None else max(2, layers)
     layers = make_layers(cfg, R, 1000 * (rank + 1) + cfg, device, torch, gdnspec, wl, batch)
     footprint = sum(ly.nbytes() for ly in layers)
 
@@ -261,7 +261,7 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
                   "frac": round(achieved / peak, 4), "traffic": None,
                   "peak_kind": peak_kind + " hbm_gbs (copy)",
                   "kernel": "gdn_commit_chain_verify (chain_kernel)" if chain else
-                            "gdn_commit_tree_verify (tree_prep_kernel + tree_contract_kernel)",
+                            "gdn_commit_tree_verify (tree_prep_tc_kernel + tree_contract_tc_kernel)",
                   "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_layer_s * 1e6, 3)},
         gpu_launches=launches_per_call * R * steps,
     )
@@ -372,6 +372,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
     ap.add_argument("--profile", action="store_true",
                     help="for profiler runs: no clock soak, no e2e leg, no CPU baseline")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="for profiler runs: rotate this many layers instead of >= 4x L2 of them")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -396,7 +398,7 @@ def main():
     if world > 1:
         dist.barrier()
     r = run_gpu(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
-                args.batch)
+                args.batch, args.layers)
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or args.profile or world > 1 else cpu_baseline(args.config)
@@ -411,7 +413,9 @@ def main():
                        "step": "per layer: pending commit fused into the next %s verify"
                                % ("chain" if r["chain"] else "tree"),
                        "layers_rotated": r["R"], "footprint_bytes": r["footprint"], "l2_bytes": r["l2"],
-                       "l2_policy": "inputs larger than L2: %d-layer rotation, footprint >= 4x L2" % r["R"],
+                       "l2_policy": ("inputs larger than L2: %d-layer rotation, footprint >= 4x L2" % r["R"])
+                       if r["footprint"] >= 4 * r["l2"] else
+                       "profiling rotation of %d layers (footprint below 4x L2)" % r["R"],
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
             "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
