@@ -262,3 +262,80 @@ def custom_workload(B: int, N: int, H: int, dk: int, dv: int, parent: np.ndarray
     spec = Spec("custom", B, N, H, dk, dv, dtype, "custom", int(depth.max()), "custom", s0_std, seed)
     return Workload(spec, B, N, H, dk, dv, dtype, _store(q, dtype), _store(k, dtype), _store(v, dtype),
                     alpha, beta, parent, S0, np.asarray(path, dtype=np.int32))
+
+
+# ---------------------------------------------------------------------------
+# full GDN layer decode step
+# ---------------------------------------------------------------------------
+WEIGHT_STD = 0.02
+
+
+@dataclasses.dataclass
+class LayerWorkload:
+    """Inputs of one GDN layer decode step over B draft trees.
+
+    Row blocks of W_in, in order: q (H d_k), k (H d_k), v (H d_v), output gate
+    z (H d_v), alpha pre-activation a (H), beta pre-activation b (H).  Conv
+    channels are the q | k | v rows; conv_w tap 0 is the oldest position.
+    """
+    spec: Spec
+    B: int
+    N: int
+    H: int
+    dk: int
+    dv: int
+    hidden: int
+    X: np.ndarray           # bf16 bits [B, N, hidden]
+    W_in: np.ndarray        # bf16 bits [2 H dk + 2 H dv + 2 H, hidden]
+    conv_w: np.ndarray      # float32 [H (2 dk + dv), 4]
+    conv_state: np.ndarray  # float32 [B, 3, H (2 dk + dv)], oldest row first
+    W_o: np.ndarray         # bf16 bits [hidden, H dv]
+    parent: np.ndarray      # int32 [B, N]
+    S0: np.ndarray          # float32 [B, H, dv, dk]
+    path: np.ndarray        # int32 [B, Lmax]
+
+    @property
+    def conv_channels(self) -> int:
+        return self.H * (2 * self.dk + self.dv)
+
+    @property
+    def in_rows(self) -> int:
+        return 2 * self.H * self.dk + 2 * self.H * self.dv + 2 * self.H
+
+    def widened(self, name: str) -> np.ndarray:
+        x = getattr(self, name)
+        if x.dtype == np.uint16:
+            return bf16_bits_to_f64(x)
+        return x.astype(np.float64)
+
+
+def make_layer_workload(cfg=4, seed: Optional[int] = None, B: Optional[int] = None, N: Optional[int] = None,
+                        H: Optional[int] = None, dk: Optional[int] = None, dv: Optional[int] = None,
+                        hidden: Optional[int] = None, maxdepth: Optional[int] = None,
+                        tree: Optional[str] = None) -> LayerWorkload:
+    """Draw one full-layer workload (SPECS[4] by default; any field may be overridden).
+
+    X ~ N(0, 1) and the weights ~ N(0, 0.02), rounded to bf16; conv weights
+    ~ N(0, 0.02) in fp32; the committed conv history ~ N(0, (0.02 sqrt(hidden))^2),
+    the spread of a projected N(0, 1) hidden row; S0 ~ N(0, s0_std).  Draw
+    order: trees, X, W_in, conv_w, conv history, W_o, S0, accepted paths.
+    """
+    base = SPECS[cfg] if isinstance(cfg, int) else cfg
+    spec = dataclasses.replace(
+        base, B=base.B if B is None else B, N=base.N if N is None else N, H=base.H if H is None else H,
+        dk=base.dk if dk is None else dk, dv=base.dv if dv is None else dv,
+        hidden=base.hidden if hidden is None else hidden,
+        maxdepth=base.maxdepth if maxdepth is None else maxdepth, tree=base.tree if tree is None else tree)
+    rng = np.random.default_rng(spec.seed if seed is None else seed)
+    B, N, H, dk, dv, hid = spec.B, spec.N, spec.H, spec.dk, spec.dv, spec.hidden
+    parent = draw_trees(rng, spec, B).astype(np.int32)
+    C = H * (2 * dk + dv)
+    rows = 2 * H * dk + 2 * H * dv + 2 * H
+    X = f32_to_bf16_bits(rng.standard_normal((B, N, hid)).astype(np.float32))
+    W_in = f32_to_bf16_bits((rng.standard_normal((rows, hid)) * WEIGHT_STD).astype(np.float32))
+    conv_w = (rng.standard_normal((C, 4)) * WEIGHT_STD).astype(np.float32)
+    conv_state = (rng.standard_normal((B, 3, C)) * (WEIGHT_STD * np.sqrt(hid))).astype(np.float32)
+    W_o = f32_to_bf16_bits((rng.standard_normal((hid, H * dv)) * WEIGHT_STD).astype(np.float32))
+    S0 = (rng.standard_normal((B, H, dv, dk)) * spec.s0_std).astype(np.float32)
+    path = draw_paths(rng, spec, parent)
+    return LayerWorkload(spec, B, N, H, dk, dv, hid, X, W_in, conv_w, conv_state, W_o, parent, S0, path)
