@@ -57,6 +57,28 @@ def algorithmic_bytes(B, N, H, dk, dv, esz, L_total, Lmax, chain):
     return state + inputs + outputs + factors_out + commit_in
 
 
+# DRAM traffic of one layer call (dram__bytes_read.sum + dram__bytes_write.sum of
+# every kernel the call launches) from one ncu capture per workload, with the
+# hash of the kernel sources it was taken on: a changed kernel reports null.
+NCU_TRAFFIC = {
+    "chain8_b1_h8_d256": (2.306e6, ("gdn_chain.cu", "gdn_internal.cuh"), "5d1de7f6fc17dd70"),
+    "tree64_depth8_b16_h8_d256": (60.97e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
+                                            "gdn_internal.cuh"), "fcf4e0ee97fbc56c"),
+}
+
+
+def ncu_traffic(workload):
+    import hashlib
+    if workload not in NCU_TRAFFIC:
+        return None
+    nbytes, files, digest = NCU_TRAFFIC[workload]
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "speculative_decoding_linear_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return nbytes if m.hexdigest()[:16] == digest else None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -258,7 +280,7 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
         value=value, ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
         spec=spec, B=B, N=N, H=H, dk=dk, dv=dv, chain=chain,
         roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                  "frac": round(achieved / peak, 4), "traffic": None,
+                  "frac": round(achieved / peak, 4), "traffic": ncu_traffic(spec.name),
                   "peak_kind": peak_kind + " hbm_gbs (copy)",
                   "kernel": "gdn_commit_chain_verify (chain_kernel)" if chain else
                             "gdn_commit_tree_verify (tree_prep_tc_kernel + tree_contract_tc_kernel)",
