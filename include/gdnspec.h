@@ -197,6 +197,52 @@ int gdn_commit_chain_verify(float* S, const void* prev_factors, int N_prev,
                             cudaStream_t stream);
 
 /*
+ * Full GDN layer decode step over B draft trees ("Pith review of SpecLA",
+ * Referee Report, major comment 1: one GDN layer, h_v heads of d_k = d_v,
+ * causal depthwise convolution of kernel size 4, SiLU output gating; "Core
+ * claim": every node sees the recurrence along its own root-to-node path).
+ * For every node t of every tree, in one call on `stream`:
+ *   Y_t   = W_in x_t = [q~ | k~ | v~ | z | a | b]_t            (bf16 GEMM, fp32)
+ *   c_t   = sum_i conv_w[:, i] * u_i over the window u_0..u_3 = the pre-conv
+ *           q~|k~|v~ rows of (great-grandparent, grandparent, parent, t); window
+ *           positions above a root take the committed conv history (no bias,
+ *           no activation)
+ *   q_t, k_t = c_t's q and k parts L2-normalised per head; v_t = c_t's v part
+ *   alpha_t = exp(-softplus(a_t)), beta_t = sigmoid(b_t)             (per head)
+ *   o_t   = gated delta rule along path(t) from S (gdn_commit_tree_verify)
+ *   out_t = W_o (o_t * SiLU(z_t))                      (bf16 GEMM, fp32 out)
+ * The previous step's accepted path is committed first (delayed update): S
+ * and the conv history move along prev_path using prev_record.
+ *   X           bf16 [B][N][hidden]
+ *   W_in        bf16 [2 H d_k + 2 H d_v + 2 H][hidden], row blocks q, k, v, z, a, b
+ *   conv_w      fp32 [H (2 d_k + d_v)][4], tap 0 = oldest window position
+ *   W_o         bf16 [hidden][H d_v]
+ *   parent_idx  int32 [B][N], as gdn_tree_verify
+ *   S           fp32 [B][H][d_v][d_k]; in: state before prev_path, out: committed
+ *   conv_state  fp32 [B][3][H (2 d_k + d_v)], oldest row first; in/out like S
+ *   prev_record the record written by the previous step (N_prev nodes per tree),
+ *               with prev_path int32 [B][Lmax] (root first, -1 padded); both NULL
+ *               when there is nothing to commit
+ *   out         fp32 [B][N][hidden]
+ *   record      gdn_layer_record_bytes bytes: this step's projections Y (fp32,
+ *               row stride rounded up to 4 elements) and its factor record
+ *               (fp32 keys); keep it until the next step's commit.  Must not
+ *               overlap prev_record, workspace or out.
+ *   workspace   gdn_layer_workspace_bytes bytes of intermediates (q, k, v,
+ *               alpha, beta, o, the bf16 hi/lo terms of the gated output)
+ * hidden a multiple of 64; H d_v a multiple of 64; d_k, d_v, N as gdn_tree_verify.
+ * The caller owns every buffer; the call allocates nothing.  Errors: as
+ * gdn_commit_tree_verify (GDN_ERR_TREE / GDN_ERR_PATH in the error word).
+ */
+int gdn_layer_record_bytes(int B, int N, int H, int hidden, int dk, int dv, size_t* bytes);
+int gdn_layer_workspace_bytes(int B, int N, int H, int hidden, int dk, int dv, size_t* bytes);
+int gdn_layer_tree_step(const void* X, const void* W_in, const float* conv_w, const void* W_o,
+                        const int32_t* parent_idx, float* S, float* conv_state, const void* prev_record,
+                        int N_prev, const int32_t* prev_path, int Lmax, float* out, void* record,
+                        void* workspace, int B, int N, int H, int hidden, int dk, int dv,
+                        cudaStream_t stream);
+
+/*
  * Launch overlap between consecutive calls (process-wide switch, default off;
  * returns the previous setting).  When on, the first kernel of every call is
  * launched as a programmatic dependent of the kernel before it on the stream:

@@ -39,6 +39,10 @@ SIGNATURES = {
                                     _I, _I, _I, _I, _I, _P]),
     "gdn_commit_chain_verify": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P,
                                      _I, _I, _I, _I, _I, _P]),
+    "gdn_layer_record_bytes": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
+    "gdn_layer_workspace_bytes": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
+    "gdn_layer_tree_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P,
+                                 _I, _I, _I, _I, _I, _I, _P]),
     "gdn_set_launch_overlap": (_I, [_I]),
     "gdn_last_error": (_I, [_P]),
     "gdn_strerror": (ctypes.c_char_p, [_I]),
@@ -207,6 +211,31 @@ def gdn_commit_chain_verify(S, prev_factors, N_prev, prev_path, q, k, v, alpha, 
            "gdn_commit_chain_verify")
 
 
+def gdn_layer_record_bytes(B, N, H, hidden, dk, dv) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_layer_record_bytes(B, N, H, hidden, dk, dv, ctypes.byref(out)), "gdn_layer_record_bytes")
+    return out.value
+
+
+def gdn_layer_workspace_bytes(B, N, H, hidden, dk, dv) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_layer_workspace_bytes(B, N, H, hidden, dk, dv, ctypes.byref(out)),
+           "gdn_layer_workspace_bytes")
+    return out.value
+
+
+def gdn_layer_tree_step(X, W_in, conv_w, W_o, parent_idx, S, conv_state, prev_record, N_prev, prev_path,
+                        out, record, workspace, H, dk, dv, stream=None):
+    """One GDN layer decode step over B draft trees (see include/gdnspec.h).  prev_record and
+    prev_path are both None when there is no pending commit."""
+    B, N, hidden = X.shape
+    Lmax = 0 if prev_path is None else prev_path.shape[1]
+    _check(lib().gdn_layer_tree_step(_ptr(X), _ptr(W_in), _ptr(conv_w), _ptr(W_o), _ptr(parent_idx), _ptr(S),
+                                     _ptr(conv_state), _ptr(prev_record), int(N_prev), _ptr(prev_path), Lmax,
+                                     _ptr(out), _ptr(record), _ptr(workspace), B, N, H, hidden, dk, dv,
+                                     _stream(stream)), "gdn_layer_tree_step")
+
+
 def gdn_set_launch_overlap(enable: bool) -> bool:
     """Process-wide switch; returns the previous setting (see include/gdnspec.h)."""
     return bool(lib().gdn_set_launch_overlap(1 if enable else 0))
@@ -236,3 +265,29 @@ def factor_views(buf, B, N, H, dk, dv, dtype):
     g = buf[o_g: o_g + BHN * 4].view(torch.float32).view(B, H, N)
     par = buf[o_par: o_par + B * N * 4].view(torch.int32).view(B, N)
     return delta, key, g, par
+
+
+def layer_record_views(buf, B, N, H, hidden, dk, dv):
+    """(Y [B*N, rows] fp32 projections, factor-buffer slice) views of a layer record."""
+    rows = 2 * H * dk + 2 * H * dv + 2 * H
+    ldy = (rows + 3) // 4 * 4
+    y_bytes = B * N * ldy * 4
+    Y = buf[:y_bytes].view(torch.float32).view(B * N, ldy)[:, :rows]
+    fac = buf[_align(y_bytes):]
+    return Y, fac
+
+
+def layer_workspace_views(buf, B, N, H, hidden, dk, dv):
+    """q, k [B,N,H,dk], v, o [B,N,H,dv], alpha, beta [B,N,H] fp32 and y_hi, y_lo [B*N, H*dv] bf16."""
+    BN = B * N
+    sizes = [("q", BN * H * dk * 4), ("k", BN * H * dk * 4), ("v", BN * H * dv * 4), ("alpha", BN * H * 4),
+             ("beta", BN * H * 4), ("o", BN * H * dv * 4), ("yhi", BN * H * dv * 2), ("ylo", BN * H * dv * 2)]
+    out, off = {}, 0
+    for name, n in sizes:
+        out[name] = buf[off:off + n]
+        off = _align(off + n)
+    f32 = lambda x, *shape: x.view(torch.float32).view(*shape)
+    return dict(q=f32(out["q"], B, N, H, dk), k=f32(out["k"], B, N, H, dk), v=f32(out["v"], B, N, H, dv),
+                alpha=f32(out["alpha"], B, N, H), beta=f32(out["beta"], B, N, H), o=f32(out["o"], B, N, H, dv),
+                yhi=out["yhi"].view(torch.bfloat16).view(BN, H * dv),
+                ylo=out["ylo"].view(torch.bfloat16).view(BN, H * dv))

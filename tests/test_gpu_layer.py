@@ -1,0 +1,128 @@
+"""Full GDN layer decode step on the GPU against the fp64 layer oracle.
+
+Every intermediate the library keeps (projections, normalised q/k, v, gates,
+recurrence outputs, factor record) and the layer output are compared element
+by element; two consecutive steps check the fused commit of the recurrent
+state and of the convolution history.  Shapes span several GEMM tiles with
+ragged tails; the last case is the full 64 x 64-node, hidden-2048 workload.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL, assert_close
+from speculative_decoding_linear_gb300 import gdnspec
+from speculative_decoding_linear_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16(bits):
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+
+def f32(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+
+
+class LayerRun:
+    """Device buffers of one layer instance; ping-pong records across steps."""
+
+    def __init__(self, w):
+        self.w = w
+        self.W_in, self.W_o = bf16(w.W_in), bf16(w.W_o)
+        self.conv_w = f32(w.conv_w)
+        self.S = f32(w.S0)
+        self.conv_state = f32(w.conv_state)
+        self.recs = []
+
+    def step(self, X, parent, prev_path=None, N_prev=0):
+        w = self.w
+        B, N = parent.shape
+        rec = torch.empty(gdnspec.gdn_layer_record_bytes(B, N, w.H, w.hidden, w.dk, w.dv), dtype=torch.uint8,
+                          device="cuda")
+        ws = torch.empty(gdnspec.gdn_layer_workspace_bytes(B, N, w.H, w.hidden, w.dk, w.dv), dtype=torch.uint8,
+                         device="cuda")
+        out = torch.empty((B, N, w.hidden), dtype=torch.float32, device="cuda")
+        prev = self.recs[-1] if prev_path is not None else None
+        gdnspec.gdn_layer_tree_step(bf16(X), self.W_in, self.conv_w, self.W_o, torch.from_numpy(parent.astype(np.int32)).cuda(),
+                                    self.S, self.conv_state, prev, N_prev,
+                                    None if prev_path is None else torch.from_numpy(prev_path).cuda(),
+                                    out, rec, ws, w.H, w.dk, w.dv)
+        assert gdnspec.gdn_last_error() == gdnspec.OK
+        self.recs.append(rec)
+        Y, fac = gdnspec.layer_record_views(rec, B, N, w.H, w.hidden, w.dk, w.dv)
+        views = gdnspec.layer_workspace_views(ws, B, N, w.H, w.hidden, w.dk, w.dv)
+        return out, Y, fac, views
+
+
+def oracle_step(layer, w, X, parent, S0, conv_state):
+    return layer.layer_step(wl.bf16_bits_to_f64(X), w.widened("W_in"), w.widened("conv_w"), conv_state,
+                            w.widened("W_o"), parent, S0, w.H, w.dk, w.dv)
+
+
+def compare(w, r, out, Y, fac, views, parent):
+    B, N = parent.shape
+    H, dk, dv = w.H, w.dk, w.dv
+    Yh = Y.cpu().numpy().reshape(B, N, -1)
+    C = H * (2 * dk + dv)
+    assert_close(Yh[..., :C], r["pre"], "projections (q|k|v)", tol=1e-4)
+    assert_close(Yh[..., C:C + H * dv], r["z"], "projections (gate)", tol=1e-4)
+    assert_close(views["q"].cpu().numpy(), r["q"], "q")
+    assert_close(views["k"].cpu().numpy(), r["k"], "k")
+    assert_close(views["v"].cpu().numpy(), r["v"], "v")
+    np.testing.assert_allclose(views["alpha"].cpu().numpy(), r["alpha"], rtol=2e-5, atol=1e-6)
+    np.testing.assert_allclose(views["beta"].cpu().numpy(), r["beta"], rtol=2e-5, atol=1e-6)
+    assert_close(views["o"].cpu().numpy(), r["o"], "o")
+    delta, key, g, par = gdnspec.factor_views(fac, B, N, H, dk, dv, "f32")
+    assert_close(delta.cpu().numpy(), r["delta"], "delta")
+    assert np.array_equal(par.cpu().numpy(), parent)
+    return assert_close(out.cpu().numpy(), r["out"], "layer output")
+
+
+SMALL = [  # (B, N, H, dk, dv, hidden, maxdepth): ragged GEMM tiles in M, N and K
+    (2, 16, 2, 64, 64, 128, 4),
+    (3, 37, 2, 32, 64, 192, 8),
+    (5, 64, 1, 128, 128, 256, 8),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL)
+def test_layer_step_matches_oracle(oracle_mod, shape):
+    from oracle import layer
+    B, N, H, dk, dv, hid, md = shape
+    w = wl.make_layer_workload(4, seed=41 + B, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=md)
+    run = LayerRun(w)
+    out, Y, fac, views = run.step(w.X, w.parent)
+    r = oracle_step(layer, w, w.X, w.parent, w.widened("S0"), w.widened("conv_state"))
+    compare(w, r, out, Y, fac, views, w.parent)
+    # no pending commit: state and conv history untouched
+    assert torch.equal(run.S.cpu(), torch.from_numpy(w.S0))
+    assert torch.equal(run.conv_state.cpu(), torch.from_numpy(w.conv_state))
+
+
+@pytest.mark.parametrize("shape", SMALL[:2])
+def test_two_steps_commit_state_and_conv_history(oracle_mod, shape):
+    from oracle import layer
+    B, N, H, dk, dv, hid, md = shape
+    w = wl.make_layer_workload(4, seed=77 + B, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=md)
+    w2 = wl.make_layer_workload(4, seed=78 + B, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=md)
+    run = LayerRun(w)
+    run.step(w.X, w.parent)
+    r1 = oracle_step(layer, w, w.X, w.parent, w.widened("S0"), w.widened("conv_state"))
+    S1, hist1 = layer.layer_commit(r1, w.parent, w.widened("S0"), w.widened("conv_state"), w.path)
+    out, Y, fac, views = run.step(w2.X, w2.parent, prev_path=w.path, N_prev=N)
+    assert_close(run.S.cpu().numpy(), S1, "committed state")
+    assert_close(run.conv_state.cpu().numpy(), hist1, "committed conv history", tol=1e-5)
+    r2 = oracle_step(layer, w, w2.X, w2.parent, S1, hist1)
+    compare(w, r2, out, Y, fac, views, w2.parent)
+
+
+def test_layer_full_size(oracle_mod):
+    """64 sequences x 64-node trees (depth <= 8), hidden 2048, 8 heads of 256: every element."""
+    from oracle import layer
+    w = wl.make_layer_workload(4)
+    run = LayerRun(w)
+    out, Y, fac, views = run.step(w.X, w.parent)
+    r = oracle_step(layer, w, w.X, w.parent, w.widened("S0"), w.widened("conv_state"))
+    compare(w, r, out, Y, fac, views, w.parent)
