@@ -289,6 +289,227 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
     )
 
 
+# ---------------------------------------------------------------------------
+# full GDN layer decode step: projections, ancestor-window conv, gates, tree
+# verification with the pending commit fused in, output gate, o_proj
+# ---------------------------------------------------------------------------
+def layer_flops(B, N, H, hidden, dk, dv):
+    """Dense tensor-core work of one layer call: input and output projections (useful flops)."""
+    rows = 2 * H * dk + 2 * H * dv + 2 * H
+    return 2.0 * B * N * hidden * rows + 2.0 * B * N * H * dv * hidden
+
+
+class LayerStep:
+    """One full-layer instance: weights, state, conv history, this step's draft, ping-pong records."""
+
+    def __init__(self, w, device, torch, gdnspec):
+        def bf(bits):
+            return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(device)
+
+        def f(x):
+            return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+        self.w = w
+        self.X, self.W_in, self.W_o, self.conv_w = bf(w.X), bf(w.W_in), bf(w.W_o), f(w.conv_w)
+        self.parent = torch.from_numpy(w.parent).to(device)
+        self.path = torch.from_numpy(w.path).to(device)
+        self.S, self.conv_state = f(w.S0), f(w.conv_state)
+        nb = gdnspec.gdn_layer_record_bytes(w.B, w.N, w.H, w.hidden, w.dk, w.dv)
+        self.rec = [torch.empty(nb, dtype=torch.uint8, device=device) for _ in range(2)]
+        self.ws = torch.empty(gdnspec.gdn_layer_workspace_bytes(w.B, w.N, w.H, w.hidden, w.dk, w.dv),
+                              dtype=torch.uint8, device=device)
+        self.out = torch.empty((w.B, w.N, w.hidden), dtype=torch.float32, device=device)
+
+    def nbytes(self):
+        ts = [self.X, self.W_in, self.W_o, self.conv_w, self.parent, self.path, self.S, self.conv_state,
+              self.ws, self.out] + self.rec
+        return sum(t.numel() * t.element_size() for t in ts)
+
+    def call(self, gdnspec, parity, first=False):
+        w = self.w
+        if first:
+            gdnspec.gdn_layer_tree_step(self.X, self.W_in, self.conv_w, self.W_o, self.parent, self.S,
+                                        self.conv_state, None, 0, None, self.out, self.rec[0], self.ws,
+                                        w.H, w.dk, w.dv)
+        else:
+            gdnspec.gdn_layer_tree_step(self.X, self.W_in, self.conv_w, self.W_o, self.parent, self.S,
+                                        self.conv_state, self.rec[parity], w.N, self.path, self.out,
+                                        self.rec[1 - parity], self.ws, w.H, w.dk, w.dv)
+
+
+def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile=False, layers=None):
+    from speculative_decoding_linear_gb300 import gdnspec
+    from speculative_decoding_linear_gb300 import workloads as wl
+
+    torch.cuda.set_device(device_index)
+    device = torch.device("cuda", device_index)
+    spec = wl.SPECS[4]
+    props = torch.cuda.get_device_properties(device_index)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
+    first = LayerStep(wl.make_layer_workload(4, seed=1000 * (rank + 1) + 4), device, torch, gdnspec)
+    per_layer = first.nbytes()
+    R = max(2, -(-4 * l2 // per_layer)) if layers is None else max(2, layers)
+    lys = [first] + [LayerStep(wl.make_layer_workload(4, seed=1000 * (rank + 1) + 4 + 7919 * r), device, torch,
+                               gdnspec) for r in range(1, R)]
+    footprint = sum(ly.nbytes() for ly in lys)
+    stream = torch.cuda.Stream(device=device)
+    with torch.cuda.stream(stream):
+        for ly in lys:
+            ly.call(gdnspec, 0, first=True)
+        assert gdnspec.gdn_last_error(stream) == 0
+        for parity in (0, 1):
+            for ly in lys:
+                ly.call(gdnspec, parity)
+        assert gdnspec.gdn_last_error(stream) == 0
+        graphs = []
+        for parity in (0, 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for ly in lys:
+                    ly.call(gdnspec, parity)
+            graphs.append(g)
+        for i in range(max(warmup, 3)):
+            graphs[i % 2].replay()
+        stream.synchronize()
+        assert gdnspec.gdn_last_error(stream) == 0
+        sampler = ClockSampler(device_index)
+        sampler.start()
+        t_soak = time.time()
+        i = 0
+        while not profile and time.time() - t_soak < 1.0:
+            graphs[i % 2].replay()
+            i += 1
+            if i % 4 == 0:
+                stream.synchronize()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s_ in range(steps):
+            graphs[s_ % 2].replay()
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        clocks = sampler.stop()
+        ms_local = e0.elapsed_time(e1)
+        assert gdnspec.gdn_last_error(stream) == 0
+
+        seq = None if profile else run_sequential_baseline(lys[0], gdnspec, torch, stream, steps=3)
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    e2e = None if profile else run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device)
+    w0 = lys[0].w
+    t_layer_s = ms / 1e3 / (steps * R)
+    flops = layer_flops(w0.B, w0.N, w0.H, w0.hidden, w0.dk, w0.dv)
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / t_layer_s / 1e12
+    nodes = w0.B * w0.N * R * steps * world
+    return dict(
+        value=nodes / (ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
+        spec=spec, B=w0.B, N=w0.N, H=w0.H, dk=w0.dk, dv=w0.dv, hidden=w0.hidden, chain=False, layer=True,
+        sequential=seq,
+        roofline={"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                  "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                  "kernel": "gdn_layer_tree_step (input/output projection GEMMs on tcgen05, conv, "
+                            "tree verify + commit, gate)",
+                  "algorithmic_flops_per_call": flops, "t_call_us": round(t_layer_s * 1e6, 3)},
+        gpu_launches=6 * R * steps,
+    )
+
+
+def measured_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops_sustained"]), "measured bf16_tflops_sustained (cuBLAS, long loop)"
+    return 1700.0, "fallback"
+
+
+def run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device):
+    """Layer step through the public API with X, parent_idx and the accepted path copied in from pinned
+    host memory and the layer output copied out, every step."""
+    names = ["X", "parent", "path"]
+    host = [{n: getattr(ly, n).cpu().pin_memory() for n in names} for ly in lys]
+    outs = [torch.empty(ly.out.shape, dtype=ly.out.dtype).pin_memory() for ly in lys]
+    h2d = sum(t.numel() * t.element_size() for hd in host for t in hd.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    k = max(1, min(steps, 5))
+    with torch.cuda.stream(stream):
+        def one(parity):
+            for ly, hd in zip(lys, host):
+                for n in names:
+                    getattr(ly, n).copy_(hd[n], non_blocking=True)
+                ly.call(gdnspec, parity)
+                outs[lys.index(ly)].copy_(ly.out, non_blocking=True)
+        one(0)
+        one(1)
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for s_ in range(k):
+            one(s_ % 2)
+        stream.synchronize()
+        t1 = time.perf_counter()
+    sec = t1 - t0
+    if world > 1:
+        t = torch.tensor([sec], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    w = lys[0].w
+    return {"value": w.B * w.N * len(lys) * k * world / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": 1e3 * sec / k}
+
+
+def run_sequential_baseline(ly, gdnspec, torch, stream, steps=3):
+    """The same layer decoded node by node (gdn_layer_token_step for t = 0 .. N-1), each node from its
+    parent's materialised state: the per-token decoder the tree step replaces.  One pass over the N
+    nodes is captured as a CUDA graph and replayed; returns nodes/s and ms per layer step."""
+    w = ly.w
+    dev = ly.S.device
+    S_nodes = torch.empty((w.N, w.B, w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+    rec = torch.empty(gdnspec.gdn_layer_record_bytes(w.B, w.N, w.H, w.hidden, w.dk, w.dv), dtype=torch.uint8,
+                      device=dev)
+    ws = torch.empty(gdnspec.gdn_layer_workspace_bytes(w.B, w.N, w.H, w.hidden, w.dk, w.dv), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty_like(ly.out)
+
+    def one_pass():
+        for t in range(w.N):
+            gdnspec.gdn_layer_token_step(ly.X, ly.W_in, ly.conv_w, ly.W_o, ly.parent, ly.S, ly.conv_state, S_nodes,
+                                         t, out, rec, ws, w.H, w.dk, w.dv)
+    one_pass()
+    assert gdnspec.gdn_last_error(stream) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        one_pass()
+    g.replay()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    assert gdnspec.gdn_last_error(stream) == 0
+    ms = e0.elapsed_time(e1) / steps
+    res = {"value": w.B * w.N / (ms / 1e3), "unit": UNIT, "ms_per_layer_step": round(ms, 4), "passes": steps,
+           "gpu_launches_per_layer_step": 5 * w.N, "node_state_bytes": S_nodes.numel() * 4,
+           "what": "gdn_layer_token_step for t = 0..N-1: per-node projection, conv, one delta-rule step "
+                   "from the parent's materialised state, gate, o_proj"}
+    del S_nodes, rec, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device):
     """Same metric through the public API; H2D of each step's inputs and D2H of its outputs timed."""
     names = ["q", "k", "v", "alpha", "beta", "path"] + ([] if chain else ["parent"])
@@ -341,11 +562,31 @@ def oracle_layer_seconds(w, nthreads):
     return time.perf_counter() - t0
 
 
+def oracle_full_layer_seconds(w, nthreads):
+    """One full-layer decode step of a layer workload with the fp64 layer oracle, plus its commit."""
+    from oracle import layer
+    X, W_in, cw, cs, W_o, S0 = (w.widened(n) for n in ("X", "W_in", "conv_w", "conv_state", "W_o", "S0"))
+    t0 = time.perf_counter()
+    r = layer.layer_step(X, W_in, cw, cs, W_o, w.parent, S0, w.H, w.dk, w.dv, nthreads=nthreads)
+    layer.layer_commit(r, w.parent, S0, cs, w.path, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(cfg, budget_s=10.0):
     import oracle
     from speculative_decoding_linear_gb300 import workloads as wl
     oracle.build()
     cores = os.cpu_count() or 1
+    if cfg == 4:
+        w = wl.make_layer_workload(4, B=2)
+        n, sec = 0, 0.0
+        while sec < budget_s:
+            sec += oracle_full_layer_seconds(w, cores)
+            n += 1
+        return {"value": w.B * w.N * n / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": "%d repetitions of one full-layer step of 2 of the 64 sequences of %s (numpy "
+                          "fp64 projections/conv/o_proj + path-walk recurrence + commit), %d threads"
+                          % (n, w.spec.name, cores)}
     w = wl.make_workload(cfg)
     n, sec = 0, 0.0
     while sec < budget_s:
@@ -365,16 +606,21 @@ def run_reference(args):
         return
     oracle.build()
     cores = os.cpu_count() or 1
-    w = wl.make_workload(args.config)
+    if args.config == 4:
+        w = wl.make_layer_workload(4, B=2)
+        timer = oracle_full_layer_seconds
+    else:
+        w = wl.make_workload(args.config)
+        timer = oracle_layer_seconds
     for _ in range(max(args.warmup, 1)):
-        oracle_layer_seconds(w, cores)
-    sec = sum(oracle_layer_seconds(w, cores) for _ in range(args.steps))
+        timer(w, cores)
+    sec = sum(timer(w, cores) for _ in range(args.steps))
     value = w.B * w.N * args.steps / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.spec.name, "B": w.B, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv},
+            "config": {"workload": w.spec.name, "B": w.spec.B, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": "one layer instance of %s per step (verify all nodes by path "
                                        "walks + commit), fp64, %d threads" % (w.spec.name, cores)},
@@ -388,7 +634,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3])
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
@@ -419,8 +665,11 @@ def main():
         __graft_entry__.build()
     if world > 1:
         dist.barrier()
-    r = run_gpu(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
-                args.batch, args.layers)
+    if args.config == 4:
+        r = run_gpu_layer(args.steps, args.warmup, rank, world, local, torch, dist, args.profile, args.layers)
+    else:
+        r = run_gpu(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
+                    args.batch, args.layers)
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or args.profile or world > 1 else cpu_baseline(args.config)
@@ -432,7 +681,10 @@ def main():
             "data": "synthetic",
             "config": {"workload": spec.name, "B": r["B"], "N": r["N"], "H": r["H"], "dk": r["dk"],
                        "dv": r["dv"], "qkv": spec.dtype, "state": "f32",
-                       "step": "per layer: pending commit fused into the next %s verify"
+                       "step": ("full GDN layer step: projections, ancestor-window conv, gates, tree "
+                                "verify with the pending commit (state + conv history) fused in, output "
+                                "gate, o_proj") if r.get("layer") else
+                               "per layer: pending commit fused into the next %s verify"
                                % ("chain" if r["chain"] else "tree"),
                        "layers_rotated": r["R"], "footprint_bytes": r["footprint"], "l2_bytes": r["l2"],
                        "l2_policy": ("inputs larger than L2: %d-layer rotation, footprint >= 4x L2" % r["R"])
@@ -442,6 +694,12 @@ def main():
             "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
             "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
         }
+        if r.get("layer"):
+            line["config"]["hidden"] = r["hidden"]
+            seq = r["sequential"]
+            if seq:
+                seq["tree_step_speedup"] = round(r["value"] / seq["value"], 2)
+            line["sequential_decode"] = seq
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

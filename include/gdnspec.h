@@ -243,6 +243,29 @@ int gdn_layer_tree_step(const void* X, const void* W_in, const float* conv_w, co
                         cudaStream_t stream);
 
 /*
+ * Per-token decoding of the same layer, for comparison with the tree step:
+ * node t of every tree is decoded on its own (input projection at B rows,
+ * its conv window, one delta-rule step from the parent's materialised state,
+ * output gate, output projection), as a sequential decoder that keeps one
+ * state per draft node would do ("Pith review of SpecLA", "Core claim": the
+ * tree verifier replaces this node-by-node recurrence).  Calling it for
+ * t = 0 .. N-1 in order yields the outputs of gdn_layer_tree_step.
+ *   S0          fp32 [B][H][d_v][d_k] committed state (read only)
+ *   conv_state  fp32 [B][3][H (2 d_k + d_v)] committed conv history (read only)
+ *   S_nodes     fp32 [N][B][H][d_v][d_k]: the state after node t is written to
+ *               S_nodes[t]; node t reads its parent's entry (S0 for a root)
+ *   record, workspace: as gdn_layer_tree_step (only the projection rows and the
+ *               intermediates are used); node t's projection row is written and its
+ *               ancestors' rows, written by earlier calls, are read
+ *   out         fp32 [B][N][hidden]: row t of every sequence is written
+ * Other arguments as gdn_layer_tree_step.  0 <= t < N.
+ */
+int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, const void* W_o,
+                         const int32_t* parent_idx, const float* S0, const float* conv_state, float* S_nodes,
+                         int t, float* out, void* record, void* workspace, int B, int N, int H, int hidden,
+                         int dk, int dv, cudaStream_t stream);
+
+/*
  * Launch overlap between consecutive calls (process-wide switch, default off;
  * returns the previous setting).  When on, the first kernel of every call is
  * launched as a programmatic dependent of the kernel before it on the stream:

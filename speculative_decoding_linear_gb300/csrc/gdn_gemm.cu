@@ -24,18 +24,20 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kBM = 128, kBK = 64;
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kATile = kBM * kBK * 2;   // 16 KiB
-constexpr uint32_t kBTile = kBN * kBK * 2;   // 32 KiB
-constexpr uint32_t kAccCols = 256;
-constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN);
 
-template <int NA>
+// Tile 128 x BN (BN = 256 for large problems, 64 when 256-wide tiles would
+// leave most SMs idle, e.g. one token per sequence).
+template <int NA, int BN>
 struct GemmGeom {
-    static constexpr int kStages = NA == 1 ? 4 : 3;
+    static constexpr uint32_t kBTile = BN * kBK * 2;
     static constexpr uint32_t kStageBytes = NA * kATile + kBTile;
+    static constexpr int kStages = (int)((192u * 1024u) / kStageBytes) < 8 ? (int)((192u * 1024u) / kStageBytes) : 8;
     static constexpr uint32_t kBarOff = kStages * kStageBytes;
+    static constexpr uint32_t kAccCols = BN;                  // per accumulator buffer (two buffers)
+    static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN);
     static constexpr uint32_t kSmem = kBarOff + 256 + 1024;   // barriers, TMEM holder, 1 KiB alignment slack
 };
 
@@ -73,11 +75,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
     }
 }
 
-template <int NA>
+template <int NA, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                      const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
-    using G = GemmGeom<NA>;
+    using G = GemmGeom<NA, BN>;
+    constexpr uint32_t kAccCols = G::kAccCols;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t* holder = reinterpret_cast<uint32_t*>(sm + G::kBarOff + 16 * G::kStages + 40);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(holder + 1);
 
-    const int tiles_m = (g.M + kBM - 1) / kBM, tiles_n = (g.Nc + kBN - 1) / kBN;
+    const int tiles_m = (g.M + kBM - 1) / kBM, tiles_n = (g.Nc + BN - 1) / BN;
     const int ntiles = tiles_m * tiles_n, kblocks = g.K / kBK;
 
     if (tid == 0) {
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int s = 0;
             uint32_t ph = 0;
             for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-                const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * kBN;
+                const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * BN;
                 bool ok = true;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!wait_or_abort(empty0 + 8u * s, ph ^ 1u, g.err, abort_flag)) {
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                         for (int a = 0; a < NA; ++a)
                             mma_bf16(d, sw128_desc(st + a * kATile + 32 * k), sw128_desc(st + NA * kATile + 32 * k),
-                                     kIdesc, (kb | k | a) != 0);
+                                     G::kIdesc, (kb | k | a) != 0);
                     mma_commit(empty0 + 8u * s);
                     if (++s == G::kStages) {
                         s = 0;
@@ -184,12 +187,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int buf = lt & 1;
             if (!wait_or_abort(accf0 + 8u * buf, ((uint32_t)lt >> 1) & 1u, g.err, abort_flag)) break;
             tc_fence_after();
-            const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * kBN;
+            const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * BN;
             const int row = m0 + 32 * qtr + lane;
             const uint32_t t = tmem + buf * kAccCols + ((uint32_t)(32 * qtr) << 16);
             float* crow = g.C + (size_t)row * g.ldc;
 #pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
+            for (int c = 0; c < BN / 32; ++c) {
                 const int col = n0 + 32 * c;
                 if (col >= g.Nc) break;            // warp-uniform
                 float v[32];
@@ -234,12 +237,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_2d() {
     return fn;
 }
 
-// Row-major bf16 [rows][K] operand; box = 64 columns (128 bytes) x box_rows rows.
-bool make_operand_map(CUtensorMap* m, const void* ptr, long long rows, int K, int box_rows) {
+// Row-major bf16 [rows][K] operand with a row stride of ld elements; box = 64
+// columns (128 bytes) x box_rows rows.
+bool make_operand_map(CUtensorMap* m, const void* ptr, long long rows, int K, long long ld, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_2d();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -259,29 +263,34 @@ int sm_count() {
     return n[dev];
 }
 
+template <int NA, int BN>
+cudaError_t launch_tiles(const CUtensorMap& ta0, const CUtensorMap& ta1, const CUtensorMap& tb, const GemmArgs& g,
+                         cudaStream_t s) {
+    using G = GemmGeom<NA, BN>;
+    static bool attr[64];
+    cudaError_t e = ensure_smem(gemm_bf16_kernel<NA, BN>, G::kSmem, attr);
+    if (e != cudaSuccess) return e;
+    const int ntiles = ((g.M + kBM - 1) / kBM) * ((g.Nc + BN - 1) / BN);
+    const int grid = ntiles < sm_count() ? ntiles : sm_count();
+    return launch_kernel(gemm_bf16_kernel<NA, BN>, dim3(grid), dim3(kGemmThreads), G::kSmem, s, false, ta0, ta1, tb,
+                         g);
+}
+
 }  // namespace
 
-cudaError_t launch_gemm_bf16(const void* A0, const void* A1, int nA, const void* B, float* C, long long ldc,
-                             int M, int Nc, int K, int* err, cudaStream_t s) {
-    static bool attr1[64], attr2[64];
-    if (M < 1 || Nc < 1 || K < kBK || K % kBK != 0 || (nA != 1 && nA != 2)) return cudaErrorInvalidValue;
+cudaError_t launch_gemm_bf16(const void* A0, const void* A1, int nA, long long lda, const void* B, float* C,
+                             long long ldc, int M, int Nc, int K, int* err, cudaStream_t s) {
+    if (M < 1 || Nc < 1 || K < kBK || K % kBK != 0 || (nA != 1 && nA != 2) || lda < K || lda % 8 != 0)
+        return cudaErrorInvalidValue;
+    const bool wide = (long long)((M + kBM - 1) / kBM) * ((Nc + 255) / 256) >= sm_count() / 2;
     CUtensorMap ta0, ta1, tb;
-    if (!make_operand_map(&ta0, A0, M, K, kBM) || !make_operand_map(&tb, B, Nc, K, kBN)) return cudaErrorInvalidValue;
-    if (nA == 2 && !make_operand_map(&ta1, A1, M, K, kBM)) return cudaErrorInvalidValue;
+    if (!make_operand_map(&ta0, A0, M, K, lda, kBM) || !make_operand_map(&tb, B, Nc, K, K, wide ? 256 : 64))
+        return cudaErrorInvalidValue;
+    if (nA == 2 && !make_operand_map(&ta1, A1, M, K, lda, kBM)) return cudaErrorInvalidValue;
     if (nA == 1) ta1 = ta0;
-    GemmArgs g{C, ldc, M, Nc, K, err};
-    const int ntiles = ((M + kBM - 1) / kBM) * ((Nc + kBN - 1) / kBN);
-    const int grid = ntiles < sm_count() ? ntiles : sm_count();
-    if (nA == 1) {
-        cudaError_t e = ensure_smem(gemm_bf16_kernel<1>, GemmGeom<1>::kSmem, attr1);
-        if (e != cudaSuccess) return e;
-        return launch_kernel(gemm_bf16_kernel<1>, dim3(grid), dim3(kGemmThreads), GemmGeom<1>::kSmem, s, false, ta0,
-                             ta1, tb, g);
-    }
-    cudaError_t e = ensure_smem(gemm_bf16_kernel<2>, GemmGeom<2>::kSmem, attr2);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(gemm_bf16_kernel<2>, dim3(grid), dim3(kGemmThreads), GemmGeom<2>::kSmem, s, false, ta0, ta1,
-                         tb, g);
+    const GemmArgs g{C, ldc, M, Nc, K, err};
+    if (nA == 1) return wide ? launch_tiles<1, 256>(ta0, ta1, tb, g, s) : launch_tiles<1, 64>(ta0, ta1, tb, g, s);
+    return wide ? launch_tiles<2, 256>(ta0, ta1, tb, g, s) : launch_tiles<2, 64>(ta0, ta1, tb, g, s);
 }
 
 }  // namespace gdn

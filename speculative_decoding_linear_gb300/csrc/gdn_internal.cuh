@@ -118,6 +118,9 @@ struct VerifyArgs {
     int* err;
     bool overlap;              // launch the call's first kernel as a programmatic dependent
     bool tc;                   // the tensor-core contraction runs: prologue writes its operand form
+    // fp32 q/k on the tensor-core path: bf16 q_hi, k_hi, q_lo, k_lo with x = hi + lo to
+    // ~2^-16 (same layout as q/k); all nullptr otherwise
+    const void* split[4] = {nullptr, nullptr, nullptr, nullptr};
 };
 
 struct CommitArgs {

@@ -37,17 +37,25 @@ struct ConvArgs {
     float* q;                  // [B][N][H][dk]
     float* k;
     float* v;                  // [B][N][H][dv]
+    __nv_bfloat16* qk_split[4];   // bf16 q_hi, k_hi, q_lo, k_lo [B][N][H][dk] (tensor-core verify)
     float* alpha;              // [B][N][H]
     float* beta;
     int B, N, H, dk, dv;
+    int t0, t1;                // nodes whose outputs this launch computes
     int* err;
 };
+
+// Dynamic shared memory of the conv kernel: this block's channels of every
+// projection row that a window of nodes t0..t1-1 reads.
+inline size_t conv_smem_bytes(int N, int dk, int dv) { return (size_t)N * (dk > dv ? dk : dv) * 4; }
 
 // Grid (B, 3H + 1): block (b, j < 3H) owns one head's channels of q, k or v
 // (channel blocks never share a channel, so the in-place history commit is
 // race-free); block (b, 3H) computes the gates.
 __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
+    extern __shared__ __align__(16) float s_y[];   // [N][d]
     __shared__ int s_win[kMaxNodes][3];       // window sources: >= 0 node, -1 - r history row r
+    __shared__ int s_need[kMaxNodes];
     __shared__ float s_red[kConvThreads / 32][kMaxNodes];
     __shared__ float s_rn[kMaxNodes];
     __shared__ int s_path[kMaxPath];
@@ -60,8 +68,8 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
 
     if (blk == 3 * H) {                       // gates
         const long long ga = 2LL * H * dk + 2LL * H * dv;
-        for (int i = tid; i < N * H; i += kConvThreads) {
-            const int t = i / H, h = i % H;
+        for (int i = tid; i < (a.t1 - a.t0) * H; i += kConvThreads) {
+            const int t = a.t0 + i / H, h = i % H;
             const float x = Yb[(size_t)t * a.ldy + ga + h];
             const float y = Yb[(size_t)t * a.ldy + ga + H + h];
             const size_t o = ((size_t)b * N + t) * H + h;
@@ -92,8 +100,12 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         }
         s_L = L;
     }
+    if (tid < kMaxNodes) s_need[tid] = 0;
+    __syncthreads();
     if (tid < N) {
         const int32_t* par = a.parent + (size_t)b * N;
+        const bool mine = tid >= a.t0 && tid < a.t1;
+        if (mine) s_need[tid] = 1;
         int cur = tid, hist = 2;
         for (int i = 2; i >= 0; --i) {        // i = 2: parent, 1: grandparent, 0: great-grandparent
             int p = cur >= 0 ? par[cur] : -1;
@@ -104,6 +116,7 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
             if (p >= 0) {
                 cur = p;
                 s_win[tid][i] = p;
+                if (mine) s_need[p] = 1;
             } else {
                 cur = -1;
                 s_win[tid][i] = -1 - hist;
@@ -112,6 +125,11 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         }
     }
     __syncthreads();
+    // stage the rows the windows read (this block's d channels of each), 16 bytes per copy
+    for (int i = tid; i < N * (d / 4); i += kConvThreads) {
+        const int t = i / (d / 4), c4 = i % (d / 4);
+        if (s_need[t]) cp_async16(s_y + t * d + 4 * c4, Yb + (size_t)t * a.ldy + cb + 4 * c4);
+    }
 
     const int c = cb + tid;
     const bool act = tid < d;
@@ -135,19 +153,21 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         w[2] = wv.z;
         w[3] = wv.w;
     }
+    cp_async_wait_all();
+    __syncthreads();
 
     float val[kMaxNodes];
 #pragma unroll
     for (int t = 0; t < kMaxNodes; ++t) {
         val[t] = 0.f;
-        if (t < N && act) {
+        if (t >= a.t0 && t < a.t1 && act) {
             float x[kConvTaps];
 #pragma unroll
             for (int i = 0; i < 3; ++i) {
-                const int s = s_win[t][i];
-                x[i] = s >= 0 ? Yb[(size_t)s * a.ldy + c] : hrow[-1 - s];
+                const int sidx = s_win[t][i];
+                x[i] = sidx >= 0 ? s_y[sidx * d + tid] : (sidx == -1 ? hrow[0] : sidx == -2 ? hrow[1] : hrow[2]);
             }
-            x[3] = Yb[(size_t)t * a.ldy + c];
+            x[3] = s_y[t * d + tid];
             val[t] = w[0] * x[0] + w[1] * x[1] + w[2] * x[2] + w[3] * x[3];
         }
     }
@@ -156,7 +176,7 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         if (act) {
 #pragma unroll
             for (int t = 0; t < kMaxNodes; ++t)
-                if (t < N) a.v[(((size_t)b * N + t) * H + h) * dv + tid] = val[t];
+                if (t >= a.t0 && t < a.t1) a.v[(((size_t)b * N + t) * H + h) * dv + tid] = val[t];
         }
         griddep_launch();
         return;
@@ -165,13 +185,13 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     const int warp = tid >> 5, lane = tid & 31;
 #pragma unroll
     for (int t = 0; t < kMaxNodes; ++t) {
-        if (t < N) {
+        if (t >= a.t0 && t < a.t1) {
             const float ss = warp_sum(val[t] * val[t]);
             if (lane == 0) s_red[warp][t] = ss;
         }
     }
     __syncthreads();
-    if (tid < N) {
+    if (tid >= a.t0 && tid < a.t1) {
         float ss = 0.f;
         for (int i = 0; i < kConvThreads / 32; ++i) ss += s_red[i][tid];
         s_rn[tid] = 1.f / sqrtf(ss);
@@ -179,9 +199,21 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     __syncthreads();
     if (act) {
         float* dst = seg == 0 ? a.q : a.k;
+        __nv_bfloat16* dhi = a.qk_split[seg];
+        __nv_bfloat16* dlo = a.qk_split[2 + seg];
 #pragma unroll
-        for (int t = 0; t < kMaxNodes; ++t)
-            if (t < N) dst[(((size_t)b * N + t) * H + h) * dk + tid] = val[t] * s_rn[t];
+        for (int t = 0; t < kMaxNodes; ++t) {
+            if (t >= a.t0 && t < a.t1) {
+                const size_t o = (((size_t)b * N + t) * H + h) * dk + tid;
+                const float y = val[t] * s_rn[t];
+                dst[o] = y;
+                if (dhi != nullptr) {
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(y);
+                    dhi[o] = hi;
+                    dlo[o] = __float2bfloat16_rn(y - __bfloat162float(hi));
+                }
+            }
+        }
     }
     griddep_launch();
 }
@@ -192,7 +224,8 @@ struct GateArgs {
     long long ldy, zoff;
     __nv_bfloat16* yhi;        // [B*N][H*dv]
     __nv_bfloat16* ylo;
-    long long rows;
+    long long rows;            // rows processed; row r is row r * rstride + roff of every array
+    long long rstride, roff;
     int width;                 // H*dv
 };
 
@@ -203,7 +236,7 @@ __global__ void __launch_bounds__(kGateThreads) layer_gate_kernel(GateArgs a) {
     const long long n = a.rows * per_row;
     for (long long i = blockIdx.x * (long long)kGateThreads + threadIdx.x; i < n;
          i += (long long)gridDim.x * kGateThreads) {
-        const long long r = i / per_row, c = (i % per_row) * 4;
+        const long long r = (i / per_row) * a.rstride + a.roff, c = (i % per_row) * 4;
         const float4 o = *reinterpret_cast<const float4*>(a.o + r * a.width + c);
         const float4 z = *reinterpret_cast<const float4*>(a.Y + r * a.ldy + a.zoff + c);
         const float y0 = o.x * (z.x / (1.f + expf(-z.x)));
@@ -225,6 +258,96 @@ __global__ void __launch_bounds__(kGateThreads) layer_gate_kernel(GateArgs a) {
         *reinterpret_cast<uint2*>(a.ylo + r * a.width + c) = lv;
     }
     griddep_launch();
+}
+
+struct TokenArgs {
+    const float* q;            // [B][N][H][dk]
+    const float* k;
+    const float* v;            // [B][N][H][dv]
+    const float* alpha;        // [B][N][H]
+    const float* beta;
+    const int32_t* parent;     // [B][N]
+    const float* S0;           // [B][H][dv][dk], state above the roots
+    float* S_nodes;            // [N][B][H][dv][dk], state after each node
+    float* o;                  // [B][N][H][dv]
+    int t, B, N, H, dk, dv;
+    int* err;
+};
+
+constexpr int kTokThreads = 256, kTokRows = 16;
+
+// One token of per-token decoding: S_t = alpha S_p + delta k^T with
+// delta = beta (v - alpha S_p k), o_t = S_t q, for node t of every sequence,
+// S_p the parent's materialised state (S0 above a root).  Grid (B H, dv / 16);
+// one warp per state row, two rows per warp.
+__global__ void __launch_bounds__(kTokThreads) token_step_kernel(TokenArgs a) {
+    const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = a.t, dk = a.dk, dv = a.dv;
+    griddep_wait();
+    int p = a.parent[(size_t)b * a.N + t];
+    if (p >= t || p < -1) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) set_error(a.err, GDN_ERR_TREE);
+        p = -1;
+    }
+    const size_t st = (size_t)dv * dk;
+    const float* Sp = p >= 0 ? a.S_nodes + (((size_t)p * a.B + b) * a.H + h) * st : a.S0 + ((size_t)b * a.H + h) * st;
+    float* St = a.S_nodes + (((size_t)t * a.B + b) * a.H + h) * st;
+    const size_t node = ((size_t)b * a.N + t) * a.H + h;
+    const float* kk = a.k + node * dk;
+    const float* qq = a.q + node * dk;
+    const float al = a.alpha[node], be = a.beta[node];
+    float4 kv[2], qv[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = 4 * lane + 128 * j;
+        kv[j] = i < dk ? *reinterpret_cast<const float4*>(kk + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        qv[j] = i < dk ? *reinterpret_cast<const float4*>(qq + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int rr = 0; rr < kTokRows / (kTokThreads / 32); ++rr) {
+        const int r = blockIdx.y * kTokRows + warp * (kTokRows / (kTokThreads / 32)) + rr;
+        if (r >= dv) break;
+        float4 x[2];
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = 4 * lane + 128 * j;
+            x[j] = i < dk ? *reinterpret_cast<const float4*>(Sp + (size_t)r * dk + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            s += x[j].x * kv[j].x + x[j].y * kv[j].y + x[j].z * kv[j].z + x[j].w * kv[j].w;
+        }
+        s = warp_sum(s);
+        const float d = be * (a.v[node * dv + r] - al * s);
+        float o = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int i = 4 * lane + 128 * j;
+            if (i < dk) {
+                const float4 y = make_float4(al * x[j].x + d * kv[j].x, al * x[j].y + d * kv[j].y,
+                                             al * x[j].z + d * kv[j].z, al * x[j].w + d * kv[j].w);
+                *reinterpret_cast<float4*>(St + (size_t)r * dk + i) = y;
+                o += y.x * qv[j].x + y.y * qv[j].y + y.z * qv[j].z + y.w * qv[j].w;
+            }
+        }
+        o = warp_sum(o);
+        if (lane == 0) a.o[node * dv + r] = o;
+    }
+    griddep_launch();
+}
+
+cudaError_t launch_conv(const ConvArgs& ca, cudaStream_t s) {
+    static size_t attr_set[64];    // dynamic shared memory opted into, per device (the kernel also has static)
+    const size_t smem = conv_smem_bytes(ca.N, ca.dk, ca.dv);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (smem > 48 * 1024 && attr_set[dev] < smem) {
+        e = cudaFuncSetAttribute(layer_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = smem;
+    }
+    return launch_kernel(layer_conv_kernel, dim3(ca.B, 3 * ca.H + 1), dim3(kConvThreads), smem, s, false, ca);
 }
 
 bool ok16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -274,6 +397,7 @@ LayerLayout layer_layout(int B, int N, int H, int hidden, int dk, int dv) {
     L.alpha_off = take(BN * H * 4);
     L.beta_off = take(BN * H * 4);
     L.o_off = take(BN * H * dv * 4);
+    for (int i = 0; i < 4; ++i) L.split_off[i] = take(BN * H * dk * 2);
     L.yhi_off = take(BN * H * dv * 2);
     L.ylo_off = take(BN * H * dv * 2);
     L.tws_off = take((size_t)B * H * ws_layout(N).record);
@@ -333,7 +457,7 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
     float* Y = reinterpret_cast<float*>(rec + Ly.y_off);
     const long long M = (long long)B * N;
 
-    cudaError_t e = launch_gemm_bf16(X, nullptr, 1, W_in, Y, Ly.ldy, (int)M, Ly.rows, hidden, err, stream);
+    cudaError_t e = launch_gemm_bf16(X, nullptr, 1, hidden, W_in, Y, Ly.ldy, (int)M, Ly.rows, hidden, err, stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
 
     ConvArgs ca;
@@ -356,8 +480,11 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
     ca.H = H;
     ca.dk = dk;
     ca.dv = dv;
+    for (int i = 0; i < 4; ++i) ca.qk_split[i] = reinterpret_cast<__nv_bfloat16*>(ws + Ly.split_off[i]);
+    ca.t0 = 0;
+    ca.t1 = N;
     ca.err = err;
-    e = launch_kernel(layer_conv_kernel, dim3(B, 3 * H + 1), dim3(kConvThreads), 0, stream, false, ca);
+    e = launch_conv(ca, stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
 
     VerifyArgs va;
@@ -383,6 +510,7 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
     } else {
         va.commit = CommitSrc{nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0};
     }
+    for (int i = 0; i < 4; ++i) va.split[i] = ca.qk_split[i];
     va.err = err;
     va.overlap = false;
     va.tc = false;
@@ -397,6 +525,8 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
     gaa.yhi = reinterpret_cast<__nv_bfloat16*>(ws + Ly.yhi_off);
     gaa.ylo = reinterpret_cast<__nv_bfloat16*>(ws + Ly.ylo_off);
     gaa.rows = M;
+    gaa.rstride = 1;
+    gaa.roff = 0;
     gaa.width = H * dv;
     const long long work = M * (H * dv / 4);
     long long blocks = (work + kGateThreads - 1) / kGateThreads;
@@ -404,6 +534,103 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
     e = launch_kernel(layer_gate_kernel, dim3((unsigned)blocks), dim3(kGateThreads), 0, stream, false, gaa);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
 
-    e = launch_gemm_bf16(gaa.yhi, gaa.ylo, 2, W_o, out, hidden, (int)M, hidden, H * dv, err, stream);
+    e = launch_gemm_bf16(gaa.yhi, gaa.ylo, 2, H * dv, W_o, out, hidden, (int)M, hidden, H * dv, err, stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, const void* W_o,
+                                    const int32_t* parent_idx, const float* S0, const float* conv_state,
+                                    float* S_nodes, int t, float* out, void* record, void* workspace, int B, int N,
+                                    int H, int hidden, int dk, int dv, cudaStream_t stream) {
+    if (!layer_shape_ok(B, N, H, hidden, dk, dv) || t < 0 || t >= N) return GDN_ERR_ARG;
+    if (!ok16(X) || !ok16(W_in) || !ok16(conv_w) || !ok16(W_o) || !ok16(parent_idx) || !ok16(S0) ||
+        !ok16(conv_state) || !ok16(S_nodes) || !ok16(out) || !ok16(record) || !ok16(workspace))
+        return GDN_ERR_ARG;
+    const LayerLayout Ly = layer_layout(B, N, H, hidden, dk, dv);
+    const size_t out_bytes = (size_t)B * N * hidden * 4;
+    const size_t node_bytes = (size_t)N * B * H * dv * dk * 4;
+    if (!disjoint(record, Ly.record_bytes, workspace, Ly.workspace_bytes) ||
+        !disjoint(out, out_bytes, record, Ly.record_bytes) || !disjoint(out, out_bytes, workspace, Ly.workspace_bytes) ||
+        !disjoint(S_nodes, node_bytes, record, Ly.record_bytes) ||
+        !disjoint(S_nodes, node_bytes, workspace, Ly.workspace_bytes) || !disjoint(S_nodes, node_bytes, out, out_bytes))
+        return GDN_ERR_ARG;
+    int st = GDN_OK;
+    int* err = current_error_word(&st);
+    if (err == nullptr) return st;
+
+    char* ws = static_cast<char*>(workspace);
+    float* Y = reinterpret_cast<float*>(static_cast<char*>(record) + Ly.y_off);
+    const __nv_bfloat16* Xt = static_cast<const __nv_bfloat16*>(X) + (size_t)t * hidden;
+    cudaError_t e = launch_gemm_bf16(Xt, nullptr, 1, (long long)N * hidden, W_in, Y + (size_t)t * Ly.ldy,
+                                     (long long)N * Ly.ldy, B, Ly.rows, hidden, err, stream);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+
+    ConvArgs ca;
+    ca.Y = Y;
+    ca.ldy = Ly.ldy;
+    ca.conv_w = conv_w;
+    ca.conv_state = const_cast<float*>(conv_state);   // read only: no accepted path to commit
+    ca.prevY = nullptr;
+    ca.N_prev = 0;
+    ca.prev_path = nullptr;
+    ca.Lmax = 0;
+    ca.parent = parent_idx;
+    ca.q = reinterpret_cast<float*>(ws + Ly.q_off);
+    ca.k = reinterpret_cast<float*>(ws + Ly.k_off);
+    ca.v = reinterpret_cast<float*>(ws + Ly.v_off);
+    ca.alpha = reinterpret_cast<float*>(ws + Ly.alpha_off);
+    ca.beta = reinterpret_cast<float*>(ws + Ly.beta_off);
+    ca.B = B;
+    ca.N = N;
+    ca.H = H;
+    ca.dk = dk;
+    ca.dv = dv;
+    for (int i = 0; i < 4; ++i) ca.qk_split[i] = nullptr;
+    ca.t0 = t;
+    ca.t1 = t + 1;
+    ca.err = err;
+    e = launch_conv(ca, stream);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+
+    TokenArgs ta;
+    ta.q = ca.q;
+    ta.k = ca.k;
+    ta.v = ca.v;
+    ta.alpha = ca.alpha;
+    ta.beta = ca.beta;
+    ta.parent = parent_idx;
+    ta.S0 = S0;
+    ta.S_nodes = S_nodes;
+    ta.o = reinterpret_cast<float*>(ws + Ly.o_off);
+    ta.t = t;
+    ta.B = B;
+    ta.N = N;
+    ta.H = H;
+    ta.dk = dk;
+    ta.dv = dv;
+    ta.err = err;
+    e = launch_kernel(token_step_kernel, dim3(B * H, (dv + kTokRows - 1) / kTokRows), dim3(kTokThreads), 0, stream,
+                      false, ta);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+
+    GateArgs gaa;
+    gaa.o = ta.o;
+    gaa.Y = Y;
+    gaa.ldy = Ly.ldy;
+    gaa.zoff = 2LL * H * dk + (long long)H * dv;
+    gaa.yhi = reinterpret_cast<__nv_bfloat16*>(ws + Ly.yhi_off);
+    gaa.ylo = reinterpret_cast<__nv_bfloat16*>(ws + Ly.ylo_off);
+    gaa.rows = B;
+    gaa.rstride = N;
+    gaa.roff = t;
+    gaa.width = H * dv;
+    const long long work = (long long)B * (H * dv / 4);
+    e = launch_kernel(layer_gate_kernel, dim3((unsigned)((work + kGateThreads - 1) / kGateThreads)),
+                      dim3(kGateThreads), 0, stream, false, gaa);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+
+    const size_t ro = (size_t)t * H * dv;
+    e = launch_gemm_bf16(gaa.yhi + ro, gaa.ylo + ro, 2, (long long)N * H * dv, W_o, out + (size_t)t * hidden,
+                         (long long)N * hidden, B, hidden, H * dv, err, stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

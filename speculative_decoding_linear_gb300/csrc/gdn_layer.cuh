@@ -10,11 +10,11 @@ namespace gdn {
 constexpr int kConvTaps = 4;      // causal depthwise convolution, kernel size 4
 
 // C[M x Nc] (fp32, row stride ldc elements) = sum_s A_s[M x K] B[Nc x K]^T with
-// bf16 row-major operands (K contiguous).  nA = 1, or 2 for an fp32 left
-// operand carried as two bf16 terms (hi + lo).  K must be a multiple of 64;
-// rows of every operand 16-byte aligned.
-cudaError_t launch_gemm_bf16(const void* A0, const void* A1, int nA, const void* B, float* C, long long ldc,
-                             int M, int Nc, int K, int* err, cudaStream_t s);
+// bf16 row-major operands (K contiguous; A rows lda elements apart, B rows K).
+// nA = 1, or 2 for an fp32 left operand carried as two bf16 terms (hi + lo).
+// K must be a multiple of 64, lda a multiple of 8; operands 16-byte aligned.
+cudaError_t launch_gemm_bf16(const void* A0, const void* A1, int nA, long long lda, const void* B, float* C,
+                             long long ldc, int M, int Nc, int K, int* err, cudaStream_t s);
 
 // Sizes of the layer's record (kept until the next step's commit) and workspace.
 struct LayerLayout {
@@ -25,7 +25,8 @@ struct LayerLayout {
     // record
     size_t y_off, fac_off, record_bytes;
     // workspace
-    size_t q_off, k_off, v_off, alpha_off, beta_off, o_off, yhi_off, ylo_off, tws_off, workspace_bytes;
+    size_t q_off, k_off, v_off, alpha_off, beta_off, o_off, split_off[4], yhi_off, ylo_off, tws_off,
+        workspace_bytes;
 };
 
 LayerLayout layer_layout(int B, int N, int H, int hidden, int dk, int dv);

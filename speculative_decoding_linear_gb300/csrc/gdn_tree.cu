@@ -452,6 +452,10 @@ cudaError_t launch_tree_verify(const VerifyArgs& args, int dtype, cudaStream_t s
     VerifyArgs a = args;
     cudaError_t e;
     if (dtype == GDN_DTYPE_F32) {
+        if (a.split[0] != nullptr && tc_contract_eligible(a)) {   // fp32 q/k with bf16 hi/lo terms
+            a.tc = true;
+            return launch_tree_tc(a, s);
+        }
         a.tc = false;
         e = launch_tree_prep<float>(a, s);
         if (e != cudaSuccess) return e;

@@ -54,7 +54,8 @@ constexpr int kDk = 256;           // d_k handled by this kernel
 constexpr int kSlabs = kDk / kSlab;
 constexpr int kNodeRows = 64;      // B operand: Q rows 0..63, K rows 64..127 (MMA N = 128)
 constexpr int kBufBytes = kTileV * 128;        // one 128-row x 128-byte operand buffer (16 KiB)
-constexpr int kStageBytes = 3 * kBufBytes;     // A_hi, A_lo, B
+// Stage: A_hi, A_lo, B (bf16 q/k), plus B_lo when fp32 q/k enter as bf16 hi + lo.
+__host__ __device__ constexpr int stage_bytes(bool split) { return (split ? 4 : 3) * kBufBytes; }
 constexpr uint32_t kTmemCols = 256;     // Y in columns 0..127, [Delta | P R] in 128..255
 constexpr int kMaxTcPath = 16;
 constexpr uint32_t kIdesc = idesc_bf16(128, 128);   // D fp32, A/B bf16 K-major, M = N = 128
@@ -62,11 +63,11 @@ constexpr uint32_t kIdesc = idesc_bf16(128, 128);   // D fp32, A/B bf16 K-major,
 struct TcLayout {
     // offsets from the 1024-aligned base
     int cd, key, coef, nodes, bars, misc, egbt, total;
-    __host__ __device__ TcLayout(int Lcap) {
-        int o = 2 * kStageBytes;
+    __host__ __device__ TcLayout(int Lcap, bool split) {
+        int o = 2 * stage_bytes(split);
         auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
         cd = take(Lcap * kTileV * 4);
-        key = take(Lcap * kDk * 2);
+        key = take(Lcap * kDk * (split ? 4 : 2));
         coef = take(kMaxPath * 4);
         nodes = take(kMaxPath * 4);
         bars = take(64);
@@ -75,6 +76,9 @@ struct TcLayout {
         total = o + 1024;   // slack for aligning the base to 1024 bytes
     }
 };
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 // One state slab (this thread's 8 float4 of a 128 x 64 fp32 block) and its
 // conversion to the bf16 hi/lo A-operand buffers of one stage.
@@ -87,8 +91,9 @@ __device__ __forceinline__ void load_slab(float4 (&x)[8], const float* S, size_t
 // S <- e^{g_a} S + sum_i cd_i[row] k_i[col..col+3], path node outermost (one key
 // quad per node serves the thread's 8 rows); per element the same order of
 // operations as commit_quad, so the result is bit-identical to gdn_commit.
+template <typename KT>
 __device__ __forceinline__ void commit_slab(float4 (&x)[8], float ega, int L, const float* s_cd,
-                                            const __nv_bfloat16* s_key, int rbase, int col) {
+                                            const KT* s_key, int rbase, int col) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         x[j].x *= ega;
@@ -97,7 +102,7 @@ __device__ __forceinline__ void commit_slab(float4 (&x)[8], float ega, int L, co
         x[j].w *= ega;
     }
     for (int i = 0; i < L; ++i) {
-        const float4 kq = ld4<__nv_bfloat16>(s_key, (size_t)i * kDk + col);
+        const float4 kq = ld4<KT>(s_key, (size_t)i * kDk + col);
         const float* cdi = s_cd + i * kTileV + rbase;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -137,7 +142,10 @@ __device__ __forceinline__ void convert_slab(const float4 (&x)[8], unsigned char
     }
 }
 
-// Four K-steps of one slab, hi and lo terms, into the Y accumulator.
+// Four K-steps of one slab into the Y accumulator: state hi and lo terms times
+// bf16 q/k, plus state hi times the lo term of fp32 q/k (the lo.lo product,
+// ~2^-16 of the hi.lo ones, is dropped).
+template <bool kSplit>
 __device__ __forceinline__ void issue_slab_mma(uint32_t tmem, uint32_t stage_s, bool first) {
     const uint32_t a_hi = stage_s, a_lo = stage_s + kBufBytes, bsm = stage_s + 2 * kBufBytes;
 #pragma unroll
@@ -145,26 +153,37 @@ __device__ __forceinline__ void issue_slab_mma(uint32_t tmem, uint32_t stage_s, 
         const uint64_t bd = sw128_desc(bsm + kk * 32);
         mma_bf16(tmem, sw128_desc(a_hi + kk * 32), bd, kIdesc, (!first || kk > 0) ? 1u : 0u);
         mma_bf16(tmem, sw128_desc(a_lo + kk * 32), bd, kIdesc, 1u);
+        if (kSplit) mma_bf16(tmem, sw128_desc(a_hi + kk * 32), sw128_desc(bsm + kBufBytes + kk * 32), kIdesc, 1u);
     }
 }
 
-__device__ __forceinline__ void issue_qk_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint32_t stage_s,
-                                             int ks, int h, int row0, uint32_t bar) {
+template <bool kSplit>
+__device__ __forceinline__ void issue_qk_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmQl,
+                                             const CUtensorMap* tmKl, uint32_t stage_s, int ks, int h, int row0,
+                                             uint32_t bar) {
     const uint32_t bsm = stage_s + 2 * kBufBytes;
-    mbar_expect_tx(bar, 2 * kNodeRows * 128);
+    mbar_expect_tx(bar, (kSplit ? 4 : 2) * kNodeRows * 128);
     tma_load_3d(bsm, tmQ, ks * kSlab, h, row0, bar);
     tma_load_3d(bsm + kNodeRows * 128, tmK, ks * kSlab, h, row0, bar);
+    if (kSplit) {
+        tma_load_3d(bsm + kBufBytes, tmQl, ks * kSlab, h, row0, bar);
+        tma_load_3d(bsm + kBufBytes + kNodeRows * 128, tmKl, ks * kSlab, h, row0, bar);
+    }
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 2)
     tree_contract_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmQl, const __grid_constant__ CUtensorMap tmKl,
                             VerifyArgs a) {
+    using KT = typename std::conditional<kSplit, float, __nv_bfloat16>::type;   // key / v element type
+    constexpr int kStageBytes = stage_bytes(kSplit);
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     unsigned char* base = smem_raw + (base_s - raw_s);
     const bool fused = a.commit.path != nullptr;
-    const TcLayout Ly(fused ? a.commit.Lmax : 0);
+    const TcLayout Ly(fused ? a.commit.Lmax : 0, kSplit);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;
@@ -173,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int v0 = blockIdx.y * kTileV;
 
     float* s_cd = reinterpret_cast<float*>(base + Ly.cd);
-    __nv_bfloat16* s_key = reinterpret_cast<__nv_bfloat16*>(base + Ly.key);
+    KT* s_key = reinterpret_cast<KT*>(base + Ly.key);
     float* s_coef = reinterpret_cast<float*>(base + Ly.coef);
     int* s_nodes = reinterpret_cast<int*>(base + Ly.nodes);
     const uint32_t bar_tma0 = base_s + Ly.bars, bar_mma0 = base_s + Ly.bars + 16;
@@ -225,11 +244,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         const int L = *s_flag;
         if (L > 0) {
-            const __nv_bfloat16* key_bh =
-                static_cast<const __nv_bfloat16*>(a.commit.key) + (size_t)bh * a.commit.N * kDk;
+            const KT* key_bh = static_cast<const KT*>(a.commit.key) + (size_t)bh * a.commit.N * kDk;
             for (int i = 0; i < L; ++i)
-                cp_async_block(s_key + (size_t)i * kDk, key_bh + (size_t)s_nodes[i] * kDk, kDk * 2, tid,
-                               kThreads);
+                cp_async_block(s_key + (size_t)i * kDk, key_bh + (size_t)s_nodes[i] * kDk, kDk * (int)sizeof(KT),
+                               tid, kThreads);
             const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
             for (int i = tid; i < L * kTileV; i += kThreads) {
                 const int j = i / kTileV, r = i % kTileV;
@@ -276,27 +294,27 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (run) {
         if (tid == 0) {
-            issue_qk_tma(&tmQ, &tmK, stage0, 0, h, b * N, bar_tma0);
-            issue_qk_tma(&tmQ, &tmK, stage1, 1, h, b * N, bar_tma0 + 8);
+            issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage0, 0, h, b * N, bar_tma0);
+            issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage1, 1, h, b * N, bar_tma0 + 8);
             mbar_expect_tx(bar_eg, 2 * kNodeRows * 4);
             bulk_copy_g2s(smem_u32(seg), rec + wl.eg, kNodeRows * 4, bar_eg);
             bulk_copy_g2s(smem_u32(sbt), rec + wl.bt, kNodeRows * 4, bar_eg);
             ok = mbar_wait(bar_tma0, 0, a.err);
             if (ok) {
                 tc_fence_after();
-                issue_slab_mma(tmem, stage0, true);
+                issue_slab_mma<kSplit>(tmem, stage0, true);
                 mma_commit(bar_mma0);
                 ok = mbar_wait(bar_tma0 + 8, 0, a.err);
             }
             if (ok) {
                 tc_fence_after();
-                issue_slab_mma(tmem, stage1, false);
+                issue_slab_mma<kSplit>(tmem, stage1, false);
                 mma_commit(bar_mma0 + 8);
             }
         }
         // slabs 2 and 3 reuse the stages once the MMAs of slabs 0 and 1 are done
         ok = mbar_wait(bar_mma0, 0, a.err) && ok;
-        if (tid == 0 && ok) issue_qk_tma(&tmQ, &tmK, stage0, 2, h, b * N, bar_tma0);
+        if (tid == 0 && ok) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage0, 2, h, b * N, bar_tma0);
         convert_slab(x2, base, rbase, c4);
         fence_proxy_async_smem();
         __syncthreads();
@@ -304,12 +322,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             ok = mbar_wait(bar_tma0, 1, a.err);
             if (ok) {
                 tc_fence_after();
-                issue_slab_mma(tmem, stage0, false);
+                issue_slab_mma<kSplit>(tmem, stage0, false);
                 mma_commit(bar_mma0);
             }
         }
         ok = mbar_wait(bar_mma0 + 8, 0, a.err) && ok;
-        if (tid == 0 && ok) issue_qk_tma(&tmQ, &tmK, stage1, 3, h, b * N, bar_tma0 + 8);
+        if (tid == 0 && ok) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage1, 3, h, b * N, bar_tma0 + 8);
         convert_slab(x3, base + kStageBytes, rbase, c4);
         fence_proxy_async_smem();
         __syncthreads();
@@ -317,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             ok = mbar_wait(bar_tma0 + 8, 1, a.err);
             if (ok) {
                 tc_fence_after();
-                issue_slab_mma(tmem, stage1, false);
+                issue_slab_mma<kSplit>(tmem, stage1, false);
                 mma_commit(bar_mma0 + 8);
             }
         }
@@ -331,14 +349,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t v_s = stage0 + 2 * kBufBytes;                   // v rows: [t][128] bf16
         if (ok && warp == 0) {
             if (lane == 0) {
-                mbar_expect_tx(bar_op, (uint32_t)(kTcOperandBytes + N * kTileV * 2));
+                mbar_expect_tx(bar_op, (uint32_t)(kTcOperandBytes + N * kTileV * (int)sizeof(KT)));
                 bulk_copy_g2s(op_s, rec + wl.op, (uint32_t)kTcOperandBytes, bar_op);
             }
             __syncwarp();
-            const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(a.v);
+            const KT* vv = static_cast<const KT*>(a.v);
             for (int t = lane; t < N; t += 32)
-                bulk_copy_g2s(v_s + t * kTileV * 2, vv + (((size_t)b * N + t) * a.H + h) * dv + v0,
-                              kTileV * 2, bar_op);
+                bulk_copy_g2s(v_s + t * kTileV * (int)sizeof(KT), vv + (((size_t)b * N + t) * a.H + h) * dv + v0,
+                              kTileV * (int)sizeof(KT), bar_op);
         }
         if (ok) ok = mbar_wait(bar_mma0 + 8, 1, a.err);                // Y complete
         if (ok) ok = mbar_wait(bar_op, 0, a.err);                      // operand and v rows landed
@@ -348,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         const int v = 32 * (warp & 3) + lane;            // state row of this thread (TMEM lane)
         const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const __nv_bfloat16* vsm = reinterpret_cast<const __nv_bfloat16*>(base + 2 * kBufBytes);
+        const KT* vsm = reinterpret_cast<const KT*>(base + 2 * kBufBytes);   // v rows: [t][128]
         if (ok) {
             // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) as bf16 hi + lo rows of
             // the second MMA's A operand (row v, 64 columns t); warps 0-3 take t < 32, warps 4-7 the rest
@@ -364,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int e = 0; e < 4; ++e) {
                     const int i0 = 8 * q8 + 2 * e, i1 = i0 + 1;
                     const int t0 = 32 * c + i0, t1 = t0 + 1;
-                    const float r0 = t0 < N ? sbt[t0] * (__bfloat162float(vsm[t0 * kTileV + v]) - seg[t0] * yk[i0]) : 0.f;
-                    const float r1 = t1 < N ? sbt[t1] * (__bfloat162float(vsm[t1 * kTileV + v]) - seg[t1] * yk[i1]) : 0.f;
+                    const float r0 = t0 < N ? sbt[t0] * (to_f32(vsm[t0 * kTileV + v]) - seg[t0] * yk[i0]) : 0.f;
+                    const float r1 = t1 < N ? sbt[t1] * (to_f32(vsm[t1 * kTileV + v]) - seg[t1] * yk[i1]) : 0.f;
                     const __nv_bfloat162 hh = __floats2bfloat162_rn(r0, r1);
                     const float2 hf = __bfloat1622float2(hh);
                     const __nv_bfloat162 ll = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
@@ -448,14 +466,14 @@ struct PrepTcLayout {
     // Once the Gram MMA has consumed them and the keys are copied out, the
     // A, Attn and T tables reuse that space.
     int G, A, At, T, plist, par, anc, la, g, beta, depth, bars, misc, total, ld;
-    __host__ __device__ PrepTcLayout(int N) {
+    __host__ __device__ PrepTcLayout(int N, bool split) {
         ld = N + 1;
         int o = 0;
         auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
         A = take(N * ld * 4);
         At = take(N * ld * 4);
         T = take(N * ld * 4);
-        o = kSlabs * kBufBytes;
+        o = kSlabs * kBufBytes * (split ? 2 : 1);   // [Q; K] hi, then lo for fp32 q/k
         G = take(128 * 65 * 4);          // Gram rows: q_t.k_j (rows 0..63), k_t.k_j (rows 64..127)
         plist = take(N * 64);
         par = take(N * 4);
@@ -478,15 +496,18 @@ struct PrepTcLayout {
 // form of [T; P].
 // At most 128 registers per thread, so that a prologue CTA and a contraction
 // CTA (of the previous or the same call) fit on one SM together.
+template <bool kSplit>
 __global__ void __launch_bounds__(kPrepThreads, 2)
     tree_prep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmQl, const __grid_constant__ CUtensorMap tmKl,
                         VerifyArgs a) {
+    constexpr uint32_t kLoOff = kSlabs * kBufBytes;     // [Q; K] lo terms (fp32 q/k only)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     unsigned char* base = smem_raw + (base_s - raw_s);
     const int N = a.N, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const PrepTcLayout Ly(N);
+    const PrepTcLayout Ly(N, kSplit);
     const int ld = Ly.ld;
     float* sG = reinterpret_cast<float*>(base + Ly.G);
     float* sA = reinterpret_cast<float*>(base + Ly.A);
@@ -524,11 +545,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     griddep_launch();
 
     if (tid == 0) {
-        mbar_expect_tx(bar_tma, (uint32_t)(kSlabs * 2 * kNodeRows * 128));
+        mbar_expect_tx(bar_tma, (uint32_t)(kSlabs * 2 * kNodeRows * 128 * (kSplit ? 2 : 1)));
 #pragma unroll
         for (int sl = 0; sl < kSlabs; ++sl) {
             tma_load_3d(base_s + sl * kBufBytes, &tmQ, sl * kSlab, h, b * N, bar_tma);
             tma_load_3d(base_s + sl * kBufBytes + kNodeRows * 128, &tmK, sl * kSlab, h, b * N, bar_tma);
+            if (kSplit) {
+                tma_load_3d(base_s + kLoOff + sl * kBufBytes, &tmQl, sl * kSlab, h, b * N, bar_tma);
+                tma_load_3d(base_s + kLoOff + sl * kBufBytes + kNodeRows * 128, &tmKl, sl * kSlab, h, b * N,
+                            bar_tma);
+            }
         }
     }
     bool bad = false;
@@ -556,11 +582,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                     const uint32_t q_s = base_s + sl * kBufBytes + kk * 32;
                     mma_bf16(tmem, sw128_desc(q_s), sw128_desc(q_s + kNodeRows * 128), kGramIdesc,
                              (sl > 0 || kk > 0) ? 1u : 0u);
+                    if (kSplit) {             // hi.lo and lo.hi terms of fp32 q/k
+                        mma_bf16(tmem, sw128_desc(q_s), sw128_desc(q_s + kLoOff + kNodeRows * 128), kGramIdesc, 1u);
+                        mma_bf16(tmem, sw128_desc(q_s + kLoOff), sw128_desc(q_s + kNodeRows * 128), kGramIdesc, 1u);
+                    }
                 }
             mma_commit(bar_mma);
         }
         if (tid < N) {
             prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
+        } else if (kSplit) {
+            // fp32 keys into the factor record, from the fp32 inputs
+            float* key_out = static_cast<float*>(a.f.key) + (size_t)bh * N * kDk;
+            const float* kin = static_cast<const float*>(a.k);
+            for (int item = tid - N; item < N * (kDk / 4); item += kPrepThreads - N) {
+                const int t = item / (kDk / 4), c4 = item % (kDk / 4);
+                *reinterpret_cast<float4*>(key_out + (size_t)t * kDk + 4 * c4) =
+                    *reinterpret_cast<const float4*>(kin + (((size_t)b * N + t) * a.H + h) * kDk + 4 * c4);
+            }
         } else {
             // keys into the factor record, unswizzled from the K half of the operand
             __nv_bfloat16* key_out = static_cast<__nv_bfloat16*>(a.f.key) + (size_t)bh * N * kDk;
@@ -642,22 +681,39 @@ bool tc_contract_eligible(const VerifyArgs& a) {
     return encode_fn() != nullptr;
 }
 
-cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s) {
+template <bool kSplit>
+cudaError_t launch_tree_tc_impl(const VerifyArgs& a, cudaStream_t s) {
     static bool attr_p[64], attr_c[64];
-    CUtensorMap tq, tk;
-    if (!make_qk_map(&tq, a.q, a.B, a.N, a.H) || !make_qk_map(&tk, a.k, a.B, a.N, a.H))
-        return cudaErrorInvalidValue;
-    const PrepTcLayout Lp(a.N);
-    cudaError_t e = ensure_smem(tree_prep_tc_kernel, Lp.total, attr_p);
+    CUtensorMap tq, tk, tql, tkl;
+    const void* qh = kSplit ? a.split[0] : a.q;
+    const void* kh = kSplit ? a.split[1] : a.k;
+    if (!make_qk_map(&tq, qh, a.B, a.N, a.H) || !make_qk_map(&tk, kh, a.B, a.N, a.H)) return cudaErrorInvalidValue;
+    if (kSplit) {
+        if (!make_qk_map(&tql, a.split[2], a.B, a.N, a.H) || !make_qk_map(&tkl, a.split[3], a.B, a.N, a.H))
+            return cudaErrorInvalidValue;
+    } else {
+        tql = tq;
+        tkl = tk;
+    }
+    const PrepTcLayout Lp(a.N, kSplit);
+    cudaError_t e = ensure_smem(tree_prep_tc_kernel<kSplit>, Lp.total, attr_p);
     if (e != cudaSuccess) return e;
-    e = launch_kernel(tree_prep_tc_kernel, dim3(a.B * a.H), dim3(kPrepThreads), Lp.total, s, a.overlap, tq, tk, a);
+    e = launch_kernel(tree_prep_tc_kernel<kSplit>, dim3(a.B * a.H), dim3(kPrepThreads), Lp.total, s, a.overlap, tq, tk,
+                      tql, tkl, a);
     if (e != cudaSuccess) return e;
-    const TcLayout Ly(a.commit.path ? a.commit.Lmax : 0);
-    e = ensure_smem(tree_contract_tc_kernel, Ly.total, attr_c);
+    const TcLayout Ly(a.commit.path ? a.commit.Lmax : 0, kSplit);
+    e = ensure_smem(tree_contract_tc_kernel<kSplit>, Ly.total, attr_c);
     if (e != cudaSuccess) return e;
     dim3 grid(a.B * a.H, a.dv / kTileV);
     // always a programmatic dependent of the prologue kernel launched just before it
-    return launch_kernel(tree_contract_tc_kernel, grid, dim3(kThreads), Ly.total, s, true, tq, tk, a);
+    return launch_kernel(tree_contract_tc_kernel<kSplit>, grid, dim3(kThreads), Ly.total, s, true, tq, tk, tql, tkl,
+                         a);
+}
+
+// bf16 q/k (or fp32 q/k with their bf16 hi/lo terms in `split`) with the
+// tensor-core kernels: see launch_tree_verify.
+cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s) {
+    return a.split[0] != nullptr ? launch_tree_tc_impl<true>(a, s) : launch_tree_tc_impl<false>(a, s);
 }
 
 }  // namespace gdn

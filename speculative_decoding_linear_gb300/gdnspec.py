@@ -43,6 +43,8 @@ SIGNATURES = {
     "gdn_layer_workspace_bytes": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
     "gdn_layer_tree_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P,
                                  _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_layer_token_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
+                                  _I, _I, _I, _I, _I, _I, _P]),
     "gdn_set_launch_overlap": (_I, [_I]),
     "gdn_last_error": (_I, [_P]),
     "gdn_strerror": (ctypes.c_char_p, [_I]),
@@ -236,6 +238,17 @@ def gdn_layer_tree_step(X, W_in, conv_w, W_o, parent_idx, S, conv_state, prev_re
                                      _stream(stream)), "gdn_layer_tree_step")
 
 
+def gdn_layer_token_step(X, W_in, conv_w, W_o, parent_idx, S0, conv_state, S_nodes, t, out, record, workspace,
+                         H, dk, dv, stream=None):
+    """Decode node t of every tree on its own from its parent's materialised state (see
+    include/gdnspec.h); S_nodes is [N, B, H, dv, dk] fp32."""
+    B, N, hidden = X.shape
+    _check(lib().gdn_layer_token_step(_ptr(X), _ptr(W_in), _ptr(conv_w), _ptr(W_o), _ptr(parent_idx), _ptr(S0),
+                                      _ptr(conv_state), _ptr(S_nodes), int(t), _ptr(out), _ptr(record),
+                                      _ptr(workspace), B, N, H, hidden, dk, dv, _stream(stream)),
+           "gdn_layer_token_step")
+
+
 def gdn_set_launch_overlap(enable: bool) -> bool:
     """Process-wide switch; returns the previous setting (see include/gdnspec.h)."""
     return bool(lib().gdn_set_launch_overlap(1 if enable else 0))
@@ -278,10 +291,13 @@ def layer_record_views(buf, B, N, H, hidden, dk, dv):
 
 
 def layer_workspace_views(buf, B, N, H, hidden, dk, dv):
-    """q, k [B,N,H,dk], v, o [B,N,H,dv], alpha, beta [B,N,H] fp32 and y_hi, y_lo [B*N, H*dv] bf16."""
+    """q, k [B,N,H,dk], v, o [B,N,H,dv], alpha, beta [B,N,H] fp32; the bf16 hi/lo terms of q and k;
+    y_hi, y_lo [B*N, H*dv] bf16."""
     BN = B * N
     sizes = [("q", BN * H * dk * 4), ("k", BN * H * dk * 4), ("v", BN * H * dv * 4), ("alpha", BN * H * 4),
-             ("beta", BN * H * 4), ("o", BN * H * dv * 4), ("yhi", BN * H * dv * 2), ("ylo", BN * H * dv * 2)]
+             ("beta", BN * H * 4), ("o", BN * H * dv * 4), ("qhi", BN * H * dk * 2), ("khi", BN * H * dk * 2),
+             ("qlo", BN * H * dk * 2), ("klo", BN * H * dk * 2), ("yhi", BN * H * dv * 2),
+             ("ylo", BN * H * dv * 2)]
     out, off = {}, 0
     for name, n in sizes:
         out[name] = buf[off:off + n]

@@ -84,6 +84,8 @@ SMALL = [  # (B, N, H, dk, dv, hidden, maxdepth): ragged GEMM tiles in M, N and 
     (2, 16, 2, 64, 64, 128, 4),
     (3, 37, 2, 32, 64, 192, 8),
     (5, 64, 1, 128, 128, 256, 8),
+    (3, 64, 2, 256, 256, 256, 8),      # d_k = 256: tensor-core verification with split fp32 q/k
+    (4, 23, 1, 256, 128, 128, 3),
 ]
 
 
@@ -101,7 +103,7 @@ def test_layer_step_matches_oracle(oracle_mod, shape):
     assert torch.equal(run.conv_state.cpu(), torch.from_numpy(w.conv_state))
 
 
-@pytest.mark.parametrize("shape", SMALL[:2])
+@pytest.mark.parametrize("shape", SMALL[:2] + SMALL[3:])
 def test_two_steps_commit_state_and_conv_history(oracle_mod, shape):
     from oracle import layer
     B, N, H, dk, dv, hid, md = shape
@@ -126,3 +128,32 @@ def test_layer_full_size(oracle_mod):
     out, Y, fac, views = run.step(w.X, w.parent)
     r = oracle_step(layer, w, w.X, w.parent, w.widened("S0"), w.widened("conv_state"))
     compare(w, r, out, Y, fac, views, w.parent)
+
+
+@pytest.mark.parametrize("shape", SMALL[:2])
+def test_per_token_decode_matches_oracle(oracle_mod, shape):
+    """Node-by-node decoding from materialised parent states gives the tree step's outputs."""
+    from oracle import layer
+    B, N, H, dk, dv, hid, md = shape
+    w = wl.make_layer_workload(4, seed=91 + B, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=md)
+    X = bf16(w.X)
+    W_in, W_o, cw = bf16(w.W_in), bf16(w.W_o), f32(w.conv_w)
+    S0, cs = f32(w.S0), f32(w.conv_state)
+    parent = torch.from_numpy(w.parent).cuda()
+    rec = torch.empty(gdnspec.gdn_layer_record_bytes(B, N, H, hid, dk, dv), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(gdnspec.gdn_layer_workspace_bytes(B, N, H, hid, dk, dv), dtype=torch.uint8, device="cuda")
+    S_nodes = torch.empty((N, B, H, dv, dk), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, N, hid), dtype=torch.float32, device="cuda")
+    for t in range(N):
+        gdnspec.gdn_layer_token_step(X, W_in, cw, W_o, parent, S0, cs, S_nodes, t, out, rec, ws, H, dk, dv)
+    assert gdnspec.gdn_last_error() == gdnspec.OK
+    r = oracle_step(layer, w, w.X, w.parent, w.widened("S0"), w.widened("conv_state"))
+    views = gdnspec.layer_workspace_views(ws, B, N, H, hid, dk, dv)
+    assert_close(views["o"].cpu().numpy(), r["o"], "o")
+    assert_close(out.cpu().numpy(), r["out"], "layer output")
+    # the materialised state of each accepted end node equals the oracle's commit of its path
+    S_ref = oracle_mod.commit(r["k"], r["v"], r["alpha"], r["beta"], w.parent, w.widened("S0"), w.path)
+    ends = [int(p[p >= 0][-1]) for p in w.path]
+    got = np.stack([S_nodes[ends[b], b].cpu().numpy() for b in range(B)])
+    assert_close(got, S_ref, "node state")
+    assert torch.equal(cs.cpu(), torch.from_numpy(w.conv_state))
