@@ -156,39 +156,38 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     cp_async_wait_all();
     __syncthreads();
 
-    float val[kMaxNodes];
-#pragma unroll
-    for (int t = 0; t < kMaxNodes; ++t) {
-        val[t] = 0.f;
-        if (t >= a.t0 && t < a.t1 && act) {
-            float x[kConvTaps];
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                const int sidx = s_win[t][i];
-                x[i] = sidx >= 0 ? s_y[sidx * d + tid] : (sidx == -1 ? hrow[0] : sidx == -2 ? hrow[1] : hrow[2]);
-            }
-            x[3] = s_y[t * d + tid];
-            val[t] = w[0] * x[0] + w[1] * x[1] + w[2] * x[2] + w[3] * x[3];
+    // Depthwise: thread `tid` only ever touches channel column tid of s_y, so each
+    // output overwrites its own input in place.  Descending node order keeps every
+    // window's ancestor rows (lower indices) unmodified until they are read.
+    const int warp = tid >> 5, lane = tid & 31;
+    if (act) {
+        const float h0 = hrow[0], h1 = hrow[1], h2 = hrow[2];
+#pragma unroll 1
+        for (int t = a.t1 - 1; t >= a.t0; --t) {
+            const int s0 = s_win[t][0], s1 = s_win[t][1], s2 = s_win[t][2];
+            const float x0 = s0 >= 0 ? s_y[s0 * d + tid] : (s0 == -1 ? h0 : s0 == -2 ? h1 : h2);
+            const float x1 = s1 >= 0 ? s_y[s1 * d + tid] : (s1 == -1 ? h0 : s1 == -2 ? h1 : h2);
+            const float x2 = s2 >= 0 ? s_y[s2 * d + tid] : (s2 == -1 ? h0 : s2 == -2 ? h1 : h2);
+            const float x3 = s_y[t * d + tid];
+            s_y[t * d + tid] = w[0] * x0 + w[1] * x1 + w[2] * x2 + w[3] * x3;
         }
     }
 
     if (seg == 2) {
         if (act) {
-#pragma unroll
-            for (int t = 0; t < kMaxNodes; ++t)
-                if (t >= a.t0 && t < a.t1) a.v[(((size_t)b * N + t) * H + h) * dv + tid] = val[t];
+#pragma unroll 1
+            for (int t = a.t0; t < a.t1; ++t) a.v[(((size_t)b * N + t) * H + h) * dv + tid] = s_y[t * d + tid];
         }
         griddep_launch();
         return;
     }
 
-    const int warp = tid >> 5, lane = tid & 31;
-#pragma unroll
-    for (int t = 0; t < kMaxNodes; ++t) {
-        if (t >= a.t0 && t < a.t1) {
-            const float ss = warp_sum(val[t] * val[t]);
-            if (lane == 0) s_red[warp][t] = ss;
-        }
+    // per-node squared norms: warp partial sums, then across the block's warps
+#pragma unroll 1
+    for (int t = a.t0; t < a.t1; ++t) {
+        const float y = act ? s_y[t * d + tid] : 0.f;
+        const float ss = warp_sum(y * y);
+        if (lane == 0) s_red[warp][t] = ss;
     }
     __syncthreads();
     if (tid >= a.t0 && tid < a.t1) {
@@ -201,17 +200,15 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         float* dst = seg == 0 ? a.q : a.k;
         __nv_bfloat16* dhi = a.qk_split[seg];
         __nv_bfloat16* dlo = a.qk_split[2 + seg];
-#pragma unroll
-        for (int t = 0; t < kMaxNodes; ++t) {
-            if (t >= a.t0 && t < a.t1) {
-                const size_t o = (((size_t)b * N + t) * H + h) * dk + tid;
-                const float y = val[t] * s_rn[t];
-                dst[o] = y;
-                if (dhi != nullptr) {
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(y);
-                    dhi[o] = hi;
-                    dlo[o] = __float2bfloat16_rn(y - __bfloat162float(hi));
-                }
+#pragma unroll 1
+        for (int t = a.t0; t < a.t1; ++t) {
+            const size_t o = (((size_t)b * N + t) * H + h) * dk + tid;
+            const float y = s_y[t * d + tid] * s_rn[t];
+            dst[o] = y;
+            if (dhi != nullptr) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(y);
+                dhi[o] = hi;
+                dlo[o] = __float2bfloat16_rn(y - __bfloat162float(hi));
             }
         }
     }
