@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     extern __shared__ __align__(16) float s_y[];   // [N][d]
     __shared__ int s_win[kMaxNodes][3];       // window sources: >= 0 node, -1 - r history row r
     __shared__ int s_need[kMaxNodes];
-    __shared__ float s_red[kConvThreads / 32][kMaxNodes];
+    __shared__ int s_par[kMaxNodes];
     __shared__ float s_rn[kMaxNodes];
     __shared__ int s_path[kMaxPath];
     __shared__ int s_L;
@@ -84,31 +84,36 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     const int d = seg == 2 ? dv : dk;
     const int cb = seg == 0 ? h * dk : seg == 1 ? H * dk + h * dk : 2 * H * dk + h * dv;
 
-    if (tid == 0) {
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp == 1) {                          // accepted path of the previous step: length and nodes
         int L = 0;
         if (a.prev_path != nullptr) {
             const int32_t* p = a.prev_path + (size_t)b * a.Lmax;
-            while (L < a.Lmax && p[L] >= 0) {
-                if (p[L] >= a.N_prev) {
-                    set_error(a.err, GDN_ERR_PATH);
-                    L = 0;
-                    break;
-                }
-                s_path[L] = p[L];
-                ++L;
+            const int p0 = lane < a.Lmax ? p[lane] : -1;
+            const int p1 = lane + 32 < a.Lmax ? p[lane + 32] : -1;
+            const unsigned n0 = __ballot_sync(0xffffffffu, p0 < 0), n1 = __ballot_sync(0xffffffffu, p1 < 0);
+            L = n0 ? __ffs(n0) - 1 : (n1 ? 32 + __ffs(n1) - 1 : 64);
+            const bool bad = (lane < L && p0 >= a.N_prev) || (lane + 32 < L && p1 >= a.N_prev);
+            if (__any_sync(0xffffffffu, bad)) {
+                if (lane == 0) set_error(a.err, GDN_ERR_PATH);
+                L = 0;
             }
+            if (lane < L) s_path[lane] = p0;
+            if (lane + 32 < L) s_path[lane + 32] = p1;
         }
-        s_L = L;
+        if (lane == 0) s_L = L;
     }
-    if (tid < kMaxNodes) s_need[tid] = 0;
+    if (tid < kMaxNodes) {
+        s_need[tid] = 0;
+        s_par[tid] = tid < N ? a.parent[(size_t)b * N + tid] : -1;
+    }
     __syncthreads();
     if (tid < N) {
-        const int32_t* par = a.parent + (size_t)b * N;
         const bool mine = tid >= a.t0 && tid < a.t1;
         if (mine) s_need[tid] = 1;
         int cur = tid, hist = 2;
         for (int i = 2; i >= 0; --i) {        // i = 2: parent, 1: grandparent, 0: great-grandparent
-            int p = cur >= 0 ? par[cur] : -1;
+            int p = cur >= 0 ? s_par[cur] : -1;
             if (cur >= 0 && (p >= cur || p < -1)) {
                 set_error(a.err, GDN_ERR_TREE);
                 p = -1;
@@ -158,49 +163,58 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
 
     // Depthwise: thread `tid` only ever touches channel column tid of s_y, so each
     // output overwrites its own input in place.  Descending node order keeps every
-    // window's ancestor rows (lower indices) unmodified until they are read.
-    const int warp = tid >> 5, lane = tid & 31;
+    // window's ancestor rows (lower indices) unmodified until they are read; a
+    // chunk of 8 nodes loads all its inputs before it stores any output.
     if (act) {
         const float h0 = hrow[0], h1 = hrow[1], h2 = hrow[2];
-#pragma unroll 1
-        for (int t = a.t1 - 1; t >= a.t0; --t) {
+        auto conv_at = [&](int t) {
             const int s0 = s_win[t][0], s1 = s_win[t][1], s2 = s_win[t][2];
             const float x0 = s0 >= 0 ? s_y[s0 * d + tid] : (s0 == -1 ? h0 : s0 == -2 ? h1 : h2);
             const float x1 = s1 >= 0 ? s_y[s1 * d + tid] : (s1 == -1 ? h0 : s1 == -2 ? h1 : h2);
             const float x2 = s2 >= 0 ? s_y[s2 * d + tid] : (s2 == -1 ? h0 : s2 == -2 ? h1 : h2);
             const float x3 = s_y[t * d + tid];
-            s_y[t * d + tid] = w[0] * x0 + w[1] * x1 + w[2] * x2 + w[3] * x3;
+            return w[0] * x0 + w[1] * x1 + w[2] * x2 + w[3] * x3;
+        };
+        int t = a.t1 - 1;
+#pragma unroll 1
+        for (; t - 7 >= a.t0; t -= 8) {
+            float r[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) r[u] = conv_at(t - u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s_y[(t - u) * d + tid] = r[u];
         }
+#pragma unroll 1
+        for (; t >= a.t0; --t) s_y[t * d + tid] = conv_at(t);
     }
 
     if (seg == 2) {
         if (act) {
-#pragma unroll 1
+#pragma unroll 4
             for (int t = a.t0; t < a.t1; ++t) a.v[(((size_t)b * N + t) * H + h) * dv + tid] = s_y[t * d + tid];
         }
         griddep_launch();
         return;
     }
 
-    // per-node squared norms: warp partial sums, then across the block's warps
-#pragma unroll 1
-    for (int t = a.t0; t < a.t1; ++t) {
-        const float y = act ? s_y[t * d + tid] : 0.f;
-        const float ss = warp_sum(y * y);
-        if (lane == 0) s_red[warp][t] = ss;
-    }
+    // per-node norms: warp w reduces nodes t0 + w, t0 + w + 8, ... over all d channels
     __syncthreads();
-    if (tid >= a.t0 && tid < a.t1) {
+#pragma unroll 1
+    for (int t = a.t0 + warp; t < a.t1; t += kConvThreads / 32) {
         float ss = 0.f;
-        for (int i = 0; i < kConvThreads / 32; ++i) ss += s_red[i][tid];
-        s_rn[tid] = 1.f / sqrtf(ss);
+        for (int cc = lane; cc < d; cc += 32) {
+            const float y = s_y[t * d + cc];
+            ss = fmaf(y, y, ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) s_rn[t] = 1.f / sqrtf(ss);
     }
     __syncthreads();
     if (act) {
         float* dst = seg == 0 ? a.q : a.k;
         __nv_bfloat16* dhi = a.qk_split[seg];
         __nv_bfloat16* dlo = a.qk_split[2 + seg];
-#pragma unroll 1
+#pragma unroll 4
         for (int t = a.t0; t < a.t1; ++t) {
             const size_t o = (((size_t)b * N + t) * H + h) * dk + tid;
             const float y = s_y[t * d + tid] * s_rn[t];
