@@ -264,6 +264,8 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
 
     # ---- end to end through the public API: pinned host inputs in, outputs out, every step
     e2e = None if profile else run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device)
+    baselines = None if (profile or chain) else run_replay_baselines(layers, gdnspec, torch, stream,
+                                                                     max(5, min(steps, 20)))
 
     w0 = layers[0].w
     B, N, H, dk, dv = w0.B, w0.N, w0.H, w0.dk, w0.dv
@@ -285,8 +287,63 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
                   "kernel": "gdn_commit_chain_verify (chain_kernel)" if chain else
                             "gdn_commit_tree_verify (tree_prep_tc_kernel + tree_contract_tc_kernel)",
                   "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_layer_s * 1e6, 3)},
-        gpu_launches=launches_per_call * R * steps,
+        gpu_launches=launches_per_call * R * steps, baselines=baselines,
     )
+
+
+# ---------------------------------------------------------------------------
+# replay baselines: what tree verification and the factor-buffer commit replace
+# ---------------------------------------------------------------------------
+def run_replay_baselines(layers, gdnspec, torch, stream, steps):
+    """Per-call device time of tree verification vs replaying every root-to-leaf path, and of the
+    factor-buffer commit vs replaying the accepted tokens, on the same layer rotation (no launch
+    overlap for either side).  Commits write to a scratch state so the inputs stay unchanged."""
+    prev = gdnspec.gdn_set_launch_overlap(False)
+    scratch = [torch.empty_like(ly.S) for ly in layers]
+    w0 = layers[0].w
+
+    def variant(name):
+        def call(ly, sc):
+            w = ly.w
+            if name == "tree_verify":
+                gdnspec.gdn_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out, ly.fac[0], ly.ws)
+            elif name == "replay_verify":
+                gdnspec.gdn_replay_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out)
+            elif name == "factor_commit":
+                gdnspec.gdn_commit(ly.S, ly.fac[0], ly.path, sc, w.N, w.dtype)
+            else:
+                gdnspec.gdn_replay_commit(ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.path, sc)
+        with torch.cuda.stream(stream):
+            for ly, sc in zip(layers, scratch):
+                call(ly, sc)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for ly, sc in zip(layers, scratch):
+                    call(ly, sc)
+            for _ in range(3):
+                g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        assert gdnspec.gdn_last_error(stream) == 0
+        return e0.elapsed_time(e1) * 1e3 / (steps * len(layers))
+
+    with torch.cuda.stream(stream):
+        for ly in layers:                 # the factor record the commits read
+            gdnspec.gdn_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out, ly.fac[0], ly.ws)
+    us = {n: variant(n) for n in ("tree_verify", "replay_verify", "factor_commit", "replay_commit")}
+    gdnspec.gdn_set_launch_overlap(prev)
+    del scratch
+    return {"us_per_call": {k: round(v, 3) for k, v in us.items()},
+            "replay_verify_over_tree_verify": round(us["replay_verify"] / us["tree_verify"], 2),
+            "replay_commit_over_factor_commit": round(us["replay_commit"] / us["factor_commit"], 2),
+            "what": "per layer call, %s, same rotation of %d layers; replay = every root-to-leaf path "
+                    "(verify) or the accepted tokens (commit) run token by token from S0"
+                    % (w0.spec.name, len(layers))}
 
 
 # ---------------------------------------------------------------------------
@@ -694,6 +751,8 @@ def main():
             "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
             "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
         }
+        if r.get("baselines"):
+            line["replay_baselines"] = r["baselines"]
         if r.get("layer"):
             line["config"]["hidden"] = r["hidden"]
             seq = r["sequential"]

@@ -266,6 +266,29 @@ int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, c
                          int dk, int dv, cudaStream_t stream);
 
 /*
+ * Replay baselines: what tree verification and the factor-buffer commit
+ * replace ("Pith review of SpecLA", "Core claim": tree verification against
+ * replaying every root-to-leaf path; accepted-state recovery from buffered
+ * factors against replaying the accepted tokens).  Same tensors and layouts
+ * as gdn_tree_verify / gdn_commit; fp32 state throughout.
+ *
+ * gdn_replay_tree_verify: every leaf's root-to-leaf path is run token by token
+ * from S0 and o_t is written for each node on it (a node shared by several
+ * leaves is recomputed by each, with identical results).  No factor record.
+ *
+ * gdn_replay_commit: the accepted root-first path (int32 [B][Lmax], -1 padded,
+ * validated against parent_idx) is run token by token from S0 and the final
+ * state is written to S_new (which may equal S0).  Invalid path ->
+ * GDN_ERR_PATH in the error word, S_new untouched.
+ */
+int gdn_replay_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                           const float* beta, const int32_t* parent_idx, const float* S0, float* out, int B,
+                           int N, int H, int dk, int dv, cudaStream_t stream);
+int gdn_replay_commit(const void* k, const void* v, int dtype, const float* alpha, const float* beta,
+                      const int32_t* parent_idx, const float* S0, const int32_t* accepted_path, int Lmax,
+                      float* S_new, int B, int N, int H, int dk, int dv, cudaStream_t stream);
+
+/*
  * Launch overlap between consecutive calls (process-wide switch, default off;
  * returns the previous setting).  When on, the first kernel of every call is
  * launched as a programmatic dependent of the kernel before it on the stream:

@@ -45,6 +45,8 @@ SIGNATURES = {
                                  _I, _I, _I, _I, _I, _I, _P]),
     "gdn_layer_token_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                                   _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_replay_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_set_launch_overlap": (_I, [_I]),
     "gdn_last_error": (_I, [_P]),
     "gdn_strerror": (ctypes.c_char_p, [_I]),
@@ -247,6 +249,22 @@ def gdn_layer_token_step(X, W_in, conv_w, W_o, parent_idx, S0, conv_state, S_nod
                                       _ptr(conv_state), _ptr(S_nodes), int(t), _ptr(out), _ptr(record),
                                       _ptr(workspace), B, N, H, hidden, dk, dv, _stream(stream)),
            "gdn_layer_token_step")
+
+
+def gdn_replay_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, stream=None):
+    """Baseline: replay every root-to-leaf path token by token (see include/gdnspec.h)."""
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_replay_tree_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha), _ptr(beta),
+                                        _ptr(parent_idx), _ptr(S0), _ptr(out), B, N, H, dk, dv, _stream(stream)),
+           "gdn_replay_tree_verify")
+
+
+def gdn_replay_commit(k, v, alpha, beta, parent_idx, S0, accepted_path, S_new, stream=None):
+    """Baseline: replay the accepted tokens from S0 into S_new (see include/gdnspec.h)."""
+    B, N, H, dk, dv = _dims(k, v)
+    _check(lib().gdn_replay_commit(_ptr(k), _ptr(v), dtype_code(k.dtype), _ptr(alpha), _ptr(beta), _ptr(parent_idx),
+                                   _ptr(S0), _ptr(accepted_path), accepted_path.shape[1], _ptr(S_new), B, N, H, dk,
+                                   dv, _stream(stream)), "gdn_replay_commit")
 
 
 def gdn_set_launch_overlap(enable: bool) -> bool:

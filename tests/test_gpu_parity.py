@@ -351,3 +351,32 @@ def test_tensor_core_fused_commit(oracle_mod, L):
     assert_close(S.cpu().numpy(), S_ref, "committed S")
     w2.S0 = S.cpu().numpy()
     check_verify(w2, out2, fac2, oracle_mod)
+
+
+# ---------------------------------------------------------------------------
+# replay baselines (what the tree verifier and the factor commit replace)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [0, 2, 3])
+def test_replay_baselines_match_oracle(oracle_mod, cfg):
+    w = wl.make_workload(cfg)
+    d = dev_inputs(w)
+    out = torch.full((w.B, w.N, w.H, w.dv), float("nan"), dtype=torch.float32, device="cuda")
+    gdnspec.gdn_replay_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out)
+    S_new = torch.empty_like(d["S0"])
+    gdnspec.gdn_replay_commit(d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], d["path"], S_new)
+    assert gdnspec.gdn_last_error() == 0
+    x = oracle_inputs(w)
+    o_ref, _, _ = oracle_mod.tree_verify(**x)
+    assert_close(out.cpu().numpy(), o_ref, "replay verify")
+    S_ref = oracle_mod.commit(x["k"], x["v"], x["alpha"], x["beta"], w.parent, x["S0"], w.path)
+    assert_close(S_new.cpu().numpy(), S_ref, "replay commit")
+
+
+def test_replay_commit_rejects_bad_path():
+    w = wl.make_workload(2)
+    d = dev_inputs(w)
+    bad = d["path"].clone()
+    bad[0, 0] = 5 if int(w.parent[0, 5]) >= 0 else 6      # not a root
+    S_new = torch.zeros_like(d["S0"])
+    gdnspec.gdn_replay_commit(d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], bad, S_new)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_PATH
