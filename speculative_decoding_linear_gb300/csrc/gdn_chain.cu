@@ -136,6 +136,18 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         }
     }
 
+    // This layer's q/k/v rows into L2 while the previous kernel finishes (the
+    // CTAs of one (sequence, head) split the tokens between them).
+    if (tid == 0) {
+        const int rowq = dk * (int)sizeof(T), rowv = dv * (int)sizeof(T);
+        for (int t = blockIdx.y; t < N; t += gridDim.y) {
+            const size_t rt = ((size_t)b * N + t) * a.H + h;
+            prefetch_l2(static_cast<const T*>(a.q) + rt * dk, rowq);
+            prefetch_l2(static_cast<const T*>(a.k) + rt * dk, rowq);
+            prefetch_l2(static_cast<const T*>(a.v) + rt * dv, rowv);
+        }
+    }
+
     // Everything above only read memory.  Writes and this layer's inputs come
     // after the programmatic wait.
     griddep_wait();

@@ -325,6 +325,12 @@ __device__ __forceinline__ void cp_async_block(void* smem, const void* gmem, int
 // this library calls griddep_launch() only after its own griddep_wait(), so a
 // kernel's pre-wait section always sees the writes of every kernel launched
 // two or more positions earlier on the stream.
+// Warm L2 with `bytes` (a multiple of 16, 16-byte aligned) at `src`; no data
+// reaches the thread.  L2 is the point of coherence, so a prefetch issued
+// before griddep_wait never makes a later load see stale data.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");

@@ -540,7 +540,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    // This layer's inputs may come from the previous kernel on the stream.
+    // This layer's q/k/v rows into L2 while the previous kernel on the stream
+    // finishes; its inputs may come from that kernel, so they are read only
+    // after the wait.
+    if (tid < N) {
+        const size_t rt = ((size_t)b * N + tid) * a.H + h;
+        const uint32_t esz = kSplit ? 4u : 2u;
+        if (kSplit) {
+            for (int i = 0; i < 4; ++i) prefetch_l2(static_cast<const __nv_bfloat16*>(a.split[i]) + rt * kDk, kDk * 2);
+            prefetch_l2(static_cast<const float*>(a.k) + rt * kDk, kDk * 4);
+            prefetch_l2(static_cast<const float*>(a.v) + rt * a.dv, (uint32_t)a.dv * 4);
+        } else {
+            prefetch_l2(static_cast<const __nv_bfloat16*>(a.q) + rt * kDk, kDk * esz);
+            prefetch_l2(static_cast<const __nv_bfloat16*>(a.k) + rt * kDk, kDk * esz);
+            prefetch_l2(static_cast<const __nv_bfloat16*>(a.v) + rt * a.dv, (uint32_t)a.dv * esz);
+        }
+    }
     griddep_wait();
     griddep_launch();
 
