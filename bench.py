@@ -266,6 +266,8 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
     e2e = None if profile else run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device)
     baselines = None if (profile or chain) else run_replay_baselines(layers, gdnspec, torch, stream,
                                                                      max(5, min(steps, 20)))
+    hybrid = None if (profile or chain) else run_hybrid_comparison(layers, gdnspec, torch, stream,
+                                                                   max(5, min(steps, 20)), device, wl)
 
     w0 = layers[0].w
     B, N, H, dk, dv = w0.B, w0.N, w0.H, w0.dk, w0.dv
@@ -287,7 +289,7 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
                   "kernel": "gdn_commit_chain_verify (chain_kernel)" if chain else
                             "gdn_commit_tree_verify (tree_prep_tc_kernel + tree_contract_tc_kernel)",
                   "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_layer_s * 1e6, 3)},
-        gpu_launches=launches_per_call * R * steps, baselines=baselines,
+        gpu_launches=launches_per_call * R * steps, baselines=baselines, hybrid=hybrid,
     )
 
 
@@ -344,6 +346,55 @@ def run_replay_baselines(layers, gdnspec, torch, stream, steps):
             "what": "per layer call, %s, same rotation of %d layers; replay = every root-to-leaf path "
                     "(verify) or the accepted tokens (commit) run token by token from S0"
                     % (w0.spec.name, len(layers))}
+
+
+# ---------------------------------------------------------------------------
+# chain-decomposed (hybrid) verification vs the tree verifier
+# ---------------------------------------------------------------------------
+def time_calls(calls, torch, stream, steps):
+    """Device time per call of a list of zero-argument launches, replayed as one CUDA graph."""
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c()
+        for _ in range(3):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (steps * len(calls))
+
+
+def run_hybrid_comparison(layers, gdnspec, torch, stream, steps, device, wl):
+    """Tree verifier vs chain-decomposed verification on the bench's trees and on deep, narrow trees of
+    the same size (a trunk of 8 nodes and 4 chains of 14), launch overlap off for both."""
+    prev = gdnspec.gdn_set_launch_overlap(False)
+    w0 = layers[0].w
+    res = {}
+    narrow = [Layer(wl.custom_workload(w0.B, w0.N, w0.H, w0.dk, w0.dv, wl.narrow_tree(w0.N, 4, 8), seed=9000 + r),
+                    device, torch, gdnspec) for r in range(len(layers))]
+    for name, lys in (("bench_trees", layers), ("narrow_trees", narrow)):
+        tree = [lambda ly=ly: gdnspec.gdn_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out,
+                                                      ly.fac[0], ly.ws) for ly in lys]
+        hyb = [lambda ly=ly: gdnspec.gdn_hybrid_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S,
+                                                            ly.out, ly.fac[0]) for ly in lys]
+        t_tree = time_calls(tree, torch, stream, steps)
+        t_hyb = time_calls(hyb, torch, stream, steps)
+        rc = gdnspec.gdn_last_error(stream)
+        res[name] = {"tree_verify_us": round(t_tree, 3),
+                     "hybrid_verify_us": round(t_hyb, 3) if rc == 0 else None,
+                     "hybrid_status": gdnspec.strerror(rc) if rc else "ok"}
+    gdnspec.gdn_set_launch_overlap(prev)
+    res["what"] = ("per call, %d sequences x %d nodes; narrow_trees = trunk of 8 + 4 chains of 14"
+                   % (w0.B, w0.N))
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -753,6 +804,8 @@ def main():
         }
         if r.get("baselines"):
             line["replay_baselines"] = r["baselines"]
+        if r.get("hybrid"):
+            line["hybrid_verify"] = r["hybrid"]
         if r.get("layer"):
             line["config"]["hidden"] = r["hidden"]
             seq = r["sequential"]

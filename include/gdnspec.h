@@ -57,7 +57,8 @@ extern "C" {
 #define GDN_ERR_TIMEOUT (-4)  /* a bounded device wait ran out (device-detected) */
 #define GDN_ERR_CUDA (-5)     /* a CUDA runtime call or launch failed */
 #define GDN_ERR_DEVICE (-6)   /* current device is not sm_103 */
-#define GDN_ERR_CAPACITY (-7) /* request larger than gdn_tree_verify_noalloc's fixed scratch */
+#define GDN_ERR_CAPACITY (-7) /* request larger than a fixed on-device capacity: gdn_tree_verify_noalloc's
+                                 scratch, gdn_hybrid_tree_verify's branch-state slots */
 
 /* ---- q/k/v element types ------------------------------------------------ */
 #define GDN_DTYPE_BF16 0
@@ -264,6 +265,24 @@ int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, c
                          const int32_t* parent_idx, const float* S0, const float* conv_state, float* S_nodes,
                          int t, float* out, void* record, void* workspace, int B, int N, int H, int hidden,
                          int dk, int dv, cudaStream_t stream);
+
+/*
+ * Chain-decomposed tree verification: serial within chains, parallel across
+ * the chains that are ready ("Pith review of SpecLA", "What carries the
+ * argument": V-dimension tiling for the serial chain path, next to the
+ * factorized tree form).  The tree is cut into chains (a chain starts at a
+ * root or at a child of a node with two or more children and follows
+ * only-children); chains whose parent chain is done run concurrently, each
+ * token by token on state rows held in registers; a chain ending at a
+ * branching node keeps its state rows on chip for the chains below.  Same
+ * tensors, outputs and factor record as gdn_tree_verify (so gdn_commit applies
+ * to its factors), no workspace.  Suited to deep, narrow trees.  At most 24
+ * branching nodes (nodes with two or more children) per tree: more records
+ * GDN_ERR_CAPACITY in the error word and writes nothing.
+ */
+int gdn_hybrid_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                           const float* beta, const int32_t* parent_idx, const float* S0, float* out,
+                           void* factors, int B, int N, int H, int dk, int dv, cudaStream_t stream);
 
 /*
  * Replay baselines: what tree verification and the factor-buffer commit

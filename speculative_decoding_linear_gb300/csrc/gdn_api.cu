@@ -247,7 +247,9 @@ const char* gdn_strerror(int code) {
         case GDN_ERR_TIMEOUT: return "a bounded device wait ran out";
         case GDN_ERR_CUDA: return "CUDA runtime error";
         case GDN_ERR_DEVICE: return "current device is not an sm_103 GPU";
-        case GDN_ERR_CAPACITY: return "request exceeds the fixed scratch capacity of gdn_tree_verify_noalloc";
+        case GDN_ERR_CAPACITY:
+            return "request exceeds a fixed on-device capacity (gdn_tree_verify_noalloc's scratch array, "
+                   "gdn_hybrid_tree_verify's branch-state slots)";
         default: return "unknown status";
     }
 }

@@ -1,0 +1,309 @@
+// gdn_hybrid.cu -- chain-decomposed tree verification: serial within chains,
+// parallel across the chains that are ready.
+//
+// Review of SpecLA (pith.science 7ERME3HB): "What carries the argument" names
+// V-dimension tiling for the serial chain path next to the factorized tree
+// form, and the Referee Report's Fig. 6 discussion contrasts them on deep,
+// narrow trees.  Here the tree is cut into chains: a chain starts at a root or
+// at a child of a node with two or more children, and follows only-children
+// down to a leaf or a branching node.  Chains whose parent chain is done run
+// concurrently, one per warp; inside a chain the gated delta rule runs token by
+// token on the state rows held in registers,
+//
+//     delta_t = beta_t (v_t - alpha_t S k_t),  S <- alpha_t S + delta_t k_t^T,
+//     o_t = S q_t,
+//
+// and a chain that ends at a branching node leaves its state rows in shared
+// memory for the chains below it.  Every node is computed once, as in the
+// tree verifier, and the factor record (delta, k, g, parent) is the same, so
+// gdn_commit applies to it unchanged.
+//
+// One CTA owns kRows rows of one (sequence, head) state; its warps take the
+// chains of one level of the chain tree at a time.  At most kMaxBranch
+// branching nodes per tree (their state rows live in shared memory); more
+// records GDN_ERR_CAPACITY and writes nothing.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kRows = 4;             // state rows per CTA; every warp holds all of them for its chain
+constexpr int kEPL = kMaxDim / 32;   // state columns per lane
+constexpr int kMaxBranch = 24;
+
+struct HybridSmem {
+    int total;
+    __host__ __device__ explicit HybridSmem(int dk) : total(kMaxBranch * kRows * dk * 4) {}
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
+    extern __shared__ __align__(16) float s_branch[];       // [slot][kRows][dk]
+    __shared__ int s_par[kMaxNodes], s_nch[kMaxNodes], s_only[kMaxNodes], s_slot[kMaxNodes];
+    __shared__ int s_chain_of[kMaxNodes], s_nodes[kMaxNodes];
+    __shared__ int s_coff[kMaxNodes + 1], s_clevel[kMaxNodes], s_order[kMaxNodes], s_loff[kMaxNodes + 2];
+    __shared__ float s_g[kMaxNodes];
+    __shared__ int s_nc, s_nlev, s_fail;
+    const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int N = a.N, dk = a.dk, dv = a.dv;
+    const int v0 = blockIdx.y * kRows;
+
+    // this layer's rows into L2 while the previous kernel finishes (read after the wait)
+    if (tid < N) {
+        const size_t rt = ((size_t)b * N + tid) * a.H + h;
+        prefetch_l2(static_cast<const T*>(a.q) + rt * dk, dk * (int)sizeof(T));
+        prefetch_l2(static_cast<const T*>(a.k) + rt * dk, dk * (int)sizeof(T));
+    }
+    griddep_wait();
+    griddep_launch();
+
+    if (tid < N) {
+        s_par[tid] = a.parent[(size_t)b * N + tid];
+        s_nch[tid] = 0;
+        s_only[tid] = -1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // chain decomposition (N <= 64 nodes, one thread)
+        int fail = 0;
+        for (int t = 0; t < N; ++t) {
+            const int p = s_par[t];
+            if (p < -1 || p >= t) fail = GDN_ERR_TREE;
+            else if (p >= 0) {
+                ++s_nch[p];
+                s_only[p] = t;
+            }
+        }
+        int nb = 0;
+        for (int t = 0; t < N && !fail; ++t) s_slot[t] = s_nch[t] >= 2 ? nb++ : -1;
+        if (!fail && nb > kMaxBranch) fail = GDN_ERR_CAPACITY;
+        int nc = 0, off = 0, nlev = 0;
+        if (!fail) {
+            for (int t = 0; t < N; ++t) {
+                const int p = s_par[t];
+                if (p >= 0 && s_nch[p] < 2) continue;     // continues its parent's chain
+                const int c = nc++;
+                s_coff[c] = off;
+                s_clevel[c] = p < 0 ? 0 : s_clevel[s_chain_of[p]] + 1;
+                nlev = max(nlev, s_clevel[c] + 1);
+                for (int u = t;; u = s_only[u]) {
+                    s_nodes[off++] = u;
+                    s_chain_of[u] = c;
+                    if (s_nch[u] != 1) break;
+                }
+            }
+            s_coff[nc] = off;
+            // chains ordered by level (counting sort)
+            for (int l = 0; l <= nlev; ++l) s_loff[l] = 0;
+            for (int c = 0; c < nc; ++c) ++s_loff[s_clevel[c] + 1];
+            for (int l = 0; l < nlev; ++l) s_loff[l + 1] += s_loff[l];
+            int fill[kMaxNodes + 1];
+            for (int l = 0; l <= nlev; ++l) fill[l] = s_loff[l];
+            for (int c = 0; c < nc; ++c) s_order[fill[s_clevel[c]]++] = c;
+        }
+        s_nc = nc;
+        s_nlev = nlev;
+        s_fail = fail;
+        if (fail) set_error(a.err, fail);
+    }
+    __syncthreads();
+    if (s_fail) return;
+
+    const T* qg = static_cast<const T*>(a.q);
+    const T* kg = static_cast<const T*>(a.k);
+    const T* vg = static_cast<const T*>(a.v);
+    auto load_tok = [&](int t, float (&kt)[kEPL], float (&qt)[kEPL], float (&vt)[kRows], float& al, float& be) {
+        const size_t gi = ((size_t)b * N + t) * a.H + h;
+#pragma unroll
+        for (int e = 0; e < kEPL; ++e) {
+            const int c = lane + 32 * e;
+            kt[e] = c < dk ? ld_elem<T>(kg, gi * dk + c) : 0.f;
+            qt[e] = c < dk ? ld_elem<T>(qg, gi * dk + c) : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) vt[r] = v0 + r < dv ? ld_elem<T>(vg, gi * dv + v0 + r) : 0.f;
+        al = a.alpha[gi];
+        be = a.beta[gi];
+    };
+
+    for (int lvl = 0; lvl < s_nlev; ++lvl) {
+        for (int ci = s_loff[lvl] + warp; ci < s_loff[lvl + 1]; ci += kWarps) {
+            const int c = s_order[ci];
+            const int first = s_nodes[s_coff[c]], len = s_coff[c + 1] - s_coff[c];
+            const int p = s_par[first];
+            float S[kRows][kEPL];
+            if (p < 0) {
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const float* row = a.S + ((size_t)bh * dv + v0 + r) * dk;
+#pragma unroll
+                    for (int e = 0; e < kEPL; ++e) {
+                        const int cc = lane + 32 * e;
+                        S[r][e] = (v0 + r < dv && cc < dk) ? row[cc] : 0.f;
+                    }
+                }
+            } else {
+                const float* st = s_branch + (size_t)s_slot[p] * kRows * dk;
+#pragma unroll
+                for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                    for (int e = 0; e < kEPL; ++e) {
+                        const int cc = lane + 32 * e;
+                        S[r][e] = cc < dk ? st[r * dk + cc] : 0.f;
+                    }
+            }
+            float g = p < 0 ? 0.f : s_g[p];
+            float kt[kEPL], qt[kEPL], vt[kRows], al, be;
+            load_tok(first, kt, qt, vt, al, be);
+            for (int i = 0; i < len; ++i) {
+                const int t = s_nodes[s_coff[c] + i];
+                float kn[kEPL], qn[kEPL], vn[kRows], aln = 0.f, ben = 0.f;
+                if (i + 1 < len) load_tok(s_nodes[s_coff[c] + i + 1], kn, qn, vn, aln, ben);
+                float kq = 0.f;
+#pragma unroll
+                for (int e = 0; e < kEPL; ++e) kq = fmaf(kt[e], qt[e], kq);
+                float sk[kRows], sq[kRows];
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    float x = 0.f, y = 0.f;
+#pragma unroll
+                    for (int e = 0; e < kEPL; ++e) {
+                        x = fmaf(S[r][e], kt[e], x);
+                        y = fmaf(S[r][e], qt[e], y);
+                    }
+                    sk[r] = x;
+                    sq[r] = y;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    kq += __shfl_xor_sync(0xffffffffu, kq, o);
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r) {
+                        sk[r] += __shfl_xor_sync(0xffffffffu, sk[r], o);
+                        sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
+                    }
+                }
+                g += logf(al);
+                float outv = 0.f, dv_lane = 0.f;
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    const float dlt = be * (vt[r] - al * sk[r]);
+#pragma unroll
+                    for (int e = 0; e < kEPL; ++e) S[r][e] = fmaf(al, S[r][e], dlt * kt[e]);
+                    const float o = fmaf(al, sq[r], dlt * kq);
+                    if (lane == r) {
+                        outv = o;
+                        dv_lane = dlt;
+                    }
+                }
+                if (lane < kRows && v0 + lane < dv) {
+                    a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + lane] = outv;
+                    a.f.delta[((size_t)bh * N + t) * dv + v0 + lane] = dv_lane;
+                }
+                if (lane == 0) s_g[t] = g;
+                if (i + 1 < len) {
+#pragma unroll
+                    for (int e = 0; e < kEPL; ++e) {
+                        kt[e] = kn[e];
+                        qt[e] = qn[e];
+                    }
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r) vt[r] = vn[r];
+                    al = aln;
+                    be = ben;
+                }
+            }
+            const int last = s_nodes[s_coff[c + 1] - 1];
+            if (s_slot[last] >= 0) {                  // branching node: rows for the chains below
+                float* st = s_branch + (size_t)s_slot[last] * kRows * dk;
+#pragma unroll
+                for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                    for (int e = 0; e < kEPL; ++e) {
+                        const int cc = lane + 32 * e;
+                        if (cc < dk) st[r * dk + cc] = S[r][e];
+                    }
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+    }
+
+    // rest of the factor record: g, keys and parents, spread over the CTAs of this (b, h)
+    if (blockIdx.y == 0 && tid < N) a.f.g[(size_t)bh * N + tid] = s_g[tid];
+    if (blockIdx.y == 0 && h == 0 && tid < N) a.f.parent[(size_t)b * N + tid] = s_par[tid];
+    T* key_out = static_cast<T*>(a.f.key);
+    for (int t = blockIdx.y; t < N; t += gridDim.y) {
+        const size_t gi = ((size_t)b * N + t) * a.H + h;
+        for (int c = tid; c < dk; c += kWarps * 32) key_out[((size_t)bh * N + t) * dk + c] = kg[gi * dk + c];
+    }
+}
+
+template <typename T>
+cudaError_t launch_hybrid_t(const VerifyArgs& a, cudaStream_t s) {
+    static int attr_set[64];    // dynamic shared memory opted into, per device (the kernel also has static)
+    const HybridSmem L(a.dk);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (L.total > 48 * 1024 && attr_set[dev] < L.total) {
+        e = cudaFuncSetAttribute(hybrid_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = L.total;
+    }
+    dim3 grid(a.B * a.H, (a.dv + kRows - 1) / kRows);
+    return launch_kernel(hybrid_kernel<T>, grid, dim3(kWarps * 32), L.total, s, a.overlap, a);
+}
+
+}  // namespace
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" int gdn_hybrid_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                                      const float* beta, const int32_t* parent_idx, const float* S0, float* out,
+                                      void* factors, int B, int N, int H, int dk, int dv, cudaStream_t stream) {
+    auto ok16 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    auto dim_ok = [](int d) { return d >= 16 && d <= kMaxDim && d % 16 == 0; };
+    if (B < 1 || H < 1 || N < 1 || N > kMaxNodes || !dim_ok(dk) || !dim_ok(dv) || (long long)B * H > 0x7fffffffLL)
+        return GDN_ERR_ARG;
+    if (dtype != GDN_DTYPE_BF16 && dtype != GDN_DTYPE_F32) return GDN_ERR_ARG;
+    if (!ok16(q) || !ok16(k) || !ok16(v) || !ok16(alpha) || !ok16(beta) || !ok16(parent_idx) || !ok16(S0) ||
+        !ok16(out) || !ok16(factors))
+        return GDN_ERR_ARG;
+    const size_t fbytes = factor_layout(B, N, H, dk, dv, dtype).total;
+    const size_t obytes = (size_t)B * N * H * dv * 4;
+    const char* o = reinterpret_cast<const char*>(out);
+    const char* f = static_cast<const char*>(factors);
+    if (o < f + fbytes && f < o + obytes) return GDN_ERR_ARG;
+    int st = GDN_OK;
+    int* err = current_error_word(&st);
+    if (err == nullptr) return st;
+    VerifyArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.parent = parent_idx;
+    a.S = const_cast<float*>(S0);
+    a.out = out;
+    a.f = factors_view(factors, B, N, H, dk, dv, dtype);
+    a.ws = nullptr;
+    a.B = B;
+    a.N = N;
+    a.H = H;
+    a.dk = dk;
+    a.dv = dv;
+    a.commit = CommitSrc{nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0};
+    a.err = err;
+    a.overlap = launch_overlap_enabled();
+    a.tc = false;
+    const cudaError_t e = dtype == GDN_DTYPE_F32 ? launch_hybrid_t<float>(a, stream)
+                                                 : launch_hybrid_t<__nv_bfloat16>(a, stream);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

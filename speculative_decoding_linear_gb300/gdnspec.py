@@ -45,6 +45,7 @@ SIGNATURES = {
                                  _I, _I, _I, _I, _I, _I, _P]),
     "gdn_layer_token_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                                   _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_hybrid_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_set_launch_overlap": (_I, [_I]),
@@ -249,6 +250,15 @@ def gdn_layer_token_step(X, W_in, conv_w, W_o, parent_idx, S0, conv_state, S_nod
                                       _ptr(conv_state), _ptr(S_nodes), int(t), _ptr(out), _ptr(record),
                                       _ptr(workspace), B, N, H, hidden, dk, dv, _stream(stream)),
            "gdn_layer_token_step")
+
+
+def gdn_hybrid_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, stream=None):
+    """Chain-decomposed tree verification (see include/gdnspec.h); same outputs and factor record as
+    gdn_tree_verify, no workspace."""
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_hybrid_tree_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha), _ptr(beta),
+                                        _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(factors), B, N, H, dk, dv,
+                                        _stream(stream)), "gdn_hybrid_tree_verify")
 
 
 def gdn_replay_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, stream=None):

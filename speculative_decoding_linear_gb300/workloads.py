@@ -78,6 +78,20 @@ def random_tree(rng: np.random.Generator, n: int, maxdepth: int) -> np.ndarray:
     return parent
 
 
+def narrow_tree(n: int, chains: int, trunk: int) -> np.ndarray:
+    """Deep, narrow draft tree: a trunk of ``trunk`` nodes (0 .. trunk-1) and ``chains`` chains
+    hanging from its last node, numbered chain by chain; the last chain takes the remainder."""
+    assert 1 <= trunk <= n and chains >= 1
+    parent = chain_tree(trunk).tolist()
+    rest = n - trunk
+    per = rest // chains
+    for c in range(chains):
+        length = per if c < chains - 1 else rest - per * (chains - 1)
+        for i in range(length):
+            parent.append(trunk - 1 if i == 0 else len(parent) - 1)
+    return np.asarray(parent, dtype=np.int32)
+
+
 def node_depths(parent: np.ndarray) -> np.ndarray:
     """Depth of every node of a topologically ordered parent array (roots have depth 0)."""
     d = np.zeros(len(parent), dtype=np.int64)

@@ -380,3 +380,44 @@ def test_replay_commit_rejects_bad_path():
     S_new = torch.zeros_like(d["S0"])
     gdnspec.gdn_replay_commit(d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], bad, S_new)
     assert gdnspec.gdn_last_error() == gdnspec.ERR_PATH
+
+
+# ---------------------------------------------------------------------------
+# chain-decomposed (hybrid) verification
+# ---------------------------------------------------------------------------
+def _hybrid_cases():
+    return [
+        ("tiny_binary7", lambda: wl.make_workload(0)),
+        ("chain8", lambda: wl.make_workload(1)),
+        ("tree32", lambda: wl.make_workload(2)),
+        ("narrow_b4_n64", lambda: wl.custom_workload(4, 64, 8, 256, 256, wl.narrow_tree(64, 4, 8), seed=61)),
+        ("narrow_b3_n37_f32", lambda: wl.custom_workload(3, 37, 2, 64, 128, wl.narrow_tree(37, 3, 5), seed=62,
+                                                         dtype=wl.F32)),
+        ("forest_b2", lambda: wl.custom_workload(2, 16, 4, 256, 256, np.full(16, -1, np.int32), seed=63)),
+    ]
+
+
+@pytest.mark.parametrize("name,make", _hybrid_cases())
+def test_hybrid_verify_matches_oracle(oracle_mod, name, make):
+    w = make()
+    d = dev_inputs(w)
+    out, fac, _ = alloc_outputs(w)
+    gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out, fac)
+    assert gdnspec.gdn_last_error() == 0
+    check_verify(w, out, fac, oracle_mod)
+    # its factor record commits like the tree verifier's
+    S_new = torch.empty_like(d["S0"])
+    gdnspec.gdn_commit(d["S0"], fac, d["path"], S_new, w.N, w.dtype)
+    assert gdnspec.gdn_last_error() == 0
+    x = oracle_inputs(w)
+    S_ref = oracle_mod.commit(x["k"], x["v"], x["alpha"], x["beta"], w.parent, x["S0"], w.path)
+    assert_close(S_new.cpu().numpy(), S_ref, "commit of hybrid factors")
+
+
+def test_hybrid_rejects_too_many_branching_nodes():
+    full_binary = np.array([-1] + [(t - 1) // 2 for t in range(1, 63)], dtype=np.int32)   # 31 branching nodes
+    w = wl.custom_workload(1, 63, 2, 64, 64, full_binary, seed=64)
+    d = dev_inputs(w)
+    out, fac, _ = alloc_outputs(w)
+    gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out, fac)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_CAPACITY

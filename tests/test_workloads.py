@@ -57,3 +57,12 @@ def test_tiny_and_chain_topologies():
     assert w1.parent[0].tolist() == list(range(-1, 7))
     L = int(np.sum(w1.path[0] >= 0))
     assert w1.path[0, :L].tolist() == list(range(L))
+
+
+def test_narrow_tree_shape():
+    p = wl.narrow_tree(64, 4, 8)
+    assert len(p) == 64 and p[0] == -1
+    assert all(0 <= p[t] < t for t in range(1, 64))
+    kids = np.bincount(p[p >= 0], minlength=64)
+    assert kids[7] == 4 and np.count_nonzero(kids >= 2) == 1
+    assert wl.node_depths(p).max() == 7 + 14
