@@ -374,7 +374,7 @@ def time_calls(calls, torch, stream, steps):
 
 def run_hybrid_comparison(layers, gdnspec, torch, stream, steps, device, wl):
     """Tree verifier vs chain-decomposed verification on the bench's trees and on deep, narrow trees of
-    the same size (a trunk of 8 nodes and 4 chains of 14), launch overlap off for both."""
+    the same size (a trunk of 8 nodes and 4 chains below it), launch overlap off for both."""
     prev = gdnspec.gdn_set_launch_overlap(False)
     w0 = layers[0].w
     res = {}
@@ -392,8 +392,8 @@ def run_hybrid_comparison(layers, gdnspec, torch, stream, steps, device, wl):
                      "hybrid_verify_us": round(t_hyb, 3) if rc == 0 else None,
                      "hybrid_status": gdnspec.strerror(rc) if rc else "ok"}
     gdnspec.gdn_set_launch_overlap(prev)
-    res["what"] = ("per call, %d sequences x %d nodes; narrow_trees = trunk of 8 + 4 chains of 14"
-                   % (w0.B, w0.N))
+    res["what"] = ("per call, %d sequences x %d nodes; narrow_trees = a trunk of 8 nodes and 4 chains of %d "
+                   "hanging from it" % (w0.B, w0.N, (w0.N - 8) // 4))
     return res
 
 

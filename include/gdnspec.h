@@ -276,7 +276,7 @@ int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, c
  * token by token on state rows held in registers; a chain ending at a
  * branching node keeps its state rows on chip for the chains below.  Same
  * tensors, outputs and factor record as gdn_tree_verify (so gdn_commit applies
- * to its factors), no workspace.  Suited to deep, narrow trees.  At most 24
+ * to its factors), no workspace.  Suited to deep, narrow trees.  At most 8
  * branching nodes (nodes with two or more children) per tree: more records
  * GDN_ERR_CAPACITY in the error word and writes nothing.
  */

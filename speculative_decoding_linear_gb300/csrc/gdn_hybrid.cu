@@ -28,18 +28,26 @@ namespace gdn {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kRows = 4;             // state rows per CTA; every warp holds all of them for its chain
+constexpr int kRows = 8;             // state rows per CTA; every warp holds all of them for its chain
 constexpr int kEPL = kMaxDim / 32;   // state columns per lane
-constexpr int kMaxBranch = 24;
+constexpr int kMaxBranch = 8;
+constexpr int kChunk = 8;            // chain tokens staged per warp at a time
 
+// dynamic smem: branch-state slots [kMaxBranch][kRows][dk] fp32, then per warp
+// a token chunk [kChunk][k | q][dk] of the input type
 struct HybridSmem {
-    int total;
-    __host__ __device__ explicit HybridSmem(int dk) : total(kMaxBranch * kRows * dk * 4) {}
+    int branch, tok, total;
+    __host__ __device__ HybridSmem(int dk, int esz)
+        : branch(0), tok(kMaxBranch * kRows * dk * 4), total(tok + kWarps * kChunk * 2 * dk * esz) {}
 };
 
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) float s_branch[];       // [slot][kRows][dk]
+    extern __shared__ __align__(16) unsigned char smem[];
+    const HybridSmem Ls(a.dk, (int)sizeof(T));
+    float* s_branch = reinterpret_cast<float*>(smem + Ls.branch);
+    __shared__ float s_v[kWarps][kChunk][kRows];
+    __shared__ float s_al[kWarps][kChunk], s_be[kWarps][kChunk];
     __shared__ int s_par[kMaxNodes], s_nch[kMaxNodes], s_only[kMaxNodes], s_slot[kMaxNodes];
     __shared__ int s_chain_of[kMaxNodes], s_nodes[kMaxNodes];
     __shared__ int s_coff[kMaxNodes + 1], s_clevel[kMaxNodes], s_order[kMaxNodes], s_loff[kMaxNodes + 2];
@@ -114,19 +122,8 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
     const T* qg = static_cast<const T*>(a.q);
     const T* kg = static_cast<const T*>(a.k);
     const T* vg = static_cast<const T*>(a.v);
-    auto load_tok = [&](int t, float (&kt)[kEPL], float (&qt)[kEPL], float (&vt)[kRows], float& al, float& be) {
-        const size_t gi = ((size_t)b * N + t) * a.H + h;
-#pragma unroll
-        for (int e = 0; e < kEPL; ++e) {
-            const int c = lane + 32 * e;
-            kt[e] = c < dk ? ld_elem<T>(kg, gi * dk + c) : 0.f;
-            qt[e] = c < dk ? ld_elem<T>(qg, gi * dk + c) : 0.f;
-        }
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) vt[r] = v0 + r < dv ? ld_elem<T>(vg, gi * dv + v0 + r) : 0.f;
-        al = a.alpha[gi];
-        be = a.beta[gi];
-    };
+    T* tok = reinterpret_cast<T*>(smem + Ls.tok) + (size_t)warp * kChunk * 2 * dk;
+    const int rowb = dk * (int)sizeof(T);
 
     for (int lvl = 0; lvl < s_nlev; ++lvl) {
         for (int ci = s_loff[lvl] + warp; ci < s_loff[lvl + 1]; ci += kWarps) {
@@ -155,64 +152,81 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
                     }
             }
             float g = p < 0 ? 0.f : s_g[p];
-            float kt[kEPL], qt[kEPL], vt[kRows], al, be;
-            load_tok(first, kt, qt, vt, al, be);
-            for (int i = 0; i < len; ++i) {
-                const int t = s_nodes[s_coff[c] + i];
-                float kn[kEPL], qn[kEPL], vn[kRows], aln = 0.f, ben = 0.f;
-                if (i + 1 < len) load_tok(s_nodes[s_coff[c] + i + 1], kn, qn, vn, aln, ben);
-                float kq = 0.f;
-#pragma unroll
-                for (int e = 0; e < kEPL; ++e) kq = fmaf(kt[e], qt[e], kq);
-                float sk[kRows], sq[kRows];
-#pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    float x = 0.f, y = 0.f;
+            for (int c0 = 0; c0 < len; c0 += kChunk) {
+                const int n = min(kChunk, len - c0);
+                __syncwarp();                              // the previous chunk is consumed
+                for (int i = 0; i < n; ++i) {
+                    const size_t gi = ((size_t)b * N + s_nodes[s_coff[c] + c0 + i]) * a.H + h;
+                    for (int o = lane * 16; o < rowb; o += 32 * 16) {
+                        cp_async16(reinterpret_cast<char*>(tok + (size_t)(2 * i) * dk) + o,
+                                   reinterpret_cast<const char*>(kg + gi * dk) + o);
+                        cp_async16(reinterpret_cast<char*>(tok + (size_t)(2 * i + 1) * dk) + o,
+                                   reinterpret_cast<const char*>(qg + gi * dk) + o);
+                    }
+                }
+                for (int idx = lane; idx < n * kRows; idx += 32) {
+                    const int i = idx / kRows, r = idx % kRows;
+                    const size_t gi = ((size_t)b * N + s_nodes[s_coff[c] + c0 + i]) * a.H + h;
+                    s_v[warp][i][r] = v0 + r < dv ? ld_elem<T>(vg, gi * dv + v0 + r) : 0.f;
+                }
+                if (lane < n) {
+                    const size_t gi = ((size_t)b * N + s_nodes[s_coff[c] + c0 + lane]) * a.H + h;
+                    s_al[warp][lane] = a.alpha[gi];
+                    s_be[warp][lane] = a.beta[gi];
+                }
+                cp_async_wait_all();
+                __syncwarp();
+                for (int i = 0; i < n; ++i) {
+                    const int t = s_nodes[s_coff[c] + c0 + i];
+                    float kt[kEPL], qt[kEPL];
+                    float kq = 0.f;
 #pragma unroll
                     for (int e = 0; e < kEPL; ++e) {
-                        x = fmaf(S[r][e], kt[e], x);
-                        y = fmaf(S[r][e], qt[e], y);
+                        const int cc = lane + 32 * e;
+                        kt[e] = cc < dk ? ld_elem<T>(tok, (size_t)(2 * i) * dk + cc) : 0.f;
+                        qt[e] = cc < dk ? ld_elem<T>(tok, (size_t)(2 * i + 1) * dk + cc) : 0.f;
+                        kq = fmaf(kt[e], qt[e], kq);
                     }
-                    sk[r] = x;
-                    sq[r] = y;
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    kq += __shfl_xor_sync(0xffffffffu, kq, o);
+                    float sk[kRows], sq[kRows];
 #pragma unroll
                     for (int r = 0; r < kRows; ++r) {
-                        sk[r] += __shfl_xor_sync(0xffffffffu, sk[r], o);
-                        sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
-                    }
-                }
-                g += logf(al);
-                float outv = 0.f, dv_lane = 0.f;
+                        float x = 0.f, y = 0.f;
 #pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    const float dlt = be * (vt[r] - al * sk[r]);
-#pragma unroll
-                    for (int e = 0; e < kEPL; ++e) S[r][e] = fmaf(al, S[r][e], dlt * kt[e]);
-                    const float o = fmaf(al, sq[r], dlt * kq);
-                    if (lane == r) {
-                        outv = o;
-                        dv_lane = dlt;
-                    }
-                }
-                if (lane < kRows && v0 + lane < dv) {
-                    a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + lane] = outv;
-                    a.f.delta[((size_t)bh * N + t) * dv + v0 + lane] = dv_lane;
-                }
-                if (lane == 0) s_g[t] = g;
-                if (i + 1 < len) {
-#pragma unroll
-                    for (int e = 0; e < kEPL; ++e) {
-                        kt[e] = kn[e];
-                        qt[e] = qn[e];
+                        for (int e = 0; e < kEPL; ++e) {
+                            x = fmaf(S[r][e], kt[e], x);
+                            y = fmaf(S[r][e], qt[e], y);
+                        }
+                        sk[r] = x;
+                        sq[r] = y;
                     }
 #pragma unroll
-                    for (int r = 0; r < kRows; ++r) vt[r] = vn[r];
-                    al = aln;
-                    be = ben;
+                    for (int o = 16; o > 0; o >>= 1) {
+                        kq += __shfl_xor_sync(0xffffffffu, kq, o);
+#pragma unroll
+                        for (int r = 0; r < kRows; ++r) {
+                            sk[r] += __shfl_xor_sync(0xffffffffu, sk[r], o);
+                            sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
+                        }
+                    }
+                    const float al = s_al[warp][i], be = s_be[warp][i];
+                    g += logf(al);
+                    float outv = 0.f, d_lane = 0.f;
+#pragma unroll
+                    for (int r = 0; r < kRows; ++r) {
+                        const float dlt = be * (s_v[warp][i][r] - al * sk[r]);
+#pragma unroll
+                        for (int e = 0; e < kEPL; ++e) S[r][e] = fmaf(al, S[r][e], dlt * kt[e]);
+                        const float o = fmaf(al, sq[r], dlt * kq);
+                        if (lane == r) {
+                            outv = o;
+                            d_lane = dlt;
+                        }
+                    }
+                    if (lane < kRows && v0 + lane < dv) {
+                        a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + lane] = outv;
+                        a.f.delta[((size_t)bh * N + t) * dv + v0 + lane] = d_lane;
+                    }
+                    if (lane == 0) s_g[t] = g;
                 }
             }
             const int last = s_nodes[s_coff[c + 1] - 1];
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
 template <typename T>
 cudaError_t launch_hybrid_t(const VerifyArgs& a, cudaStream_t s) {
     static int attr_set[64];    // dynamic shared memory opted into, per device (the kernel also has static)
-    const HybridSmem L(a.dk);
+    const HybridSmem L(a.dk, (int)sizeof(T));
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -389,7 +389,8 @@ def _hybrid_cases():
     return [
         ("tiny_binary7", lambda: wl.make_workload(0)),
         ("chain8", lambda: wl.make_workload(1)),
-        ("tree32", lambda: wl.make_workload(2)),
+        ("two_level_narrow", lambda: wl.custom_workload(
+            2, 28, 8, 256, 256, np.concatenate([wl.narrow_tree(20, 3, 4), [9, 20, 21, 22, 9, 24, 25, 26]]), seed=60)),
         ("narrow_b4_n64", lambda: wl.custom_workload(4, 64, 8, 256, 256, wl.narrow_tree(64, 4, 8), seed=61)),
         ("narrow_b3_n37_f32", lambda: wl.custom_workload(3, 37, 2, 64, 128, wl.narrow_tree(37, 3, 5), seed=62,
                                                          dtype=wl.F32)),
