@@ -83,16 +83,20 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     const int rows = min(kRows, dv - v0);
     const bool fused = a.commit.path != nullptr;
 
-    // 1. state rows -> registers (loads in flight while the commit is set up)
+    // 1. state rows -> registers (loads in flight while the commit is set up).  Lane
+    // `lane` holds columns c0 .. c0+7 of each of its warp's rows, c0 = 8 lane (all
+    // of them or none: d_k is a multiple of 16), so every access is a vector access.
+    const int c0 = 8 * lane;
+    const bool lane_on = c0 < dk;
     float S[RPW][kEPL];
 #pragma unroll
     for (int rr = 0; rr < RPW; ++rr) {
         const int r = warp * RPW + rr;
-        const float* row = a.S + ((size_t)bh * dv + v0 + r) * dk;
+        if (r < rows && lane_on) {
+            ld8<float>(a.S + ((size_t)bh * dv + v0 + r) * dk + c0, S[rr]);
+        } else {
 #pragma unroll
-        for (int e = 0; e < kEPL; ++e) {
-            const int c = lane + 32 * e;
-            S[rr][e] = (r < rows && c < dk) ? row[c] : 0.f;
+            for (int e = 0; e < kEPL; ++e) S[rr][e] = 0.f;
         }
     }
     int nL = 0;
@@ -120,17 +124,19 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         __syncthreads();
         // 2. commit in registers (same arithmetic order as gdn_commit)
         const float ega = *s_ega;
+        if (lane_on) {
 #pragma unroll
-        for (int rr = 0; rr < RPW; ++rr) {
-            const int r = warp * RPW + rr;
+            for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
-            for (int e = 0; e < kEPL; ++e) {
-                const int c = lane + 32 * e;
-                if (r < rows && c < dk) {
-                    float acc = ega * S[rr][e];
-                    for (int i = 0; i < nL; ++i)
-                        acc = fmaf(s_cd[i * kRows + r], ld_elem<T>(s_key, (size_t)i * dk + c), acc);
-                    S[rr][e] = acc;
+                for (int e = 0; e < kEPL; ++e) S[rr][e] *= ega;
+            for (int i = 0; i < nL; ++i) {
+                float kv[kEPL];
+                ld8<T>(s_key + (size_t)i * dk + c0, kv);
+#pragma unroll
+                for (int rr = 0; rr < RPW; ++rr) {
+                    const float w = s_cd[i * kRows + warp * RPW + rr];
+#pragma unroll
+                    for (int e = 0; e < kEPL; ++e) S[rr][e] = fmaf(w, kv[e], S[rr][e]);
                 }
             }
         }
@@ -152,19 +158,6 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     // after the programmatic wait.
     griddep_wait();
     griddep_launch();
-    if (fused) {    // committed rows written back once
-#pragma unroll
-        for (int rr = 0; rr < RPW; ++rr) {
-            const int r = warp * RPW + rr;
-            float* row = a.S + ((size_t)bh * dv + v0 + r) * dk;
-#pragma unroll
-            for (int e = 0; e < kEPL; ++e) {
-                const int c = lane + 32 * e;
-                if (r < rows && c < dk) row[c] = S[rr][e];
-            }
-        }
-    }
-
     // 3. this layer's draft inputs
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
@@ -175,15 +168,48 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         cp_async_block(s_qk + (size_t)(2 * t) * dk, k + rt, rowb, tid, kWarps * 32);
         cp_async_block(s_qk + (size_t)(2 * t + 1) * dk, q + rt, rowb, tid, kWarps * 32);
     }
-    for (int i = tid; i < N * kRows; i += kWarps * 32) {
-        const int t = i / kRows, r = i % kRows;
-        if (r < rows) s_v[i] = vv[(((size_t)b * N + t) * a.H + h) * dv + v0 + r];
+    // v, alpha, beta into registers first (one item per thread when N * kRows <= 128),
+    // the committed rows' stores behind them, then the values into shared memory
+    const bool one_pass = N * kRows <= kWarps * 32;
+    float v_reg = 0.f, al_reg = 0.f, be_reg = 0.f;
+    if (one_pass) {
+        if (tid < N * kRows && tid % kRows < rows)
+            v_reg = ld_elem<T>(vv, (((size_t)b * N + tid / kRows) * a.H + h) * dv + v0 + tid % kRows);
+        if (tid < N) {
+            const size_t gi = ((size_t)b * N + tid) * a.H + h;
+            al_reg = a.alpha[gi];
+            be_reg = a.beta[gi];
+        }
     }
-    for (int t = tid; t < N; t += kWarps * 32) {
-        const size_t gi = ((size_t)b * N + t) * a.H + h;
-        s_alpha[t] = a.alpha[gi];
-        s_beta[t] = a.beta[gi];
+    if (fused) {    // committed rows written back once
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int r = warp * RPW + rr;
+            if (r < rows && lane_on) {
+                float4* row = reinterpret_cast<float4*>(a.S + ((size_t)bh * dv + v0 + r) * dk + c0);
+                row[0] = make_float4(S[rr][0], S[rr][1], S[rr][2], S[rr][3]);
+                row[1] = make_float4(S[rr][4], S[rr][5], S[rr][6], S[rr][7]);
+            }
+        }
     }
+    if (one_pass) {
+        if (tid < N * kRows) s_v[tid] = v_reg;
+        if (tid < N) {
+            s_alpha[tid] = al_reg;
+            s_beta[tid] = be_reg;
+        }
+    } else {
+        for (int i = tid; i < N * kRows; i += kWarps * 32) {
+            const int t = i / kRows, r = i % kRows;
+            s_v[i] = r < rows ? ld_elem<T>(vv, (((size_t)b * N + t) * a.H + h) * dv + v0 + r) : 0.f;
+        }
+        for (int t = tid; t < N; t += kWarps * 32) {
+            const size_t gi = ((size_t)b * N + t) * a.H + h;
+            s_alpha[t] = a.alpha[gi];
+            s_beta[t] = a.beta[gi];
+        }
+    }
+
     cp_async_wait_all();
     __syncthreads();
 
@@ -191,13 +217,15 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     for (int t = 0; t < N; ++t) {
         float kt[kEPL], qt[kEPL];
         float kq = 0.f;
+        if (lane_on) {
+            ld8<T>(s_qk + (size_t)(2 * t) * dk + c0, kt);
+            ld8<T>(s_qk + (size_t)(2 * t + 1) * dk + c0, qt);
+        } else {
 #pragma unroll
-        for (int e = 0; e < kEPL; ++e) {
-            const int c = lane + 32 * e;
-            kt[e] = c < dk ? ld_elem<T>(s_qk, (size_t)(2 * t) * dk + c) : 0.f;
-            qt[e] = c < dk ? ld_elem<T>(s_qk, (size_t)(2 * t + 1) * dk + c) : 0.f;
-            kq = fmaf(kt[e], qt[e], kq);
+            for (int e = 0; e < kEPL; ++e) kt[e] = qt[e] = 0.f;
         }
+#pragma unroll
+        for (int e = 0; e < kEPL; ++e) kq = fmaf(kt[e], qt[e], kq);
         float sk[RPW], sq[RPW];
 #pragma unroll
         for (int rr = 0; rr < RPW; ++rr) {

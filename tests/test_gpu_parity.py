@@ -104,10 +104,17 @@ def test_sibling_isolation_on_gpu():
 # ---------------------------------------------------------------------------
 # chain verify (state-resident serial path)
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("case", ["cfg1", "n1", "n64", "d16_f32", "b3_h5"])
+@pytest.mark.parametrize("case", ["cfg1", "n1", "n64", "d16_f32", "b3_h5", "n5_f32_d32", "n8_b4", "n7_dv48"])
 def test_chain_verify(oracle_mod, case):
+    """Chains of up to 8 tokens take the factorized form, longer ones the serial loop."""
     if case == "cfg1":
         w = wl.make_workload(1)
+    elif case == "n5_f32_d32":
+        w = wl.custom_workload(2, 5, 3, 32, 32, wl.chain_tree(5), seed=8, dtype=wl.F32)
+    elif case == "n8_b4":
+        w = wl.custom_workload(4, 8, 8, 256, 256, wl.chain_tree(8), seed=10)
+    elif case == "n7_dv48":
+        w = wl.custom_workload(1, 7, 2, 256, 48, wl.chain_tree(7), seed=11)
     elif case == "n1":
         w = wl.custom_workload(1, 1, 8, 256, 256, wl.chain_tree(1), seed=3)
     elif case == "n64":
