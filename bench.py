@@ -79,6 +79,22 @@ def ncu_traffic(workload):
     return nbytes if m.hexdigest()[:16] == digest else None
 
 
+def max_over_ranks(x, dist, world, device="cpu"):
+    """The largest value of x over all ranks (x itself on one rank): step times are the max over ranks."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds):
+    """Units processed by all ranks per second of the slowest rank (weak scaling: every rank runs
+    its own replica of the workload)."""
+    return units_per_rank * world / seconds
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -256,11 +272,7 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
         ms_local = e0.elapsed_time(e1)
         assert gdnspec.gdn_last_error(stream) == 0
 
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms_local, dist, world, device)
 
     # ---- end to end through the public API: pinned host inputs in, outputs out, every step
     e2e = None if profile else run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device)
@@ -277,8 +289,7 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
     t_layer_s = ms / 1e3 / (steps * R)
     peak, peak_kind = measured_peaks()
     achieved = per_call / t_layer_s / 1e9
-    nodes = B * N * R * steps * world
-    value = nodes / (ms / 1e3)
+    value = whole_job_rate(B * N * R * steps, world, ms / 1e3)
     launches_per_call = 1 if chain else 2
     return dict(
         value=value, ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
@@ -506,11 +517,7 @@ def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile
         assert gdnspec.gdn_last_error(stream) == 0
 
         seq = None if profile else run_sequential_baseline(lys[0], gdnspec, torch, stream, steps=3)
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms_local, dist, world, device)
 
     e2e = None if profile else run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device)
     w0 = lys[0].w
@@ -518,9 +525,8 @@ def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile
     flops = layer_flops(w0.B, w0.N, w0.H, w0.hidden, w0.dk, w0.dv)
     peak, peak_kind = measured_tensor_peak()
     achieved = flops / t_layer_s / 1e12
-    nodes = w0.B * w0.N * R * steps * world
     return dict(
-        value=nodes / (ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
+        value=whole_job_rate(w0.B * w0.N * R * steps, world, ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
         spec=spec, B=w0.B, N=w0.N, H=w0.H, dk=w0.dk, dv=w0.dv, hidden=w0.hidden, chain=False, layer=True,
         sequential=seq,
         roofline={"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
@@ -566,13 +572,9 @@ def run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device):
             one(s_ % 2)
         stream.synchronize()
         t1 = time.perf_counter()
-    sec = t1 - t0
-    if world > 1:
-        t = torch.tensor([sec], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+    sec = max_over_ranks(t1 - t0, dist, world, device)
     w = lys[0].w
-    return {"value": w.B * w.N * len(lys) * k * world / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": whole_job_rate(w.B * w.N * len(lys) * k, world, sec), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": 1e3 * sec / k}
 
 
@@ -645,15 +647,10 @@ def run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device):
             one(s % 2)
         stream.synchronize()
         t1 = time.perf_counter()
-    sec = t1 - t0
-    if world > 1:
-        t = torch.tensor([sec], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+    sec = max_over_ranks(t1 - t0, dist, world, device)
     w = layers[0].w
-    nodes = w.B * w.N * len(layers) * k * world
-    return {"value": nodes / sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": k, "ms_per_step": 1e3 * sec / k}
+    return {"value": whole_job_rate(w.B * w.N * len(layers) * k, world, sec), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": 1e3 * sec / k}
 
 
 # ---------------------------------------------------------------------------

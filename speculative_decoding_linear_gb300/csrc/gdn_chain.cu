@@ -315,7 +315,7 @@ template <typename T>
 cudaError_t launch_chain_dt(const VerifyArgs& a, cudaStream_t s) {
     // Small problems: 8-row CTAs so that more SMs stream the state.
     const long long ctas16 = (long long)a.B * a.H * ((a.dv + 15) / 16);
-    return ctas16 < 2 * 148 ? launch_chain_t<T, 2>(a, s) : launch_chain_t<T, 4>(a, s);
+    return ctas16 < 2 * 152 ? launch_chain_t<T, 2>(a, s) : launch_chain_t<T, 4>(a, s);
 }
 
 }  // namespace
