@@ -223,10 +223,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    // ---- 1. the state tile, before the wait: the whole HBM stream of this CTA ----
-    // (Only this call's prologue kernel runs before the wait releases, and it
-    // touches neither S nor the previous factors; every kernel before it has
-    // completed.  So the committed state may be written here.)
+    // ---- 1. before the wait: the state tile (the whole HBM stream of this CTA) and
+    // Y = S [Q; K]^T.  Only this call's prologue kernel runs before the wait
+    // releases (it starts this kernel after its own wait), and it touches neither
+    // S, the previous factors nor q/k/v; every kernel before it has completed.
+    // So the committed state may be written, and q/k read, here.
+    if (tid == 0) {
+        issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage0, 0, h, b * N, bar_tma0);
+        issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage1, 1, h, b * N, bar_tma0 + 8);
+    }
     const size_t srow0 = ((size_t)bh * dv + v0) * kDk;
     const int c4 = tid & 15;         // column quad within a slab
     const int rbase = tid >> 4;      // rows rbase + 16 j, j = 0..7
@@ -284,36 +289,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_proxy_async_smem();
     __syncthreads();
 
-    // ---- 2. wait for the prologue kernel (and this layer's q/k/v) ----
-    griddep_wait();
-    griddep_launch();
-    const WsLayout wl = ws_layout(N);
-    const char* rec = a.ws + (size_t)bh * wl.record;
-    const bool run = commit_ok && *reinterpret_cast<const uint64_t*>(rec + wl.anc) != ~0ull;
-    bool ok = run;
-
-    if (run) {
-        if (tid == 0) {
-            issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage0, 0, h, b * N, bar_tma0);
-            issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage1, 1, h, b * N, bar_tma0 + 8);
-            mbar_expect_tx(bar_eg, 2 * kNodeRows * 4);
-            bulk_copy_g2s(smem_u32(seg), rec + wl.eg, kNodeRows * 4, bar_eg);
-            bulk_copy_g2s(smem_u32(sbt), rec + wl.bt, kNodeRows * 4, bar_eg);
-            ok = mbar_wait(bar_tma0, 0, a.err);
-            if (ok) {
-                tc_fence_after();
-                issue_slab_mma<kSplit>(tmem, stage0, true);
-                mma_commit(bar_mma0);
-                ok = mbar_wait(bar_tma0 + 8, 0, a.err);
-            }
-            if (ok) {
-                tc_fence_after();
-                issue_slab_mma<kSplit>(tmem, stage1, false);
-                mma_commit(bar_mma0 + 8);
-            }
+    // Y slabs 0 and 1 (their q/k copies were issued at the start; both must land
+    // before the CTA may exit), then slabs 2 and 3 through the freed stages
+    bool ok = commit_ok;
+    if (tid == 0) {
+        const bool l0 = mbar_wait(bar_tma0, 0, a.err);
+        if (ok && l0) {
+            tc_fence_after();
+            issue_slab_mma<kSplit>(tmem, stage0, true);
+            mma_commit(bar_mma0);
         }
-        // slabs 2 and 3 reuse the stages once the MMAs of slabs 0 and 1 are done
-        ok = mbar_wait(bar_mma0, 0, a.err) && ok;
+        const bool l1 = mbar_wait(bar_tma0 + 8, 0, a.err);
+        if (ok && l0 && l1) {
+            tc_fence_after();
+            issue_slab_mma<kSplit>(tmem, stage1, false);
+            mma_commit(bar_mma0 + 8);
+        }
+        ok = ok && l0 && l1;
+    }
+    ok = __syncthreads_and(ok);
+    if (ok) {
+        ok = mbar_wait(bar_mma0, 0, a.err);
         if (tid == 0 && ok) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage0, 2, h, b * N, bar_tma0);
         convert_slab(x2, base, rbase, c4);
         fence_proxy_async_smem();
@@ -339,15 +335,30 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mma_commit(bar_mma0 + 8);
             }
         }
+    }
+    const bool y_issued = __syncthreads_and(ok);
 
+    // ---- 2. wait for the prologue kernel's outputs ----
+    griddep_wait();
+    griddep_launch();
+    const WsLayout wl = ws_layout(N);
+    const char* rec = a.ws + (size_t)bh * wl.record;
+    const bool run = y_issued && *reinterpret_cast<const uint64_t*>(rec + wl.anc) != ~0ull;
+    ok = y_issued;
+
+    if (y_issued) {                               // the Y MMAs are in flight: wait for them in any case
+        if (tid == 0 && run) {
+            mbar_expect_tx(bar_eg, 2 * kNodeRows * 4);
+            bulk_copy_g2s(smem_u32(seg), rec + wl.eg, kNodeRows * 4, bar_eg);
+            bulk_copy_g2s(smem_u32(sbt), rec + wl.bt, kNodeRows * 4, bar_eg);
+        }
         // Stage 0 is free once slab 2 is done: the [T; P] operand (bf16 hi, lo) into its
         // A buffers and this tile's v rows into its B buffer, by bulk copies.
-        ok = __syncthreads_and(ok);
-        if (ok) ok = mbar_wait(bar_mma0, 1, a.err);
+        ok = mbar_wait(bar_mma0, 1, a.err);
         const uint32_t op_s = stage0;                                  // B2: hi, then lo (16 KiB each)
         const uint32_t r_s = stage1;                                   // A2: R hi, then lo (stage 1)
         const uint32_t v_s = stage0 + 2 * kBufBytes;                   // v rows: [t][128] bf16
-        if (ok && warp == 0) {
+        if (ok && run && warp == 0) {
             if (lane == 0) {
                 mbar_expect_tx(bar_op, (uint32_t)(kTcOperandBytes + N * kTileV * (int)sizeof(KT)));
                 bulk_copy_g2s(op_s, rec + wl.op, (uint32_t)kTcOperandBytes, bar_op);
@@ -359,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                               kTileV * (int)sizeof(KT), bar_op);
         }
         if (ok) ok = mbar_wait(bar_mma0 + 8, 1, a.err);                // Y complete
+        ok = ok && run;
         if (ok) ok = mbar_wait(bar_op, 0, a.err);                      // operand and v rows landed
         if (ok) ok = mbar_wait(bar_eg, 0, a.err);                      // e^g and beta landed
         ok = __syncthreads_and(ok);
