@@ -317,8 +317,9 @@ int gdn_replay_commit(const void* k, const void* v, int dtype, const float* alph
  * layer-major sweep ("Pith review of SpecLA", "What carries the argument":
  * layer-major verification keeps per-layer state streaming back to back).
  * Contract while on: the state S, S0 and factor buffers of a call must not be
- * written by the kernel immediately before it on the stream -- e.g. the calls
- * of a sweep visit different layers, each with its own state and factors.
+ * read or written by the previous call on the stream (whose kernels may still
+ * run) -- e.g. the calls of a sweep visit different layers, each with its own
+ * state and factors.
  */
 int gdn_set_launch_overlap(int enable);
 
