@@ -280,6 +280,8 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
                                                                      max(5, min(steps, 20)))
     hybrid = None if (profile or chain) else run_hybrid_comparison(layers, gdnspec, torch, stream,
                                                                    max(5, min(steps, 20)), device, wl)
+    prune = None if (profile or chain) else run_prune_timing(gdnspec, torch, stream, device, wl, B=layers[0].w.B,
+                                                             N=layers[0].w.N)
 
     w0 = layers[0].w
     B, N, H, dk, dv = w0.B, w0.N, w0.H, w0.dk, w0.dv
@@ -300,7 +302,7 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
                   "kernel": "gdn_commit_chain_verify (chain_kernel)" if chain else
                             "gdn_commit_tree_verify (tree_prep_tc_kernel + tree_contract_tc_kernel)",
                   "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_layer_s * 1e6, 3)},
-        gpu_launches=launches_per_call * R * steps, baselines=baselines, hybrid=hybrid,
+        gpu_launches=launches_per_call * R * steps, baselines=baselines, hybrid=hybrid, prune=prune,
     )
 
 
@@ -517,6 +519,7 @@ def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile
         assert gdnspec.gdn_last_error(stream) == 0
 
         seq = None if profile else run_sequential_baseline(lys[0], gdnspec, torch, stream, steps=3)
+        model = None if profile else run_model_step(gdnspec, torch, stream, device, wl)
     ms = max_over_ranks(ms_local, dist, world, device)
 
     e2e = None if profile else run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device)
@@ -528,7 +531,7 @@ def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile
     return dict(
         value=whole_job_rate(w0.B * w0.N * R * steps, world, ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
         spec=spec, B=w0.B, N=w0.N, H=w0.H, dk=w0.dk, dv=w0.dv, hidden=w0.hidden, chain=False, layer=True,
-        sequential=seq,
+        sequential=seq, model=model,
         roofline={"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                   "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
                   "kernel": "gdn_layer_tree_step (input/output projection GEMMs on tcgen05, conv, "
@@ -536,6 +539,64 @@ def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile
                   "algorithmic_flops_per_call": flops, "t_call_us": round(t_layer_s * 1e6, 3)},
         gpu_launches=6 * R * steps,
     )
+
+
+def run_model_step(gdnspec, torch, stream, device, wl, n_layers=4, steps=5):
+    """n_layers full layers back to back on a residual stream (h_{l+1} = h_l + out_l), each step committing
+    the previous step's accepted path in every layer: time per model step as one CUDA graph per parity."""
+    lys = [LayerStep(wl.make_layer_workload(4, seed=5000 + 11 * l), device, torch, gdnspec) for l in range(n_layers)]
+    w = lys[0].w
+    ws = torch.empty(gdnspec.gdn_model_workspace_bytes(n_layers, w.B, w.N, w.H, w.hidden, w.dk, w.dv),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty((w.B, w.N, w.hidden), dtype=torch.float32, device=device)
+    per = dict(W_in=[ly.W_in for ly in lys], conv_w=[ly.conv_w for ly in lys], W_o=[ly.W_o for ly in lys],
+               S=[ly.S for ly in lys], conv_state=[ly.conv_state for ly in lys])
+
+    def step(parity, first=False):
+        gdnspec.gdn_model_tree_step(lys[0].X, per["W_in"], per["conv_w"], per["W_o"], lys[0].parent, per["S"],
+                                    per["conv_state"], None if first else [ly.rec[parity] for ly in lys], w.N,
+                                    None if first else lys[0].path, out, [ly.rec[1 - parity] for ly in lys], ws,
+                                    w.H, w.dk, w.dv)
+    with torch.cuda.stream(stream):
+        step(1, first=True)                    # writes rec[0]
+        step(0)
+        step(1)
+        graphs = []
+        for parity in (0, 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(parity)
+            graphs.append(g)
+        for i in range(3):
+            graphs[i % 2].replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % 2].replay()
+        e1.record(stream)
+        e1.synchronize()
+    assert gdnspec.gdn_last_error(stream) == 0
+    ms = e0.elapsed_time(e1) / steps
+    del lys, ws
+    torch.cuda.empty_cache()
+    return {"layers": n_layers, "ms_per_model_step": round(ms, 4), "us_per_layer": round(1e3 * ms / n_layers, 2),
+            "nodes_per_s_per_layer": round(w.B * w.N * n_layers / (ms / 1e3), 1),
+            "what": "gdn_model_tree_step: %d layers back to back on a residual stream h_(l+1) = h_l + out_l, "
+                    "every layer committing the previous step's accepted path" % n_layers}
+
+
+def run_prune_timing(gdnspec, torch, stream, device, wl, B, N, steps=50):
+    """Device time of one gdn_prune_tree call on B random trees of N nodes."""
+    rng = np.random.default_rng(77)
+    parent = torch.from_numpy(np.stack([wl.random_tree(rng, N, 8) for _ in range(B)])).to(device)
+    logp = torch.from_numpy((-rng.exponential(1.0, (B, N))).astype(np.float32)).to(device)
+    idx = torch.empty((B, N), dtype=torch.int32, device=device)
+    npar = torch.empty((B, N), dtype=torch.int32, device=device)
+    nk = torch.empty(B, dtype=torch.int32, device=device)
+    us = time_calls([lambda: gdnspec.gdn_prune_tree(parent, logp, 1.0, N // 2, idx, npar, nk)], torch, stream, steps)
+    assert gdnspec.gdn_last_error(stream) == 0
+    return {"us_per_call": round(us, 3), "B": B, "N": N, "tau": 1.0, "budget": N // 2}
 
 
 def measured_tensor_peak():
@@ -803,6 +864,10 @@ def main():
             line["replay_baselines"] = r["baselines"]
         if r.get("hybrid"):
             line["hybrid_verify"] = r["hybrid"]
+        if r.get("prune"):
+            line["prune_tree"] = r["prune"]
+        if r.get("model"):
+            line["model_step"] = r["model"]
         if r.get("layer"):
             line["config"]["hidden"] = r["hidden"]
             seq = r["sequential"]

@@ -244,6 +244,27 @@ int gdn_layer_tree_step(const void* X, const void* W_in, const float* conv_w, co
                         cudaStream_t stream);
 
 /*
+ * L GDN layers back to back over the same draft trees (layer-major
+ * verification, "Pith review of SpecLA", "What carries the argument": the
+ * layers are verified one after another, each streaming its own state).  Layer
+ * l runs the layer step of gdn_layer_tree_step on input h_l with its own
+ * weights, state, convolution history and records, on a residual stream:
+ * h_0 = X, h_{l+1} = h_l + out_l in fp32 (entering each input projection as
+ * two bf16 terms, hi + lo).  `out` (fp32 [B][N][hidden]) receives h_L.
+ *   W_in, conv_w, W_o, S, conv_state, records, prev_records: host arrays of L
+ *           device pointers, each as in gdn_layer_tree_step (prev_records and
+ *           prev_path both NULL when there is nothing to commit)
+ *   workspace  gdn_model_workspace_bytes bytes (one layer's workspace, the layer
+ *           output and the residual stream in fp32 and as bf16 hi/lo terms)
+ */
+int gdn_model_workspace_bytes(int L, int B, int N, int H, int hidden, int dk, int dv, size_t* bytes);
+int gdn_model_tree_step(int L, const void* X, const void* const* W_in, const float* const* conv_w,
+                        const void* const* W_o, const int32_t* parent_idx, float* const* S, float* const* conv_state,
+                        void* const* prev_records, int N_prev, const int32_t* prev_path, int Lmax, float* out,
+                        void* const* records, void* workspace, int B, int N, int H, int hidden, int dk, int dv,
+                        cudaStream_t stream);
+
+/*
  * Per-token decoding of the same layer, for comparison with the tree step:
  * node t of every tree is decoded on its own (input projection at B rows,
  * its conv window, one delta-rule step from the parent's materialised state,
@@ -283,6 +304,28 @@ int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, c
 int gdn_hybrid_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
                            const float* beta, const int32_t* parent_idx, const float* S0, float* out,
                            void* factors, int B, int N, int H, int dk, int dv, cudaStream_t stream);
+
+/*
+ * Confidence-guided pruning of B draft trees before verification ("Pith review
+ * of SpecLA": confidence-guided tree pruning with a tree margin tau_tree and a
+ * draft budget; the pages do not define them, the rule here is):
+ *   score(t) = logp[t] + score(parent(t)), root first, fp32, where logp[t] is
+ *              the drafter's log-probability of node t given its parent (<= 0)
+ *   node t survives if score(t) >= max over its siblings (same parent, t
+ *              included) of score minus tau, and its parent survives
+ *   of the survivors the `budget` highest scores are kept (ties to the lower
+ *              index), a set closed under ancestors; kept nodes keep their order
+ *   parent_idx  int32 [B][N], topological (as gdn_tree_verify)
+ *   logp        fp32 [B][N]
+ *   new_index   int32 [B][N]: new number of each node, -1 if pruned
+ *   new_parent  int32 [B][N]: parents of the kept nodes in their new numbering;
+ *               entries from n_kept[b] on are -1
+ *   n_kept      int32 [B]
+ * tau >= 0 (may be +inf), budget >= 0.  Invalid parent_idx -> GDN_ERR_TREE in
+ * the error word, outputs untouched.
+ */
+int gdn_prune_tree(const int32_t* parent_idx, const float* logp, float tau, int budget, int32_t* new_index,
+                   int32_t* new_parent, int32_t* n_kept, int B, int N, cudaStream_t stream);
 
 /*
  * Replay baselines: what tree verification and the factor-buffer commit

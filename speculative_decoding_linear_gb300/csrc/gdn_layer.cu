@@ -432,13 +432,16 @@ extern "C" int gdn_layer_workspace_bytes(int B, int N, int H, int hidden, int dk
     return GDN_OK;
 }
 
-extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float* conv_w, const void* W_o,
-                                   const int32_t* parent_idx, float* S, float* conv_state, const void* prev_record,
-                                   int N_prev, const int32_t* prev_path, int Lmax, float* out, void* record,
-                                   void* workspace, int B, int N, int H, int hidden, int dk, int dv,
-                                   cudaStream_t stream) {
+namespace gdn {
+namespace {
+
+// One layer step; X_lo (may be null) is the bf16 lo term of an fp32 input X = X + X_lo.
+int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const float* conv_w, const void* W_o,
+                    const int32_t* parent_idx, float* S, float* conv_state, const void* prev_record, int N_prev,
+                    const int32_t* prev_path, int Lmax, float* out, void* record, void* workspace, int B, int N, int H,
+                    int hidden, int dk, int dv, cudaStream_t stream) {
     if (!layer_shape_ok(B, N, H, hidden, dk, dv)) return GDN_ERR_ARG;
-    if (!ok16(X) || !ok16(W_in) || !ok16(conv_w) || !ok16(W_o) || !ok16(parent_idx) || !ok16(S) ||
+    if ((X_lo != nullptr && !ok16(X_lo)) || !ok16(X) || !ok16(W_in) || !ok16(conv_w) || !ok16(W_o) || !ok16(parent_idx) || !ok16(S) ||
         !ok16(conv_state) || !ok16(out) || !ok16(record) || !ok16(workspace))
         return GDN_ERR_ARG;
     const bool commit = prev_path != nullptr;
@@ -468,7 +471,8 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
     float* Y = reinterpret_cast<float*>(rec + Ly.y_off);
     const long long M = (long long)B * N;
 
-    cudaError_t e = launch_gemm_bf16(X, nullptr, 1, hidden, W_in, Y, Ly.ldy, (int)M, Ly.rows, hidden, err, stream);
+    cudaError_t e = launch_gemm_bf16(X, X_lo, X_lo ? 2 : 1, hidden, W_in, Y, Ly.ldy, (int)M, Ly.rows, hidden, err,
+                                     stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
 
     ConvArgs ca;
@@ -547,6 +551,18 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
 
     e = launch_gemm_bf16(gaa.yhi, gaa.ylo, 2, H * dv, W_o, out, hidden, (int)M, hidden, H * dv, err, stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float* conv_w, const void* W_o,
+                                   const int32_t* parent_idx, float* S, float* conv_state, const void* prev_record,
+                                   int N_prev, const int32_t* prev_path, int Lmax, float* out, void* record,
+                                   void* workspace, int B, int N, int H, int hidden, int dk, int dv,
+                                   cudaStream_t stream) {
+    return layer_tree_step(X, nullptr, W_in, conv_w, W_o, parent_idx, S, conv_state, prev_record, N_prev, prev_path,
+                           Lmax, out, record, workspace, B, N, H, hidden, dk, dv, stream);
 }
 
 extern "C" int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, const void* W_o,
@@ -644,4 +660,102 @@ extern "C" int gdn_layer_token_step(const void* X, const void* W_in, const float
     e = launch_gemm_bf16(gaa.yhi + ro, gaa.ylo + ro, 2, (long long)N * H * dv, W_o, out + (size_t)t * hidden,
                          (long long)N * hidden, B, hidden, H * dv, err, stream);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// several layers back to back (layer-major step of a GDN stack)
+// ---------------------------------------------------------------------------
+namespace gdn {
+namespace {
+
+// Residual stream between layers: h = (h_in ? h_in : float(x0)) + o, stored fp32 and
+// as bf16 hi + lo terms (the next layer's input projection takes both).  Four
+// elements per thread.
+__global__ void __launch_bounds__(256) residual_kernel(const __nv_bfloat16* x0, const float* h_in, const float* o,
+                                                        float* h_out, __nv_bfloat16* hi, __nv_bfloat16* lo,
+                                                        long long n4) {
+    griddep_wait();
+    for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n4; i += (long long)gridDim.x * 256) {
+        float4 h;
+        if (h_in != nullptr) {
+            h = reinterpret_cast<const float4*>(h_in)[i];
+        } else {
+            const uint2 u = reinterpret_cast<const uint2*>(x0)[i];
+            h = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                            __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+        }
+        const float4 d = reinterpret_cast<const float4*>(o)[i];
+        h.x += d.x;
+        h.y += d.y;
+        h.z += d.z;
+        h.w += d.w;
+        reinterpret_cast<float4*>(h_out)[i] = h;
+        if (hi != nullptr) {
+            const __nv_bfloat162 a = __floats2bfloat162_rn(h.x, h.y), b = __floats2bfloat162_rn(h.z, h.w);
+            const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+            const __nv_bfloat162 la = __floats2bfloat162_rn(h.x - fa.x, h.y - fa.y);
+            const __nv_bfloat162 lb = __floats2bfloat162_rn(h.z - fb.x, h.w - fb.y);
+            uint2 uh, ul;
+            uh.x = *reinterpret_cast<const uint32_t*>(&a);
+            uh.y = *reinterpret_cast<const uint32_t*>(&b);
+            ul.x = *reinterpret_cast<const uint32_t*>(&la);
+            ul.y = *reinterpret_cast<const uint32_t*>(&lb);
+            reinterpret_cast<uint2*>(hi)[i] = uh;
+            reinterpret_cast<uint2*>(lo)[i] = ul;
+        }
+    }
+    griddep_launch();
+}
+
+// layer output o and residual stream h (fp32), then h as bf16 hi and lo terms
+size_t model_extra_bytes(int B, int N, int hidden) {
+    return 2 * align_up((size_t)B * N * hidden * 4, 256) + 2 * align_up((size_t)B * N * hidden * 2, 256);
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" int gdn_model_workspace_bytes(int L, int B, int N, int H, int hidden, int dk, int dv, size_t* bytes) {
+    if (bytes == nullptr || L < 1 || L > 4096 || !layer_shape_ok(B, N, H, hidden, dk, dv)) return GDN_ERR_ARG;
+    *bytes = align_up(layer_layout(B, N, H, hidden, dk, dv).workspace_bytes, 256) + model_extra_bytes(B, N, hidden);
+    return GDN_OK;
+}
+
+extern "C" int gdn_model_tree_step(int L, const void* X, const void* const* W_in, const float* const* conv_w,
+                                   const void* const* W_o, const int32_t* parent_idx, float* const* S,
+                                   float* const* conv_state, void* const* prev_records, int N_prev,
+                                   const int32_t* prev_path, int Lmax, float* out, void* const* records,
+                                   void* workspace, int B, int N, int H, int hidden, int dk, int dv,
+                                   cudaStream_t stream) {
+    if (L < 1 || L > 4096 || W_in == nullptr || conv_w == nullptr || W_o == nullptr || S == nullptr ||
+        conv_state == nullptr || records == nullptr || !layer_shape_ok(B, N, H, hidden, dk, dv))
+        return GDN_ERR_ARG;
+    if ((prev_path != nullptr) != (prev_records != nullptr) || !ok16(workspace) || !ok16(X) || !ok16(out))
+        return GDN_ERR_ARG;
+    const LayerLayout Ly = layer_layout(B, N, H, hidden, dk, dv);
+    char* ws = static_cast<char*>(workspace);
+    const size_t f32b = align_up((size_t)B * N * hidden * 4, 256), b16b = align_up((size_t)B * N * hidden * 2, 256);
+    char* extra = ws + align_up(Ly.workspace_bytes, 256);
+    float* o = reinterpret_cast<float*>(extra);                       // this layer's output
+    float* h = reinterpret_cast<float*>(extra + f32b);                // residual stream
+    __nv_bfloat16* hhi = reinterpret_cast<__nv_bfloat16*>(extra + 2 * f32b);
+    __nv_bfloat16* hlo = reinterpret_cast<__nv_bfloat16*>(extra + 2 * f32b + b16b);
+    const long long n4 = (long long)B * N * hidden / 4;
+    long long blocks = (n4 + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    for (int l = 0; l < L; ++l) {
+        const int rc = layer_tree_step(l == 0 ? X : hhi, l == 0 ? nullptr : hlo, W_in[l], conv_w[l], W_o[l],
+                                       parent_idx, S[l], conv_state[l], prev_records ? prev_records[l] : nullptr,
+                                       N_prev, prev_path, Lmax, o, records[l], workspace, B, N, H, hidden, dk, dv,
+                                       stream);
+        if (rc != GDN_OK) return rc;
+        const bool last = l == L - 1;
+        if (launch_kernel(residual_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, false,
+                          l == 0 ? static_cast<const __nv_bfloat16*>(X) : nullptr,
+                          l == 0 ? (const float*)nullptr : (const float*)h, (const float*)o, last ? out : h,
+                          last ? (__nv_bfloat16*)nullptr : hhi, last ? (__nv_bfloat16*)nullptr : hlo, n4) !=
+            cudaSuccess)
+            return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
 }

@@ -45,6 +45,10 @@ SIGNATURES = {
                                  _I, _I, _I, _I, _I, _I, _P]),
     "gdn_layer_token_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                                   _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_model_workspace_bytes": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
+    "gdn_model_tree_step": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P,
+                                 _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_prune_tree": (_I, [_P, _P, ctypes.c_float, _I, _P, _P, _P, _I, _I, _P]),
     "gdn_hybrid_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
@@ -250,6 +254,41 @@ def gdn_layer_token_step(X, W_in, conv_w, W_o, parent_idx, S0, conv_state, S_nod
                                       _ptr(conv_state), _ptr(S_nodes), int(t), _ptr(out), _ptr(record),
                                       _ptr(workspace), B, N, H, hidden, dk, dv, _stream(stream)),
            "gdn_layer_token_step")
+
+
+def gdn_model_workspace_bytes(L, B, N, H, hidden, dk, dv) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_model_workspace_bytes(L, B, N, H, hidden, dk, dv, ctypes.byref(out)),
+           "gdn_model_workspace_bytes")
+    return out.value
+
+
+def _ptr_array(xs):
+    if xs is None:
+        return None
+    arr = (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+    return ctypes.cast(arr, ctypes.c_void_p), arr      # keep the array alive with the call
+
+
+def gdn_model_tree_step(X, W_in, conv_w, W_o, parent_idx, S, conv_state, prev_records, N_prev, prev_path, out,
+                        records, workspace, H, dk, dv, stream=None):
+    """L layers back to back (see include/gdnspec.h); the per-layer arguments are lists of L tensors."""
+    B, N, hidden = X.shape
+    L = len(W_in)
+    arrs = [_ptr_array(x) for x in (W_in, conv_w, W_o, S, conv_state, prev_records, records)]
+    ptrs = [a[0] if a is not None else None for a in arrs]
+    Lmax = 0 if prev_path is None else prev_path.shape[1]
+    _check(lib().gdn_model_tree_step(L, _ptr(X), ptrs[0], ptrs[1], ptrs[2], _ptr(parent_idx), ptrs[3], ptrs[4],
+                                     ptrs[5], int(N_prev), _ptr(prev_path), Lmax, _ptr(out), ptrs[6],
+                                     _ptr(workspace), B, N, H, hidden, dk, dv, _stream(stream)),
+           "gdn_model_tree_step")
+
+
+def gdn_prune_tree(parent_idx, logp, tau, budget, new_index, new_parent, n_kept, stream=None):
+    """Confidence-guided pruning of B draft trees (see include/gdnspec.h)."""
+    B, N = parent_idx.shape
+    _check(lib().gdn_prune_tree(_ptr(parent_idx), _ptr(logp), float(tau), int(budget), _ptr(new_index),
+                                _ptr(new_parent), _ptr(n_kept), B, N, _stream(stream)), "gdn_prune_tree")
 
 
 def gdn_hybrid_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, stream=None):

@@ -157,3 +157,44 @@ def test_per_token_decode_matches_oracle(oracle_mod, shape):
     got = np.stack([S_nodes[ends[b], b].cpu().numpy() for b in range(B)])
     assert_close(got, S_ref, "node state")
     assert torch.equal(cs.cpu(), torch.from_numpy(w.conv_state))
+
+
+@pytest.mark.parametrize("shape", [SMALL[0], SMALL[3]])
+def test_model_step_layers_back_to_back(oracle_mod, shape):
+    """Three layers on a residual stream (h_{l+1} = h_l + out_l), then a second step committing every layer."""
+    from oracle import layer
+    B, N, H, dk, dv, hid, md = shape
+    L = 3
+    ws_ = [wl.make_layer_workload(4, seed=300 + 7 * l + B, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=md)
+           for l in range(L)]
+    w0 = ws_[0]
+    runs = [LayerRun(w) for w in ws_]
+    X = bf16(w0.X)
+    parent = torch.from_numpy(w0.parent.astype(np.int32)).cuda()
+    rec_bytes = gdnspec.gdn_layer_record_bytes(B, N, H, hid, dk, dv)
+    recs = [[torch.empty(rec_bytes, dtype=torch.uint8, device="cuda") for _ in range(L)] for _ in range(2)]
+    ws = torch.empty(gdnspec.gdn_model_workspace_bytes(L, B, N, H, hid, dk, dv), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, N, hid), dtype=torch.float32, device="cuda")
+    args = dict(W_in=[r.W_in for r in runs], conv_w=[r.conv_w for r in runs], W_o=[r.W_o for r in runs],
+                S=[r.S for r in runs], conv_state=[r.conv_state for r in runs])
+    gdnspec.gdn_model_tree_step(X, args["W_in"], args["conv_w"], args["W_o"], parent, args["S"], args["conv_state"],
+                                None, 0, None, out, recs[0], ws, H, dk, dv)
+    assert gdnspec.gdn_last_error() == gdnspec.OK
+    lays = [dict(W_in=w.widened("W_in"), conv_w=w.widened("conv_w"), conv_state=w.widened("conv_state"),
+                 W_o=w.widened("W_o"), S0=w.widened("S0")) for w in ws_]
+    res, h = layer.model_step(w0.widened("X"), lays, w0.parent, H, dk, dv)
+    assert_close(out.cpu().numpy(), h, "residual stream after the last layer")
+    # second step: every layer commits the first step's accepted path, then verifies a new tree
+    w2 = wl.make_layer_workload(4, seed=399 + B, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=md)
+    parent2 = torch.from_numpy(w2.parent.astype(np.int32)).cuda()
+    path = torch.from_numpy(w0.path).cuda()
+    gdnspec.gdn_model_tree_step(bf16(w2.X), args["W_in"], args["conv_w"], args["W_o"], parent2, args["S"],
+                                args["conv_state"], recs[0], N, path, out, recs[1], ws, H, dk, dv)
+    assert gdnspec.gdn_last_error() == gdnspec.OK
+    for l in range(L):
+        S1, hist1 = layer.layer_commit(res[l], w0.parent, lays[l]["S0"], lays[l]["conv_state"], w0.path)
+        assert_close(runs[l].S.cpu().numpy(), S1, "committed state, layer %d" % l)
+        assert_close(runs[l].conv_state.cpu().numpy(), hist1, "committed conv history, layer %d" % l, tol=1e-4)
+        lays[l]["S0"], lays[l]["conv_state"] = S1, hist1
+    _, h2 = layer.model_step(w2.widened("X"), lays, w2.parent, H, dk, dv)
+    assert_close(out.cpu().numpy(), h2, "residual stream, second step")

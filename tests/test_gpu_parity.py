@@ -429,3 +429,39 @@ def test_hybrid_rejects_too_many_branching_nodes():
     out, fac, _ = alloc_outputs(w)
     gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out, fac)
     assert gdnspec.gdn_last_error() == gdnspec.ERR_CAPACITY
+
+
+# ---------------------------------------------------------------------------
+# confidence-guided pruning (index work: bit-exact against the oracle)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(4))
+def test_prune_matches_oracle(seed):
+    from oracle import prune as P
+    rng = np.random.default_rng(700 + seed)
+    B, N = 12, [64, 37, 7, 64][seed]
+    parent = np.stack([wl.random_tree(rng, N, int(rng.integers(0, 9))) for _ in range(B)])
+    logp = (-rng.exponential(1.0, (B, N))).astype(np.float32)
+    logp[:, ::5] = 0.0                                   # exact ties
+    for tau, budget in [(np.inf, 64), (0.0, 64), (0.7, 20), (2.0, 5), (1.0, 0)]:
+        d_par = torch.from_numpy(parent).cuda()
+        d_lp = torch.from_numpy(logp).cuda()
+        idx = torch.empty((B, N), dtype=torch.int32, device="cuda")
+        npar = torch.empty((B, N), dtype=torch.int32, device="cuda")
+        nk = torch.empty(B, dtype=torch.int32, device="cuda")
+        gdnspec.gdn_prune_tree(d_par, d_lp, tau, budget, idx, npar, nk)
+        assert gdnspec.gdn_last_error() == 0
+        for b in range(B):
+            ri, rp, rn = P.prune(parent[b], logp[b], tau, budget)
+            assert int(nk[b]) == rn
+            assert np.array_equal(idx[b].cpu().numpy(), ri)
+            got = npar[b].cpu().numpy()
+            assert np.array_equal(got[:rn], rp) and np.all(got[rn:] == -1)
+
+
+def test_prune_rejects_invalid_tree():
+    parent = torch.tensor([[-1, 0, 3, 1]], dtype=torch.int32, device="cuda")
+    lp = torch.zeros((1, 4), dtype=torch.float32, device="cuda")
+    out = [torch.empty((1, 4), dtype=torch.int32, device="cuda") for _ in range(2)] + \
+          [torch.empty(1, dtype=torch.int32, device="cuda")]
+    gdnspec.gdn_prune_tree(parent, lp, 1.0, 4, *out)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_TREE
