@@ -485,7 +485,7 @@ struct PrepTcLayout {
         A = take(N * ld * 4);
         At = take(N * ld * 4);
         T = take(N * ld * 4);
-        o = kSlabs * kBufBytes * (split ? 2 : 1);   // [Q; K] hi, then lo for fp32 q/k
+        o = kSlabs * kBufBytes;   // [Q; K]: four slabs, or for fp32 q/k two (hi, lo) slab pairs in turn
         G = take(128 * 65 * 4);          // Gram rows: q_t.k_j (rows 0..63), k_t.k_j (rows 64..127)
         plist = take(N * 64);
         par = take(N * 4);
@@ -494,7 +494,7 @@ struct PrepTcLayout {
         g = take(N * 4);
         beta = take(N * 4);
         depth = take(N * 4);
-        bars = take(16);
+        bars = take(48);
         misc = take(16);
         total = o + 1024;
     }
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tree_prep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmQl, const __grid_constant__ CUtensorMap tmKl,
                         VerifyArgs a) {
-    constexpr uint32_t kLoOff = kSlabs * kBufBytes;     // [Q; K] lo terms (fp32 q/k only)
+    constexpr uint32_t kPair = 2 * kBufBytes;           // fp32 q/k: one slab's hi and lo terms (32 KiB)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -533,6 +533,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     float* sbeta = reinterpret_cast<float*>(base + Ly.beta);
     int* sdepth = reinterpret_cast<int*>(base + Ly.depth);
     const uint32_t bar_tma = base_s + Ly.bars, bar_mma = base_s + Ly.bars + 8;
+    const uint32_t bar_tma1 = base_s + Ly.bars + 16, bar_free0 = base_s + Ly.bars + 24,
+                   bar_free1 = base_s + Ly.bars + 32;    // fp32 q/k: second slab buffer
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
 
     const int bh = blockIdx.x;
@@ -543,6 +545,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_tma1, 1);
+        mbar_init(bar_free0, 1);
+        mbar_init(bar_free1, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         fence_proxy_async_smem();
     }
@@ -571,16 +576,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     griddep_wait();
     griddep_launch();
 
+    // fp32 q/k: slab sl's hi and lo terms into pair buffer j (hi at +0, lo at +16 KiB)
+    auto load_pair = [&](int sl, int j, uint32_t bar) {
+        const uint32_t dst = base_s + j * kPair;
+        mbar_expect_tx(bar, 2 * 2 * kNodeRows * 128);
+        tma_load_3d(dst, &tmQ, sl * kSlab, h, b * N, bar);
+        tma_load_3d(dst + kNodeRows * 128, &tmK, sl * kSlab, h, b * N, bar);
+        tma_load_3d(dst + kBufBytes, &tmQl, sl * kSlab, h, b * N, bar);
+        tma_load_3d(dst + kBufBytes + kNodeRows * 128, &tmKl, sl * kSlab, h, b * N, bar);
+    };
     if (tid == 0) {
-        mbar_expect_tx(bar_tma, (uint32_t)(kSlabs * 2 * kNodeRows * 128 * (kSplit ? 2 : 1)));
+        if (kSplit) {
+            load_pair(0, 0, bar_tma);
+            load_pair(1, 1, bar_tma1);
+        } else {
+            mbar_expect_tx(bar_tma, (uint32_t)(kSlabs * 2 * kNodeRows * 128));
 #pragma unroll
-        for (int sl = 0; sl < kSlabs; ++sl) {
-            tma_load_3d(base_s + sl * kBufBytes, &tmQ, sl * kSlab, h, b * N, bar_tma);
-            tma_load_3d(base_s + sl * kBufBytes + kNodeRows * 128, &tmK, sl * kSlab, h, b * N, bar_tma);
-            if (kSplit) {
-                tma_load_3d(base_s + kLoOff + sl * kBufBytes, &tmQl, sl * kSlab, h, b * N, bar_tma);
-                tma_load_3d(base_s + kLoOff + sl * kBufBytes + kNodeRows * 128, &tmKl, sl * kSlab, h, b * N,
-                            bar_tma);
+            for (int sl = 0; sl < kSlabs; ++sl) {
+                tma_load_3d(base_s + sl * kBufBytes, &tmQ, sl * kSlab, h, b * N, bar_tma);
+                tma_load_3d(base_s + sl * kBufBytes + kNodeRows * 128, &tmK, sl * kSlab, h, b * N, bar_tma);
             }
         }
     }
@@ -595,6 +609,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     bad = __syncthreads_or(bad);
     bool ok = mbar_wait(bar_tma, 0, a.err);       // the copies land even if the tree is rejected
+    if (kSplit) ok = mbar_wait(bar_tma1, 0, a.err) && ok;
     if (bad && tid == 0) {
         set_error(a.err, GDN_ERR_TREE);
         *reinterpret_cast<uint64_t*>(rec + wl.anc) = ~0ull;   // record marked invalid
@@ -602,19 +617,48 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     if (!bad) {
         if (tid == 128 && ok) {                  // a warp with no per-node work issues the Gram MMA
             tc_fence_after();
+            if (kSplit) {
+                // hi.hi, hi.lo and lo.hi terms, two slabs at a time through the two pair buffers
+                auto pair_mma = [&](int sl, int j) {
 #pragma unroll
-            for (int sl = 0; sl < kSlabs; ++sl)
-#pragma unroll
-                for (int kk = 0; kk < kSlab / 16; ++kk) {
-                    const uint32_t q_s = base_s + sl * kBufBytes + kk * 32;
-                    mma_bf16(tmem, sw128_desc(q_s), sw128_desc(q_s + kNodeRows * 128), kGramIdesc,
-                             (sl > 0 || kk > 0) ? 1u : 0u);
-                    if (kSplit) {             // hi.lo and lo.hi terms of fp32 q/k
-                        mma_bf16(tmem, sw128_desc(q_s), sw128_desc(q_s + kLoOff + kNodeRows * 128), kGramIdesc, 1u);
-                        mma_bf16(tmem, sw128_desc(q_s + kLoOff), sw128_desc(q_s + kNodeRows * 128), kGramIdesc, 1u);
+                    for (int kk = 0; kk < kSlab / 16; ++kk) {
+                        const uint32_t q_s = base_s + j * kPair + kk * 32, l_s = q_s + kBufBytes;
+                        mma_bf16(tmem, sw128_desc(q_s), sw128_desc(q_s + kNodeRows * 128), kGramIdesc,
+                                 (sl > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16(tmem, sw128_desc(q_s), sw128_desc(l_s + kNodeRows * 128), kGramIdesc, 1u);
+                        mma_bf16(tmem, sw128_desc(l_s), sw128_desc(q_s + kNodeRows * 128), kGramIdesc, 1u);
                     }
+                };
+                pair_mma(0, 0);
+                mma_commit(bar_free0);
+                pair_mma(1, 1);
+                mma_commit(bar_free1);
+                bool l2 = mbar_wait(bar_free0, 0, a.err);
+                if (l2) load_pair(2, 0, bar_tma);
+                bool l3 = mbar_wait(bar_free1, 0, a.err);
+                if (l3) load_pair(3, 1, bar_tma1);
+                l2 = l2 && mbar_wait(bar_tma, 1, a.err);
+                if (l2) {
+                    tc_fence_after();
+                    pair_mma(2, 0);
                 }
-            mma_commit(bar_mma);
+                l3 = l3 && mbar_wait(bar_tma1, 1, a.err);
+                if (l3) {
+                    tc_fence_after();
+                    pair_mma(3, 1);
+                }
+                if (l2 && l3) mma_commit(bar_mma);   // a lost copy leaves bar_mma open: the wait below times out
+            } else {
+#pragma unroll
+                for (int sl = 0; sl < kSlabs; ++sl)
+#pragma unroll
+                    for (int kk = 0; kk < kSlab / 16; ++kk) {
+                        const uint32_t q_s = base_s + sl * kBufBytes + kk * 32;
+                        mma_bf16(tmem, sw128_desc(q_s), sw128_desc(q_s + kNodeRows * 128), kGramIdesc,
+                                 (sl > 0 || kk > 0) ? 1u : 0u);
+                    }
+                mma_commit(bar_mma);
+            }
         }
         if (tid < N) {
             prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
