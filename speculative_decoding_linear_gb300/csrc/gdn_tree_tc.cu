@@ -54,8 +54,14 @@ constexpr int kDk = 256;           // d_k handled by this kernel
 constexpr int kSlabs = kDk / kSlab;
 constexpr int kNodeRows = 64;      // B operand: Q rows 0..63, K rows 64..127 (MMA N = 128)
 constexpr int kBufBytes = kTileV * 128;        // one 128-row x 128-byte operand buffer (16 KiB)
-// Stage: A_hi, A_lo, B (bf16 q/k), plus B_lo when fp32 q/k enter as bf16 hi + lo.
-__host__ __device__ constexpr int stage_bytes(bool split) { return (split ? 4 : 3) * kBufBytes; }
+// Operand buffers.  bf16 q/k: two stages [A_hi, A_lo, B] (96 KiB).  fp32 q/k
+// (hi + lo terms): two A stages [A_hi, A_lo] and one B buffer [B_hi, B_lo]
+// (96 KiB), so that two CTAs fit on an SM; slabs take turns in the B buffer.
+__host__ __device__ constexpr int a_off(bool split, int st) { return st * (split ? 2 : 3) * kBufBytes; }
+__host__ __device__ constexpr int b_off(bool split, int st) {
+    return split ? 4 * kBufBytes : st * 3 * kBufBytes + 2 * kBufBytes;
+}
+__host__ __device__ constexpr int operand_bytes(bool) { return 6 * kBufBytes; }
 constexpr uint32_t kTmemCols = 256;     // Y in columns 0..127, [Delta | P R] in 128..255
 constexpr int kMaxTcPath = 16;
 constexpr uint32_t kIdesc = idesc_bf16(128, 128);   // D fp32, A/B bf16 K-major, M = N = 128
@@ -64,7 +70,7 @@ struct TcLayout {
     // offsets from the 1024-aligned base
     int cd, key, coef, nodes, bars, misc, egbt, total;
     __host__ __device__ TcLayout(int Lcap, bool split) {
-        int o = 2 * stage_bytes(split);
+        int o = operand_bytes(split);
         auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
         cd = take(Lcap * kTileV * 4);
         key = take(Lcap * kDk * (split ? 4 : 2));
@@ -146,8 +152,8 @@ __device__ __forceinline__ void convert_slab(const float4 (&x)[8], unsigned char
 // bf16 q/k, plus state hi times the lo term of fp32 q/k (the lo.lo product,
 // ~2^-16 of the hi.lo ones, is dropped).
 template <bool kSplit>
-__device__ __forceinline__ void issue_slab_mma(uint32_t tmem, uint32_t stage_s, bool first) {
-    const uint32_t a_hi = stage_s, a_lo = stage_s + kBufBytes, bsm = stage_s + 2 * kBufBytes;
+__device__ __forceinline__ void issue_slab_mma(uint32_t tmem, uint32_t a_s, uint32_t bsm, bool first) {
+    const uint32_t a_hi = a_s, a_lo = a_s + kBufBytes;
 #pragma unroll
     for (int kk = 0; kk < kSlab / 16; ++kk) {
         const uint64_t bd = sw128_desc(bsm + kk * 32);
@@ -159,9 +165,8 @@ __device__ __forceinline__ void issue_slab_mma(uint32_t tmem, uint32_t stage_s, 
 
 template <bool kSplit>
 __device__ __forceinline__ void issue_qk_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmQl,
-                                             const CUtensorMap* tmKl, uint32_t stage_s, int ks, int h, int row0,
+                                             const CUtensorMap* tmKl, uint32_t bsm, int ks, int h, int row0,
                                              uint32_t bar) {
-    const uint32_t bsm = stage_s + 2 * kBufBytes;
     mbar_expect_tx(bar, (kSplit ? 4 : 2) * kNodeRows * 128);
     tma_load_3d(bsm, tmQ, ks * kSlab, h, row0, bar);
     tma_load_3d(bsm + kNodeRows * 128, tmK, ks * kSlab, h, row0, bar);
@@ -177,7 +182,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                             const __grid_constant__ CUtensorMap tmQl, const __grid_constant__ CUtensorMap tmKl,
                             VerifyArgs a) {
     using KT = typename std::conditional<kSplit, float, __nv_bfloat16>::type;   // key / v element type
-    constexpr int kStageBytes = stage_bytes(kSplit);
+    constexpr uint32_t kA0 = a_off(kSplit, 0), kA1 = a_off(kSplit, 1);
+    constexpr uint32_t kB0 = b_off(kSplit, 0), kB1 = b_off(kSplit, 1);   // the same buffer for fp32 q/k
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 8);   // path length, or -1: skip the CTA
     float* seg = reinterpret_cast<float*>(base + Ly.egbt);
     float* sbt = seg + kNodeRows;
-    const uint32_t stage0 = base_s, stage1 = base_s + kStageBytes;
+    const uint32_t a0_s = base_s + kA0, a1_s = base_s + kA1, b0_s = base_s + kB0, b1_s = base_s + kB1;
 
     if (tid == 0) {
         mbar_init(bar_tma0, 1);
@@ -229,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // S, the previous factors nor q/k/v; every kernel before it has completed.
     // So the committed state may be written, and q/k read, here.
     if (tid == 0) {
-        issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage0, 0, h, b * N, bar_tma0);
-        issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage1, 1, h, b * N, bar_tma0 + 8);
+        issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, b0_s, 0, h, b * N, bar_tma0);
+        if (!kSplit) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, b1_s, 1, h, b * N, bar_tma0 + 8);
     }
     const size_t srow0 = ((size_t)bh * dv + v0) * kDk;
     const int c4 = tid & 15;         // column quad within a slab
@@ -272,13 +278,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         commit_slab(x0, ega, L, s_cd, s_key, rbase, 4 * c4);
         store_slab(x0, a.S, srow0, rbase, 4 * c4);
     }
-    convert_slab(x0, base, rbase, c4);
+    convert_slab(x0, base + kA0, rbase, c4);
     load_slab(x2, a.S, srow0, rbase, 2 * kSlab + 4 * c4);
     if (fused && commit_ok) {
         commit_slab(x1, ega, L, s_cd, s_key, rbase, kSlab + 4 * c4);
         store_slab(x1, a.S, srow0, rbase, kSlab + 4 * c4);
     }
-    convert_slab(x1, base + kStageBytes, rbase, c4);
+    convert_slab(x1, base + kA1, rbase, c4);
     load_slab(x3, a.S, srow0, rbase, 3 * kSlab + 4 * c4);
     if (fused && commit_ok) {
         commit_slab(x2, ega, L, s_cd, s_key, rbase, 2 * kSlab + 4 * c4);
@@ -296,13 +302,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool l0 = mbar_wait(bar_tma0, 0, a.err);
         if (ok && l0) {
             tc_fence_after();
-            issue_slab_mma<kSplit>(tmem, stage0, true);
+            issue_slab_mma<kSplit>(tmem, a0_s, b0_s, true);
             mma_commit(bar_mma0);
         }
-        const bool l1 = mbar_wait(bar_tma0 + 8, 0, a.err);
+        bool l1 = true;
+        if (kSplit) {                  // slab 1 takes the B buffer once slab 0's MMAs are done
+            l1 = ok && l0 && mbar_wait(bar_mma0, 0, a.err);
+            if (l1) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, b1_s, 1, h, b * N, bar_tma0 + 8);
+        }
+        l1 = l1 && mbar_wait(bar_tma0 + 8, 0, a.err);
         if (ok && l0 && l1) {
             tc_fence_after();
-            issue_slab_mma<kSplit>(tmem, stage1, false);
+            issue_slab_mma<kSplit>(tmem, a1_s, b1_s, false);
             mma_commit(bar_mma0 + 8);
         }
         ok = ok && l0 && l1;
@@ -310,28 +321,30 @@ __global__ void __launch_bounds__(kThreads, 2)
     ok = __syncthreads_and(ok);
     if (ok) {
         ok = mbar_wait(bar_mma0, 0, a.err);
-        if (tid == 0 && ok) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage0, 2, h, b * N, bar_tma0);
-        convert_slab(x2, base, rbase, c4);
+        if (kSplit) ok = mbar_wait(bar_mma0 + 8, 0, a.err) && ok;   // B is free once slab 1 is done
+        if (tid == 0 && ok) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, b0_s, 2, h, b * N, bar_tma0);
+        convert_slab(x2, base + kA0, rbase, c4);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0 && ok) {
             ok = mbar_wait(bar_tma0, 1, a.err);
             if (ok) {
                 tc_fence_after();
-                issue_slab_mma<kSplit>(tmem, stage0, false);
+                issue_slab_mma<kSplit>(tmem, a0_s, b0_s, false);
                 mma_commit(bar_mma0);
             }
         }
         ok = mbar_wait(bar_mma0 + 8, 0, a.err) && ok;
-        if (tid == 0 && ok) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, stage1, 3, h, b * N, bar_tma0 + 8);
-        convert_slab(x3, base + kStageBytes, rbase, c4);
+        if (kSplit) ok = mbar_wait(bar_mma0, 1, a.err) && ok;       // B is free once slab 2 is done
+        if (tid == 0 && ok) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, b1_s, 3, h, b * N, bar_tma0 + 8);
+        convert_slab(x3, base + kA1, rbase, c4);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0 && ok) {
             ok = mbar_wait(bar_tma0 + 8, 1, a.err);
             if (ok) {
                 tc_fence_after();
-                issue_slab_mma<kSplit>(tmem, stage1, false);
+                issue_slab_mma<kSplit>(tmem, a1_s, b1_s, false);
                 mma_commit(bar_mma0 + 8);
             }
         }
@@ -355,9 +368,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         // Stage 0 is free once slab 2 is done: the [T; P] operand (bf16 hi, lo) into its
         // A buffers and this tile's v rows into its B buffer, by bulk copies.
         ok = mbar_wait(bar_mma0, 1, a.err);
-        const uint32_t op_s = stage0;                                  // B2: hi, then lo (16 KiB each)
-        const uint32_t r_s = stage1;                                   // A2: R hi, then lo (stage 1)
-        const uint32_t v_s = stage0 + 2 * kBufBytes;                   // v rows: [t][128] bf16
+        if (kSplit) ok = ok && mbar_wait(bar_mma0 + 8, 1, a.err);   // the v rows go into the one B buffer
+        const uint32_t op_s = a0_s;                                    // B2: hi, then lo (16 KiB each)
+        const uint32_t r_s = a1_s;                                     // A2: R hi, then lo
+        const uint32_t v_s = b0_s;                                     // v rows: [t][128]
         if (ok && run && warp == 0) {
             if (lane == 0) {
                 mbar_expect_tx(bar_op, (uint32_t)(kTcOperandBytes + N * kTileV * (int)sizeof(KT)));
@@ -378,11 +392,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         const int v = 32 * (warp & 3) + lane;            // state row of this thread (TMEM lane)
         const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const KT* vsm = reinterpret_cast<const KT*>(base + 2 * kBufBytes);   // v rows: [t][128]
+        const KT* vsm = reinterpret_cast<const KT*>(base + kB0);        // v rows: [t][128]
         if (ok) {
             // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) as bf16 hi + lo rows of
             // the second MMA's A operand (row v, 64 columns t); warps 0-3 take t < 32, warps 4-7 the rest
-            unsigned char* rhi = base + kStageBytes;
+            unsigned char* rhi = base + kA1;
             unsigned char* rlo = rhi + kBufBytes;
             const int c = warp >> 2;
             float yk[32];
