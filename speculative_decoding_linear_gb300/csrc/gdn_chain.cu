@@ -23,6 +23,7 @@
 //      q/k/v/alpha/beta staged with cp.async;
 //   4. the serial chain; outputs and the factor record.
 #include "gdn_internal.cuh"
+#include "gdn_tc_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -82,6 +83,13 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     const int v0 = blockIdx.y * kRows;
     const int rows = min(kRows, dv - v0);
     const bool fused = a.commit.path != nullptr;
+    __shared__ __align__(8) uint64_t s_bar;    // this layer's q/k rows: one bulk copy per row
+    const uint32_t bar = smem_u32(&s_bar);
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
 
     // 1. state rows -> registers (loads in flight while the commit is set up).  Lane
     // `lane` holds columns c0 .. c0+7 of each of its warp's rows, c0 = 8 lane (all
@@ -163,10 +171,13 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     const T* k = static_cast<const T*>(a.k);
     const T* vv = static_cast<const T*>(a.v);
     const int rowb = dk * (int)sizeof(T);
-    for (int t = 0; t < N; ++t) {
-        const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
-        cp_async_block(s_qk + (size_t)(2 * t) * dk, k + rt, rowb, tid, kWarps * 32);
-        cp_async_block(s_qk + (size_t)(2 * t + 1) * dk, q + rt, rowb, tid, kWarps * 32);
+    if (tid == 0) {
+        tc::mbar_expect_tx(bar, (uint32_t)(2 * N * rowb));
+        for (int t = 0; t < N; ++t) {
+            const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
+            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t) * dk), k + rt, rowb, bar);
+            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t + 1) * dk), q + rt, rowb, bar);
+        }
     }
     // v, alpha, beta into registers first (one item per thread when N * kRows <= 128),
     // the committed rows' stores behind them, then the values into shared memory
@@ -210,8 +221,8 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         }
     }
 
-    cp_async_wait_all();
-    __syncthreads();
+    const bool landed = tc::mbar_wait(bar, 0, a.err);
+    if (!__syncthreads_and(landed)) return;    // a bounded wait ran out (recorded in the error word)
 
     // 4. serial chain
     for (int t = 0; t < N; ++t) {

@@ -360,7 +360,11 @@ inline cudaError_t ensure_smem(K kernel, size_t bytes, bool* done_per_device) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (bytes > 48 * 1024 && !done_per_device[dev]) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        cudaFuncAttributes fa;                  // the opt-in limit covers static shared memory too
+        e = cudaFuncGetAttributes(&fa, kernel);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 227 * 1024 - (int)fa.sharedSizeBytes);
         if (e != cudaSuccess) return e;
         done_per_device[dev] = true;
     }
