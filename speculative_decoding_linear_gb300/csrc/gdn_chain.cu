@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     const bool landed = tc::mbar_wait(bar, 0, a.err);
     if (!__syncthreads_and(landed)) return;    // a bounded wait ran out (recorded in the error word)
 
-    // 4. serial chain
+    // 4. serial chain (unrolled by 4 so that the next tokens' shared-memory loads
+    // are issued ahead of the current token's reductions)
+#pragma unroll 4
     for (int t = 0; t < N; ++t) {
         float kt[kEPL], qt[kEPL];
         float kq = 0.f;
