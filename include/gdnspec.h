@@ -351,6 +351,21 @@ int gdn_replay_commit(const void* k, const void* v, int dtype, const float* alph
                       float* S_new, int B, int N, int H, int dk, int dv, cudaStream_t stream);
 
 /*
+ * Tree verification of decay-gated linear attention (Mamba-2 / RetNet-style:
+ * S_t = alpha_t S_parent(t) + beta_t v_t k_t^T, o_t = S_t q_t, no delta-rule
+ * erasure) through the same kernels and factor record: the review of SpecLA
+ * ("Axiom & Free-Parameter Ledger", editorial summary) names other
+ * linear-attention families for the same verify/commit runtime.  Here A = 0,
+ * T = I and the factor record holds delta_t = beta_t v_t with k_t, g_t and the
+ * parents, so gdn_commit commits it unchanged.  Arguments as gdn_tree_verify.
+ * (DeltaNet is gdn_tree_verify with alpha = 1.)
+ */
+int gdn_linear_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                           const float* beta, const int32_t* parent_idx, const float* S0, float* out,
+                           void* factors, void* workspace, int B, int N, int H, int dk, int dv,
+                           cudaStream_t stream);
+
+/*
  * Launch overlap between consecutive calls (process-wide switch, default off;
  * returns the previous setting).  When on, the first kernel of every call is
  * launched as a programmatic dependent of the kernel before it on the stream:

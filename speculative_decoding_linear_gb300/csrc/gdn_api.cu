@@ -78,7 +78,7 @@ int verify_common(const void* q, const void* k, const void* v, int dtype, const 
                   const float* beta, const int32_t* parent, bool chain, float* S, float* out,
                   void* factors, void* workspace, int B, int N, int H, int dk, int dv,
                   const void* prev_factors, int N_prev, const int32_t* prev_path, int Lmax,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, bool linear = false) {
     if (!shape_ok(B, N, H, dk, dv) || !dtype_ok(dtype)) return GDN_ERR_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(alpha) || !aligned16(beta) ||
         !aligned16(S) || !aligned16(out) || !aligned16(factors))
@@ -120,6 +120,7 @@ int verify_common(const void* q, const void* k, const void* v, int dtype, const 
                      : CommitSrc{nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0};
     a.err = g_err_ptr[dev];
     a.overlap = g_overlap.load() != 0;
+    a.linear = linear;
     return from_cuda(chain ? launch_chain_verify(a, dtype, stream) : launch_tree_verify(a, dtype, stream));
 }
 
@@ -218,6 +219,14 @@ int gdn_commit_chain_verify(float* S, const void* prev_factors, int N_prev,
     if (prev_factors == nullptr || prev_path == nullptr) return GDN_ERR_ARG;
     return verify_common(q, k, v, dtype, alpha, beta, nullptr, true, S, out, factors, nullptr, B, N,
                          H, dk, dv, prev_factors, N_prev, prev_path, Lmax, stream);
+}
+
+int gdn_linear_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                           const float* beta, const int32_t* parent_idx, const float* S0, float* out,
+                           void* factors, void* workspace, int B, int N, int H, int dk, int dv,
+                           cudaStream_t stream) {
+    return verify_common(q, k, v, dtype, alpha, beta, parent_idx, false, const_cast<float*>(S0), out,
+                         factors, workspace, B, N, H, dk, dv, nullptr, 0, nullptr, 0, stream, true);
 }
 
 int gdn_set_launch_overlap(int enable) {

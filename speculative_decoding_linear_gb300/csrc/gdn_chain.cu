@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         for (int rr = 0; rr < RPW; ++rr) {
             const int r = warp * RPW + rr;
             const float vt = r < rows ? ld_elem<T>(s_v, (size_t)t * kRows + r) : 0.f;
-            const float dlt = be * (vt - al * sk[rr]);
+            const float dlt = be * (a.linear ? vt : vt - al * sk[rr]);
             const float o = fmaf(al, sq[rr], dlt * kq);
 #pragma unroll
             for (int e = 0; e < kEPL; ++e) S[rr][e] = fmaf(al, S[rr][e], dlt * kt[e]);

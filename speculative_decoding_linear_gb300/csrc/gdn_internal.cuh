@@ -121,6 +121,9 @@ struct VerifyArgs {
     // fp32 q/k on the tensor-core path: bf16 q_hi, k_hi, q_lo, k_lo with x = hi + lo to
     // ~2^-16 (same layout as q/k); all nullptr otherwise
     const void* split[4] = {nullptr, nullptr, nullptr, nullptr};
+    // decay-gated linear attention instead of the gated delta rule: S_t = alpha_t S_p +
+    // beta_t v_t k_t^T (no erasure), i.e. A = 0, T = I and delta_t = beta_t v_t
+    bool linear = false;
 };
 
 struct CommitArgs {

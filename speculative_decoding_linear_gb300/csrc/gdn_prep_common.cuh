@@ -75,11 +75,12 @@ __device__ __forceinline__ void pair_list(int tid, int N, const int* depth, cons
 }
 
 // A and Attn entries of pair (t, j) from the raw dot products k_t.k_j and q_t.k_j.
+// A is zero without the delta rule's erasure (decay-gated linear attention).
 __device__ __forceinline__ void gram_entry(int t, int j, float kk, float qk, int ld, const float* g,
-                                           const float* beta, float* sA, float* sAt) {
+                                           const float* beta, float* sA, float* sAt, bool delta_rule = true) {
     const float gam = expf(g[t] - g[j]);
     sAt[t * ld + j] = gam * qk;
-    if (j != t) sA[t * ld + j] = beta[t] * gam * kk;
+    if (j != t) sA[t * ld + j] = delta_rule ? beta[t] * gam * kk : 0.f;
 }
 
 // Rows of T = (I + A)^-1, then P = Attn T over A.  The principal block of
@@ -132,14 +133,15 @@ __device__ __forceinline__ void solve_rows(int tid, int N, int ld, const int* de
 // Row t's A and Attn entries from its Gram rows: qk[j] = q_t.k_j, kk[j] = k_t.k_j
 // (row pointers into a Gram table), for j on path(t).  One thread per node.
 __device__ __forceinline__ void gram_row(int t, int m, const uint8_t* plist, const float* qk, const float* kk,
-                                         int ld, const float* g, const float* beta, float* sA, float* sAt) {
+                                         int ld, const float* g, const float* beta, float* sA, float* sAt,
+                                         bool delta_rule = true) {
     const uint8_t* p = plist + t * 64;
     const float gt = g[t], bt = beta[t];
     for (int i = 0; i <= m; ++i) {
         const int j = p[i];
         const float gam = expf(gt - g[j]);
         sAt[t * ld + j] = gam * qk[j];
-        if (j != t) sA[t * ld + j] = bt * gam * kk[j];
+        if (j != t) sA[t * ld + j] = delta_rule ? bt * gam * kk[j] : 0.f;
     }
 }
 

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(VerifyArgs a) {
             pkk += __shfl_xor_sync(0xffffffffu, pkk, o);
             pqk += __shfl_xor_sync(0xffffffffu, pqk, o);
         }
-        if (valid && gl == 0) prep::gram_entry(t, j, pkk, pqk, ld, sg, sbeta, sA, sAt);
+        if (valid && gl == 0) prep::gram_entry(t, j, pkk, pqk, ld, sg, sbeta, sA, sAt, !a.linear);
     }
     __syncthreads();
 
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kCThreads) tree_contract_kernel(VerifyArgs a) 
             } else if (r < nr) {
                 const int t = r - N;
                 const float vt = ld_elem<T>(vv, (((size_t)b * N + t) * a.H + h) * dv + v0 + lane);
-                sR[t * (kVT + 1) + lane] = sbt[t] * (vt - seg[t] * acc[i]);
+                sR[t * (kVT + 1) + lane] = sbt[t] * (a.linear ? vt : vt - seg[t] * acc[i]);
             }
         }
     }

@@ -408,8 +408,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int e = 0; e < 4; ++e) {
                     const int i0 = 8 * q8 + 2 * e, i1 = i0 + 1;
                     const int t0 = 32 * c + i0, t1 = t0 + 1;
-                    const float r0 = t0 < N ? sbt[t0] * (to_f32(vsm[t0 * kTileV + v]) - seg[t0] * yk[i0]) : 0.f;
-                    const float r1 = t1 < N ? sbt[t1] * (to_f32(vsm[t1 * kTileV + v]) - seg[t1] * yk[i1]) : 0.f;
+                    const float ek0 = a.linear ? 0.f : seg[t0] * yk[i0], ek1 = a.linear ? 0.f : seg[t1] * yk[i1];
+                    const float r0 = t0 < N ? sbt[t0] * (to_f32(vsm[t0 * kTileV + v]) - ek0) : 0.f;
+                    const float r1 = t1 < N ? sbt[t1] * (to_f32(vsm[t1 * kTileV + v]) - ek1) : 0.f;
                     const __nv_bfloat162 hh = __floats2bfloat162_rn(r0, r1);
                     const float2 hf = __bfloat1622float2(hh);
                     const __nv_bfloat162 ll = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
@@ -711,7 +712,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         __syncthreads();                          // [Q; K] consumed: A, Attn, T reuse its space
         if (tid < N)
             prep::gram_row(tid, sdepth[tid], plist, sG + tid * 65, sG + (kNodeRows + tid) * 65, ld, sg, sbeta,
-                           sA, sAt);
+                           sA, sAt, !a.linear);
         __syncthreads();
         prep::solve_rows_fast(tid, N, ld, sdepth, plist, sA, sAt, sT);
         prep::write_operand(tid, kPrepThreads, N, ld, anc, sA, sT, reinterpret_cast<unsigned char*>(rec + wl.op));

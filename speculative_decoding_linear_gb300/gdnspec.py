@@ -52,6 +52,7 @@ SIGNATURES = {
     "gdn_hybrid_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_linear_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_set_launch_overlap": (_I, [_I]),
     "gdn_last_error": (_I, [_P]),
     "gdn_strerror": (ctypes.c_char_p, [_I]),
@@ -314,6 +315,14 @@ def gdn_replay_commit(k, v, alpha, beta, parent_idx, S0, accepted_path, S_new, s
     _check(lib().gdn_replay_commit(_ptr(k), _ptr(v), dtype_code(k.dtype), _ptr(alpha), _ptr(beta), _ptr(parent_idx),
                                    _ptr(S0), _ptr(accepted_path), accepted_path.shape[1], _ptr(S_new), B, N, H, dk,
                                    dv, _stream(stream)), "gdn_replay_commit")
+
+
+def gdn_linear_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, workspace, stream=None):
+    """Decay-gated linear attention (no delta-rule erasure) over a draft tree; see include/gdnspec.h."""
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_linear_tree_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha), _ptr(beta),
+                                        _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(factors), _ptr(workspace),
+                                        B, N, H, dk, dv, _stream(stream)), "gdn_linear_tree_verify")
 
 
 def gdn_set_launch_overlap(enable: bool) -> bool:

@@ -465,3 +465,41 @@ def test_prune_rejects_invalid_tree():
           [torch.empty(1, dtype=torch.int32, device="cuda")]
     gdnspec.gdn_prune_tree(parent, lp, 1.0, 4, *out)
     assert gdnspec.gdn_last_error() == gdnspec.ERR_TREE
+
+
+# ---------------------------------------------------------------------------
+# decay-gated linear attention and DeltaNet through the same kernels and commit
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", ["tiny", "tree32_h2", "b3_n64_tc", "chain8"])
+def test_linear_attention_verify_and_commit(case):
+    from oracle import linear as LA
+    if case == "tiny":
+        w = wl.make_workload(0)
+    elif case == "tree32_h2":
+        w = wl.custom_workload(1, 32, 2, 256, 256, wl.random_tree(np.random.default_rng(31), 32, 6), seed=31)
+    elif case == "b3_n64_tc":
+        w = wl.custom_workload(3, 64, 2, 256, 256, wl.random_tree(np.random.default_rng(32), 64, 8), seed=32)
+    else:
+        w = wl.custom_workload(2, 8, 2, 64, 64, wl.chain_tree(8), seed=33)
+    d = dev_inputs(w)
+    out, fac, ws = alloc_outputs(w)
+    gdnspec.gdn_linear_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out, fac, ws)
+    assert gdnspec.gdn_last_error() == 0
+    x = oracle_inputs(w)
+    o_ref, d_ref, g_ref = LA.tree_verify(x["q"], x["k"], x["v"], x["alpha"], x["beta"], w.parent, x["S0"])
+    delta, key, g, par = gdnspec.factor_views(fac, w.B, w.N, w.H, w.dk, w.dv, w.dtype)
+    assert_close(out.cpu().numpy(), o_ref, "linear-attention output")
+    assert_close(delta.cpu().numpy(), d_ref, "factor delta = beta v")
+    np.testing.assert_allclose(g.cpu().numpy(), g_ref, rtol=1e-5, atol=1e-5)
+    S_new = torch.empty_like(d["S0"])
+    gdnspec.gdn_commit(d["S0"], fac, d["path"], S_new, w.N, w.dtype)
+    assert gdnspec.gdn_last_error() == 0
+    S_ref = LA.commit(x["k"], x["v"], x["alpha"], x["beta"], w.parent, x["S0"], w.path)
+    assert_close(S_new.cpu().numpy(), S_ref, "commit of linear-attention factors")
+
+
+def test_deltanet_is_gdn_with_unit_gates(oracle_mod):
+    w = wl.make_workload(2)
+    w.alpha[:] = 1.0
+    d, out, fac = run_tree_verify(w)
+    check_verify(w, out, fac, oracle_mod)
