@@ -38,15 +38,14 @@ struct ChainGeom {
 
 // dynamic smem layout (byte offsets), all 16-byte aligned
 struct ChainSmem {
-    int qk, key, v, alpha, beta, o, d, cd, coef, nodes, misc, total;
+    int qk, key, v, gate, o, d, cd, coef, nodes, misc, total;
     __host__ __device__ ChainSmem(int N, int dk, int Lcap, int rows, int esz) {
         int off = 0;
         auto take = [&](int bytes) { int o = off; off += (bytes + 15) / 16 * 16; return o; };
         qk = take(N * 2 * dk * esz);     // [t][k | q][dk], input element type
         key = take(Lcap * dk * esz);     // commit path keys
         v = take(N * rows * esz);        // [t][row]
-        alpha = take(N * 4);
-        beta = take(N * 4);
+        gate = take(N * 16);             // [t][alpha, beta, k_t . q_t, -]
         o = take(N * rows * 4);
         d = take(N * rows * 4);
         cd = take(Lcap * rows * 4);      // e^{g_a - g_j} delta_j[row]
@@ -57,6 +56,29 @@ struct ChainSmem {
     }
 };
 
+// Reduce-scatter over the warp: M values per lane (M a power of two, <= 32) are
+// summed over all 32 lanes; lane l returns the total of value l / (32 / M).  Each
+// halving step sends half of the remaining values to the partner lane, so the M
+// sums take M - 1 + log2(32 / M) shuffles instead of 5 M.
+template <int M>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[M], int lane) {
+    int s = 16;
+#pragma unroll
+    for (int m = M; m > 1; m >>= 1, s >>= 1) {
+        const bool up = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < m / 2; ++i) {
+            const float keep = up ? v[m / 2 + i] : v[i];
+            const float send = up ? v[i] : v[m / 2 + i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (; s > 0; s >>= 1) x += __shfl_xor_sync(0xffffffffu, x, s);
+    return x;
+}
+
 template <typename T, int RPW>
 __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     constexpr int kRows = ChainGeom<RPW>::kRows;
@@ -66,8 +88,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     T* s_qk = reinterpret_cast<T*>(smem + L.qk);
     T* s_key = reinterpret_cast<T*>(smem + L.key);
     T* s_v = reinterpret_cast<T*>(smem + L.v);
-    float* s_alpha = reinterpret_cast<float*>(smem + L.alpha);
-    float* s_beta = reinterpret_cast<float*>(smem + L.beta);
+    float* s_gate = reinterpret_cast<float*>(smem + L.gate);
     float* s_o = reinterpret_cast<float*>(smem + L.o);
     float* s_d = reinterpret_cast<float*>(smem + L.d);
     float* s_cd = reinterpret_cast<float*>(smem + L.cd);
@@ -161,26 +182,23 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
             prefetch_l2(static_cast<const T*>(a.v) + rt * dv, rowv);
         }
     }
+    if (tid < N) {
+        const size_t gi = ((size_t)b * N + tid) * a.H + h;
+        prefetch_line_l2(a.alpha + gi);
+        prefetch_line_l2(a.beta + gi);
+    }
 
     // Everything above only read memory.  Writes and this layer's inputs come
     // after the programmatic wait.
     griddep_wait();
     griddep_launch();
-    // 3. this layer's draft inputs
+    // 3. this layer's draft inputs: v, alpha, beta loads issued first (one item per
+    // thread when N * kRows <= 128), then the q/k row copies (one token per lane of
+    // warp 0), then the committed rows' stores, then the values into shared memory
     const T* q = static_cast<const T*>(a.q);
     const T* k = static_cast<const T*>(a.k);
     const T* vv = static_cast<const T*>(a.v);
     const int rowb = dk * (int)sizeof(T);
-    if (tid == 0) {
-        tc::mbar_expect_tx(bar, (uint32_t)(2 * N * rowb));
-        for (int t = 0; t < N; ++t) {
-            const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
-            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t) * dk), k + rt, rowb, bar);
-            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t + 1) * dk), q + rt, rowb, bar);
-        }
-    }
-    // v, alpha, beta into registers first (one item per thread when N * kRows <= 128),
-    // the committed rows' stores behind them, then the values into shared memory
     const bool one_pass = N * kRows <= kWarps * 32;
     float v_reg = 0.f, al_reg = 0.f, be_reg = 0.f;
     if (one_pass) {
@@ -190,6 +208,15 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
             const size_t gi = ((size_t)b * N + tid) * a.H + h;
             al_reg = a.alpha[gi];
             be_reg = a.beta[gi];
+        }
+    }
+    if (warp == 0) {
+        if (lane == 0) tc::mbar_expect_tx(bar, (uint32_t)(2 * N * rowb));
+        __syncwarp();
+        for (int t = lane; t < N; t += 32) {
+            const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
+            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t) * dk), k + rt, rowb, bar);
+            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t + 1) * dk), q + rt, rowb, bar);
         }
     }
     if (fused) {    // committed rows written back once
@@ -206,8 +233,8 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     if (one_pass) {
         if (tid < N * kRows) s_v[tid] = v_reg;
         if (tid < N) {
-            s_alpha[tid] = al_reg;
-            s_beta[tid] = be_reg;
+            s_gate[4 * tid] = al_reg;
+            s_gate[4 * tid + 1] = be_reg;
         }
     } else {
         for (int i = tid; i < N * kRows; i += kWarps * 32) {
@@ -216,20 +243,43 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         }
         for (int t = tid; t < N; t += kWarps * 32) {
             const size_t gi = ((size_t)b * N + t) * a.H + h;
-            s_alpha[t] = a.alpha[gi];
-            s_beta[t] = a.beta[gi];
+            s_gate[4 * t] = a.alpha[gi];
+            s_gate[4 * t + 1] = a.beta[gi];
         }
     }
 
     const bool landed = tc::mbar_wait(bar, 0, a.err);
+    // k_t . q_t of every token (the warps take turns), off the serial path
+    if (__all_sync(0xffffffffu, landed)) {
+        for (int t = warp; t < N; t += kWarps) {
+            float kt[kEPL], qt[kEPL];
+            float kq = 0.f;
+            if (lane_on) {
+                ld8<T>(s_qk + (size_t)(2 * t) * dk + c0, kt);
+                ld8<T>(s_qk + (size_t)(2 * t + 1) * dk + c0, qt);
+#pragma unroll
+                for (int e = 0; e < kEPL; ++e) kq = fmaf(kt[e], qt[e], kq);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+            if (lane == 0) s_gate[4 * t + 2] = kq;
+        }
+    }
     if (!__syncthreads_and(landed)) return;    // a bounded wait ran out (recorded in the error word)
 
-    // 4. serial chain (unrolled by 4 so that the next tokens' shared-memory loads
-    // are issued ahead of the current token's reductions)
+    // 4. serial chain.  Per token the warp sums 2 RPW dot products (S_row . k_t and
+    // S_row . q_t of its RPW rows) with one reduce-scatter butterfly; afterwards lane
+    // l holds value l / kGroup.  The lanes holding S_row . k_t form delta_t of their
+    // row and broadcast it; the lanes holding S_row . q_t form o_t.  Unrolled by 4
+    // so that the next tokens' shared-memory loads are issued ahead.
+    constexpr int kGroup = 32 / (2 * RPW);
+    const int held = lane / kGroup;                 // value index held after the reduction
+    const int rr_held = held % RPW;
+    const int r_held = warp * RPW + rr_held;        // its state row
+    const bool holds_q = held >= RPW && lane % kGroup == 0 && r_held < rows;
 #pragma unroll 4
     for (int t = 0; t < N; ++t) {
         float kt[kEPL], qt[kEPL];
-        float kq = 0.f;
         if (lane_on) {
             ld8<T>(s_qk + (size_t)(2 * t) * dk + c0, kt);
             ld8<T>(s_qk + (size_t)(2 * t + 1) * dk + c0, qt);
@@ -237,9 +287,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
 #pragma unroll
             for (int e = 0; e < kEPL; ++e) kt[e] = qt[e] = 0.f;
         }
-#pragma unroll
-        for (int e = 0; e < kEPL; ++e) kq = fmaf(kt[e], qt[e], kq);
-        float sk[RPW], sq[RPW];
+        float val[2 * RPW];
 #pragma unroll
         for (int rr = 0; rr < RPW; ++rr) {
             float x = 0.f, y = 0.f;
@@ -248,32 +296,29 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
                 x = fmaf(S[rr][e], kt[e], x);
                 y = fmaf(S[rr][e], qt[e], y);
             }
-            sk[rr] = x;
-            sq[rr] = y;
+            val[rr] = x;
+            val[RPW + rr] = y;
+        }
+        const float tot = warp_reduce_scatter<2 * RPW>(val, lane);
+        const float4 gt = *reinterpret_cast<const float4*>(s_gate + 4 * t);   // alpha, beta, k.q
+        const float al = gt.x, be = gt.y;
+        const float vt = r_held < rows ? ld_elem<T>(s_v, (size_t)t * kRows + r_held) : 0.f;
+        const float dl = be * (a.linear ? vt : vt - al * tot);             // meaningful where held < RPW
+        float dlt[RPW];
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) dlt[rr] = __shfl_sync(0xffffffffu, dl, rr * kGroup);
+        if (holds_q) {
+            float d = dlt[0];
+#pragma unroll
+            for (int rr = 1; rr < RPW; ++rr)
+                if (rr_held == rr) d = dlt[rr];
+            s_o[t * kRows + r_held] = fmaf(al, tot, d * gt.z);
+            s_d[t * kRows + r_held] = d;
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
-            for (int rr = 0; rr < RPW; ++rr) {
-                sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
-                sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
-            }
-        }
-        const float al = s_alpha[t], be = s_beta[t];
-#pragma unroll
-        for (int rr = 0; rr < RPW; ++rr) {
-            const int r = warp * RPW + rr;
-            const float vt = r < rows ? ld_elem<T>(s_v, (size_t)t * kRows + r) : 0.f;
-            const float dlt = be * (a.linear ? vt : vt - al * sk[rr]);
-            const float o = fmaf(al, sq[rr], dlt * kq);
-#pragma unroll
-            for (int e = 0; e < kEPL; ++e) S[rr][e] = fmaf(al, S[rr][e], dlt * kt[e]);
-            if (lane == 0) {
-                s_o[t * kRows + r] = o;
-                s_d[t * kRows + r] = dlt;
-            }
-        }
+            for (int e = 0; e < kEPL; ++e) S[rr][e] = fmaf(al, S[rr][e], dlt[rr] * kt[e]);
     }
     __syncthreads();
 
@@ -297,7 +342,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         float carry = 0.f;
         for (int t0 = 0; t0 < N; t0 += 32) {
             const int t = t0 + lane;
-            float x = t < N ? logf(s_alpha[t]) : 0.f;
+            float x = t < N ? logf(s_gate[4 * t]) : 0.f;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, o);

@@ -334,6 +334,10 @@ __device__ __forceinline__ void cp_async_block(void* smem, const void* gmem, int
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
+// The same for the one L2 line holding `p` (no alignment or size rule).
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
