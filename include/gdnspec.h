@@ -369,9 +369,10 @@ int gdn_linear_tree_verify(const void* q, const void* k, const void* v, int dtyp
  * Launch overlap between consecutive calls (process-wide switch, default off;
  * returns the previous setting).  When on, the first kernel of every call is
  * launched as a programmatic dependent of the kernel before it on the stream:
- * it starts streaming its state tiles and pending-commit factors while that
- * kernel finishes, and waits for it before reading q/k/v/alpha/beta/parent_idx
- * and before writing anything.  This hides launch and prologue latency in a
+ * it starts streaming its state tiles and pending-commit factors (and may
+ * write the committed state back) while that kernel finishes, and waits for it
+ * before reading q/k/v/alpha/beta/parent_idx and before writing anything
+ * else.  This hides launch and prologue latency in a
  * layer-major sweep ("Pith review of SpecLA", "What carries the argument":
  * layer-major verification keeps per-layer state streaming back to back).
  * Contract while on: the state S, S0 and factor buffers of a call must not be

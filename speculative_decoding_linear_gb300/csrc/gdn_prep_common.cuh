@@ -149,14 +149,25 @@ __device__ __forceinline__ void gram_row(int t, int m, const uint8_t* plist, con
 // = root.  Row t of T: x_0 = 1, x_i = -sum_{j < i} x_j A[q_j, q_i]; row t of
 // P: P[t, q_i] = sum_{j <= i} Attn[t, q_j] T[q_j, q_i].  Fully unrolled for
 // depth < kRegDepth (independent shared-memory loads), the generic loops of
-// solve_rows otherwise.  Call with every thread; contains barriers.
+// solve_rows otherwise (always, with `unrolled` false: less code for kernels
+// that run it once per CTA).  Call with every thread of the block, or with
+// `group` > 0 with the first `group` threads, which then synchronise on named
+// barrier 1 only; contains barriers.
 constexpr int kRegDepth = 12;
 
+__device__ __forceinline__ void group_sync(int group) {
+    if (group == 0)
+        __syncthreads();
+    else
+        asm volatile("bar.sync 1, %0;\n" ::"r"(group) : "memory");
+}
+
 __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const int* depth, const uint8_t* plist,
-                                                float* sA, const float* sAt, float* sT) {
+                                                float* sA, const float* sAt, float* sT, int group = 0,
+                                                bool unrolled = true) {
     const int t = tid;
     const int m = tid < N ? depth[t] : 0;
-    const bool fast = tid < N && m < kRegDepth;
+    const bool fast = unrolled && tid < N && m < kRegDepth;
     int q[kRegDepth];
     float x[kRegDepth];
     if (fast) {
@@ -188,7 +199,7 @@ __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const in
             row[pk] = -x0;
         }
     }
-    __syncthreads();
+    group_sync(group);
     if (fast) {
         float at[kRegDepth];
 #pragma unroll
@@ -212,7 +223,7 @@ __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const in
             sA[t * ld + pk] = x0;
         }
     }
-    __syncthreads();
+    group_sync(group);
 }
 
 // [T; P] as the tensor-core contraction's second MMA operand: 128 rows (T rows

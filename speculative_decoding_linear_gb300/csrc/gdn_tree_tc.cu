@@ -728,6 +728,515 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
+// the whole call in one kernel: one CTA per (sequence, head), d_v = 256
+// ---------------------------------------------------------------------------
+// A CTA owns its (sequence, head)'s whole state (two 128-row MMA tiles, u = 0,
+// 1) and runs the prologue itself, so a call is a single launch:
+//   before the wait: the state is streamed, the pending commit applied in
+//     registers and written back; slabs 0 and 1 become bf16 hi/lo operand
+//     stages, slabs 2 and 3 stay in registers;
+//   after the wait: q/k slabs by TMA; per slab the Y MMAs of both tiles and
+//     the Gram MMA ([Q; K] K^T: M = 128 rows, N = 64 keys) on the same operand
+//     buffer; the node metadata meanwhile;
+//   then warps 0-7 turn the Gram rows into the A and Attn tables, solve T,
+//     form P and the [T; P] operand, while warps 8-15 form R of both tiles
+//     from Y_K, v and the gates; one MMA group per tile gives [Delta | P R];
+//     every warp stores Delta or O rows.
+// TMEM, 512 columns: Y of tile u in 128u .. 128u+127 ([Y_Q | Y_K]); the Gram
+// in 256 .. 319 until it is read; [Delta | P R] of tile u in 256+128u .. +127.
+constexpr int kFThreads = 512;
+constexpr int kFRows = 256;                          // state rows per CTA (= d_v)
+constexpr uint32_t kFTmemCols = 512;
+constexpr int kFAStage = 4 * kBufBytes;              // one slab of both tiles: [hi 0, lo 0, hi 1, lo 1]
+constexpr uint32_t kFGramIdesc = idesc_bf16(128, 64);
+constexpr int kFSmemLimit = 227 * 1024;
+constexpr int kFIssuerWarp = 4;                      // lane 0 issues the TMA copies and the MMAs; the
+                                                     // other lanes wait at __syncwarp, not on mbarriers
+
+struct FusedLayout {
+    // offsets from the 1024-aligned base.  The operand region holds two A
+    // stages and nB q/k buffers during Y, then R (both tiles), the A / Attn / T
+    // tables and the [T; P] operand.
+    int nB, bsz, ops, R, A, At, T, op;
+    int cd, key, nodes, coef, par, la, g, beta, eg, depth, anc, plist, bars, misc, total;
+    __host__ __device__ FusedLayout(int N, int Lcap, bool split) {
+        bsz = (split ? 2 : 1) * kBufBytes;
+        build(N, Lcap, split, 2);
+        if (total > kFSmemLimit) build(N, Lcap, split, 1);
+    }
+    __host__ __device__ void build(int N, int Lcap, bool split, int nb) {
+        nB = nb;
+        ops = 2 * kFAStage + nb * bsz;
+        int o = 0;
+        auto take = [&](int bytes) { int r = o; o += (bytes + 15) / 16 * 16; return r; };
+        R = take(2 * 2 * kBufBytes);
+        A = take(N * (N + 1) * 4);
+        At = take(N * (N + 1) * 4);
+        T = take(N * (N + 1) * 4);
+        o = (o + 1023) / 1024 * 1024;
+        op = take((int)kTcOperandBytes);
+        if (o > ops) {   // cannot happen for N <= 64; flagged as too large
+            total = 1 << 30;
+            return;
+        }
+        o = ops;
+        cd = take(Lcap * kFRows * 4);
+        key = take(Lcap * kDk * (split ? 4 : 2));
+        nodes = take(kMaxPath * 4);
+        coef = take(kMaxPath * 4);
+        par = take(kMaxNodes * 4);
+        la = take(kMaxNodes * 4);
+        g = take(kMaxNodes * 4);
+        beta = take(kMaxNodes * 4);
+        eg = take(kMaxNodes * 4);
+        depth = take(kMaxNodes * 4);
+        anc = take(kMaxNodes * 8);
+        plist = take(kMaxNodes * 64);
+        bars = take(16 * 8);
+        misc = take(16);
+        total = o + 1024;   // slack for aligning the base to 1024 bytes
+    }
+};
+
+// Rows rbase + 32 j (j = 0..7) of a 256-row state slab: j < 4 lie in tile 0,
+// j >= 4 in tile 1.
+__device__ __forceinline__ void f_load_slab(float4 (&x)[8], const float* S, size_t srow0, int rbase, int col) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        x[j] = *reinterpret_cast<const float4*>(S + srow0 + (size_t)(rbase + 32 * j) * kDk + col);
+}
+__device__ __forceinline__ void f_store_slab(const float4 (&x)[8], float* S, size_t srow0, int rbase, int col) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(S + srow0 + (size_t)(rbase + 32 * j) * kDk + col) = x[j];
+}
+// Same arithmetic order per element as commit_slab (and gdn_commit).
+template <typename KT>
+__device__ __forceinline__ void f_commit_slab(float4 (&x)[8], float ega, int L, const float* s_cd,
+                                              const KT* s_key, int rbase, int col) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        x[j].x *= ega;
+        x[j].y *= ega;
+        x[j].z *= ega;
+        x[j].w *= ega;
+    }
+    for (int i = 0; i < L; ++i) {
+        const float4 kq = ld4<KT>(s_key, (size_t)i * kDk + col);
+        const float* cdi = s_cd + i * kFRows + rbase;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float w = cdi[32 * j];
+            x[j].x = fmaf(w, kq.x, x[j].x);
+            x[j].y = fmaf(w, kq.y, x[j].y);
+            x[j].z = fmaf(w, kq.z, x[j].z);
+            x[j].w = fmaf(w, kq.w, x[j].w);
+        }
+    }
+}
+// hi/lo split into one A stage ([tile 0 hi, tile 0 lo, tile 1 hi, tile 1 lo]).
+__device__ __forceinline__ void f_convert_slab(const float4 (&x)[8], unsigned char* stage, int rbase, int c4) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        unsigned char* ahi = stage + (j >> 2) * 2 * kBufBytes;
+        unsigned char* alo = ahi + kBufBytes;
+        const int r = rbase + 32 * (j & 3);
+        const float4 v = x[j];
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        uint2 hi, lo;
+        hi.x = *reinterpret_cast<const uint32_t*>(&h01);
+        hi.y = *reinterpret_cast<const uint32_t*>(&h23);
+        lo.x = pack_bf16(v.x - f01.x, v.y - f01.y);
+        lo.y = pack_bf16(v.z - f23.x, v.w - f23.y);
+        const uint32_t off = sw128_quad(r, c4);
+        *reinterpret_cast<uint2*>(ahi + off) = hi;
+        *reinterpret_cast<uint2*>(alo + off) = lo;
+    }
+}
+
+// Y of both tiles and the Gram for one slab (one thread issues).  Not inlined:
+// the fused kernel runs each of its code paths once per CTA, so its size in
+// the instruction cache matters more than a call.
+template <bool kSplit>
+__device__ __noinline__ void f_issue_slab(uint32_t tmem, uint32_t a_stage, uint32_t bsm, bool first) {
+    issue_slab_mma<kSplit>(tmem, a_stage, bsm, first);
+    issue_slab_mma<kSplit>(tmem + 128, a_stage + 2 * kBufBytes, bsm, first);
+#pragma unroll
+    for (int kk = 0; kk < kSlab / 16; ++kk) {
+        const uint32_t q_s = bsm + kk * 32;
+        const uint64_t a_hi = sw128_desc(q_s), k_hi = sw128_desc(q_s + kNodeRows * 128);
+        mma_bf16(tmem + 256, a_hi, k_hi, kFGramIdesc, (!first || kk > 0) ? 1u : 0u);
+        if (kSplit) {
+            const uint32_t l_s = q_s + kBufBytes;
+            mma_bf16(tmem + 256, a_hi, sw128_desc(l_s + kNodeRows * 128), kFGramIdesc, 1u);
+            mma_bf16(tmem + 256, sw128_desc(l_s), k_hi, kFGramIdesc, 1u);
+        }
+    }
+}
+
+template <bool kSplit>
+__global__ void __launch_bounds__(kFThreads, 1)
+    tree_fused_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmQl, const __grid_constant__ CUtensorMap tmKl,
+                         VerifyArgs a) {
+    using KT = typename std::conditional<kSplit, float, __nv_bfloat16>::type;   // key / v element type
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    unsigned char* base = smem_raw + (base_s - raw_s);
+    const bool fused = a.commit.path != nullptr;
+    const int N = a.N, H = a.H, ld = N + 1;
+    const FusedLayout Ly(N, fused ? a.commit.Lmax : 0, kSplit);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+
+    float* s_cd = reinterpret_cast<float*>(base + Ly.cd);
+    KT* s_key = reinterpret_cast<KT*>(base + Ly.key);
+    int* s_nodes = reinterpret_cast<int*>(base + Ly.nodes);
+    float* s_coef = reinterpret_cast<float*>(base + Ly.coef);
+    int* par = reinterpret_cast<int*>(base + Ly.par);
+    float* la = reinterpret_cast<float*>(base + Ly.la);
+    float* sg = reinterpret_cast<float*>(base + Ly.g);
+    float* sbeta = reinterpret_cast<float*>(base + Ly.beta);
+    float* seg = reinterpret_cast<float*>(base + Ly.eg);
+    int* sdepth = reinterpret_cast<int*>(base + Ly.depth);
+    uint64_t* anc = reinterpret_cast<uint64_t*>(base + Ly.anc);
+    uint8_t* plist = reinterpret_cast<uint8_t*>(base + Ly.plist);
+    float* sA = reinterpret_cast<float*>(base + Ly.A);
+    float* sAt = reinterpret_cast<float*>(base + Ly.At);
+    float* sT = reinterpret_cast<float*>(base + Ly.T);
+    const uint32_t bars = base_s + Ly.bars;
+    const uint32_t bar_e = bars + 64;                         // bars + 8 s: slab s copied; + 32 + 8 s: its MMAs done
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
+    int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 4);    // path length, or -1: skip the CTA
+    float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 8);
+    const uint32_t stage0 = base_s, stage1 = base_s + kFAStage, bbase = base_s + 2 * kFAStage;
+    const int nB = Ly.nB;
+    auto bbuf = [&](int s) { return bbase + (nB == 2 ? (uint32_t)((s & 1) * Ly.bsz) : 0u); };
+
+    if (tid == 0) {
+        for (int i = 0; i < 9; ++i) mbar_init(bars + 8 * i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        fence_proxy_async_smem();
+        *s_flag = 0;
+        *s_ega = 1.f;
+    }
+    if (warp == 1) tmem_alloc(smem_u32(s_tmem), kFTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    // ---- 1. before the wait: the state stream (it only reads the state and the
+    // previous factors, which the previous call on the stream does not touch) ----
+    const size_t srow0 = (size_t)bh * kFRows * kDk;
+    const int c4 = tid & 15;          // column quad within a slab
+    const int rbase = tid >> 4;       // rows rbase + 32 j
+    if (tid < 16) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * 16 * kDk, 16 * kDk * 4);
+    if (tid < N) {                    // this call's inputs into L2; read only after the wait
+        const size_t rt = ((size_t)b * N + tid) * H + h;
+        if (kSplit) {
+            for (int i = 0; i < 4; ++i) prefetch_l2(static_cast<const __nv_bfloat16*>(a.split[i]) + rt * kDk, kDk * 2);
+        } else {
+            prefetch_l2(static_cast<const KT*>(a.q) + rt * kDk, kDk * (int)sizeof(KT));
+        }
+        prefetch_l2(static_cast<const KT*>(a.k) + rt * kDk, kDk * (int)sizeof(KT));
+        prefetch_l2(static_cast<const KT*>(a.v) + rt * kFRows, kFRows * (int)sizeof(KT));
+        prefetch_line_l2(a.alpha + rt);
+        prefetch_line_l2(a.beta + rt);
+        prefetch_line_l2(a.parent + (size_t)b * N + tid);
+    }
+    float4 x0[8], x1[8], x2[8], x3[8];
+    f_load_slab(x0, a.S, srow0, rbase, 4 * c4);
+    if (fused) {
+        if (warp == 2) {
+            const int L = commit_path_setup(a.commit, b, h, H, s_nodes, s_coef, s_ega);
+            if (lane == 0) {
+                *s_flag = L;
+                if (L < 0) set_error(a.err, GDN_ERR_PATH);
+            }
+        }
+        __syncthreads();
+        const int L = *s_flag;
+        if (L > 0) {
+            const KT* key_bh = static_cast<const KT*>(a.commit.key) + (size_t)bh * a.commit.N * kDk;
+            for (int i = 0; i < L; ++i)
+                cp_async_block(s_key + (size_t)i * kDk, key_bh + (size_t)s_nodes[i] * kDk, kDk * (int)sizeof(KT),
+                               tid, kFThreads);
+            const float* dl = a.commit.delta + (size_t)bh * a.commit.N * kFRows;
+            for (int i = tid; i < L * kFRows; i += kFThreads) {
+                const int j = i / kFRows, r = i % kFRows;
+                s_cd[i] = s_coef[j] * dl[(size_t)s_nodes[j] * kFRows + r];
+            }
+            cp_async_wait_all();
+        }
+    }
+    __syncthreads();
+    const int L = fused ? *s_flag : 0;
+    bool ok = L >= 0;
+    if (ok) {
+        const float ega = *s_ega;
+        f_load_slab(x1, a.S, srow0, rbase, kSlab + 4 * c4);
+        if (fused) {
+            f_commit_slab(x0, ega, L, s_cd, s_key, rbase, 4 * c4);
+            f_store_slab(x0, a.S, srow0, rbase, 4 * c4);
+        }
+        f_convert_slab(x0, base, rbase, c4);
+        f_load_slab(x2, a.S, srow0, rbase, 2 * kSlab + 4 * c4);
+        if (fused) {
+            f_commit_slab(x1, ega, L, s_cd, s_key, rbase, kSlab + 4 * c4);
+            f_store_slab(x1, a.S, srow0, rbase, kSlab + 4 * c4);
+        }
+        f_convert_slab(x1, base + kFAStage, rbase, c4);
+        f_load_slab(x3, a.S, srow0, rbase, 3 * kSlab + 4 * c4);
+        if (fused) {
+            f_commit_slab(x2, ega, L, s_cd, s_key, rbase, 2 * kSlab + 4 * c4);
+            f_store_slab(x2, a.S, srow0, rbase, 2 * kSlab + 4 * c4);
+            f_commit_slab(x3, ega, L, s_cd, s_key, rbase, 3 * kSlab + 4 * c4);
+            f_store_slab(x3, a.S, srow0, rbase, 3 * kSlab + 4 * c4);
+        }
+        fence_proxy_async_smem();
+    }
+
+    // ---- 2. this call's inputs ----
+    griddep_wait();
+    griddep_launch();
+    if (ok) {
+        if (warp == kFIssuerWarp && lane == 0) {
+            issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(0), 0, h, b * N, bars);
+            if (nB == 2) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
+        }
+        bool bad = false;
+        if (tid < N) {
+            const int p = a.parent[(size_t)b * N + tid];
+            bad = p < -1 || p >= tid;
+            par[tid] = p;
+            const size_t gi = ((size_t)b * N + tid) * H + h;
+            la[tid] = logf(a.alpha[gi]);
+            sbeta[tid] = a.beta[gi];
+        }
+        bad = __syncthreads_or(bad);
+        if (bad) {
+            if (tid == 0) set_error(a.err, GDN_ERR_TREE);
+        } else if (tid < N) {
+            prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
+            seg[tid] = expf(sg[tid]);
+            a.f.g[(size_t)bh * N + tid] = sg[tid];
+            if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
+        }
+
+        // ---- 3. Y of both tiles and the Gram, slab by slab (slabs 2 and 3 are
+        // converted into the stages that slabs 0 and 1 free) ----
+        if (warp == kFIssuerWarp) {
+            if (lane == 0) {
+            bool l = mbar_wait(bars, 0, a.err);
+            if (l) {
+                tc_fence_after();
+                f_issue_slab<kSplit>(tmem, stage0, bbuf(0), true);
+                mma_commit(bars + 32);
+            }
+            if (nB == 1) {
+                l = l && mbar_wait(bars + 32, 0, a.err);
+                if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
+            }
+            l = l && mbar_wait(bars + 8, 0, a.err);
+            if (l) {
+                tc_fence_after();
+                f_issue_slab<kSplit>(tmem, stage1, bbuf(1), false);
+                mma_commit(bars + 40);
+            }
+            l = l && mbar_wait(bars + (nB == 2 ? 32 : 40), 0, a.err);   // slab 2's buffer free
+            if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(2), 2, h, b * N, bars + 16);
+            }
+            __syncwarp();
+        }
+        ok = mbar_wait(bars + 32, 0, a.err);
+        if (ok) f_convert_slab(x2, base, rbase, c4);
+        fence_proxy_async_smem();
+        ok = __syncthreads_and(ok);
+        if (ok && warp == kFIssuerWarp) {
+            if (lane == 0) {
+                bool l = mbar_wait(bars + 16, 0, a.err);
+                if (l) {
+                    tc_fence_after();
+                    f_issue_slab<kSplit>(tmem, stage0, bbuf(2), false);
+                    mma_commit(bars + 48);
+                }
+                l = l && mbar_wait(bars + (nB == 2 ? 40 : 48), 0, a.err);   // slab 3's buffer free
+                if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(3), 3, h, b * N, bars + 24);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = mbar_wait(bars + 40, 0, a.err);
+        if (ok) f_convert_slab(x3, base + kFAStage, rbase, c4);
+        fence_proxy_async_smem();
+        ok = __syncthreads_and(ok);
+        if (ok && warp == kFIssuerWarp) {
+            if (lane == 0 && mbar_wait(bars + 24, 0, a.err)) {
+                tc_fence_after();
+                f_issue_slab<kSplit>(tmem, stage1, bbuf(3), false);
+                mma_commit(bars + 56);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = mbar_wait(bars + 56, 0, a.err);              // Y and the Gram complete
+        ok = __syncthreads_and(ok) && !bad;
+        tc_fence_after();
+
+        // ---- 4. warps 0-7: tables, T, P and the [T; P] operand; warps 8-15: R ----
+        if (ok) {
+            if (warp < 4) {
+                // raw Gram rows into the tables, in place of the entries gram_row turns into
+                // A and Attn: TMEM lane r < 64 holds q_r . k_j, lane 64 + r holds k_r . k_j
+                const int t = tid & 63;
+                float* row = (tid < 64 ? sAt : sA) + t * ld;
+                const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16) + 256;
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    float gr[32];
+                    tmem_ld32(t_lane + 32 * c, gr);
+                    if (t < N) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i < N) row[32 * c + i] = gr[i];
+                    }
+                }
+            }
+            if (tid < 256) {
+                prep::group_sync(256);
+                if (tid < N)
+                    prep::gram_row(tid, sdepth[tid], plist, sAt + tid * ld, sA + tid * ld, ld, sg, sbeta, sA, sAt,
+                                   !a.linear);
+                prep::group_sync(256);
+                prep::solve_rows_fast(tid, N, ld, sdepth, plist, sA, sAt, sT, 256, false);
+                prep::write_operand(tid, 256, N, ld, anc, sA, sT, base + Ly.op);
+            } else {
+                // keys into the factor record
+                constexpr int kVec = 16 / (int)sizeof(KT);
+                const KT* kin = static_cast<const KT*>(a.k);
+                KT* kout = static_cast<KT*>(a.f.key) + (size_t)bh * N * kDk;
+                for (int item = tid - 256; item < N * (kDk / kVec); item += kFThreads - 256) {
+                    const int t = item / (kDk / kVec), c = item % (kDk / kVec);
+                    *reinterpret_cast<uint4*>(kout + (size_t)t * kDk + c * kVec) =
+                        *reinterpret_cast<const uint4*>(kin + (((size_t)b * N + t) * H + h) * kDk + c * kVec);
+                }
+                // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) of tile u as bf16
+                // hi + lo rows of the second MMA's A operand (row v, 64 columns t)
+                const int u = (warp - 8) >> 2;
+                const int v = 32 * (warp & 3) + lane;               // row within the tile = TMEM lane
+                const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * u + kNodeRows;
+                unsigned char* rhi = base + Ly.R + u * 2 * kBufBytes;
+                unsigned char* rlo = rhi + kBufBytes;
+                const KT* vin = static_cast<const KT*>(a.v) + (size_t)h * kFRows + 128 * u + v;
+                const size_t vstride = (size_t)H * kFRows;          // between consecutive nodes
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    float yk[32], vt[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * c + i;
+                        vt[i] = t < N ? to_f32(vin[((size_t)b * N + t) * vstride]) : 0.f;
+                    }
+                    tmem_ld32(t_lane + 32 * c, yk);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i0 = 8 * q8 + 2 * e, i1 = i0 + 1;
+                            const int t0 = 32 * c + i0, t1 = t0 + 1;
+                            const float ek0 = a.linear || t0 >= N ? 0.f : seg[t0] * yk[i0];
+                            const float ek1 = a.linear || t1 >= N ? 0.f : seg[t1] * yk[i1];
+                            const float r0 = t0 < N ? sbeta[t0] * (vt[i0] - ek0) : 0.f;
+                            const float r1 = t1 < N ? sbeta[t1] * (vt[i1] - ek1) : 0.f;
+                            const __nv_bfloat162 hh = __floats2bfloat162_rn(r0, r1);
+                            const float2 hf = __bfloat1622float2(hh);
+                            const __nv_bfloat162 ll = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
+                            hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                            lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
+                        }
+                        const int cc = 4 * c + q8;                   // 16-byte chunk = 8 nodes
+                        const uint32_t off = (uint32_t)(v * 128 + ((cc ^ (v & 7)) << 4));
+                        *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4*>(rlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- 5. [Delta | P R] = R [T; P]^T per tile: three bf16 terms (hi.hi, hi.lo, lo.hi) ----
+        if (ok && warp == kFIssuerWarp) {
+            if (lane == 0) {
+            tc_fence_after();
+            const uint32_t op_s = base_s + Ly.op;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t r_s = base_s + Ly.R + u * 2 * kBufBytes;
+#pragma unroll
+                for (int kk = 0; kk < kNodeRows / 16; ++kk) {
+                    const uint64_t ahi = sw128_desc(r_s + kk * 32), alo = sw128_desc(r_s + kBufBytes + kk * 32);
+                    const uint64_t bhi = sw128_desc(op_s + kk * 32), blo = sw128_desc(op_s + kBufBytes + kk * 32);
+                    const uint32_t d = tmem + 256 + 128 * u;
+                    mma_bf16(d, ahi, bhi, kIdesc, kk > 0 ? 1u : 0u);
+                    mma_bf16(d, ahi, blo, kIdesc, 1u);
+                    mma_bf16(d, alo, bhi, kIdesc, 1u);
+                }
+            }
+            mma_commit(bar_e);
+            }
+            __syncwarp();
+        }
+        if (ok) ok = mbar_wait(bar_e, 0, a.err);
+        tc_fence_after();
+        if (ok) {
+            // warps 0-3 / 8-11: Delta of tile 0 / 1; warps 4-7 / 12-15: O of tile 0 / 1
+            const int u = warp >> 3;
+            const int row = 128 * u + 32 * (warp & 3) + lane;
+            const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+            if (((warp >> 2) & 1) == 0) {
+#pragma unroll 1
+                for (int c = 0; c < kNodeRows / 32; ++c) {
+                    if (32 * c >= N) break;
+                    float d[32];
+                    tmem_ld32(t_lane + 256 + 128 * u + 32 * c, d);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * c + i;
+                        if (t < N) a.f.delta[((size_t)bh * N + t) * kFRows + row] = d[i];
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < kNodeRows / 32; ++c) {
+                    if (32 * c >= N) break;
+                    float yq[32], pr[32];
+                    tmem_ld32(t_lane + 128 * u + 32 * c, yq);
+                    tmem_ld32(t_lane + 256 + 128 * u + kNodeRows + 32 * c, pr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = 32 * c + i;
+                        if (t < N) a.out[(((size_t)b * N + t) * H + h) * kFRows + row] = fmaf(seg[t], yq[i], pr[i]);
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: TMEM is always released ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kFTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -796,10 +1305,42 @@ cudaError_t launch_tree_tc_impl(const VerifyArgs& a, cudaStream_t s) {
                          a);
 }
 
+// d_v = 256 with the layout within the shared-memory limit: the single-kernel path.
+bool fused_eligible(const VerifyArgs& a, bool split) {
+    if (a.dk != kDk || a.dv != kFRows || a.N > kMaxNodes) return false;
+    const FusedLayout L(a.N, a.commit.path ? a.commit.Lmax : 0, split);
+    return L.total <= kFSmemLimit;
+}
+
+template <bool kSplit>
+cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s) {
+    static bool attr[64];
+    CUtensorMap tq, tk, tql, tkl;
+    const void* qh = kSplit ? a.split[0] : a.q;
+    const void* kh = kSplit ? a.split[1] : a.k;
+    if (!make_qk_map(&tq, qh, a.B, a.N, a.H) || !make_qk_map(&tk, kh, a.B, a.N, a.H)) return cudaErrorInvalidValue;
+    if (kSplit) {
+        if (!make_qk_map(&tql, a.split[2], a.B, a.N, a.H) || !make_qk_map(&tkl, a.split[3], a.B, a.N, a.H))
+            return cudaErrorInvalidValue;
+    } else {
+        tql = tq;
+        tkl = tk;
+    }
+    const FusedLayout L(a.N, a.commit.path ? a.commit.Lmax : 0, kSplit);
+    cudaError_t e = ensure_smem(tree_fused_tc_kernel<kSplit>, L.total, attr);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(tree_fused_tc_kernel<kSplit>, dim3(a.B * a.H), dim3(kFThreads), L.total, s, a.overlap, tq,
+                         tk, tql, tkl, a);
+}
+
 // bf16 q/k (or fp32 q/k with their bf16 hi/lo terms in `split`) with the
-// tensor-core kernels: see launch_tree_verify.
+// tensor-core kernels: one fused kernel for d_v = 256, otherwise the prologue
+// and the contraction kernel.  See launch_tree_verify.
 cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s) {
-    return a.split[0] != nullptr ? launch_tree_tc_impl<true>(a, s) : launch_tree_tc_impl<false>(a, s);
+    const bool split = a.split[0] != nullptr;
+    if (fused_eligible(a, split))
+        return split ? launch_tree_fused_impl<true>(a, s) : launch_tree_fused_impl<false>(a, s);
+    return split ? launch_tree_tc_impl<true>(a, s) : launch_tree_tc_impl<false>(a, s);
 }
 
 }  // namespace gdn
