@@ -142,9 +142,11 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
         if (nL < 0) return;
         const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
         const T* key_bh = static_cast<const T*>(a.commit.key) + (size_t)bh * a.commit.N * dk;
+#pragma unroll 1
         for (int i = 0; i < nL; ++i)
             cp_async_block(s_key + (size_t)i * dk, key_bh + (size_t)s_nodes[i] * dk, dk * (int)sizeof(T),
                            tid, kWarps * 32);
+#pragma unroll 1
         for (int i = tid; i < nL * kRows; i += kWarps * 32) {
             const int j = i / kRows, r = i % kRows;
             s_cd[i] = r < rows ? s_coef[j] * dl[(size_t)s_nodes[j] * dv + v0 + r] : 0.f;
@@ -158,6 +160,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
             for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
                 for (int e = 0; e < kEPL; ++e) S[rr][e] *= ega;
+#pragma unroll 1
             for (int i = 0; i < nL; ++i) {
                 float kv[kEPL];
                 ld8<T>(s_key + (size_t)i * dk + c0, kv);
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     // CTAs of one (sequence, head) split the tokens between them).
     if (tid == 0) {
         const int rowq = dk * (int)sizeof(T), rowv = dv * (int)sizeof(T);
+#pragma unroll 1
         for (int t = blockIdx.y; t < N; t += gridDim.y) {
             const size_t rt = ((size_t)b * N + t) * a.H + h;
             prefetch_l2(static_cast<const T*>(a.q) + rt * dk, rowq);
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     if (warp == 0) {
         if (lane == 0) tc::mbar_expect_tx(bar, (uint32_t)(2 * N * rowb));
         __syncwarp();
+#pragma unroll 1
         for (int t = lane; t < N; t += 32) {
             const size_t rt = (((size_t)b * N + t) * a.H + h) * dk;
             tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t) * dk), k + rt, rowb, bar);
@@ -237,10 +242,12 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
             s_gate[4 * tid + 1] = be_reg;
         }
     } else {
+#pragma unroll 1
         for (int i = tid; i < N * kRows; i += kWarps * 32) {
             const int t = i / kRows, r = i % kRows;
             s_v[i] = r < rows ? ld_elem<T>(vv, (((size_t)b * N + t) * a.H + h) * dv + v0 + r) : 0.f;
         }
+#pragma unroll 1
         for (int t = tid; t < N; t += kWarps * 32) {
             const size_t gi = ((size_t)b * N + t) * a.H + h;
             s_gate[4 * t] = a.alpha[gi];
@@ -251,6 +258,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     const bool landed = tc::mbar_wait(bar, 0, a.err);
     // k_t . q_t of every token (the warps take turns), off the serial path
     if (__all_sync(0xffffffffu, landed)) {
+#pragma unroll 1
         for (int t = warp; t < N; t += kWarps) {
             float kt[kEPL], qt[kEPL];
             float kq = 0.f;
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     const int rr_held = held % RPW;
     const int r_held = warp * RPW + rr_held;        // its state row
     const bool holds_q = held >= RPW && lane % kGroup == 0 && r_held < rows;
-#pragma unroll 4
+#pragma unroll 1
     for (int t = 0; t < N; ++t) {
         float kt[kEPL], qt[kEPL];
         if (lane_on) {
@@ -323,6 +331,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     __syncthreads();
 
     // outputs and factors (coalesced along d_v)
+#pragma unroll 1
     for (int i = tid; i < N * kRows; i += kWarps * 32) {
         const int t = i / kRows, r = i % kRows;
         if (r >= rows) continue;
@@ -332,14 +341,17 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     // key copy (from smem), gates and parents: spread over the CTAs of this (b, h)
     T* key_out = static_cast<T*>(a.f.key);
     const int vecs = rowb / 16;
+#pragma unroll 1
     for (int t = blockIdx.y; t < N; t += gridDim.y) {
         const uint4* src = reinterpret_cast<const uint4*>(s_qk + (size_t)(2 * t) * dk);
         uint4* dst = reinterpret_cast<uint4*>(key_out + ((size_t)bh * N + t) * dk);
+#pragma unroll 1
         for (int i = tid; i < vecs; i += kWarps * 32) dst[i] = src[i];
     }
     if (blockIdx.y == 0 && warp == 0) {
         // g_t = sum_{i <= t} log alpha_i : warp scan over chunks of 32 nodes
         float carry = 0.f;
+#pragma unroll 1
         for (int t0 = 0; t0 < N; t0 += 32) {
             const int t = t0 + lane;
             float x = t < N ? logf(s_gate[4 * t]) : 0.f;

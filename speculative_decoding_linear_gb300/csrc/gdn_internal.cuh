@@ -285,6 +285,7 @@ __device__ __forceinline__ float4 commit_quad(float4 s, float ega, int L, const 
     a.y = ega * s.y;
     a.z = ega * s.z;
     a.w = ega * s.w;
+#pragma unroll 1
     for (int i = 0; i < L; ++i) {
         const float w = cd[i * cd_stride];
         const float4 kq = ld4<KT>(keys, (size_t)i * dk + c);
@@ -318,6 +319,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void cp_async_block(void* smem, const void* gmem, int bytes, int tid, int nthr) {
     char* d = static_cast<char*>(smem);
     const char* s = static_cast<const char*>(gmem);
+#pragma unroll 1
     for (int o = tid * 16; o < bytes; o += nthr * 16) cp_async16(d + o, s + o);
 }
 

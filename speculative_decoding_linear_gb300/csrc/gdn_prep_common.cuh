@@ -25,6 +25,7 @@ __device__ __forceinline__ void node_meta(int tid, int N, const int* par, const 
     if (tid < N) {
         uint64_t m = 0;
         int d = 0;
+#pragma unroll 1
         for (int j = par[tid]; j >= 0; j = par[j]) {
             m |= 1ull << j;
             ++d;
@@ -34,6 +35,7 @@ __device__ __forceinline__ void node_meta(int tid, int N, const int* par, const 
         uint8_t* pl = plist + tid * 64;
         float gs = 0.f;
         int i = 0;
+#pragma unroll 1
         for (uint64_t r = m; r; r &= r - 1) {
             const int j = __ffsll((long long)r) - 1;
             gs += la[j];
@@ -51,6 +53,7 @@ __device__ __forceinline__ void pair_list(int tid, int N, const int* depth, cons
     const int warp = tid >> 5, lane = tid & 31;
     if (warp == 0) {
         int carry = 0;
+#pragma unroll 1
         for (int t0 = 0; t0 < N; t0 += 32) {
             const int t = t0 + lane;
             int x = t < N ? depth[t] + 1 : 0;
@@ -67,6 +70,7 @@ __device__ __forceinline__ void pair_list(int tid, int N, const int* depth, cons
     __syncthreads();
     if (tid < N) {
         int o = off[tid];
+#pragma unroll 1
         for (uint64_t r = anc[tid]; r; r &= r - 1)
             pairs[o++] = (uint16_t)((tid << 8) | (__ffsll((long long)r) - 1));
         pairs[o] = (uint16_t)((tid << 8) | tid);
@@ -97,6 +101,7 @@ __device__ __forceinline__ void solve_rows(int tid, int N, int ld, const int* de
         const uint8_t* p = plist + t * 64;
         float* row = sT + t * ld;
         row[t] = 1.f;
+#pragma unroll 1
         for (int k = m - 1; k >= 0; --k) {
             const int pk = p[k];
             float x0 = 0.f, x1 = 0.f;
@@ -114,6 +119,7 @@ __device__ __forceinline__ void solve_rows(int tid, int N, int ld, const int* de
     if (tid < N) {
         const int t = tid, m = depth[t];
         const uint8_t* p = plist + t * 64;
+#pragma unroll 1
         for (int k = 0; k <= m; ++k) {
             const int pk = p[k];
             float x0 = 0.f, x1 = 0.f;
@@ -137,6 +143,7 @@ __device__ __forceinline__ void gram_row(int t, int m, const uint8_t* plist, con
                                          bool delta_rule = true) {
     const uint8_t* p = plist + t * 64;
     const float gt = g[t], bt = beta[t];
+#pragma unroll 1
     for (int i = 0; i <= m; ++i) {
         const int j = p[i];
         const float gam = expf(gt - g[j]);
@@ -148,13 +155,10 @@ __device__ __forceinline__ void gram_row(int t, int m, const uint8_t* plist, con
 // solve_rows with the path held in registers: q_0 = t, q_1 = parent, ..., q_m
 // = root.  Row t of T: x_0 = 1, x_i = -sum_{j < i} x_j A[q_j, q_i]; row t of
 // P: P[t, q_i] = sum_{j <= i} Attn[t, q_j] T[q_j, q_i].  Fully unrolled for
-// depth < kRegDepth (independent shared-memory loads), the generic loops of
-// solve_rows otherwise (always, with `unrolled` false: less code for kernels
-// that run it once per CTA).  Call with every thread of the block, or with
-// `group` > 0 with the first `group` threads, which then synchronise on named
-// barrier 1 only; contains barriers.
-constexpr int kRegDepth = 12;
-
+// depth < kRegDepth (independent shared-memory loads; the code grows as
+// kRegDepth^2), the generic loops of solve_rows otherwise.  Call with every
+// thread of the block, or with `group` > 0 with the first `group` threads,
+// which then synchronise on named barrier 1 only; contains barriers.
 __device__ __forceinline__ void group_sync(int group) {
     if (group == 0)
         __syncthreads();
@@ -162,12 +166,12 @@ __device__ __forceinline__ void group_sync(int group) {
         asm volatile("bar.sync 1, %0;\n" ::"r"(group) : "memory");
 }
 
+template <int kRegDepth = 12>
 __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const int* depth, const uint8_t* plist,
-                                                float* sA, const float* sAt, float* sT, int group = 0,
-                                                bool unrolled = true) {
+                                                float* sA, const float* sAt, float* sT, int group = 0) {
     const int t = tid;
     const int m = tid < N ? depth[t] : 0;
-    const bool fast = unrolled && tid < N && m < kRegDepth;
+    const bool fast = tid < N && m < kRegDepth;
     int q[kRegDepth];
     float x[kRegDepth];
     if (fast) {
@@ -192,9 +196,11 @@ __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const in
         const uint8_t* p = plist + t * 64;
         float* row = sT + t * ld;
         row[t] = 1.f;
+#pragma unroll 1
         for (int k = m - 1; k >= 0; --k) {
             const int pk = p[k];
             float x0 = 0.f;
+#pragma unroll 1
             for (int i = k + 1; i <= m; ++i) x0 = fmaf(row[p[i]], sA[p[i] * ld + pk], x0);
             row[pk] = -x0;
         }
@@ -216,9 +222,11 @@ __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const in
         }
     } else if (tid < N) {
         const uint8_t* p = plist + t * 64;
+#pragma unroll 1
         for (int k = 0; k <= m; ++k) {
             const int pk = p[k];
             float x0 = 0.f;
+#pragma unroll 1
             for (int i = k; i <= m; ++i) x0 = fmaf(sAt[t * ld + p[i]], sT[p[i] * ld + pk], x0);
             sA[t * ld + pk] = x0;
         }

@@ -33,9 +33,10 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 // Bounded wait for the completion of the mbarrier phase with this parity.
-// Returns false (and records GDN_ERR_TIMEOUT) after about one second.
-__device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Returns false (and records GDN_ERR_TIMEOUT) after about one second.  The
+// polling loop is out of line: kernels wait at many places, and each inlined
+// copy would cost instruction-cache space.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int* err) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         for (int i = 0; i < 64; ++i)
@@ -45,6 +46,9 @@ __device__ inline bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, err);
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint32_t bar) {
@@ -118,6 +122,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 consecutive TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of

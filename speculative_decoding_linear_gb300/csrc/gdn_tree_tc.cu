@@ -734,7 +734,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // 1) and runs the prologue itself, so a call is a single launch:
 //   before the wait: the state is streamed, the pending commit applied in
 //     registers and written back; slabs 0 and 1 become bf16 hi/lo operand
-//     stages, slabs 2 and 3 stay in registers;
+//     stages (slabs 2 and 3 are read back from L2 after the wait and take
+//     the stages over once slabs 0 and 1 are consumed);
 //   after the wait: q/k slabs by TMA; per slab the Y MMAs of both tiles and
 //     the Gram MMA ([Q; K] K^T: M = 128 rows, N = 64 keys) on the same operand
 //     buffer; the node metadata meanwhile;
@@ -758,7 +759,7 @@ struct FusedLayout {
     // stages and nB q/k buffers during Y, then R (both tiles), the A / Attn / T
     // tables and the [T; P] operand.
     int nB, bsz, ops, R, A, At, T, op;
-    int cd, key, nodes, coef, par, la, g, beta, eg, depth, anc, plist, bars, misc, total;
+    int cd, key, vs, nodes, coef, par, la, g, beta, eg, depth, anc, plist, bars, misc, total;
     __host__ __device__ FusedLayout(int N, int Lcap, bool split) {
         bsz = (split ? 2 : 1) * kBufBytes;
         build(N, Lcap, split, 2);
@@ -782,6 +783,7 @@ struct FusedLayout {
         o = ops;
         cd = take(Lcap * kFRows * 4);
         key = take(Lcap * kDk * (split ? 4 : 2));
+        vs = take(split ? 0 : N * kFRows * 2);      // bf16 v rows [t][256], copied after the wait
         nodes = take(kMaxPath * 4);
         coef = take(kMaxPath * 4);
         par = take(kMaxNodes * 4);
@@ -798,17 +800,41 @@ struct FusedLayout {
     }
 };
 
+// L2 cache policies: the state is read and written once per call, so its
+// lines go first (the call's inputs and the kernel stay resident); the two
+// slabs read back after the wait are kept.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+    return p;
+}
+
 // Rows rbase + 32 j (j = 0..7) of a 256-row state slab: j < 4 lie in tile 0,
 // j >= 4 in tile 1.
-__device__ __forceinline__ void f_load_slab(float4 (&x)[8], const float* S, size_t srow0, int rbase, int col) {
+__device__ __forceinline__ void f_load_slab(float4 (&x)[8], const float* S, size_t srow0, int rbase, int col,
+                                            uint64_t pol) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        x[j] = *reinterpret_cast<const float4*>(S + srow0 + (size_t)(rbase + 32 * j) * kDk + col);
+    for (int j = 0; j < 8; ++j) {
+        const float* p = S + srow0 + (size_t)(rbase + 32 * j) * kDk + col;
+        asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;\n"
+                     : "=f"(x[j].x), "=f"(x[j].y), "=f"(x[j].z), "=f"(x[j].w)
+                     : "l"(p), "l"(pol));
+    }
 }
-__device__ __forceinline__ void f_store_slab(const float4 (&x)[8], float* S, size_t srow0, int rbase, int col) {
+__device__ __forceinline__ void f_store_slab(const float4 (&x)[8], float* S, size_t srow0, int rbase, int col,
+                                             uint64_t pol) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<float4*>(S + srow0 + (size_t)(rbase + 32 * j) * kDk + col) = x[j];
+    for (int j = 0; j < 8; ++j) {
+        float* p = S + srow0 + (size_t)(rbase + 32 * j) * kDk + col;
+        asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;\n" ::"l"(p), "f"(x[j].x),
+                     "f"(x[j].y), "f"(x[j].z), "f"(x[j].w), "l"(pol)
+                     : "memory");
+    }
 }
 // Same arithmetic order per element as commit_slab (and gdn_commit).
 template <typename KT>
@@ -909,6 +935,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float* sT = reinterpret_cast<float*>(base + Ly.T);
     const uint32_t bars = base_s + Ly.bars;
     const uint32_t bar_e = bars + 64;                         // bars + 8 s: slab s copied; + 32 + 8 s: its MMAs done
+    const uint32_t bar_v = bars + 72;                         // v rows landed (bf16 inputs)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
     int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 4);    // path length, or -1: skip the CTA
     float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 8);
@@ -917,7 +944,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     auto bbuf = [&](int s) { return bbase + (nB == 2 ? (uint32_t)((s & 1) * Ly.bsz) : 0u); };
 
     if (tid == 0) {
-        for (int i = 0; i < 9; ++i) mbar_init(bars + 8 * i, 1);
+        for (int i = 0; i < 10; ++i) mbar_init(bars + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         fence_proxy_async_smem();
         *s_flag = 0;
@@ -948,8 +975,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
         prefetch_line_l2(a.beta + rt);
         prefetch_line_l2(a.parent + (size_t)b * N + tid);
     }
-    float4 x0[8], x1[8], x2[8], x3[8];
-    f_load_slab(x0, a.S, srow0, rbase, 4 * c4);
+    const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
+    float4 cur[8], nxt[8];
+    f_load_slab(cur, a.S, srow0, rbase, 4 * c4, pol_first);
     if (fused) {
         if (warp == 2) {
             const int L = commit_path_setup(a.commit, b, h, H, s_nodes, s_coef, s_ega);
@@ -977,25 +1005,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int L = fused ? *s_flag : 0;
     bool ok = L >= 0;
     if (ok) {
+        // slab by slab, the next one's loads in flight: commit, write back; slabs 0
+        // and 1 into the operand stages (2 and 3 are read back after the wait)
         const float ega = *s_ega;
-        f_load_slab(x1, a.S, srow0, rbase, kSlab + 4 * c4);
-        if (fused) {
-            f_commit_slab(x0, ega, L, s_cd, s_key, rbase, 4 * c4);
-            f_store_slab(x0, a.S, srow0, rbase, 4 * c4);
-        }
-        f_convert_slab(x0, base, rbase, c4);
-        f_load_slab(x2, a.S, srow0, rbase, 2 * kSlab + 4 * c4);
-        if (fused) {
-            f_commit_slab(x1, ega, L, s_cd, s_key, rbase, kSlab + 4 * c4);
-            f_store_slab(x1, a.S, srow0, rbase, kSlab + 4 * c4);
-        }
-        f_convert_slab(x1, base + kFAStage, rbase, c4);
-        f_load_slab(x3, a.S, srow0, rbase, 3 * kSlab + 4 * c4);
-        if (fused) {
-            f_commit_slab(x2, ega, L, s_cd, s_key, rbase, 2 * kSlab + 4 * c4);
-            f_store_slab(x2, a.S, srow0, rbase, 2 * kSlab + 4 * c4);
-            f_commit_slab(x3, ega, L, s_cd, s_key, rbase, 3 * kSlab + 4 * c4);
-            f_store_slab(x3, a.S, srow0, rbase, 3 * kSlab + 4 * c4);
+#pragma unroll 1
+        for (int sl = 0; sl < kSlabs; ++sl) {
+            if (sl + 1 < kSlabs) f_load_slab(nxt, a.S, srow0, rbase, (sl + 1) * kSlab + 4 * c4, pol_first);
+            if (fused) {
+                f_commit_slab(cur, ega, L, s_cd, s_key, rbase, sl * kSlab + 4 * c4);
+                f_store_slab(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, sl < 2 ? pol_first : pol_last);
+            }
+            if (sl < 2) f_convert_slab(cur, base + sl * kFAStage, rbase, c4);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
         }
         fence_proxy_async_smem();
     }
@@ -1004,9 +1026,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
     griddep_wait();
     griddep_launch();
     if (ok) {
+        // this thread's part of the committed slabs 2 and 3, written above (L2)
+        f_load_slab(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
+        f_load_slab(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
         if (warp == kFIssuerWarp && lane == 0) {
             issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(0), 0, h, b * N, bars);
             if (nB == 2) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
+        }
+        if (!kSplit && warp == kFIssuerWarp + 1) {   // this (sequence, head)'s v rows, one node per lane
+            if (lane == 0) mbar_expect_tx(bar_v, (uint32_t)(N * kFRows * 2));
+            __syncwarp();
+            for (int t = lane; t < N; t += 32)
+                bulk_copy_g2s(base_s + Ly.vs + t * kFRows * 2,
+                              static_cast<const KT*>(a.v) + (((size_t)b * N + t) * H + h) * kFRows, kFRows * 2, bar_v);
         }
         bool bad = false;
         if (tid < N) {
@@ -1027,59 +1059,36 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
         }
 
-        // ---- 3. Y of both tiles and the Gram, slab by slab (slabs 2 and 3 are
-        // converted into the stages that slabs 0 and 1 free) ----
-        if (warp == kFIssuerWarp) {
-            if (lane == 0) {
-            bool l = mbar_wait(bars, 0, a.err);
-            if (l) {
-                tc_fence_after();
-                f_issue_slab<kSplit>(tmem, stage0, bbuf(0), true);
-                mma_commit(bars + 32);
+        // ---- 3. Y of both tiles and the Gram, slab by slab.  Slab s: (s >= 2) its
+        // state part into the stage slab s - 2 has freed; lane 0 of the issuer warp
+        // issues its MMAs once its q/k copy has landed, then the copy into the q/k
+        // buffer that the MMAs of slab s + 1 - nB free ----
+#pragma unroll 1
+        for (int sl = 0; sl < kSlabs; ++sl) {
+            if (sl >= 2) {
+                ok = ok && mbar_wait(bars + 32 + 8 * (sl - 2), 0, a.err);
+                if (ok) f_convert_slab(cur, base + (sl & 1) * kFAStage, rbase, c4);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+                fence_proxy_async_smem();
+                ok = __syncthreads_and(ok);
             }
-            if (nB == 1) {
-                l = l && mbar_wait(bars + 32, 0, a.err);
-                if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
-            }
-            l = l && mbar_wait(bars + 8, 0, a.err);
-            if (l) {
-                tc_fence_after();
-                f_issue_slab<kSplit>(tmem, stage1, bbuf(1), false);
-                mma_commit(bars + 40);
-            }
-            l = l && mbar_wait(bars + (nB == 2 ? 32 : 40), 0, a.err);   // slab 2's buffer free
-            if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(2), 2, h, b * N, bars + 16);
-            }
-            __syncwarp();
-        }
-        ok = mbar_wait(bars + 32, 0, a.err);
-        if (ok) f_convert_slab(x2, base, rbase, c4);
-        fence_proxy_async_smem();
-        ok = __syncthreads_and(ok);
-        if (ok && warp == kFIssuerWarp) {
-            if (lane == 0) {
-                bool l = mbar_wait(bars + 16, 0, a.err);
-                if (l) {
-                    tc_fence_after();
-                    f_issue_slab<kSplit>(tmem, stage0, bbuf(2), false);
-                    mma_commit(bars + 48);
+            if (ok && warp == kFIssuerWarp) {
+                if (lane == 0) {
+                    bool l = mbar_wait(bars + 8 * sl, 0, a.err);
+                    if (l) {
+                        tc_fence_after();
+                        f_issue_slab<kSplit>(tmem, (sl & 1) ? stage1 : stage0, bbuf(sl), sl == 0);
+                        mma_commit(bars + 32 + 8 * sl);
+                    }
+                    const int sn = sl + nB;                             // next copy into bbuf(sl)
+                    if (sn < kSlabs) {
+                        l = l && mbar_wait(bars + 32 + 8 * sl, 0, a.err);
+                        if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(sn), sn, h, b * N, bars + 8 * sn);
+                    }
                 }
-                l = l && mbar_wait(bars + (nB == 2 ? 40 : 48), 0, a.err);   // slab 3's buffer free
-                if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(3), 3, h, b * N, bars + 24);
+                __syncwarp();
             }
-            __syncwarp();
-        }
-        if (ok) ok = mbar_wait(bars + 40, 0, a.err);
-        if (ok) f_convert_slab(x3, base + kFAStage, rbase, c4);
-        fence_proxy_async_smem();
-        ok = __syncthreads_and(ok);
-        if (ok && warp == kFIssuerWarp) {
-            if (lane == 0 && mbar_wait(bars + 24, 0, a.err)) {
-                tc_fence_after();
-                f_issue_slab<kSplit>(tmem, stage1, bbuf(3), false);
-                mma_commit(bars + 56);
-            }
-            __syncwarp();
         }
         if (ok) ok = mbar_wait(bars + 56, 0, a.err);              // Y and the Gram complete
         ok = __syncthreads_and(ok) && !bad;
@@ -1094,13 +1103,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 float* row = (tid < 64 ? sAt : sA) + t * ld;
                 const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16) + 256;
 #pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    float gr[32];
-                    tmem_ld32(t_lane + 32 * c, gr);
+                for (int c = 0; c < N; c += 8) {
+                    float gr[8];
+                    tmem_ld8(t_lane + c, gr);
                     if (t < N) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (32 * c + i < N) row[32 * c + i] = gr[i];
+                        for (int i = 0; i < 8; ++i)
+                            if (c + i < N) row[c + i] = gr[i];
                     }
                 }
             }
@@ -1110,7 +1119,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     prep::gram_row(tid, sdepth[tid], plist, sAt + tid * ld, sA + tid * ld, ld, sg, sbeta, sA, sAt,
                                    !a.linear);
                 prep::group_sync(256);
-                prep::solve_rows_fast(tid, N, ld, sdepth, plist, sA, sAt, sT, 256, false);
+                prep::solve_rows_fast<9>(tid, N, ld, sdepth, plist, sA, sAt, sT, 256);
                 prep::write_operand(tid, 256, N, ld, anc, sA, sT, base + Ly.op);
             } else {
                 // keys into the factor record
@@ -1129,38 +1138,58 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * u + kNodeRows;
                 unsigned char* rhi = base + Ly.R + u * 2 * kBufBytes;
                 unsigned char* rlo = rhi + kBufBytes;
-                const KT* vin = static_cast<const KT*>(a.v) + (size_t)h * kFRows + 128 * u + v;
-                const size_t vstride = (size_t)H * kFRows;          // between consecutive nodes
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                    float yk[32], vt[32];
+                // one 16-byte chunk of R (8 nodes from t0) from Y_K, the gates and v
+                auto r_chunk = [&](int t0, const float (&yk)[8], const float (&vt)[8]) {
+                    uint32_t hi[4], lo[4];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * c + i;
-                        vt[i] = t < N ? to_f32(vin[((size_t)b * N + t) * vstride]) : 0.f;
-                    }
-                    tmem_ld32(t_lane + 32 * c, yk);
+                    for (int e = 0; e < 4; ++e) {
+                        float r[2];
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i0 = 8 * q8 + 2 * e, i1 = i0 + 1;
-                            const int t0 = 32 * c + i0, t1 = t0 + 1;
-                            const float ek0 = a.linear || t0 >= N ? 0.f : seg[t0] * yk[i0];
-                            const float ek1 = a.linear || t1 >= N ? 0.f : seg[t1] * yk[i1];
-                            const float r0 = t0 < N ? sbeta[t0] * (vt[i0] - ek0) : 0.f;
-                            const float r1 = t1 < N ? sbeta[t1] * (vt[i1] - ek1) : 0.f;
-                            const __nv_bfloat162 hh = __floats2bfloat162_rn(r0, r1);
-                            const float2 hf = __bfloat1622float2(hh);
-                            const __nv_bfloat162 ll = __floats2bfloat162_rn(r0 - hf.x, r1 - hf.y);
-                            hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
-                            lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
+                        for (int q = 0; q < 2; ++q) {
+                            const int t = t0 + 2 * e + q;
+                            const float ek = a.linear ? 0.f : seg[t] * yk[2 * e + q];
+                            r[q] = t < N ? sbeta[t] * (vt[2 * e + q] - ek) : 0.f;
                         }
-                        const int cc = 4 * c + q8;                   // 16-byte chunk = 8 nodes
-                        const uint32_t off = (uint32_t)(v * 128 + ((cc ^ (v & 7)) << 4));
-                        *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<uint4*>(rlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        const __nv_bfloat162 hh = __floats2bfloat162_rn(r[0], r[1]);
+                        const float2 hf = __bfloat1622float2(hh);
+                        const __nv_bfloat162 ll = __floats2bfloat162_rn(r[0] - hf.x, r[1] - hf.y);
+                        hi[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                        lo[e] = *reinterpret_cast<const uint32_t*>(&ll);
+                    }
+                    const int cc = t0 >> 3;
+                    const uint32_t off = (uint32_t)(v * 128 + ((cc ^ (v & 7)) << 4));
+                    *reinterpret_cast<uint4*>(rhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(rlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                };
+                if constexpr (kSplit) {
+                    // fp32 v from global memory, a 32-node chunk's loads in flight together
+                    const KT* vin = static_cast<const KT*>(a.v) + ((size_t)b * N * H + h) * kFRows + 128 * u + v;
+#pragma unroll 1
+                    for (int c = 0; c < kNodeRows / 32; ++c) {
+                        float vt[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            vt[i] = 32 * c + i < N ? vin[(size_t)(32 * c + i) * H * kFRows] : 0.f;
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            float yk[8], v8[8];
+                            tmem_ld8(t_lane + 32 * c + 8 * q8, yk);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v8[i] = vt[8 * q8 + i];
+                            r_chunk(32 * c + 8 * q8, yk, v8);
+                        }
+                    }
+                } else {
+                    // bf16 v rows staged in shared memory
+                    const KT* vsm = reinterpret_cast<const KT*>(base + Ly.vs) + 128 * u + v;
+                    const bool vok = mbar_wait(bar_v, 0, a.err);
+#pragma unroll 1
+                    for (int t0 = 0; t0 < kNodeRows; t0 += 8) {
+                        float yk[8], v8[8];
+                        tmem_ld8(t_lane + t0, yk);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v8[i] = t0 + i < N && vok ? to_f32(vsm[(t0 + i) * kFRows]) : 0.f;
+                        r_chunk(t0, yk, v8);
                     }
                 }
             }
@@ -1174,7 +1203,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (lane == 0) {
             tc_fence_after();
             const uint32_t op_s = base_s + Ly.op;
-#pragma unroll
+#pragma unroll 1
             for (int u = 0; u < 2; ++u) {
                 const uint32_t r_s = base_s + Ly.R + u * 2 * kBufBytes;
 #pragma unroll
@@ -1197,37 +1226,27 @@ __global__ void __launch_bounds__(kFThreads, 1)
             // warps 0-3 / 8-11: Delta of tile 0 / 1; warps 4-7 / 12-15: O of tile 0 / 1
             const int u = warp >> 3;
             const int row = 128 * u + 32 * (warp & 3) + lane;
+            const bool is_o = ((warp >> 2) & 1) != 0;
             const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-            if (((warp >> 2) & 1) == 0) {
+            const uint32_t src = t_lane + 256 + 128 * u + (is_o ? kNodeRows : 0);   // T R or P R
+            float* dst = is_o ? a.out + ((size_t)b * N * H + h) * kFRows + row : a.f.delta + (size_t)bh * N * kFRows + row;
+            const size_t dstep = is_o ? (size_t)H * kFRows : (size_t)kFRows;
 #pragma unroll 1
-                for (int c = 0; c < kNodeRows / 32; ++c) {
-                    if (32 * c >= N) break;
-                    float d[32];
-                    tmem_ld32(t_lane + 256 + 128 * u + 32 * c, d);
+            for (int t0 = 0; t0 < N; t0 += 8) {
+                float x[8], yq[8];
+                tmem_ld8(src + t0, x);
+                if (is_o) tmem_ld8(t_lane + 128 * u + t0, yq);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * c + i;
-                        if (t < N) a.f.delta[((size_t)bh * N + t) * kFRows + row] = d[i];
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < kNodeRows / 32; ++c) {
-                    if (32 * c >= N) break;
-                    float yq[32], pr[32];
-                    tmem_ld32(t_lane + 128 * u + 32 * c, yq);
-                    tmem_ld32(t_lane + 256 + 128 * u + kNodeRows + 32 * c, pr);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * c + i;
-                        if (t < N) a.out[(((size_t)b * N + t) * H + h) * kFRows + row] = fmaf(seg[t], yq[i], pr[i]);
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const int t = t0 + i;
+                    if (t < N) dst[(size_t)t * dstep] = is_o ? fmaf(seg[t], yq[i], x[i]) : x[i];
                 }
             }
         }
     }
 
-    // ---- teardown: TMEM is always released ----
+    // ---- teardown: the v copies have landed; TMEM is always released ----
+    if (!kSplit && L >= 0 && tid == 0) mbar_wait(bar_v, 0, a.err);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
