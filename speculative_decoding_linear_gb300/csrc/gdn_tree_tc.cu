@@ -1020,6 +1020,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
         }
         fence_proxy_async_smem();
+        __syncthreads();       // every thread's part of stages 0 and 1 is in place before the first MMA
     }
 
     // ---- 2. this call's inputs ----
@@ -1040,23 +1041,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 bulk_copy_g2s(base_s + Ly.vs + t * kFRows * 2,
                               static_cast<const KT*>(a.v) + (((size_t)b * N + t) * H + h) * kFRows, kFRows * 2, bar_v);
         }
-        bool bad = false;
+        // parents and gates: loads issued now, used once the Y MMAs are under way
+        int p_in = 0;
+        float al_in = 1.f, be_in = 0.f;
         if (tid < N) {
-            const int p = a.parent[(size_t)b * N + tid];
-            bad = p < -1 || p >= tid;
-            par[tid] = p;
             const size_t gi = ((size_t)b * N + tid) * H + h;
-            la[tid] = logf(a.alpha[gi]);
-            sbeta[tid] = a.beta[gi];
-        }
-        bad = __syncthreads_or(bad);
-        if (bad) {
-            if (tid == 0) set_error(a.err, GDN_ERR_TREE);
-        } else if (tid < N) {
-            prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
-            seg[tid] = expf(sg[tid]);
-            a.f.g[(size_t)bh * N + tid] = sg[tid];
-            if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
+            p_in = a.parent[(size_t)b * N + tid];
+            al_in = a.alpha[gi];
+            be_in = a.beta[gi];
         }
 
         // ---- 3. Y of both tiles and the Gram, slab by slab.  Slab s: (s >= 2) its
@@ -1089,6 +1081,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 }
                 __syncwarp();
             }
+        }
+        // node metadata while the last slab's MMAs run
+        bool bad = false;
+        if (tid < N) {
+            bad = p_in < -1 || p_in >= tid;
+            par[tid] = p_in;
+            la[tid] = logf(al_in);
+            sbeta[tid] = be_in;
+        }
+        bad = __syncthreads_or(bad);
+        if (bad) {
+            if (tid == 0) set_error(a.err, GDN_ERR_TREE);
+        } else if (tid < N) {
+            prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
+            seg[tid] = expf(sg[tid]);
+            a.f.g[(size_t)bh * N + tid] = sg[tid];
+            if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
         }
         if (ok) ok = mbar_wait(bars + 56, 0, a.err);              // Y and the Gram complete
         ok = __syncthreads_and(ok) && !bad;
