@@ -256,8 +256,10 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     }
 
     const bool landed = tc::mbar_wait(bar, 0, a.err);
-    // k_t . q_t of every token (the warps take turns), off the serial path
-    if (__all_sync(0xffffffffu, landed)) {
+    // k_t . q_t: with RPW = 2 it rides along in the token loop's reduction (below);
+    // otherwise every token's is formed here (the warps take turns)
+    constexpr bool kFoldKq = RPW == 2;
+    if (!kFoldKq && __all_sync(0xffffffffu, landed)) {
 #pragma unroll 1
         for (int t = warp; t < N; t += kWarps) {
             float kt[kEPL], qt[kEPL];
@@ -276,16 +278,18 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     if (!__syncthreads_and(landed)) return;    // a bounded wait ran out (recorded in the error word)
 
     // 4. serial chain.  Per token the warp sums 2 RPW dot products (S_row . k_t and
-    // S_row . q_t of its RPW rows) with one reduce-scatter butterfly; afterwards lane
-    // l holds value l / kGroup.  The lanes holding S_row . k_t form delta_t of their
-    // row and broadcast it; the lanes holding S_row . q_t form o_t.  Unrolled by 4
+    // S_row . q_t of its RPW rows), and with RPW = 2 also k_t . q_t, with one
+    // reduce-scatter butterfly; afterwards lane l holds value l / kGroup.  The lanes
+    // holding S_row . k_t form delta_t of their row and broadcast it; the lanes
+    // holding S_row . q_t form o_t.  Unrolled by 2
     // so that the next tokens' shared-memory loads are issued ahead.
-    constexpr int kGroup = 32 / (2 * RPW);
+    constexpr int kVals = kFoldKq ? 8 : 2 * RPW;
+    constexpr int kGroup = 32 / kVals;
     const int held = lane / kGroup;                 // value index held after the reduction
     const int rr_held = held % RPW;
     const int r_held = warp * RPW + rr_held;        // its state row
-    const bool holds_q = held >= RPW && lane % kGroup == 0 && r_held < rows;
-#pragma unroll 1
+    const bool holds_q = held >= RPW && held < 2 * RPW && lane % kGroup == 0 && r_held < rows;
+#pragma unroll 2
     for (int t = 0; t < N; ++t) {
         float kt[kEPL], qt[kEPL];
         if (lane_on) {
@@ -295,7 +299,9 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
 #pragma unroll
             for (int e = 0; e < kEPL; ++e) kt[e] = qt[e] = 0.f;
         }
-        float val[2 * RPW];
+        float val[kVals];
+#pragma unroll
+        for (int i = 2 * RPW; i < kVals; ++i) val[i] = 0.f;
 #pragma unroll
         for (int rr = 0; rr < RPW; ++rr) {
             float x = 0.f, y = 0.f;
@@ -307,9 +313,14 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
             val[rr] = x;
             val[RPW + rr] = y;
         }
-        const float tot = warp_reduce_scatter<2 * RPW>(val, lane);
+        if (kFoldKq) {
+#pragma unroll
+            for (int e = 0; e < kEPL; ++e) val[2 * RPW] = fmaf(kt[e], qt[e], val[2 * RPW]);
+        }
+        const float tot = warp_reduce_scatter<kVals>(val, lane);
         const float4 gt = *reinterpret_cast<const float4*>(s_gate + 4 * t);   // alpha, beta, k.q
         const float al = gt.x, be = gt.y;
+        const float kq = kFoldKq ? __shfl_sync(0xffffffffu, tot, 2 * RPW * kGroup) : gt.z;
         const float vt = r_held < rows ? ld_elem<T>(s_v, (size_t)t * kRows + r_held) : 0.f;
         const float dl = be * (a.linear ? vt : vt - al * tot);             // meaningful where held < RPW
         float dlt[RPW];
@@ -320,7 +331,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
 #pragma unroll
             for (int rr = 1; rr < RPW; ++rr)
                 if (rr_held == rr) d = dlt[rr];
-            s_o[t * kRows + r_held] = fmaf(al, tot, d * gt.z);
+            s_o[t * kRows + r_held] = fmaf(al, tot, d * kq);
             s_d[t * kRows + r_held] = d;
         }
 #pragma unroll
