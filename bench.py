@@ -61,9 +61,11 @@ def algorithmic_bytes(B, N, H, dk, dv, esz, L_total, Lmax, chain):
 # every kernel the call launches) from one ncu capture per workload, with the
 # hash of the kernel sources it was taken on: a changed kernel reports null.
 NCU_TRAFFIC = {
-    "chain8_b1_h8_d256": (2.283e6, ("gdn_chain.cu", "gdn_internal.cuh"), "97e01ac6ebb532a0"),
-    "tree64_depth8_b16_h8_d256": (65.26e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
-                                            "gdn_internal.cuh"), "61eee5793fac47b5"),
+    "chain8_b1_h8_d256": (2.271e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"), "e22e48b1da7e784c"),
+    "tree32_depth6_b1_h8_d256": (2.628e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
+                                           "gdn_internal.cuh"), "4139376216024da4"),
+    "tree64_depth8_b16_h8_d256": (47.78e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
+                                            "gdn_internal.cuh"), "4139376216024da4"),
 }
 
 

@@ -360,6 +360,36 @@ def test_tensor_core_fused_commit(oracle_mod, L):
     check_verify(w2, out2, fac2, oracle_mod)
 
 
+@pytest.mark.parametrize("L", [0, 7])
+def test_tensor_core_two_kernel_path(oracle_mod, L):
+    """d_v = 128 takes the prologue + contraction kernel pair (d_v = 256 takes the single kernel):
+    verification, then a fused commit of a path of length L, against the oracle."""
+    B, N, H = 6, 40, 4
+    rng = np.random.default_rng(70 + L)
+    parent = np.stack([wl.random_tree(rng, N, 7) for _ in range(B)])
+    w1 = wl.custom_workload(B, N, H, 256, 128, parent, seed=80 + L)
+    d1, out1, fac1 = run_tree_verify(w1)
+    check_verify(w1, out1, fac1, oracle_mod)
+    paths = np.full((B, 16), -1, np.int32)
+    for b in range(B):
+        p = wl.root_path(parent[b], int(rng.integers(0, N)))[:L]
+        paths[b, :len(p)] = p
+    w2 = wl.custom_workload(B, 33, H, 256, 128, np.stack([wl.random_tree(rng, 33, 6) for _ in range(B)]),
+                            seed=90 + L)
+    d2 = dev_inputs(w2)
+    S = d1["S0"].clone()
+    out2, fac2, ws2 = alloc_outputs(w2)
+    path_dev = torch.from_numpy(paths).cuda()
+    gdnspec.gdn_commit_tree_verify(S, fac1, N, path_dev, d2["q"], d2["k"], d2["v"], d2["alpha"], d2["beta"],
+                                   d2["parent"], out2, fac2, ws2)
+    assert gdnspec.gdn_last_error() == 0
+    x1 = oracle_inputs(w1)
+    S_ref = oracle_mod.commit(x1["k"], x1["v"], x1["alpha"], x1["beta"], parent, x1["S0"], paths)
+    assert_close(S.cpu().numpy(), S_ref, "committed S")
+    w2.S0 = S.cpu().numpy()
+    check_verify(w2, out2, fac2, oracle_mod)
+
+
 # ---------------------------------------------------------------------------
 # replay baselines (what the tree verifier and the factor commit replace)
 # ---------------------------------------------------------------------------
