@@ -256,9 +256,10 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     }
 
     const bool landed = tc::mbar_wait(bar, 0, a.err);
-    // k_t . q_t: with RPW = 2 it rides along in the token loop's reduction (below);
-    // otherwise every token's is formed here (the warps take turns)
-    constexpr bool kFoldKq = RPW == 2;
+    // k_t . q_t rides along in the token loop's reduction (below) when the 2 RPW
+    // row sums leave room in a power-of-two value count; otherwise every token's is
+    // formed here (the warps take turns)
+    constexpr bool kFoldKq = RPW == 2 || RPW == 4;
     if (!kFoldKq && __all_sync(0xffffffffu, landed)) {
 #pragma unroll 1
         for (int t = warp; t < N; t += kWarps) {
@@ -278,12 +279,12 @@ __global__ void __launch_bounds__(kWarps * 32) chain_kernel(VerifyArgs a) {
     if (!__syncthreads_and(landed)) return;    // a bounded wait ran out (recorded in the error word)
 
     // 4. serial chain.  Per token the warp sums 2 RPW dot products (S_row . k_t and
-    // S_row . q_t of its RPW rows), and with RPW = 2 also k_t . q_t, with one
+    // S_row . q_t of its RPW rows) and k_t . q_t with one
     // reduce-scatter butterfly; afterwards lane l holds value l / kGroup.  The lanes
     // holding S_row . k_t form delta_t of their row and broadcast it; the lanes
     // holding S_row . q_t form o_t.  Unrolled by 2
     // so that the next tokens' shared-memory loads are issued ahead.
-    constexpr int kVals = kFoldKq ? 8 : 2 * RPW;
+    constexpr int kVals = kFoldKq ? 4 * RPW : 2 * RPW;
     constexpr int kGroup = 32 / kVals;
     const int held = lane / kGroup;                 // value index held after the reduction
     const int rr_held = held % RPW;
