@@ -103,6 +103,26 @@ def test_layer_step_matches_oracle(oracle_mod, shape):
     assert torch.equal(run.conv_state.cpu(), torch.from_numpy(w.conv_state))
 
 
+def test_two_steps_sixteen_node_path(oracle_mod):
+    """A 16-node accepted path (d = 256, fp32 q/k as bf16 hi + lo): the single-kernel verifier then
+    has room for one q/k buffer only and streams the four slabs' copies through it."""
+    from oracle import layer
+    B, N, H, dk, dv, hid = 2, 24, 2, 256, 256, 256
+    w = wl.make_layer_workload(4, seed=301, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=6)
+    w2 = wl.make_layer_workload(4, seed=302, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=6)
+    chain = np.tile(wl.chain_tree(N), (B, 1))          # first step: a chain, 16 of its nodes accepted
+    paths = np.tile(np.arange(16, dtype=np.int32), (B, 1))
+    run = LayerRun(w)
+    run.step(w.X, chain)
+    r1 = oracle_step(layer, w, w.X, chain, w.widened("S0"), w.widened("conv_state"))
+    S1, hist1 = layer.layer_commit(r1, chain, w.widened("S0"), w.widened("conv_state"), paths)
+    out, Y, fac, views = run.step(w2.X, w2.parent, prev_path=paths, N_prev=N)
+    assert_close(run.S.cpu().numpy(), S1, "committed state")
+    assert_close(run.conv_state.cpu().numpy(), hist1, "committed conv history", tol=1e-5)
+    r2 = oracle_step(layer, w, w2.X, w2.parent, S1, hist1)
+    compare(w, r2, out, Y, fac, views, w2.parent)
+
+
 @pytest.mark.parametrize("shape", SMALL[:2] + SMALL[3:])
 def test_two_steps_commit_state_and_conv_history(oracle_mod, shape):
     from oracle import layer
