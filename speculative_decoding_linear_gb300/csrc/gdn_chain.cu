@@ -393,8 +393,311 @@ cudaError_t launch_chain_t(const VerifyArgs& a, cudaStream_t s) {
     return launch_kernel(chain_kernel<T, RPW>, grid, dim3(kWarps * 32), L.total, s, a.overlap, a);
 }
 
+// ---------------------------------------------------------------------------
+// d_k = 256: eight lanes per state row
+// ---------------------------------------------------------------------------
+// The per-token step above is bound by its five-level butterfly with one warp
+// per SM sub-partition.  With d_k = 256 a row can be spread over 8 lanes (32
+// contiguous columns each) instead: a warp holds 4 rows, a CTA 16, and a token
+// costs a three-level butterfly after which every lane of the row's group holds
+// S_row . k_t, S_row . q_t and k_t . q_t, so delta_t needs no broadcast.  A
+// lane's 32 columns are interleaved with its group's (4 at a time) so that the
+// shared-memory reads of a group cover 128 contiguous bytes.  This
+// layer's q/k rows are widened to fp32 in shared memory once, so the token loop
+// reads them with 16-byte loads that the row groups share.
+constexpr int kG8Rows = 16;            // state rows per CTA
+constexpr int kG8Cols = 32;            // state columns per lane (8 groups of 4)
+
+struct G8Smem {
+    int qk, qkf, key, v, gate, o, d, cd, coef, nodes, misc, total;
+    __host__ __device__ G8Smem(int N, int Lcap, int esz) {
+        int off = 0;
+        auto take = [&](int bytes) { int o = off; off += (bytes + 15) / 16 * 16; return o; };
+        qk = take(esz == 4 ? 0 : N * 2 * kMaxDim * esz);   // bf16 rows as copied: [t][k | q][256]
+        qkf = take(N * 2 * kMaxDim * 4);                   // fp32 rows (the copy target for fp32 inputs)
+        key = take(Lcap * kMaxDim * esz);
+        v = take(N * kG8Rows * esz);
+        gate = take(N * 16);                               // [t][alpha, beta, -, -]
+        o = take(N * kG8Rows * 4);
+        d = take(N * kG8Rows * 4);
+        cd = take(Lcap * kG8Rows * 4);
+        coef = take(kMaxPath * 4);
+        nodes = take(kMaxPath * 4);
+        misc = take(16);
+        total = off;
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
+    constexpr int kRows = kG8Rows;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int Lcap = a.commit.path ? a.commit.Lmax : 0;
+    const G8Smem L(a.N, Lcap, (int)sizeof(T));
+    float* s_qkf = reinterpret_cast<float*>(smem + L.qkf);
+    T* s_qkraw = sizeof(T) == 4 ? reinterpret_cast<T*>(smem + L.qkf) : reinterpret_cast<T*>(smem + L.qk);
+    T* s_key = reinterpret_cast<T*>(smem + L.key);
+    T* s_v = reinterpret_cast<T*>(smem + L.v);
+    float* s_gate = reinterpret_cast<float*>(smem + L.gate);
+    float* s_o = reinterpret_cast<float*>(smem + L.o);
+    float* s_d = reinterpret_cast<float*>(smem + L.d);
+    float* s_cd = reinterpret_cast<float*>(smem + L.cd);
+    float* s_coef = reinterpret_cast<float*>(smem + L.coef);
+    int* s_nodes = reinterpret_cast<int*>(smem + L.nodes);
+    float* s_ega = reinterpret_cast<float*>(smem + L.misc);
+    int* s_L = reinterpret_cast<int*>(smem + L.misc + 4);
+
+    const int bh = blockIdx.x;
+    const int b = bh / a.H, h = bh % a.H;
+    const int N = a.N, dv = a.dv, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int r = warp * 4 + (lane >> 3);      // this lane's state row within the CTA
+    // Columns 32 m + cb + u (m = 0..7, u = 0..3), cb = 4 (lane & 7): the row's 8 lanes
+    // read 128 contiguous bytes per 16-byte load (no bank conflicts); S[4 m + u].
+    const int cb = 4 * (lane & 7);
+    const int v0 = blockIdx.y * kRows;
+    const int rows = min(kRows, dv - v0);
+    const bool row_on = r < rows;
+    const bool fused = a.commit.path != nullptr;
+    __shared__ __align__(8) uint64_t s_bar;
+    const uint32_t bar = smem_u32(&s_bar);
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    // 1. this lane's 32 columns of its state row
+    float S[kG8Cols];
+    const float* srow = a.S + ((size_t)bh * dv + v0 + r) * kMaxDim + cb;
+#pragma unroll
+    for (int e = 0; e < kG8Cols; e += 4) {
+        const float4 x = row_on ? *reinterpret_cast<const float4*>(srow + 8 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[e] = x.x;
+        S[e + 1] = x.y;
+        S[e + 2] = x.z;
+        S[e + 3] = x.w;
+    }
+    if (fused) {
+        if (warp == 0) {
+            const int Lp = commit_path_setup(a.commit, b, h, a.H, s_nodes, s_coef, s_ega);
+            if (lane == 0) {
+                *s_L = Lp;
+                if (Lp < 0) set_error(a.err, GDN_ERR_PATH);
+            }
+        }
+        __syncthreads();
+        const int nL = *s_L;
+        if (nL < 0) return;
+        const float* dl = a.commit.delta + (size_t)bh * a.commit.N * dv;
+        const T* key_bh = static_cast<const T*>(a.commit.key) + (size_t)bh * a.commit.N * kMaxDim;
+#pragma unroll 1
+        for (int i = 0; i < nL; ++i)
+            cp_async_block(s_key + (size_t)i * kMaxDim, key_bh + (size_t)s_nodes[i] * kMaxDim,
+                           kMaxDim * (int)sizeof(T), tid, kWarps * 32);
+#pragma unroll 1
+        for (int i = tid; i < nL * kRows; i += kWarps * 32) {
+            const int j = i / kRows, rr = i % kRows;
+            s_cd[i] = rr < rows ? s_coef[j] * dl[(size_t)s_nodes[j] * dv + v0 + rr] : 0.f;
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        // 2. commit in registers (same arithmetic order as gdn_commit)
+        const float ega = *s_ega;
+#pragma unroll
+        for (int e = 0; e < kG8Cols; ++e) S[e] *= ega;
+#pragma unroll 1
+        for (int i = 0; i < nL; ++i) {
+            const float w = s_cd[i * kRows + r];
+#pragma unroll
+            for (int e = 0; e < kG8Cols; e += 4) {
+                const float4 kv = ld4<T>(s_key, (size_t)i * kMaxDim + cb + 8 * e);
+                S[e] = fmaf(w, kv.x, S[e]);
+                S[e + 1] = fmaf(w, kv.y, S[e + 1]);
+                S[e + 2] = fmaf(w, kv.z, S[e + 2]);
+                S[e + 3] = fmaf(w, kv.w, S[e + 3]);
+            }
+        }
+    }
+
+    // This layer's q/k/v rows and gates into L2 while the previous kernel finishes.
+    if (tid == 0) {
+        const int rowq = kMaxDim * (int)sizeof(T), rowv = dv * (int)sizeof(T);
+#pragma unroll 1
+        for (int t = blockIdx.y; t < N; t += gridDim.y) {
+            const size_t rt = ((size_t)b * N + t) * a.H + h;
+            prefetch_l2(static_cast<const T*>(a.q) + rt * kMaxDim, rowq);
+            prefetch_l2(static_cast<const T*>(a.k) + rt * kMaxDim, rowq);
+            prefetch_l2(static_cast<const T*>(a.v) + rt * dv, rowv);
+        }
+    }
+    if (tid < N) {
+        const size_t gi = ((size_t)b * N + tid) * a.H + h;
+        prefetch_line_l2(a.alpha + gi);
+        prefetch_line_l2(a.beta + gi);
+    }
+
+    // Everything above only read memory.
+    griddep_wait();
+    griddep_launch();
+    // 3. this layer's draft inputs (as in chain_kernel)
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    const T* vv = static_cast<const T*>(a.v);
+    const int rowb = kMaxDim * (int)sizeof(T);
+    const bool one_pass = N * kRows <= kWarps * 32;
+    float v_reg = 0.f, al_reg = 0.f, be_reg = 0.f;
+    if (one_pass) {
+        if (tid < N * kRows && tid % kRows < rows)
+            v_reg = ld_elem<T>(vv, (((size_t)b * N + tid / kRows) * a.H + h) * dv + v0 + tid % kRows);
+        if (tid < N) {
+            const size_t gi = ((size_t)b * N + tid) * a.H + h;
+            al_reg = a.alpha[gi];
+            be_reg = a.beta[gi];
+        }
+    }
+    if (warp == 0) {
+        if (lane == 0) tc::mbar_expect_tx(bar, (uint32_t)(2 * N * rowb));
+        __syncwarp();
+#pragma unroll 1
+        for (int t = lane; t < N; t += 32) {
+            const size_t rt = (((size_t)b * N + t) * a.H + h) * kMaxDim;
+            tc::bulk_copy_g2s(smem_u32(s_qkraw + (size_t)(2 * t) * kMaxDim), k + rt, rowb, bar);
+            tc::bulk_copy_g2s(smem_u32(s_qkraw + (size_t)(2 * t + 1) * kMaxDim), q + rt, rowb, bar);
+        }
+    }
+    if (fused && row_on) {    // committed row part written back once
+        float* wrow = a.S + ((size_t)bh * dv + v0 + r) * kMaxDim + cb;
+#pragma unroll
+        for (int e = 0; e < kG8Cols; e += 4)
+            *reinterpret_cast<float4*>(wrow + 8 * e) = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
+    }
+    if (one_pass) {
+        if (tid < N * kRows) st_elem<T>(s_v, tid, v_reg);
+        if (tid < N) {
+            s_gate[4 * tid] = al_reg;
+            s_gate[4 * tid + 1] = be_reg;
+        }
+    } else {
+#pragma unroll 1
+        for (int i = tid; i < N * kRows; i += kWarps * 32) {
+            const int t = i / kRows, rr = i % kRows;
+            st_elem<T>(s_v, i, rr < rows ? ld_elem<T>(vv, (((size_t)b * N + t) * a.H + h) * dv + v0 + rr) : 0.f);
+        }
+#pragma unroll 1
+        for (int t = tid; t < N; t += kWarps * 32) {
+            const size_t gi = ((size_t)b * N + t) * a.H + h;
+            s_gate[4 * t] = a.alpha[gi];
+            s_gate[4 * t + 1] = a.beta[gi];
+        }
+    }
+    const bool landed = tc::mbar_wait(bar, 0, a.err);
+    if (sizeof(T) == 2 && __all_sync(0xffffffffu, landed)) {     // bf16 rows -> fp32
+#pragma unroll 1
+        for (int i = 8 * tid; i < N * 2 * kMaxDim; i += 8 * kWarps * 32) {
+            float x[8];
+            ld8<T>(s_qkraw + i, x);
+            *reinterpret_cast<float4*>(s_qkf + i) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(s_qkf + i + 4) = make_float4(x[4], x[5], x[6], x[7]);
+        }
+    }
+    if (!__syncthreads_and(landed)) return;    // a bounded wait ran out (recorded in the error word)
+
+    // 4. serial chain: per token three partial-sum dot products over the lane's 32
+    // columns, a three-level butterfly over the row's 8 lanes, the update
+#pragma unroll 2
+    for (int t = 0; t < N; ++t) {
+        const float* kr = s_qkf + (size_t)(2 * t) * kMaxDim + cb;
+        const float* qr = kr + kMaxDim;
+        float kt[kG8Cols];
+        float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < kG8Cols; e += 4) {
+            const float4 kv = *reinterpret_cast<const float4*>(kr + 8 * e);
+            const float4 qv = *reinterpret_cast<const float4*>(qr + 8 * e);
+            kt[e] = kv.x;
+            kt[e + 1] = kv.y;
+            kt[e + 2] = kv.z;
+            kt[e + 3] = kv.w;
+            const int p = (e >> 2) & 3;
+            x[p] = fmaf(S[e], kv.x, fmaf(S[e + 1], kv.y, fmaf(S[e + 2], kv.z, fmaf(S[e + 3], kv.w, x[p]))));
+            y[p] = fmaf(S[e], qv.x, fmaf(S[e + 1], qv.y, fmaf(S[e + 2], qv.z, fmaf(S[e + 3], qv.w, y[p]))));
+            z[p] = fmaf(kv.x, qv.x, fmaf(kv.y, qv.y, fmaf(kv.z, qv.z, fmaf(kv.w, qv.w, z[p]))));
+        }
+        float sk = (x[0] + x[1]) + (x[2] + x[3]);
+        float sq = (y[0] + y[1]) + (y[2] + y[3]);
+        float kq = (z[0] + z[1]) + (z[2] + z[3]);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        }
+        const float2 gt = *reinterpret_cast<const float2*>(s_gate + 4 * t);   // alpha, beta
+        const float al = gt.x, be = gt.y;
+        const float vt = row_on ? ld_elem<T>(s_v, (size_t)t * kRows + r) : 0.f;
+        const float dlt = be * (a.linear ? vt : vt - al * sk);
+        if ((lane & 7) == 0 && row_on) {
+            s_o[t * kRows + r] = fmaf(al, sq, dlt * kq);
+            s_d[t * kRows + r] = dlt;
+        }
+#pragma unroll
+        for (int e = 0; e < kG8Cols; ++e) S[e] = fmaf(al, S[e], dlt * kt[e]);
+    }
+    __syncthreads();
+
+    // outputs and factors (coalesced along d_v)
+#pragma unroll 1
+    for (int i = tid; i < N * kRows; i += kWarps * 32) {
+        const int t = i / kRows, rr = i % kRows;
+        if (rr >= rows) continue;
+        a.out[(((size_t)b * N + t) * a.H + h) * dv + v0 + rr] = s_o[i];
+        a.f.delta[((size_t)bh * N + t) * dv + v0 + rr] = s_d[i];
+    }
+    // key copy (the rows as copied), gates and parents: spread over the CTAs of this (b, h)
+    T* key_out = static_cast<T*>(a.f.key);
+    const int vecs = rowb / 16;
+#pragma unroll 1
+    for (int t = blockIdx.y; t < N; t += gridDim.y) {
+        const uint4* src = reinterpret_cast<const uint4*>(s_qkraw + (size_t)(2 * t) * kMaxDim);
+        uint4* dst = reinterpret_cast<uint4*>(key_out + ((size_t)bh * N + t) * kMaxDim);
+#pragma unroll 1
+        for (int i = tid; i < vecs; i += kWarps * 32) dst[i] = src[i];
+    }
+    if (blockIdx.y == 0 && warp == 0) {
+        float carry = 0.f;
+#pragma unroll 1
+        for (int t0 = 0; t0 < N; t0 += 32) {
+            const int t = t0 + lane;
+            float x = t < N ? logf(s_gate[4 * t]) : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            x += carry;
+            if (t < N) {
+                a.f.g[(size_t)bh * N + t] = x;
+                if (h == 0) a.f.parent[(size_t)b * N + t] = t - 1;
+            }
+            carry = __shfl_sync(0xffffffffu, x, 31);
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_chain_g8(const VerifyArgs& a, cudaStream_t s) {
+    static bool attr[64];
+    const G8Smem L(a.N, a.commit.path ? a.commit.Lmax : 0, (int)sizeof(T));
+    cudaError_t e = ensure_smem(chain_g8_kernel<T>, L.total, attr);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.B * a.H, (a.dv + kG8Rows - 1) / kG8Rows);
+    return launch_kernel(chain_g8_kernel<T>, grid, dim3(kWarps * 32), L.total, s, a.overlap, a);
+}
+
 template <typename T>
 cudaError_t launch_chain_dt(const VerifyArgs& a, cudaStream_t s) {
+    if (a.dk == kMaxDim) return launch_chain_g8<T>(a, s);
     // Small problems: 8-row CTAs so that more SMs stream the state.
     const long long ctas16 = (long long)a.B * a.H * ((a.dv + 15) / 16);
     return ctas16 < 2 * 152 ? launch_chain_t<T, 2>(a, s) : launch_chain_t<T, 4>(a, s);
