@@ -61,7 +61,7 @@ def algorithmic_bytes(B, N, H, dk, dv, esz, L_total, Lmax, chain):
 # every kernel the call launches) from one ncu capture per workload, with the
 # hash of the kernel sources it was taken on: a changed kernel reports null.
 NCU_TRAFFIC = {
-    "chain8_b1_h8_d256": (2.271e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"), "e22e48b1da7e784c"),
+    "chain8_b1_h8_d256": (2.279e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"), "54cc5a3d11c8708c"),
     "tree32_depth6_b1_h8_d256": (2.628e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
                                            "gdn_internal.cuh"), "4139376216024da4"),
     "tree64_depth8_b16_h8_d256": (47.78e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
@@ -294,15 +294,18 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
     peak, peak_kind = measured_peaks()
     achieved = per_call / t_layer_s / 1e9
     value = whole_job_rate(B * N * R * steps, world, ms / 1e3)
-    launches_per_call = 1 if chain else 2
+    # one launch per call: the chain kernel, or the single-kernel tree verifier (d_k = d_v = 256)
+    fused_tree = not chain and dk == 256 and dv == 256
+    launches_per_call = 1 if (chain or fused_tree) else 2
     return dict(
         value=value, ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
         spec=spec, B=B, N=N, H=H, dk=dk, dv=dv, chain=chain,
         roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                   "frac": round(achieved / peak, 4), "traffic": ncu_traffic(spec.name),
                   "peak_kind": peak_kind + " hbm_gbs (copy)",
-                  "kernel": "gdn_commit_chain_verify (chain_kernel)" if chain else
-                            "gdn_commit_tree_verify (tree_prep_tc_kernel + tree_contract_tc_kernel)",
+                  "kernel": "gdn_commit_chain_verify (chain_g8_kernel)" if chain else
+                            "gdn_commit_tree_verify (tree_fused_tc_kernel)" if fused_tree else
+                            "gdn_commit_tree_verify (prologue + contraction kernels)",
                   "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_layer_s * 1e6, 3)},
         gpu_launches=launches_per_call * R * steps, baselines=baselines, hybrid=hybrid, prune=prune,
     )
@@ -539,7 +542,8 @@ def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile
                   "kernel": "gdn_layer_tree_step (input/output projection GEMMs on tcgen05, conv, "
                             "tree verify + commit, gate)",
                   "algorithmic_flops_per_call": flops, "t_call_us": round(t_layer_s * 1e6, 3)},
-        gpu_launches=6 * R * steps,
+        # GEMM, conv, tree verifier (one kernel at d_k = d_v = 256, else two), gate, GEMM
+        gpu_launches=(5 if w0.dk == 256 and w0.dv == 256 else 6) * R * steps,
     )
 
 

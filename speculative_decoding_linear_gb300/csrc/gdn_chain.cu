@@ -402,19 +402,17 @@ cudaError_t launch_chain_t(const VerifyArgs& a, cudaStream_t s) {
 // costs a three-level butterfly after which every lane of the row's group holds
 // S_row . k_t, S_row . q_t and k_t . q_t, so delta_t needs no broadcast.  A
 // lane's 32 columns are interleaved with its group's (4 at a time) so that the
-// shared-memory reads of a group cover 128 contiguous bytes.  This
-// layer's q/k rows are widened to fp32 in shared memory once, so the token loop
-// reads them with 16-byte loads that the row groups share.
+// shared-memory reads of a group cover contiguous bytes; the four row groups of
+// a warp read the same k/q words (broadcast), widened to fp32 in registers.
 constexpr int kG8Rows = 16;            // state rows per CTA
 constexpr int kG8Cols = 32;            // state columns per lane (8 groups of 4)
 
 struct G8Smem {
-    int qk, qkf, key, v, gate, o, d, cd, coef, nodes, misc, total;
+    int qk, key, v, gate, o, d, cd, coef, nodes, misc, total;
     __host__ __device__ G8Smem(int N, int Lcap, int esz) {
         int off = 0;
         auto take = [&](int bytes) { int o = off; off += (bytes + 15) / 16 * 16; return o; };
-        qk = take(esz == 4 ? 0 : N * 2 * kMaxDim * esz);   // bf16 rows as copied: [t][k | q][256]
-        qkf = take(N * 2 * kMaxDim * 4);                   // fp32 rows (the copy target for fp32 inputs)
+        qk = take(N * 2 * kMaxDim * esz);                  // rows as copied: [t][k | q][256]
         key = take(Lcap * kMaxDim * esz);
         v = take(N * kG8Rows * esz);
         gate = take(N * 16);                               // [t][alpha, beta, -, -]
@@ -434,8 +432,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int Lcap = a.commit.path ? a.commit.Lmax : 0;
     const G8Smem L(a.N, Lcap, (int)sizeof(T));
-    float* s_qkf = reinterpret_cast<float*>(smem + L.qkf);
-    T* s_qkraw = sizeof(T) == 4 ? reinterpret_cast<T*>(smem + L.qkf) : reinterpret_cast<T*>(smem + L.qk);
+    T* s_qk = reinterpret_cast<T*>(smem + L.qk);
     T* s_key = reinterpret_cast<T*>(smem + L.key);
     T* s_v = reinterpret_cast<T*>(smem + L.v);
     float* s_gate = reinterpret_cast<float*>(smem + L.gate);
@@ -562,8 +559,8 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
 #pragma unroll 1
         for (int t = lane; t < N; t += 32) {
             const size_t rt = (((size_t)b * N + t) * a.H + h) * kMaxDim;
-            tc::bulk_copy_g2s(smem_u32(s_qkraw + (size_t)(2 * t) * kMaxDim), k + rt, rowb, bar);
-            tc::bulk_copy_g2s(smem_u32(s_qkraw + (size_t)(2 * t + 1) * kMaxDim), q + rt, rowb, bar);
+            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t) * kMaxDim), k + rt, rowb, bar);
+            tc::bulk_copy_g2s(smem_u32(s_qk + (size_t)(2 * t + 1) * kMaxDim), q + rt, rowb, bar);
         }
     }
     if (fused && row_on) {    // committed row part written back once
@@ -592,29 +589,20 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
         }
     }
     const bool landed = tc::mbar_wait(bar, 0, a.err);
-    if (sizeof(T) == 2 && __all_sync(0xffffffffu, landed)) {     // bf16 rows -> fp32
-#pragma unroll 1
-        for (int i = 8 * tid; i < N * 2 * kMaxDim; i += 8 * kWarps * 32) {
-            float x[8];
-            ld8<T>(s_qkraw + i, x);
-            *reinterpret_cast<float4*>(s_qkf + i) = make_float4(x[0], x[1], x[2], x[3]);
-            *reinterpret_cast<float4*>(s_qkf + i + 4) = make_float4(x[4], x[5], x[6], x[7]);
-        }
-    }
     if (!__syncthreads_and(landed)) return;    // a bounded wait ran out (recorded in the error word)
 
     // 4. serial chain: per token three partial-sum dot products over the lane's 32
     // columns, a three-level butterfly over the row's 8 lanes, the update
 #pragma unroll 2
     for (int t = 0; t < N; ++t) {
-        const float* kr = s_qkf + (size_t)(2 * t) * kMaxDim + cb;
-        const float* qr = kr + kMaxDim;
+        const T* kr = s_qk + (size_t)(2 * t) * kMaxDim + cb;
+        const T* qr = kr + kMaxDim;
         float kt[kG8Cols];
         float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < kG8Cols; e += 4) {
-            const float4 kv = *reinterpret_cast<const float4*>(kr + 8 * e);
-            const float4 qv = *reinterpret_cast<const float4*>(qr + 8 * e);
+            const float4 kv = ld4<T>(kr, 8 * e);
+            const float4 qv = ld4<T>(qr, 8 * e);
             kt[e] = kv.x;
             kt[e + 1] = kv.y;
             kt[e + 2] = kv.z;
@@ -659,7 +647,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
     const int vecs = rowb / 16;
 #pragma unroll 1
     for (int t = blockIdx.y; t < N; t += gridDim.y) {
-        const uint4* src = reinterpret_cast<const uint4*>(s_qkraw + (size_t)(2 * t) * kMaxDim);
+        const uint4* src = reinterpret_cast<const uint4*>(s_qk + (size_t)(2 * t) * kMaxDim);
         uint4* dst = reinterpret_cast<uint4*>(key_out + ((size_t)bh * N + t) * kMaxDim);
 #pragma unroll 1
         for (int i = tid; i < vecs; i += kWarps * 32) dst[i] = src[i];
