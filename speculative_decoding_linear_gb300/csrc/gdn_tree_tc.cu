@@ -1,4 +1,6 @@
-// gdn_tree_tc.cu -- tensor-core (tcgen05) prologue and contraction of the tree verifier.
+// gdn_tree_tc.cu -- tensor-core (tcgen05) tree verifier: for d_v = 256 one
+// kernel per call (tree_fused_tc_kernel, further below), otherwise a prologue
+// kernel and a contraction kernel over 128-row tiles (described here).
 //
 // Same mathematics as the SIMT contraction in gdn_tree.cu (review of SpecLA,
 // pith.science 7ERME3HB, "Core claim": O = Qhat S0^T - Attn (W S0^T) + Attn U):
