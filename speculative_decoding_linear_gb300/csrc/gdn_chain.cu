@@ -404,6 +404,28 @@ cudaError_t launch_chain_t(const VerifyArgs& a, cudaStream_t s) {
 // lane's 32 columns are interleaved with its group's (4 at a time) so that the
 // shared-memory reads of a group cover contiguous bytes; the four row groups of
 // a warp read the same k/q words (broadcast), widened to fp32 in registers.
+// Packed fp32 pairs (two independent round-to-nearest operations per instruction,
+// the same results as two fmaf / products).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
 constexpr int kG8Rows = 16;            // state rows per CTA
 constexpr int kG8Cols = 32;            // state columns per lane (8 groups of 4)
 
@@ -465,15 +487,13 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
     __syncthreads();
 
     // 1. this lane's 32 columns of its state row
-    float S[kG8Cols];
+    float2 S[kG8Cols / 2];                     // column pairs, for the packed fp32 arithmetic
     const float* srow = a.S + ((size_t)bh * dv + v0 + r) * kMaxDim + cb;
 #pragma unroll
     for (int e = 0; e < kG8Cols; e += 4) {
         const float4 x = row_on ? *reinterpret_cast<const float4*>(srow + 8 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        S[e] = x.x;
-        S[e + 1] = x.y;
-        S[e + 2] = x.z;
-        S[e + 3] = x.w;
+        S[e / 2] = make_float2(x.x, x.y);
+        S[e / 2 + 1] = make_float2(x.z, x.w);
     }
     if (fused) {
         if (warp == 0) {
@@ -501,18 +521,18 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
         __syncthreads();
         // 2. commit in registers (same arithmetic order as gdn_commit)
         const float ega = *s_ega;
+        const float2 ega2 = make_float2(ega, ega);
 #pragma unroll
-        for (int e = 0; e < kG8Cols; ++e) S[e] *= ega;
+        for (int i = 0; i < kG8Cols / 2; ++i) S[i] = fmul2(S[i], ega2);
 #pragma unroll 1
         for (int i = 0; i < nL; ++i) {
             const float w = s_cd[i * kRows + r];
+            const float2 w2 = make_float2(w, w);
 #pragma unroll
             for (int e = 0; e < kG8Cols; e += 4) {
                 const float4 kv = ld4<T>(s_key, (size_t)i * kMaxDim + cb + 8 * e);
-                S[e] = fmaf(w, kv.x, S[e]);
-                S[e + 1] = fmaf(w, kv.y, S[e + 1]);
-                S[e + 2] = fmaf(w, kv.z, S[e + 2]);
-                S[e + 3] = fmaf(w, kv.w, S[e + 3]);
+                S[e / 2] = ffma2(w2, make_float2(kv.x, kv.y), S[e / 2]);
+                S[e / 2 + 1] = ffma2(w2, make_float2(kv.z, kv.w), S[e / 2 + 1]);
             }
         }
     }
@@ -567,7 +587,7 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
         float* wrow = a.S + ((size_t)bh * dv + v0 + r) * kMaxDim + cb;
 #pragma unroll
         for (int e = 0; e < kG8Cols; e += 4)
-            *reinterpret_cast<float4*>(wrow + 8 * e) = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
+            *reinterpret_cast<float4*>(wrow + 8 * e) = make_float4(S[e / 2].x, S[e / 2].y, S[e / 2 + 1].x, S[e / 2 + 1].y);
     }
     if (one_pass) {
         if (tid < N * kRows) st_elem<T>(s_v, tid, v_reg);
@@ -597,24 +617,26 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
     for (int t = 0; t < N; ++t) {
         const T* kr = s_qk + (size_t)(2 * t) * kMaxDim + cb;
         const T* qr = kr + kMaxDim;
-        float kt[kG8Cols];
-        float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 kt[kG8Cols / 2];
+        float2 xa = make_float2(0.f, 0.f), xb = xa, ya = xa, yb = xa, za = xa, zb = xa;
 #pragma unroll
         for (int e = 0; e < kG8Cols; e += 4) {
             const float4 kv = ld4<T>(kr, 8 * e);
             const float4 qv = ld4<T>(qr, 8 * e);
-            kt[e] = kv.x;
-            kt[e + 1] = kv.y;
-            kt[e + 2] = kv.z;
-            kt[e + 3] = kv.w;
-            const int p = (e >> 2) & 3;
-            x[p] = fmaf(S[e], kv.x, fmaf(S[e + 1], kv.y, fmaf(S[e + 2], kv.z, fmaf(S[e + 3], kv.w, x[p]))));
-            y[p] = fmaf(S[e], qv.x, fmaf(S[e + 1], qv.y, fmaf(S[e + 2], qv.z, fmaf(S[e + 3], qv.w, y[p]))));
-            z[p] = fmaf(kv.x, qv.x, fmaf(kv.y, qv.y, fmaf(kv.z, qv.z, fmaf(kv.w, qv.w, z[p]))));
+            const float2 k01 = make_float2(kv.x, kv.y), k23 = make_float2(kv.z, kv.w);
+            const float2 q01 = make_float2(qv.x, qv.y), q23 = make_float2(qv.z, qv.w);
+            kt[e / 2] = k01;
+            kt[e / 2 + 1] = k23;
+            xa = ffma2(S[e / 2], k01, xa);
+            xb = ffma2(S[e / 2 + 1], k23, xb);
+            ya = ffma2(S[e / 2], q01, ya);
+            yb = ffma2(S[e / 2 + 1], q23, yb);
+            za = ffma2(k01, q01, za);
+            zb = ffma2(k23, q23, zb);
         }
-        float sk = (x[0] + x[1]) + (x[2] + x[3]);
-        float sq = (y[0] + y[1]) + (y[2] + y[3]);
-        float kq = (z[0] + z[1]) + (z[2] + z[3]);
+        float sk = (xa.x + xa.y) + (xb.x + xb.y);
+        float sq = (ya.x + ya.y) + (yb.x + yb.y);
+        float kq = (za.x + za.y) + (zb.x + zb.y);
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) {
             sk += __shfl_xor_sync(0xffffffffu, sk, o);
@@ -629,8 +651,9 @@ __global__ void __launch_bounds__(kWarps * 32) chain_g8_kernel(VerifyArgs a) {
             s_o[t * kRows + r] = fmaf(al, sq, dlt * kq);
             s_d[t * kRows + r] = dlt;
         }
+        const float2 al2 = make_float2(al, al), dlt2 = make_float2(dlt, dlt);
 #pragma unroll
-        for (int e = 0; e < kG8Cols; ++e) S[e] = fmaf(al, S[e], dlt * kt[e]);
+        for (int i = 0; i < kG8Cols / 2; ++i) S[i] = ffma2(al2, S[i], fmul2(dlt2, kt[i]));
     }
     __syncthreads();
 
