@@ -816,34 +816,37 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return p;
 }
 
-// Rows rbase + 32 j (j = 0..7) of a 256-row state slab: j < 4 lie in tile 0,
-// j >= 4 in tile 1.
+// Rows rbase + 32 j (j = 0 .. J-1, J = 4 per 128-row tile) of a CTA's state
+// slab: j < 4 lie in its tile 0, j >= 4 in its tile 1.
+template <int J>
 __device__ __forceinline__ void f_load_slab(float4 (&x)[8], const float* S, size_t srow0, int rbase, int col,
                                             uint64_t pol) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < J; ++j) {
         const float* p = S + srow0 + (size_t)(rbase + 32 * j) * kDk + col;
         asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;\n"
                      : "=f"(x[j].x), "=f"(x[j].y), "=f"(x[j].z), "=f"(x[j].w)
                      : "l"(p), "l"(pol));
     }
 }
+template <int J>
 __device__ __forceinline__ void f_store_slab(const float4 (&x)[8], float* S, size_t srow0, int rbase, int col,
                                              uint64_t pol) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < J; ++j) {
         float* p = S + srow0 + (size_t)(rbase + 32 * j) * kDk + col;
         asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;\n" ::"l"(p), "f"(x[j].x),
                      "f"(x[j].y), "f"(x[j].z), "f"(x[j].w), "l"(pol)
                      : "memory");
     }
 }
-// Same arithmetic order per element as commit_slab (and gdn_commit).
-template <typename KT>
+// Same arithmetic order per element as commit_slab (and gdn_commit).  s_cd rows
+// are the (sequence, head)'s 256 state rows; cd_row0 is this thread's first.
+template <int J, typename KT>
 __device__ __forceinline__ void f_commit_slab(float4 (&x)[8], float ega, int L, const float* s_cd,
-                                              const KT* s_key, int rbase, int col) {
+                                              const KT* s_key, int cd_row0, int col) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < J; ++j) {
         x[j].x *= ega;
         x[j].y *= ega;
         x[j].z *= ega;
@@ -851,9 +854,9 @@ __device__ __forceinline__ void f_commit_slab(float4 (&x)[8], float ega, int L, 
     }
     for (int i = 0; i < L; ++i) {
         const float4 kq = ld4<KT>(s_key, (size_t)i * kDk + col);
-        const float* cdi = s_cd + i * kFRows + rbase;
+        const float* cdi = s_cd + i * kFRows + cd_row0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < J; ++j) {
             const float w = cdi[32 * j];
             x[j].x = fmaf(w, kq.x, x[j].x);
             x[j].y = fmaf(w, kq.y, x[j].y);
@@ -863,9 +866,10 @@ __device__ __forceinline__ void f_commit_slab(float4 (&x)[8], float ega, int L, 
     }
 }
 // hi/lo split into one A stage ([tile 0 hi, tile 0 lo, tile 1 hi, tile 1 lo]).
+template <int J>
 __device__ __forceinline__ void f_convert_slab(const float4 (&x)[8], unsigned char* stage, int rbase, int c4) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < J; ++j) {
         unsigned char* ahi = stage + (j >> 2) * 2 * kBufBytes;
         unsigned char* alo = ahi + kBufBytes;
         const int r = rbase + 32 * (j & 3);
@@ -884,13 +888,13 @@ __device__ __forceinline__ void f_convert_slab(const float4 (&x)[8], unsigned ch
     }
 }
 
-// Y of both tiles and the Gram for one slab (one thread issues).  Not inlined:
+// Y of the CTA's kT tiles and the Gram for one slab (one thread issues).  Not inlined:
 // the fused kernel runs each of its code paths once per CTA, so its size in
 // the instruction cache matters more than a call.
-template <bool kSplit>
+template <bool kSplit, int kT>
 __device__ __noinline__ void f_issue_slab(uint32_t tmem, uint32_t a_stage, uint32_t bsm, bool first) {
     issue_slab_mma<kSplit>(tmem, a_stage, bsm, first);
-    issue_slab_mma<kSplit>(tmem + 128, a_stage + 2 * kBufBytes, bsm, first);
+    if (kT == 2) issue_slab_mma<kSplit>(tmem + 128, a_stage + 2 * kBufBytes, bsm, first);
 #pragma unroll
     for (int kk = 0; kk < kSlab / 16; ++kk) {
         const uint32_t q_s = bsm + kk * 32;
@@ -904,7 +908,11 @@ __device__ __noinline__ void f_issue_slab(uint32_t tmem, uint32_t a_stage, uint3
     }
 }
 
-template <bool kSplit>
+// kT = 2: the CTA owns all 256 state rows of its (sequence, head); kT = 1: rows
+// 128 y .. 128 y + 127 (y = blockIdx.y), the N x N prologue repeated by both CTAs
+// of a (sequence, head) -- for small batches, where the two CTAs still fit in one
+// wave and each then carries half the MMAs, R rows and stores.
+template <bool kSplit, int kT>
 __global__ void __launch_bounds__(kFThreads, 1)
     tree_fused_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmQl, const __grid_constant__ CUtensorMap tmKl,
@@ -919,6 +927,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const FusedLayout Ly(N, fused ? a.commit.Lmax : 0, kSplit);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int row0 = kT == 1 ? 128 * (int)blockIdx.y : 0;    // the CTA's first state row
+    const bool lead = row0 == 0;                            // writes the per-(b, h) factor parts
+    constexpr int kJ = 4 * kT;                              // state rows per thread and slab
 
     float* s_cd = reinterpret_cast<float*>(base + Ly.cd);
     KT* s_key = reinterpret_cast<KT*>(base + Ly.key);
@@ -960,10 +971,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
     // ---- 1. before the wait: the state stream (it only reads the state and the
     // previous factors, which the previous call on the stream does not touch) ----
-    const size_t srow0 = (size_t)bh * kFRows * kDk;
+    const size_t srow0 = ((size_t)bh * kFRows + row0) * kDk;
     const int c4 = tid & 15;          // column quad within a slab
     const int rbase = tid >> 4;       // rows rbase + 32 j
-    if (tid < 16) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * 16 * kDk, 16 * kDk * 4);
+    if (tid < 8 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * 16 * kDk, 16 * kDk * 4);
     if (tid < N) {                    // this call's inputs into L2; read only after the wait
         const size_t rt = ((size_t)b * N + tid) * H + h;
         if (kSplit) {
@@ -979,7 +990,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
     float4 cur[8], nxt[8];
-    f_load_slab(cur, a.S, srow0, rbase, 4 * c4, pol_first);
+    f_load_slab<kJ>(cur, a.S, srow0, rbase, 4 * c4, pol_first);
     if (fused) {
         if (warp == 2) {
             const int L = commit_path_setup(a.commit, b, h, H, s_nodes, s_coef, s_ega);
@@ -1012,12 +1023,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const float ega = *s_ega;
 #pragma unroll 1
         for (int sl = 0; sl < kSlabs; ++sl) {
-            if (sl + 1 < kSlabs) f_load_slab(nxt, a.S, srow0, rbase, (sl + 1) * kSlab + 4 * c4, pol_first);
+            if (sl + 1 < kSlabs) f_load_slab<kJ>(nxt, a.S, srow0, rbase, (sl + 1) * kSlab + 4 * c4, pol_first);
             if (fused) {
-                f_commit_slab(cur, ega, L, s_cd, s_key, rbase, sl * kSlab + 4 * c4);
-                f_store_slab(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, sl < 2 ? pol_first : pol_last);
+                f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, sl * kSlab + 4 * c4);
+                f_store_slab<kJ>(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, sl < 2 ? pol_first : pol_last);
             }
-            if (sl < 2) f_convert_slab(cur, base + sl * kFAStage, rbase, c4);
+            if (sl < 2) f_convert_slab<kJ>(cur, base + sl * kFAStage, rbase, c4);
 #pragma unroll
             for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
         }
@@ -1030,8 +1041,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     griddep_launch();
     if (ok) {
         // this thread's part of the committed slabs 2 and 3, written above (L2)
-        f_load_slab(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
-        f_load_slab(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
+        f_load_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
+        f_load_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
         if (warp == kFIssuerWarp && lane == 0) {
             issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(0), 0, h, b * N, bars);
             if (nB == 2) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
@@ -1061,7 +1072,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         for (int sl = 0; sl < kSlabs; ++sl) {
             if (sl >= 2) {
                 ok = ok && mbar_wait(bars + 32 + 8 * (sl - 2), 0, a.err);
-                if (ok) f_convert_slab(cur, base + (sl & 1) * kFAStage, rbase, c4);
+                if (ok) f_convert_slab<kJ>(cur, base + (sl & 1) * kFAStage, rbase, c4);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
                 fence_proxy_async_smem();
@@ -1072,7 +1083,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     bool l = mbar_wait(bars + 8 * sl, 0, a.err);
                     if (l) {
                         tc_fence_after();
-                        f_issue_slab<kSplit>(tmem, (sl & 1) ? stage1 : stage0, bbuf(sl), sl == 0);
+                        f_issue_slab<kSplit, kT>(tmem, (sl & 1) ? stage1 : stage0, bbuf(sl), sl == 0);
                         mma_commit(bars + 32 + 8 * sl);
                     }
                     const int sn = sl + nB;                             // next copy into bbuf(sl)
@@ -1098,8 +1109,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
         } else if (tid < N) {
             prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
             seg[tid] = expf(sg[tid]);
-            a.f.g[(size_t)bh * N + tid] = sg[tid];
-            if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
+            if (lead) {
+                a.f.g[(size_t)bh * N + tid] = sg[tid];
+                if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
+            }
         }
         if (ok) ok = mbar_wait(bars + 56, 0, a.err);              // Y and the Gram complete
         ok = __syncthreads_and(ok) && !bad;
@@ -1137,14 +1150,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 constexpr int kVec = 16 / (int)sizeof(KT);
                 const KT* kin = static_cast<const KT*>(a.k);
                 KT* kout = static_cast<KT*>(a.f.key) + (size_t)bh * N * kDk;
-                for (int item = tid - 256; item < N * (kDk / kVec); item += kFThreads - 256) {
+                for (int item = tid - 256; lead && item < N * (kDk / kVec); item += kFThreads - 256) {
                     const int t = item / (kDk / kVec), c = item % (kDk / kVec);
                     *reinterpret_cast<uint4*>(kout + (size_t)t * kDk + c * kVec) =
                         *reinterpret_cast<const uint4*>(kin + (((size_t)b * N + t) * H + h) * kDk + c * kVec);
                 }
                 // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) of tile u as bf16
-                // hi + lo rows of the second MMA's A operand (row v, 64 columns t)
-                const int u = (warp - 8) >> 2;
+                // hi + lo rows of the second MMA's A operand (row v, 64 columns t).  kT = 2:
+                // warps 8-11 tile 0, 12-15 tile 1; kT = 1: they split the nodes of tile 0.
+                const int u = kT == 2 ? (warp - 8) >> 2 : 0;
+                const int tbeg = kT == 2 ? 0 : 32 * ((warp - 8) >> 2), tend = kT == 2 ? kNodeRows : tbeg + 32;
                 const int v = 32 * (warp & 3) + lane;               // row within the tile = TMEM lane
                 const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * u + kNodeRows;
                 unsigned char* rhi = base + Ly.R + u * 2 * kBufBytes;
@@ -1174,9 +1189,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 };
                 if constexpr (kSplit) {
                     // fp32 v from global memory, a 32-node chunk's loads in flight together
-                    const KT* vin = static_cast<const KT*>(a.v) + ((size_t)b * N * H + h) * kFRows + 128 * u + v;
+                    const KT* vin =
+                        static_cast<const KT*>(a.v) + ((size_t)b * N * H + h) * kFRows + row0 + 128 * u + v;
 #pragma unroll 1
-                    for (int c = 0; c < kNodeRows / 32; ++c) {
+                    for (int c = tbeg / 32; c < tend / 32; ++c) {
                         float vt[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
@@ -1192,10 +1208,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     }
                 } else {
                     // bf16 v rows staged in shared memory
-                    const KT* vsm = reinterpret_cast<const KT*>(base + Ly.vs) + 128 * u + v;
+                    const KT* vsm = reinterpret_cast<const KT*>(base + Ly.vs) + row0 + 128 * u + v;
                     const bool vok = mbar_wait(bar_v, 0, a.err);
 #pragma unroll 1
-                    for (int t0 = 0; t0 < kNodeRows; t0 += 8) {
+                    for (int t0 = tbeg; t0 < tend; t0 += 8) {
                         float yk[8], v8[8];
                         tmem_ld8(t_lane + t0, yk);
 #pragma unroll
@@ -1215,7 +1231,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             tc_fence_after();
             const uint32_t op_s = base_s + Ly.op;
 #pragma unroll 1
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < kT; ++u) {
                 const uint32_t r_s = base_s + Ly.R + u * 2 * kBufBytes;
 #pragma unroll
                 for (int kk = 0; kk < kNodeRows / 16; ++kk) {
@@ -1234,23 +1250,25 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (ok) ok = mbar_wait(bar_e, 0, a.err);
         tc_fence_after();
         if (ok) {
-            // warps 0-3 / 8-11: Delta of tile 0 / 1; warps 4-7 / 12-15: O of tile 0 / 1
-            const int u = warp >> 3;
-            const int row = 128 * u + 32 * (warp & 3) + lane;
+            // kT = 2: warps 0-3 / 8-11 Delta of tile 0 / 1, warps 4-7 / 12-15 O of tile 0 / 1;
+            // kT = 1: the same split of tile 0 by nodes 0..31 (warps 0-7) and 32..63 (8-15)
+            const int u = kT == 2 ? warp >> 3 : 0;
+            const int tbeg = kT == 2 ? 0 : 32 * (warp >> 3), tend = kT == 2 ? N : min(N, tbeg + 32);
+            const int row = row0 + 128 * u + 32 * (warp & 3) + lane;
             const bool is_o = ((warp >> 2) & 1) != 0;
             const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
             const uint32_t src = t_lane + 256 + 128 * u + (is_o ? kNodeRows : 0);   // T R or P R
             float* dst = is_o ? a.out + ((size_t)b * N * H + h) * kFRows + row : a.f.delta + (size_t)bh * N * kFRows + row;
             const size_t dstep = is_o ? (size_t)H * kFRows : (size_t)kFRows;
 #pragma unroll 1
-            for (int t0 = 0; t0 < N; t0 += 8) {
+            for (int t0 = tbeg; t0 < tend; t0 += 8) {
                 float x[8], yq[8];
                 tmem_ld8(src + t0, x);
                 if (is_o) tmem_ld8(t_lane + 128 * u + t0, yq);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int t = t0 + i;
-                    if (t < N) dst[(size_t)t * dstep] = is_o ? fmaf(seg[t], yq[i], x[i]) : x[i];
+                    if (t < tend) dst[(size_t)t * dstep] = is_o ? fmaf(seg[t], yq[i], x[i]) : x[i];
                 }
             }
         }
@@ -1342,7 +1360,7 @@ bool fused_eligible(const VerifyArgs& a, bool split) {
     return L.total <= kFSmemLimit;
 }
 
-template <bool kSplit>
+template <bool kSplit, int kT>
 cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s) {
     static bool attr[64];
     CUtensorMap tq, tk, tql, tkl;
@@ -1357,10 +1375,10 @@ cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s) {
         tkl = tk;
     }
     const FusedLayout L(a.N, a.commit.path ? a.commit.Lmax : 0, kSplit);
-    cudaError_t e = ensure_smem(tree_fused_tc_kernel<kSplit>, L.total, attr);
+    cudaError_t e = ensure_smem(tree_fused_tc_kernel<kSplit, kT>, L.total, attr);
     if (e != cudaSuccess) return e;
-    return launch_kernel(tree_fused_tc_kernel<kSplit>, dim3(a.B * a.H), dim3(kFThreads), L.total, s, a.overlap, tq,
-                         tk, tql, tkl, a);
+    return launch_kernel(tree_fused_tc_kernel<kSplit, kT>, dim3(a.B * a.H, 2 / kT), dim3(kFThreads), L.total, s,
+                         a.overlap, tq, tk, tql, tkl, a);
 }
 
 // bf16 q/k (or fp32 q/k with their bf16 hi/lo terms in `split`) with the
@@ -1368,8 +1386,16 @@ cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s) {
 // and the contraction kernel.  See launch_tree_verify.
 cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s) {
     const bool split = a.split[0] != nullptr;
-    if (fused_eligible(a, split))
-        return split ? launch_tree_fused_impl<true>(a, s) : launch_tree_fused_impl<false>(a, s);
+    if (fused_eligible(a, split)) {
+        // one 128-row tile per CTA while two CTAs per (sequence, head) fit in one wave of SMs
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        if (2LL * a.B * a.H <= sms)
+            return split ? launch_tree_fused_impl<true, 1>(a, s) : launch_tree_fused_impl<false, 1>(a, s);
+        return split ? launch_tree_fused_impl<true, 2>(a, s) : launch_tree_fused_impl<false, 2>(a, s);
+    }
     return split ? launch_tree_tc_impl<true>(a, s) : launch_tree_tc_impl<false>(a, s);
 }
 
