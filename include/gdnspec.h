@@ -375,10 +375,11 @@ int gdn_linear_tree_verify(const void* q, const void* k, const void* v, int dtyp
  * else.  This hides launch and prologue latency in a
  * layer-major sweep ("Pith review of SpecLA", "What carries the argument":
  * layer-major verification keeps per-layer state streaming back to back).
- * Contract while on: the state S, S0 and factor buffers of a call must not be
- * read or written by the previous call on the stream (whose kernels may still
- * run) -- e.g. the calls of a sweep visit different layers, each with its own
- * state and factors.
+ * Contract while on: the state S, S0, the accepted path and the factor
+ * buffers of a call must not be read or written by the previous call on the
+ * stream (whose kernels may still run) -- e.g. the calls of a sweep visit
+ * different layers, each with its own state and factors, and the accepted
+ * paths are written before the sweep starts.
  */
 int gdn_set_launch_overlap(int enable);
 

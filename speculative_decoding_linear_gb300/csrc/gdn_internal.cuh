@@ -169,14 +169,25 @@ __device__ __forceinline__ float warp_sum(float x) {
 //   s_nodes[i]  accepted node i (root first), i < L
 //   s_coef[i]   e^{g_a - g_{node i}}, a = last accepted node
 //   *s_ega      e^{g_a} (1 when L == 0)
-// Returns L (0..Lmax) or -1 if the path is invalid.
+// Returns L (0..Lmax) or -1 if the path is invalid.  The path row, the previous
+// tree's parent row and head h's g row (N <= 64 entries each) are read in one
+// round trip and looked up per accepted node with shuffles, so the setup costs
+// one global-memory latency rather than three dependent ones.
 __device__ inline int commit_path_setup(const CommitSrc& c, int b, int h, int H, int* s_nodes,
                                         float* s_coef, float* s_ega) {
     const int lane = threadIdx.x & 31;
     const int32_t* row = c.path + (size_t)b * c.Lmax;
-    int n[2], prev[2];
-    n[0] = lane < c.Lmax ? row[lane] : -1;
-    n[1] = lane + 32 < c.Lmax ? row[lane + 32] : -1;
+    const int32_t* par = c.parent + (size_t)b * c.N;
+    const float* g = c.g + (size_t)(b * H + h) * c.N;
+    int n[2], p[2], prev[2];
+    float gr[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const int i = lane + 32 * s;
+        n[s] = i < c.Lmax ? row[i] : -1;
+        p[s] = i < c.N ? par[i] : -1;
+        gr[s] = i < c.N ? g[i] : 0.f;
+    }
     const unsigned nn0 = __ballot_sync(0xffffffffu, n[0] >= 0);
     const unsigned nn1 = __ballot_sync(0xffffffffu, n[1] >= 0);
     const unsigned long long nn = (unsigned long long)nn0 | ((unsigned long long)nn1 << 32);
@@ -190,23 +201,28 @@ __device__ inline int commit_path_setup(const CommitSrc& c, int b, int h, int H,
         prev[0] = -1;
         prev[1] = carry;
     }
-    const int32_t* par = c.parent + (size_t)b * c.N;
+    // parent and g of this lane's path entries: entry n of a row sits in lane n & 31 of half n >> 5
+    int pn[2];
+    float gn[2];
+#pragma unroll
     for (int s = 0; s < 2; ++s) {
+        const int src = n[s] & 31;
+        const int p0 = __shfl_sync(0xffffffffu, p[0], src), p1 = __shfl_sync(0xffffffffu, p[1], src);
+        const float g0 = __shfl_sync(0xffffffffu, gr[0], src), g1 = __shfl_sync(0xffffffffu, gr[1], src);
+        pn[s] = n[s] < 32 ? p0 : p1;
+        gn[s] = n[s] < 32 ? g0 : g1;
         const int i = lane + 32 * s;
-        if (i < L && !bad && n[s] >= 0 && n[s] < c.N && par[n[s]] != prev[s]) bad = true;
+        if (i < L && !bad && n[s] >= 0 && n[s] < c.N && pn[s] != prev[s]) bad = true;
     }
     if (__any_sync(0xffffffffu, bad)) return -1;
-    const float* g = c.g + (size_t)(b * H + h) * c.N;
     float ga = 0.f;
-    if (L > 0) {
-        const int a_node = __shfl_sync(0xffffffffu, L - 1 < 32 ? n[0] : n[1], (L - 1) & 31);
-        ga = g[a_node];
-    }
+    if (L > 0) ga = __shfl_sync(0xffffffffu, L - 1 < 32 ? gn[0] : gn[1], (L - 1) & 31);
+#pragma unroll
     for (int s = 0; s < 2; ++s) {
         const int i = lane + 32 * s;
         if (i < L) {
             s_nodes[i] = n[s];
-            s_coef[i] = expf(ga - g[n[s]]);
+            s_coef[i] = expf(ga - gn[s]);
         }
     }
     if (lane == 0) *s_ega = L > 0 ? expf(ga) : 1.f;

@@ -949,6 +949,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t bars = base_s + Ly.bars;
     const uint32_t bar_e = bars + 64;                         // bars + 8 s: slab s copied; + 32 + 8 s: its MMAs done
     const uint32_t bar_v = bars + 72;                         // v rows landed (bf16 inputs)
+    const uint32_t bar_c = bars + 80;                         // the commit's key and delta rows landed
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
     int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 4);    // path length, or -1: skip the CTA
     float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 8);
@@ -956,8 +957,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int nB = Ly.nB;
     auto bbuf = [&](int s) { return bbase + (nB == 2 ? (uint32_t)((s & 1) * Ly.bsz) : 0u); };
 
+    if (fused && warp == 2 && lane < 6) {   // the pending commit's path, parent and g rows, first of all
+        const int r = lane >> 1, half = lane & 1;
+        const char* row = r == 0   ? reinterpret_cast<const char*>(a.commit.path + (size_t)b * a.commit.Lmax)
+                          : r == 1 ? reinterpret_cast<const char*>(a.commit.parent + (size_t)b * a.commit.N)
+                                   : reinterpret_cast<const char*>(a.commit.g + (size_t)bh * a.commit.N);
+        const int bytes = 4 * (r == 0 ? a.commit.Lmax : a.commit.N);
+        if (128 * half < bytes) prefetch_line_l2(row + 128 * half);
+    }
     if (tid == 0) {
-        for (int i = 0; i < 10; ++i) mbar_init(bars + 8 * i, 1);
+        for (int i = 0; i < 11; ++i) mbar_init(bars + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         fence_proxy_async_smem();
         *s_flag = 0;
@@ -974,6 +983,27 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const size_t srow0 = ((size_t)bh * kFRows + row0) * kDk;
     const int c4 = tid & 15;          // column quad within a slab
     const int rbase = tid >> 4;       // rows rbase + 32 j
+    if (fused && warp == 2) {
+        // the path, then its key and delta rows by bulk copies issued from this warp
+        const int L = commit_path_setup(a.commit, b, h, H, s_nodes, s_coef, s_ega);
+        if (lane == 0) {
+            *s_flag = L;
+            if (L < 0) set_error(a.err, GDN_ERR_PATH);
+        }
+        if (L > 0) {
+            const KT* key_bh = static_cast<const KT*>(a.commit.key) + (size_t)bh * a.commit.N * kDk;
+            const float* dl = a.commit.delta + (size_t)bh * a.commit.N * kFRows;
+            constexpr uint32_t kKeyBytes = kDk * sizeof(KT), kCdBytes = kFRows * 4;
+            if (lane == 0) mbar_expect_tx(bar_c, (uint32_t)L * (kKeyBytes + kCdBytes));
+            __syncwarp();
+            for (int j = lane; j < L; j += 32) {     // s_nodes[j] was written by this lane
+                const int nd = s_nodes[j];
+                bulk_copy_g2s(smem_u32(s_key) + (uint32_t)j * kKeyBytes, key_bh + (size_t)nd * kDk, kKeyBytes,
+                              bar_c);
+                bulk_copy_g2s(smem_u32(s_cd + (size_t)j * kFRows), dl + (size_t)nd * kFRows, kCdBytes, bar_c);
+            }
+        }
+    }
     if (tid < 8 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * 16 * kDk, 16 * kDk * 4);
     if (tid < N) {                    // this call's inputs into L2; read only after the wait
         const size_t rt = ((size_t)b * N + tid) * H + h;
@@ -989,41 +1019,30 @@ __global__ void __launch_bounds__(kFThreads, 1)
         prefetch_line_l2(a.parent + (size_t)b * N + tid);
     }
     const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
-    float4 cur[8], nxt[8];
+    float4 cur[8], nxt[8];             // slabs 0 and 1 in flight during the commit setup
     f_load_slab<kJ>(cur, a.S, srow0, rbase, 4 * c4, pol_first);
+    f_load_slab<kJ>(nxt, a.S, srow0, rbase, kSlab + 4 * c4, pol_first);
+    bool landed = true;
     if (fused) {
-        if (warp == 2) {
-            const int L = commit_path_setup(a.commit, b, h, H, s_nodes, s_coef, s_ega);
-            if (lane == 0) {
-                *s_flag = L;
-                if (L < 0) set_error(a.err, GDN_ERR_PATH);
-            }
-        }
         __syncthreads();
         const int L = *s_flag;
         if (L > 0) {
-            const KT* key_bh = static_cast<const KT*>(a.commit.key) + (size_t)bh * a.commit.N * kDk;
-            for (int i = 0; i < L; ++i)
-                cp_async_block(s_key + (size_t)i * kDk, key_bh + (size_t)s_nodes[i] * kDk, kDk * (int)sizeof(KT),
-                               tid, kFThreads);
-            const float* dl = a.commit.delta + (size_t)bh * a.commit.N * kFRows;
-            for (int i = tid; i < L * kFRows; i += kFThreads) {
-                const int j = i / kFRows, r = i % kFRows;
-                s_cd[i] = s_coef[j] * dl[(size_t)s_nodes[j] * kFRows + r];
-            }
-            cp_async_wait_all();
+            landed = mbar_wait(bar_c, 0, a.err);
+            if (landed)
+                for (int i = tid; i < L * kFRows; i += kFThreads) s_cd[i] *= s_coef[i / kFRows];
         }
     }
-    __syncthreads();
+    landed = __syncthreads_and(landed);
     const int L = fused ? *s_flag : 0;
-    bool ok = L >= 0;
+    bool ok = L >= 0 && landed;
     if (ok) {
         // slab by slab, the next one's loads in flight: commit, write back; slabs 0
         // and 1 into the operand stages (2 and 3 are read back after the wait)
         const float ega = *s_ega;
 #pragma unroll 1
         for (int sl = 0; sl < kSlabs; ++sl) {
-            if (sl + 1 < kSlabs) f_load_slab<kJ>(nxt, a.S, srow0, rbase, (sl + 1) * kSlab + 4 * c4, pol_first);
+            if (sl > 0 && sl + 1 < kSlabs)
+                f_load_slab<kJ>(nxt, a.S, srow0, rbase, (sl + 1) * kSlab + 4 * c4, pol_first);
             if (fused) {
                 f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, sl * kSlab + 4 * c4);
                 f_store_slab<kJ>(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, sl < 2 ? pol_first : pol_last);
@@ -1275,7 +1294,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
 
     // ---- teardown: the v copies have landed; TMEM is always released ----
-    if (!kSplit && L >= 0 && tid == 0) mbar_wait(bar_v, 0, a.err);
+    if (!kSplit && L >= 0 && landed && tid == 0) mbar_wait(bar_v, 0, a.err);
+    if (!landed && tid == 0) mbar_wait(bar_c, 0, a.err);    // the commit copies, before the CTA's memory goes
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
