@@ -1004,20 +1004,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
         }
     }
-    if (tid < 8 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * 16 * kDk, 16 * kDk * 4);
-    if (tid < N) {                    // this call's inputs into L2; read only after the wait
-        const size_t rt = ((size_t)b * N + tid) * H + h;
-        if (kSplit) {
-            for (int i = 0; i < 4; ++i) prefetch_l2(static_cast<const __nv_bfloat16*>(a.split[i]) + rt * kDk, kDk * 2);
-        } else {
-            prefetch_l2(static_cast<const KT*>(a.q) + rt * kDk, kDk * (int)sizeof(KT));
-        }
-        prefetch_l2(static_cast<const KT*>(a.k) + rt * kDk, kDk * (int)sizeof(KT));
-        prefetch_l2(static_cast<const KT*>(a.v) + rt * kFRows, kFRows * (int)sizeof(KT));
-        prefetch_line_l2(a.alpha + rt);
-        prefetch_line_l2(a.beta + rt);
-        prefetch_line_l2(a.parent + (size_t)b * N + tid);
-    }
     const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
     float4 cur[8], nxt[8];             // slabs 0 and 1 in flight during the commit setup
     f_load_slab<kJ>(cur, a.S, srow0, rbase, 4 * c4, pol_first);
@@ -1035,6 +1021,22 @@ __global__ void __launch_bounds__(kFThreads, 1)
     landed = __syncthreads_and(landed);
     const int L = fused ? *s_flag : 0;
     bool ok = L >= 0 && landed;
+    // slabs 2 and 3 and this call's inputs into L2 only now: requests issued
+    // earlier queue ahead of the commit setup's loads and delay the stream
+    if (tid < 128 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * kDk + 2 * kSlab, 2 * kSlab * 4);
+    if (tid < N) {                    // this call's inputs into L2; read only after the wait
+        const size_t rt = ((size_t)b * N + tid) * H + h;
+        if (kSplit) {
+            for (int i = 0; i < 4; ++i) prefetch_l2(static_cast<const __nv_bfloat16*>(a.split[i]) + rt * kDk, kDk * 2);
+        } else {
+            prefetch_l2(static_cast<const KT*>(a.q) + rt * kDk, kDk * (int)sizeof(KT));
+        }
+        prefetch_l2(static_cast<const KT*>(a.k) + rt * kDk, kDk * (int)sizeof(KT));
+        prefetch_l2(static_cast<const KT*>(a.v) + rt * kFRows, kFRows * (int)sizeof(KT));
+        prefetch_line_l2(a.alpha + rt);
+        prefetch_line_l2(a.beta + rt);
+        prefetch_line_l2(a.parent + (size_t)b * N + tid);
+    }
     if (ok) {
         // slab by slab, the next one's loads in flight: commit, write back; slabs 0
         // and 1 into the operand stages (2 and 3 are read back after the wait)
