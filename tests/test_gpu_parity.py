@@ -104,10 +104,15 @@ def test_sibling_isolation_on_gpu():
 # ---------------------------------------------------------------------------
 # chain verify (state-resident serial path)
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("case", ["cfg1", "n1", "n64", "d16_f32", "b3_h5", "n5_f32_d32", "n8_b4", "n7_dv48"])
+@pytest.mark.parametrize("case", ["cfg1", "n1", "n64", "d16_f32", "b3_h5", "n5_f32_d32", "n8_b4", "n7_dv48",
+                                  "n9_d256", "n16_f32_d256"])
 def test_chain_verify(oracle_mod, case):
-    """Chains of up to 8 tokens take the factorized form, longer ones the serial loop."""
-    if case == "cfg1":
+    """Chain verification (the serial token loop: 8-lane rows for d_k = 256, 32-lane rows otherwise)."""
+    if case == "n9_d256":
+        w = wl.custom_workload(2, 9, 4, 256, 256, wl.chain_tree(9), seed=12)
+    elif case == "n16_f32_d256":
+        w = wl.custom_workload(1, 16, 3, 256, 256, wl.chain_tree(16), seed=13, dtype=wl.F32)
+    elif case == "cfg1":
         w = wl.make_workload(1)
     elif case == "n5_f32_d32":
         w = wl.custom_workload(2, 5, 3, 32, 32, wl.chain_tree(5), seed=8, dtype=wl.F32)
