@@ -46,15 +46,17 @@ struct ConvArgs {
 };
 
 // Dynamic shared memory of the conv kernel: this block's channels of every
-// projection row that a window of nodes t0..t1-1 reads.
-inline size_t conv_smem_bytes(int N, int dk, int dv) { return (size_t)N * (dk > dv ? dk : dv) * 4; }
+// projection row that a window of nodes t0..t1-1 reads, then the three committed
+// history rows (rows N .. N + 2, oldest first).
+inline size_t conv_smem_bytes(int N, int dk, int dv) { return (size_t)(N + 3) * (dk > dv ? dk : dv) * 4; }
 
 // Grid (B, 3H + 1): block (b, j < 3H) owns one head's channels of q, k or v
 // (channel blocks never share a channel, so the in-place history commit is
 // race-free); block (b, 3H) computes the gates.
 __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
-    extern __shared__ __align__(16) float s_y[];   // [N][d]
-    __shared__ int s_win[kMaxNodes][3];       // window sources: >= 0 node, -1 - r history row r
+    extern __shared__ __align__(16) float s_y[];   // [N + 3][d]: node rows, then history rows
+    __shared__ int s_win[kMaxNodes][3];       // window rows: node p, or N + r for history row r
+    __shared__ int4 s_off[kMaxNodes];         // element offsets of a node's window rows (oldest first)
     __shared__ int s_need[kMaxNodes];
     __shared__ int s_par[kMaxNodes];
     __shared__ float s_rn[kMaxNodes];
@@ -124,10 +126,11 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
                 if (mine) s_need[p] = 1;
             } else {
                 cur = -1;
-                s_win[tid][i] = -1 - hist;
+                s_win[tid][i] = N + hist;
                 --hist;
             }
         }
+        s_off[tid] = make_int4(s_win[tid][0] * d, s_win[tid][1] * d, s_win[tid][2] * d, tid * d);
     }
     __syncthreads();
     // stage the rows the windows read (this block's d channels of each), 16 bytes per copy
@@ -152,6 +155,8 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
 #pragma unroll
             for (int i = 0; i < 3; ++i) cs[(size_t)i * C] = hrow[i];
         }
+#pragma unroll
+        for (int i = 0; i < 3; ++i) s_y[(N + i) * d + tid] = hrow[i];
         const float4 wv = *reinterpret_cast<const float4*>(a.conv_w + (size_t)c * kConvTaps);
         w[0] = wv.x;
         w[1] = wv.y;
@@ -166,14 +171,10 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     // window's ancestor rows (lower indices) unmodified until they are read; a
     // chunk of 8 nodes loads all its inputs before it stores any output.
     if (act) {
-        const float h0 = hrow[0], h1 = hrow[1], h2 = hrow[2];
+        const float* col = s_y + tid;
         auto conv_at = [&](int t) {
-            const int s0 = s_win[t][0], s1 = s_win[t][1], s2 = s_win[t][2];
-            const float x0 = s0 >= 0 ? s_y[s0 * d + tid] : (s0 == -1 ? h0 : s0 == -2 ? h1 : h2);
-            const float x1 = s1 >= 0 ? s_y[s1 * d + tid] : (s1 == -1 ? h0 : s1 == -2 ? h1 : h2);
-            const float x2 = s2 >= 0 ? s_y[s2 * d + tid] : (s2 == -1 ? h0 : s2 == -2 ? h1 : h2);
-            const float x3 = s_y[t * d + tid];
-            return w[0] * x0 + w[1] * x1 + w[2] * x2 + w[3] * x3;
+            const int4 o = s_off[t];
+            return w[0] * col[o.x] + w[1] * col[o.y] + w[2] * col[o.z] + w[3] * col[o.w];
         };
         int t = a.t1 - 1;
 #pragma unroll 1
@@ -188,10 +189,15 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         for (; t >= a.t0; --t) s_y[t * d + tid] = conv_at(t);
     }
 
+    // Output rows four channels per thread: d / 4 threads per node, npass nodes at a time.
+    const int q4 = tid % (d / 4), tr = tid / (d / 4), npass = kConvThreads / (d / 4);
     if (seg == 2) {
-        if (act) {
-#pragma unroll 4
-            for (int t = a.t0; t < a.t1; ++t) a.v[(((size_t)b * N + t) * H + h) * dv + tid] = s_y[t * d + tid];
+        __syncthreads();
+        if (tr < npass) {
+#pragma unroll 2
+            for (int t = a.t0 + tr; t < a.t1; t += npass)
+                *reinterpret_cast<float4*>(a.v + (((size_t)b * N + t) * H + h) * dv + 4 * q4) =
+                    *reinterpret_cast<const float4*>(s_y + t * d + 4 * q4);
         }
         griddep_launch();
         return;
@@ -210,19 +216,29 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         if (lane == 0) s_rn[t] = 1.f / sqrtf(ss);
     }
     __syncthreads();
-    if (act) {
+    if (tr < npass) {
         float* dst = seg == 0 ? a.q : a.k;
         __nv_bfloat16* dhi = a.qk_split[seg];
         __nv_bfloat16* dlo = a.qk_split[2 + seg];
-#pragma unroll 4
-        for (int t = a.t0; t < a.t1; ++t) {
-            const size_t o = (((size_t)b * N + t) * H + h) * dk + tid;
-            const float y = s_y[t * d + tid] * s_rn[t];
-            dst[o] = y;
-            if (dhi != nullptr) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(y);
-                dhi[o] = hi;
-                dlo[o] = __float2bfloat16_rn(y - __bfloat162float(hi));
+#pragma unroll 2
+        for (int t = a.t0 + tr; t < a.t1; t += npass) {
+            const size_t o = (((size_t)b * N + t) * H + h) * dk + 4 * q4;
+            const float rn = s_rn[t];
+            float4 y = *reinterpret_cast<const float4*>(s_y + t * d + 4 * q4);
+            y.x *= rn;
+            y.y *= rn;
+            y.z *= rn;
+            y.w *= rn;
+            *reinterpret_cast<float4*>(dst + o) = y;
+            if (dhi != nullptr) {   // hi = bf16(y), lo = bf16(y - hi), two channels per conversion
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(y.x, y.y), h23 = __floats2bfloat162_rn(y.z, y.w);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                const __nv_bfloat162 l01 = __floats2bfloat162_rn(y.x - f01.x, y.y - f01.y);
+                const __nv_bfloat162 l23 = __floats2bfloat162_rn(y.z - f23.x, y.w - f23.y);
+                *reinterpret_cast<uint2*>(dhi + o) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+                *reinterpret_cast<uint2*>(dlo + o) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
             }
         }
     }
