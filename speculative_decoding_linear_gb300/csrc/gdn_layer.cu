@@ -142,7 +142,12 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     const int c = cb + tid;
     const bool act = tid < d;
     float hrow[3] = {0.f, 0.f, 0.f};
-    float w[kConvTaps] = {0.f, 0.f, 0.f, 0.f};
+    const bool act2 = tid < d / 2;            // the conv: channels 2 tid and 2 tid + 1
+    float4 wa = make_float4(0.f, 0.f, 0.f, 0.f), wb = wa;
+    if (act2) {
+        wa = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(cb + 2 * tid) * kConvTaps);
+        wb = *reinterpret_cast<const float4*>(a.conv_w + (size_t)(cb + 2 * tid + 1) * kConvTaps);
+    }
     if (act) {
         const int L = s_L;
         float* cs = a.conv_state + (size_t)b * 3 * C + c;
@@ -157,36 +162,36 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
         }
 #pragma unroll
         for (int i = 0; i < 3; ++i) s_y[(N + i) * d + tid] = hrow[i];
-        const float4 wv = *reinterpret_cast<const float4*>(a.conv_w + (size_t)c * kConvTaps);
-        w[0] = wv.x;
-        w[1] = wv.y;
-        w[2] = wv.z;
-        w[3] = wv.w;
     }
     cp_async_wait_all();
     __syncthreads();
 
-    // Depthwise: thread `tid` only ever touches channel column tid of s_y, so each
-    // output overwrites its own input in place.  Descending node order keeps every
-    // window's ancestor rows (lower indices) unmodified until they are read; a
-    // chunk of 8 nodes loads all its inputs before it stores any output.
-    if (act) {
-        const float* col = s_y + tid;
+    // Depthwise: thread `tid` only ever touches channel columns 2 tid and 2 tid + 1
+    // of s_y, so each output overwrites its own input in place.  Descending node
+    // order keeps every window's ancestor rows (lower indices) unmodified until
+    // they are read; a chunk of 8 nodes loads all its inputs before it stores any output.
+    if (act2) {
+        float* col = s_y + 2 * tid;
         auto conv_at = [&](int t) {
             const int4 o = s_off[t];
-            return w[0] * col[o.x] + w[1] * col[o.y] + w[2] * col[o.z] + w[3] * col[o.w];
+            const float2 x0 = *reinterpret_cast<const float2*>(col + o.x);
+            const float2 x1 = *reinterpret_cast<const float2*>(col + o.y);
+            const float2 x2 = *reinterpret_cast<const float2*>(col + o.z);
+            const float2 x3 = *reinterpret_cast<const float2*>(col + o.w);
+            return make_float2(wa.x * x0.x + wa.y * x1.x + wa.z * x2.x + wa.w * x3.x,
+                               wb.x * x0.y + wb.y * x1.y + wb.z * x2.y + wb.w * x3.y);
         };
         int t = a.t1 - 1;
 #pragma unroll 1
         for (; t - 7 >= a.t0; t -= 8) {
-            float r[8];
+            float2 r[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) r[u] = conv_at(t - u);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) s_y[(t - u) * d + tid] = r[u];
+            for (int u = 0; u < 8; ++u) *reinterpret_cast<float2*>(col + (t - u) * d) = r[u];
         }
 #pragma unroll 1
-        for (; t >= a.t0; --t) s_y[t * d + tid] = conv_at(t);
+        for (; t >= a.t0; --t) *reinterpret_cast<float2*>(col + t * d) = conv_at(t);
     }
 
     // Output rows four channels per thread: d / 4 threads per node, npass nodes at a time.
