@@ -72,6 +72,9 @@ def library_path() -> str:
 def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     """The loaded libgdnspec.so.  Builds it when absent (nvcc required); raises if it cannot."""
     global _lib
+    loaded = _lib              # once loaded, every call returns it without taking the lock
+    if loaded is not None:
+        return loaded
     with _lock:
         if _lib is None:
             path = _build.LIB
