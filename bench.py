@@ -63,9 +63,9 @@ def algorithmic_bytes(B, N, H, dk, dv, esz, L_total, Lmax, chain):
 NCU_TRAFFIC = {
     "chain8_b1_h8_d256": (2.276e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"), "4369be9a62c19566"),
     "tree32_depth6_b1_h8_d256": (2.615e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
-                                           "gdn_internal.cuh"), "dc9f94f9e5574be9"),
+                                           "gdn_internal.cuh"), "1ca8894d6f526df8"),
     "tree64_depth8_b16_h8_d256": (47.74e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
-                                            "gdn_internal.cuh"), "dc9f94f9e5574be9"),
+                                            "gdn_internal.cuh"), "1ca8894d6f526df8"),
 }
 
 

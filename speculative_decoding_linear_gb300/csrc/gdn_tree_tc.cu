@@ -734,10 +734,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // ---------------------------------------------------------------------------
 // A CTA owns its (sequence, head)'s whole state (two 128-row MMA tiles, u = 0,
 // 1) and runs the prologue itself, so a call is a single launch:
-//   before the wait: the state is streamed, the pending commit applied in
-//     registers and written back; slabs 0 and 1 become bf16 hi/lo operand
-//     stages (slabs 2 and 3 are read back from L2 after the wait and take
-//     the stages over once slabs 0 and 1 are consumed);
+//   before the wait: one warp reads the pending commit's accepted path,
+//     parents and gates in one round trip and brings the path's key and delta
+//     rows in by bulk copies, while every thread has state slabs 0 and 1 in
+//     flight; then the state is streamed, the commit applied in registers and
+//     written back; slabs 0 and 1 become bf16 hi/lo operand stages (slabs 2
+//     and 3 are read back from L2 after the wait and take the stages over once
+//     slabs 0 and 1 are consumed);
 //   after the wait: q/k slabs by TMA; per slab the Y MMAs of both tiles and
 //     the Gram MMA ([Q; K] K^T: M = 128 rows, N = 64 keys) on the same operand
 //     buffer; the node metadata meanwhile;
