@@ -15,7 +15,9 @@
 // that device.  All calls on a device share the array and it keeps the last
 // call's contents; the kernels rewrite every entry they later read, so
 // nothing needs clearing between calls.  Calls whose kernels overlap on the
-// GPU (for example on two streams at once) race on the array.
+// GPU (for example on two streams at once) race on the array.  Shapes that
+// run the single-kernel tensor-core verifier (bf16 q/k, d_k = d_v = 256) use
+// no workspace, so the array's size bounds only the other shapes.
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -75,15 +77,6 @@ extern "C" int gdn_tree_verify_noalloc(const void* q, const void* k, const void*
     const char* o = reinterpret_cast<const char*>(out);
     const char* f = static_cast<const char*>(factors);
     if (o < f + fbytes && f < o + obytes) return GDN_ERR_ARG;
-    const size_t need = (size_t)B * H * ws_layout(N).record;
-    if (need > kNoAllocScratchBytes) return GDN_ERR_CAPACITY;
-
-    int st = GDN_OK;
-    int* err = current_error_word(&st);
-    if (err == nullptr) return st;
-    void* ws = scratch_address(&st);
-    if (ws == nullptr) return st;
-
     VerifyArgs a;
     a.q = q;
     a.k = k;
@@ -94,14 +87,25 @@ extern "C" int gdn_tree_verify_noalloc(const void* q, const void* k, const void*
     a.S = const_cast<float*>(S0);
     a.out = out;
     a.f = factors_view(factors, B, N, H, dk, dv, dtype);
-    a.ws = static_cast<char*>(ws);
+    a.ws = nullptr;
     a.B = B;
     a.N = N;
     a.H = H;
     a.dk = dk;
     a.dv = dv;
     a.commit = CommitSrc{nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0};
-    a.err = err;
+    // Only the kernels that pass tables through the workspace are bounded by the
+    // scratch array; the single-kernel verifier runs at any B * H.
+    const bool uses_ws = tree_verify_uses_workspace(a, dtype);
+    if (uses_ws && (size_t)B * H * ws_layout(N).record > kNoAllocScratchBytes) return GDN_ERR_CAPACITY;
+
+    int st = GDN_OK;
+    a.err = current_error_word(&st);
+    if (a.err == nullptr) return st;
+    if (uses_ws) {
+        a.ws = static_cast<char*>(scratch_address(&st));
+        if (a.ws == nullptr) return st;
+    }
     a.overlap = launch_overlap_enabled();
     return launch_tree_verify(a, dtype, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

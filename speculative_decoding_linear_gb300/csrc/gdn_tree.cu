@@ -448,6 +448,13 @@ cudaError_t launch_tree_contract_simt(const VerifyArgs& a, cudaStream_t s) {
     return launch_kernel(tree_contract_kernel<T>, grid, dim3(kCThreads), Ly.total, s, true, a);
 }
 
+// Mirrors the dispatch of launch_tree_verify below: only the single-kernel
+// tensor-core verifier leaves the workspace untouched.
+bool tree_verify_uses_workspace(const VerifyArgs& a, int dtype) {
+    const bool tc = dtype == GDN_DTYPE_F32 ? a.split[0] != nullptr && tc_contract_eligible(a) : tc_contract_eligible(a);
+    return !tc || tc_uses_workspace(a);
+}
+
 cudaError_t launch_tree_verify(const VerifyArgs& args, int dtype, cudaStream_t s) {
     VerifyArgs a = args;
     cudaError_t e;

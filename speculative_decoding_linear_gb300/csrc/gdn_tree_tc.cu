@@ -1385,6 +1385,8 @@ bool fused_eligible(const VerifyArgs& a, bool split) {
     return L.total <= kFSmemLimit;
 }
 
+bool tc_uses_workspace(const VerifyArgs& a) { return !fused_eligible(a, a.split[0] != nullptr); }
+
 template <bool kSplit, int kT>
 cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s) {
     static bool attr[64];
