@@ -9,8 +9,9 @@
 namespace gdn {
 namespace {
 
-// First device-side error since the last gdn_last_error; one word per device.
-__device__ int g_error_word;
+// First device-side error since the last gdn_last_error, and the wait limit; one
+// block per device.
+__device__ ErrorBlock g_error_block = {0, 0, kDefaultWaitLimitNs};
 
 constexpr int kMaxDevices = 64;
 int* g_err_ptr[kMaxDevices];
@@ -35,7 +36,7 @@ int dev_setup(int* status) {
         g_dev_ok[dev] = (p.major == 10 && p.minor == 3) ? 1 : -1;
         if (g_dev_ok[dev] == 1) {
             void* ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) {
+            if (cudaGetSymbolAddress(&ptr, g_error_block) != cudaSuccess) {
                 g_dev_ok[dev] = 0;
                 *status = GDN_ERR_CUDA;
                 return -1;
@@ -239,12 +240,21 @@ int gdn_last_error(cudaStream_t stream) {
     if (dev < 0) return st;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
     int word = 0;
-    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&word, g_error_block, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
     if (word != 0) {
         const int zero = 0;
-        if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
+        if (cudaMemcpyToSymbol(g_error_block, &zero, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
     }
     return word;
+}
+
+int gdn_set_wait_limit_ns(unsigned long long ns) {
+    if (ns < 1000ull || ns > 60000000000ull) return GDN_ERR_ARG;
+    int st;
+    if (dev_setup(&st) < 0) return st;
+    return cudaMemcpyToSymbol(g_error_block, &ns, sizeof(ns), offsetof(ErrorBlock, wait_limit_ns)) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
 }
 
 const char* gdn_strerror(int code) {

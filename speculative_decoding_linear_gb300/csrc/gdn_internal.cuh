@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "gdnspec.h"
@@ -140,6 +141,20 @@ struct CommitArgs {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
 
+// The per-device error block: the error word, then (8 bytes on) the limit of
+// every bounded device wait in nanoseconds (gdn_set_wait_limit_ns, default one
+// second).  Waits read it only once their first poll has failed.
+struct ErrorBlock {
+    int code;
+    int pad;
+    unsigned long long wait_limit_ns;
+};
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ unsigned long long wait_limit_ns(const int* err) {
+    return *reinterpret_cast<const volatile unsigned long long*>(reinterpret_cast<const char*>(err) +
+                                                                 offsetof(ErrorBlock, wait_limit_ns));
+}
+
 template <typename T>
 __device__ __forceinline__ float ld_elem(const T* p, size_t i);
 template <>
@@ -243,6 +258,11 @@ int* current_error_word(int* status);
 bool launch_overlap_enabled();
 // tensor-core prologue + contraction of the tree verifier (gdn_tree_tc.cu)
 bool tc_contract_eligible(const VerifyArgs& a);
+// Whether launch_tree_tc takes the two-kernel form (which passes the tables
+// through the workspace) rather than the single-kernel verifier.
+bool tc_uses_workspace(const VerifyArgs& a);
+// Whether launch_tree_verify(a, dtype, .) reads or writes a.ws at all.
+bool tree_verify_uses_workspace(const VerifyArgs& a, int dtype);
 cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s);
 
 }  // namespace gdn

@@ -33,15 +33,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 // Bounded wait for the completion of the mbarrier phase with this parity.
-// Returns false (and records GDN_ERR_TIMEOUT) after about one second.  The
-// polling loop is out of line: kernels wait at many places, and each inlined
-// copy would cost instruction-cache space.
+// Returns false (and records GDN_ERR_TIMEOUT) once the wait limit of the error
+// block has passed (one second unless the host set another).  The polling loop
+// is out of line: kernels wait at many places, and each inlined copy would cost
+// instruction-cache space.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int* err) {
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = wait_limit_ns(err);
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
+        if (globaltimer_ns() - t0 > limit) {
             set_error(err, GDN_ERR_TIMEOUT);
             return false;
         }
