@@ -1,38 +1,51 @@
 #!/usr/bin/env python3
-"""Throughput of tree/chain verification + accepted-path commit, per GDN layer.
+"""Throughput of tree verification + accepted-path commit, per GDN layer.
 
 Metric: draft nodes verified per second per GDN layer = B * N / t_layer, where
-t_layer is the device time of one decode step of one layer: the pending
-commit of the previous step's accepted path fused into the verification of
-the new draft (the delayed state update of the SpecLA review, "Core claim").
+t_layer is the device time of one decode step of one layer.  The default
+workload is the full GDN layer step over 64 draft trees of 64 nodes (hidden
+2048, 8 heads of d_k = d_v = 256): input projection, ancestor-window conv,
+gates, tree verification with the previous accepted path's commit fused in
+(the delayed state update of the SpecLA review, "Core claim"), output gate and
+output projection.  The same line carries a sub-record for 16 trees of 64
+nodes through gdn_commit_tree_verify alone (the verifier + commit kernel).
 
 Protocol (layer-major decode, inputs larger than L2): R distinct layer
-instances, each with its own fp32 state, inputs and ping-pong factor buffers,
-R chosen so their footprint is at least 4x the L2 size; one step runs the R
-layers back to back, captured once as a CUDA graph and replayed.  Between two
-visits of a layer every other layer's data has streamed through L2, so each
-visit reads its state from HBM.  Steps are timed with CUDA events on the
-launching stream; W untimed warm-up steps come first.
+instances, each with its own state, inputs and ping-pong records, R chosen so
+their footprint is at least 4x the L2 size; one step runs the R layers back
+to back, captured once as a CUDA graph and replayed.  Between two visits of a
+layer every other layer's data has streamed through L2, so each visit reads
+its state from HBM.  W untimed warm-up steps, then exactly K timed steps
+bracketed by a barrier and a device synchronize, timed with CUDA events on
+the launching stream (max over ranks).
 
 Also reported in the same JSON line:
-  roofline      algorithmic bytes of one layer call / measured t_layer, against
-                the measured HBM copy bandwidth
+  roofline      the dominant kernel's algorithmic bytes (or flops) per launch /
+                its CUDA-event time, against the measured peak; per_kernel
+                lists every kernel of the step the same way
+  replays       median / p10 / p90 per layer call over >= 100 graph replays,
+                the cold single-call latency (L2 flushed) and the L2-warm figure
   e2e           the same metric through the public API with pinned host inputs
                 copied in and outputs copied out inside every timed step
   cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
   clocks        SM clocks and throttle reasons sampled while timing
 
 ``--impl reference`` times the oracle itself as the reference arm.
-Multi-GPU (torchrun): every rank runs its own replica (weak scaling, no
-data-path collective); the step time is the max over ranks.
+Multi-GPU: ``--gpus N`` launches N ranks (one per GPU) through torchrun when
+not already under it.  ``--shard replicas`` (default): every rank runs its own
+replica (weak scaling).  ``--shard sequences``: the batch's sequences are split
+across ranks (strong scaling).  Neither needs a collective on the data path;
+the step time is the max over ranks.
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import socket
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -42,10 +55,18 @@ sys.path.insert(0, ROOT)
 
 METRIC = "draft nodes verified/sec per GDN layer"
 UNIT = "nodes/s"
+LAYER_KERNELS = ("gemm_in", "conv", "tree_verify", "gate", "gemm_out")
+LAYER_KERNEL_NAMES = {
+    "gemm_in": "gemm_bf16_kernel<1,256> (input projection)",
+    "conv": "layer_conv_kernel (ancestor-window conv, norms, gates)",
+    "tree_verify": "tree_fused_tc_kernel<1,2> (tree verify + pending commit)",
+    "gate": "layer_gate_kernel (o * SiLU(z))",
+    "gemm_out": "gemm_bf16_kernel<2,256> (output projection, two bf16 terms)",
+}
 
 
 # ---------------------------------------------------------------------------
-# algorithmic traffic of one layer call (bytes that must cross HBM)
+# algorithmic work of one call (bytes that must cross HBM, or tensor flops)
 # ---------------------------------------------------------------------------
 def algorithmic_bytes(B, N, H, dk, dv, esz, L_total, Lmax, chain):
     """Bytes one fused commit+verify layer call must move: L_total = accepted nodes summed over B."""
@@ -57,30 +78,74 @@ def algorithmic_bytes(B, N, H, dk, dv, esz, L_total, Lmax, chain):
     return state + inputs + outputs + factors_out + commit_in
 
 
-# DRAM traffic of one layer call (dram__bytes_read.sum + dram__bytes_write.sum of
-# every kernel the call launches) from one ncu capture per workload, with the
-# hash of the kernel sources it was taken on: a changed kernel reports null.
+def layer_flops(B, N, H, hidden, dk, dv):
+    """Dense tensor-core work of one layer call: input and output projections (useful flops)."""
+    rows = 2 * H * dk + 2 * H * dv + 2 * H
+    return 2.0 * B * N * hidden * rows + 2.0 * B * N * H * dv * hidden
+
+
+def layer_kernel_work(B, N, H, hidden, dk, dv, L_total, Lmax):
+    """Per kernel of one layer step: (bound, algorithmic amount, unit).  HBM kernels count the bytes
+    their function needs to move (inputs read once, outputs written once); the GEMMs count useful
+    flops (the output GEMM issues twice as many: two bf16 terms of its fp32 left operand)."""
+    M = B * N
+    C = H * (2 * dk + dv)
+    conv = (M * C * 4                                  # read the pre-conv q|k|v projections
+            + 2 * B * 3 * C * 4                        # conv history: read, write the committed rows
+            + min(L_total, 3 * B) * C * 4              # accepted rows entering the history
+            + M * 2 * H * 4                            # gate pre-activations
+            + M * H * (dk + dv) * 4                    # k, v (fp32) for the verifier
+            + 4 * M * H * dk * 2                       # bf16 hi/lo terms of q and k
+            + 2 * M * H * 4)                           # alpha, beta
+    verify = (2 * B * H * dv * dk * 4                  # state read + committed state written
+              + 4 * M * H * dk * 2 + M * H * (dk + dv) * 4 + 2 * M * H * 4 + M * 4   # q/k terms, k, v, gates, parents
+              + M * H * dv * 4                         # o
+              + B * H * N * (dv * 4 + dk * 4 + 4) + M * 4   # factor record (fp32 keys)
+              + L_total * H * (dv * 4 + dk * 4 + 4) + B * Lmax * 4)   # pending commit's rows + path
+    gate = M * H * dv * 4 * 2 + 2 * M * H * dv * 2     # read o, z; write y hi, lo
+    rows = 2 * H * dk + 2 * H * dv + 2 * H
+    return {"gemm_in": ("tensor", 2.0 * M * hidden * rows, "flop"),
+            "conv": ("hbm", float(conv), "B"),
+            "tree_verify": ("hbm", float(verify), "B"),
+            "gate": ("hbm", float(gate), "B"),
+            "gemm_out": ("tensor", 2.0 * M * H * dv * hidden, "flop")}
+
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel from one ncu
+# capture, keyed by (workload, kernel), with the hash of the kernel sources it was taken on: a changed
+# kernel reports null.  How each figure was taken is in profiles/.
 NCU_TRAFFIC = {
-    "chain8_b1_h8_d256": (2.276e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"), "4369be9a62c19566"),
-    "tree32_depth6_b1_h8_d256": (2.615e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
-                                           "gdn_internal.cuh"), "1ca8894d6f526df8"),
-    "tree64_depth8_b16_h8_d256": (47.74e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh",
-                                            "gdn_internal.cuh"), "1ca8894d6f526df8"),
+    ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.276e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
+                                               "4369be9a62c19566"),
+    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (
+        2.615e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh", "gdn_internal.cuh"), "1ca8894d6f526df8"),
+    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (
+        47.74e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh", "gdn_internal.cuh"), "1ca8894d6f526df8"),
 }
+NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
+                    "start; writes still held in L2 when the kernel ends are not counted)")
 
 
-def ncu_traffic(workload):
+def source_digest(files):
     import hashlib
-    if workload not in NCU_TRAFFIC:
-        return None
-    nbytes, files, digest = NCU_TRAFFIC[workload]
     m = hashlib.sha256()
     for f in files:
         with open(os.path.join(ROOT, "speculative_decoding_linear_gb300", "csrc", f), "rb") as fh:
             m.update(fh.read())
-    return nbytes if m.hexdigest()[:16] == digest else None
+    return m.hexdigest()[:16]
 
 
+def ncu_traffic(workload, kernel):
+    entry = NCU_TRAFFIC.get((workload, kernel))
+    if entry is None:
+        return None
+    nbytes, files, digest = entry
+    return nbytes if source_digest(files) == digest else None
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
 def max_over_ranks(x, dist, world, device="cpu"):
     """The largest value of x over all ranks (x itself on one rank): step times are the max over ranks."""
     if world <= 1:
@@ -91,18 +156,61 @@ def max_over_ranks(x, dist, world, device="cpu"):
     return float(t.item())
 
 
+def sum_over_ranks(x, dist, world, device="cpu"):
+    """The sum of x over all ranks (units processed by the whole job)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def whole_job_rate(units_per_rank, world, seconds):
     """Units processed by all ranks per second of the slowest rank (weak scaling: every rank runs
     its own replica of the workload)."""
     return units_per_rank * world / seconds
 
 
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launcher_command(argv, gpus, port):
+    """The torchrun command that runs this script on `gpus` ranks of one node."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(gpus),
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+
+
+def check_world(args, world):
+    """--gpus must match the launched world: a lone process asked for N > 1 GPUs relaunches itself
+    under torchrun (returns the exit code to propagate); a mismatch under a launcher is an error."""
+    if world == args.gpus:
+        return None
+    if world == 1 and "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        import torch
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            sys.stderr.write("bench.py: --gpus %d but only %d GPU(s) visible\n" % (args.gpus, have))
+            return 2
+        return subprocess.call(launcher_command(sys.argv[1:], args.gpus, _free_port()))
+    sys.stderr.write("bench.py: --gpus %d does not match WORLD_SIZE=%d\n" % (args.gpus, world))
+    return 2
+
+
+# ---------------------------------------------------------------------------
+# peaks
+# ---------------------------------------------------------------------------
 def measured_peaks():
+    """HBM GB/s and bf16 TFLOP/s (burst and sustained) from MEASURED_PEAKS.json, else the fallback."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d["bf16_tflops_sustained"]), "kind": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "kind": "fallback"}
 
 
 # ---------------------------------------------------------------------------
@@ -116,11 +224,11 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+        fd, self.path = tempfile.mkstemp(prefix="gdn_clocks_", suffix=".csv")
+        os.close(fd)
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -142,6 +250,10 @@ class ClockSampler:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
                 rows.append(parts)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         sm = [float(r[1]) for r in rows]
@@ -153,7 +265,87 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# the workload: R layer instances on one GPU
+# timing helpers (CUDA events on the launching stream)
+# ---------------------------------------------------------------------------
+def soak(graphs, stream, seconds=1.0, sync_every=8):
+    """Replay the step graphs for about `seconds` so the clock sampler sees the GPU under this load."""
+    t0 = time.time()
+    i = 0
+    while time.time() - t0 < seconds:
+        graphs[i % 2].replay()
+        i += 1
+        if i % sync_every == 0:
+            stream.synchronize()
+    stream.synchronize()
+    return i
+
+
+def timed_steps(graphs, steps, stream, torch, dist, world):
+    """Exactly `steps` replays between a barrier + synchronize on both sides; the total device time
+    (ms, this rank) from CUDA events on `stream`."""
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        graphs[s % 2].replay()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    return e0.elapsed_time(e1)
+
+
+def replay_distribution(graphs, n, calls_per_step, stream, torch):
+    """Per-call device time of `n` graph replays, each bracketed by its own events: median, p10, p90."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(n):
+            graphs[i % 2].replay()
+            ev[i + 1].record(stream)
+        ev[-1].synchronize()
+    us = np.array([ev[i].elapsed_time(ev[i + 1]) * 1e3 / calls_per_step for i in range(n)])
+    return {"replays": n, "median_us_per_call": round(float(np.median(us)), 3),
+            "p10_us": round(float(np.percentile(us, 10)), 3), "p90_us": round(float(np.percentile(us, 90)), 3)}
+
+
+def cold_and_warm(call, stream, torch, l2_bytes, reps=5, warm_reps=50):
+    """Cold single-call latency (L2 flushed by writing a buffer of twice its size before each call) and
+    the L2-warm figure (the same instance called back to back), in microseconds."""
+    flush = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device="cuda")
+    cold = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            cold.append(e0.elapsed_time(e1) * 1e3)
+        call()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(warm_reps):
+                call()
+        g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+    del flush, g
+    return float(np.median(cold)), e0.elapsed_time(e1) * 1e3 / warm_reps
+
+
+# ---------------------------------------------------------------------------
+# tree / chain workloads: R layer instances on one GPU
 # ---------------------------------------------------------------------------
 class Layer:
     """One GDN layer instance: its state, this step's draft inputs, ping-pong factors."""
@@ -180,13 +372,14 @@ class Layer:
         return sum(t.numel() * t.element_size() for t in ts)
 
 
-def make_layers(cfg, R, seed0, device, torch, gdnspec, wl, batch=None):
-    return [Layer(wl.make_workload(cfg, seed=seed0 + 7919 * r, B=batch), device, torch, gdnspec)
-            for r in range(R)]
+def draw_tree_workload(wl, cfg, seed, batch, shard_mode, world, rank):
+    from speculative_decoding_linear_gb300 import shard
+    w = wl.make_workload(cfg, seed=seed, B=batch)
+    return shard.shard_workload(w, world, rank) if shard_mode == "sequences" else w
 
 
 def layer_call(gdnspec, ly, parity, chain):
-    """One decode step of one layer: commit the previous accepted path inside the new verify."""
+    """One decode step of one layer: the previous accepted path's commit fused into the new verify."""
     prev, nxt = ly.fac[parity], ly.fac[1 - parity]
     w = ly.w
     if chain:
@@ -206,7 +399,14 @@ def first_verify(gdnspec, ly, chain):
                                 ly.ws)
 
 
-def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=False, batch=None, layers=None):
+def l2_size(torch, device_index):
+    props = torch.cuda.get_device_properties(device_index)
+    return int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
+
+
+def run_tree(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=False, batch=None, layers=None,
+             shard_mode="replicas", extras=True):
+    """Commit + verify calls of workload `cfg` over a rotation of layer instances."""
     from speculative_decoding_linear_gb300 import gdnspec
     from speculative_decoding_linear_gb300 import workloads as wl
 
@@ -214,32 +414,34 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
     device = torch.device("cuda", device_index)
     spec = wl.SPECS[cfg]
     chain = spec.tree == "chain"
-    props = torch.cuda.get_device_properties(device_index)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
+    l2 = l2_size(torch, device_index)
+    # replicas: every rank its own draws; sequences: one global draw per layer, sliced by rank
+    seed_base = 1000 * (rank + 1) + cfg if shard_mode == "replicas" else 1000 + cfg
 
-    probe = Layer(wl.make_workload(cfg, B=batch), device, torch, gdnspec)
+    probe = Layer(draw_tree_workload(wl, cfg, None, batch, shard_mode, world, rank), device, torch, gdnspec)
     per_layer = probe.nbytes()
     del probe
     R = max(2, -(-4 * l2 // per_layer)) if layers is None else max(2, layers)
-    layers = make_layers(cfg, R, 1000 * (rank + 1) + cfg, device, torch, gdnspec, wl, batch)
-    footprint = sum(ly.nbytes() for ly in layers)
+    lys = [Layer(draw_tree_workload(wl, cfg, seed_base + 7919 * r, batch, shard_mode, world, rank), device, torch,
+                 gdnspec) for r in range(R)]
+    footprint = sum(ly.nbytes() for ly in lys)
 
     stream = torch.cuda.Stream(device=device)
     # consecutive calls of the sweep touch different layers: launch overlap is safe
     gdnspec.gdn_set_launch_overlap(True)
     with torch.cuda.stream(stream):
-        for ly in layers:
+        for ly in lys:
             first_verify(gdnspec, ly, chain)
         assert gdnspec.gdn_last_error(stream) == 0
         for parity in (0, 1):                    # eager warm-up of both parities before capture
-            for ly in layers:
+            for ly in lys:
                 layer_call(gdnspec, ly, parity, chain)
         assert gdnspec.gdn_last_error(stream) == 0
         graphs = []
         for parity in (0, 1):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for ly in layers:
+                for ly in lys:
                     layer_call(gdnspec, ly, parity, chain)
             graphs.append(g)
         for i in range(max(warmup, 3)):
@@ -247,67 +449,65 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
         stream.synchronize()
         assert gdnspec.gdn_last_error(stream) == 0
 
-        # soak ~1 s so the clock sampler sees the GPU under this load, then time exactly K steps
         sampler = ClockSampler(device_index)
         sampler.start()
-        t_soak = time.time()
-        i = 0
-        while not profile and time.time() - t_soak < 1.0:
-            graphs[i % 2].replay()
-            i += 1
-            if i % 16 == 0:
-                stream.synchronize()
-        stream.synchronize()
-        if world > 1:
-            dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for s in range(steps):
-            graphs[s % 2].replay()
-        e1.record(stream)
-        e1.synchronize()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        if not profile:
+            soak(graphs, stream, 1.0, 16)
+        ms_local = timed_steps(graphs, steps, stream, torch, dist, world)
         clocks = sampler.stop()
-        ms_local = e0.elapsed_time(e1)
         assert gdnspec.gdn_last_error(stream) == 0
-
+        dist_rec = None if profile else replay_distribution(graphs, max(100, steps), R, stream, torch)
     ms = max_over_ranks(ms_local, dist, world, device)
 
-    # ---- end to end through the public API: pinned host inputs in, outputs out, every step
-    e2e = None if profile else run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device)
-    baselines = None if (profile or chain) else run_replay_baselines(layers, gdnspec, torch, stream,
-                                                                     max(5, min(steps, 20)))
-    hybrid = None if (profile or chain) else run_hybrid_comparison(layers, gdnspec, torch, stream,
-                                                                   max(5, min(steps, 20)), device, wl)
-    prune = None if (profile or chain) else run_prune_timing(gdnspec, torch, stream, device, wl, B=layers[0].w.B,
-                                                             N=layers[0].w.N)
-
-    w0 = layers[0].w
+    w0 = lys[0].w
     B, N, H, dk, dv = w0.B, w0.N, w0.H, w0.dk, w0.dv
+    units = sum_over_ranks(B * N * R * steps, dist, world, device)
+    cold = warm = None
+    if not profile and extras:
+        ly0 = lys[0]
+        parity = [0]
+
+        def one():
+            layer_call(gdnspec, ly0, parity[0], chain)
+            parity[0] ^= 1
+        # the single-call figures without launch overlap: one call has nothing to overlap with
+        prev = gdnspec.gdn_set_launch_overlap(False)
+        cold, warm = cold_and_warm(one, stream, torch, l2)
+        gdnspec.gdn_set_launch_overlap(prev)
+    e2e = None if profile or not extras else run_e2e(lys, steps, chain, gdnspec, torch, stream, world, dist, device,
+                                                    shard_mode)
+    more = extras and not profile and not chain
+    baselines = run_replay_baselines(lys, gdnspec, torch, stream, max(5, min(steps, 20))) if more else None
+    hybrid = run_hybrid_comparison(lys, gdnspec, torch, stream, max(5, min(steps, 20)), device, wl) if more else None
+    prune = run_prune_timing(gdnspec, torch, stream, device, wl, B=B, N=N) if more else None
+
     esz = 2 if w0.dtype == wl.BF16 else 4
     per_call = float(np.mean([algorithmic_bytes(B, N, H, dk, dv, esz, int(np.sum(ly.w.path >= 0)),
-                                                ly.w.path.shape[1], chain) for ly in layers]))
-    t_layer_s = ms / 1e3 / (steps * R)
-    peak, peak_kind = measured_peaks()
-    achieved = per_call / t_layer_s / 1e9
-    value = whole_job_rate(B * N * R * steps, world, ms / 1e3)
-    # one launch per call: the chain kernel, or the single-kernel tree verifier (d_k = d_v = 256)
+                                                ly.w.path.shape[1], chain) for ly in lys]))
+    t_call_s = ms / 1e3 / (steps * R)
+    peaks = measured_peaks()
+    achieved = per_call / t_call_s / 1e9
     fused_tree = not chain and dk == 256 and dv == 256
-    launches_per_call = 1 if (chain or fused_tree) else 2
+    kernel = "chain_g8_kernel" if chain else "tree_fused_tc_kernel" if fused_tree else "tree_contract_tc_kernel"
+    replays = None
+    if dist_rec is not None:
+        replays = dict(dist_rec)
+        replays["cold_single_call_us"] = None if cold is None else round(cold, 3)
+        replays["l2_warm_us_per_call"] = None if warm is None else round(warm, 3)
+        replays["what"] = ("median over graph replays of the %d-layer rotation (each visit reads its state from "
+                           "HBM); cold = one call after writing a 2x-L2 buffer, launch overlap off; warm = one "
+                           "layer instance called back to back (footprint %.0f MB vs %.0f MB of L2)"
+                           % (R, per_layer / 1e6, l2 / 1e6))
     return dict(
-        value=value, ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
-        spec=spec, B=B, N=N, H=H, dk=dk, dv=dv, chain=chain,
-        roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                  "frac": round(achieved / peak, 4), "traffic": ncu_traffic(spec.name),
-                  "peak_kind": peak_kind + " hbm_gbs (copy)",
-                  "kernel": "gdn_commit_chain_verify (chain_g8_kernel)" if chain else
-                            "gdn_commit_tree_verify (tree_fused_tc_kernel)" if fused_tree else
-                            "gdn_commit_tree_verify (prologue + contraction kernels)",
-                  "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_layer_s * 1e6, 3)},
-        gpu_launches=launches_per_call * R * steps, baselines=baselines, hybrid=hybrid, prune=prune,
+        value=units / (ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
+        spec=spec, B=B, N=N, H=H, dk=dk, dv=dv, chain=chain, replays=replays,
+        roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                  "frac": round(achieved / peaks["hbm"], 4), "traffic": ncu_traffic(spec.name, kernel),
+                  "traffic_note": NCU_TRAFFIC_NOTE, "peak_kind": peaks["kind"] + " hbm_gbs (copy)",
+                  "kernel": "gdn_commit_%s_verify (%s, one launch per call)" % ("chain" if chain else "tree", kernel),
+                  "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_call_s * 1e6, 3),
+                  "t_call_from": "CUDA events around the timed graph replays / calls (launch overlap on)"},
+        gpu_launches=(1 if (chain or fused_tree) else 2) * R * steps, baselines=baselines, hybrid=hybrid, prune=prune,
     )
 
 
@@ -316,8 +516,9 @@ def run_gpu(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=
 # ---------------------------------------------------------------------------
 def run_replay_baselines(layers, gdnspec, torch, stream, steps):
     """Per-call device time of tree verification vs replaying every root-to-leaf path, and of the
-    factor-buffer commit vs replaying the accepted tokens, on the same layer rotation (no launch
-    overlap for either side).  Commits write to a scratch state so the inputs stay unchanged."""
+    factor-buffer commit vs replaying the accepted tokens and vs restoring a snapshot of the accepted
+    node's state, on the same layer rotation (no launch overlap for any side).  Commits write to a
+    scratch state so the inputs stay unchanged."""
     prev = gdnspec.gdn_set_launch_overlap(False)
     scratch = [torch.empty_like(ly.S) for ly in layers]
     w0 = layers[0].w
@@ -415,16 +616,23 @@ def run_hybrid_comparison(layers, gdnspec, torch, stream, steps, device, wl):
     return res
 
 
+def run_prune_timing(gdnspec, torch, stream, device, wl, B, N, steps=50):
+    """Device time of one gdn_prune_tree call on B random trees of N nodes."""
+    rng = np.random.default_rng(77)
+    parent = torch.from_numpy(np.stack([wl.random_tree(rng, N, 8) for _ in range(B)])).to(device)
+    logp = torch.from_numpy((-rng.exponential(1.0, (B, N))).astype(np.float32)).to(device)
+    idx = torch.empty((B, N), dtype=torch.int32, device=device)
+    npar = torch.empty((B, N), dtype=torch.int32, device=device)
+    nk = torch.empty(B, dtype=torch.int32, device=device)
+    us = time_calls([lambda: gdnspec.gdn_prune_tree(parent, logp, 1.0, N // 2, idx, npar, nk)], torch, stream, steps)
+    assert gdnspec.gdn_last_error(stream) == 0
+    return {"us_per_call": round(us, 3), "B": B, "N": N, "tau": 1.0, "budget": N // 2}
+
+
 # ---------------------------------------------------------------------------
 # full GDN layer decode step: projections, ancestor-window conv, gates, tree
 # verification with the pending commit fused in, output gate, o_proj
 # ---------------------------------------------------------------------------
-def layer_flops(B, N, H, hidden, dk, dv):
-    """Dense tensor-core work of one layer call: input and output projections (useful flops)."""
-    rows = 2 * H * dk + 2 * H * dv + 2 * H
-    return 2.0 * B * N * hidden * rows + 2.0 * B * N * H * dv * hidden
-
-
 class LayerStep:
     """One full-layer instance: weights, state, conv history, this step's draft, ping-pong records."""
 
@@ -462,19 +670,51 @@ class LayerStep:
                                         self.rec[1 - parity], self.ws, w.H, w.dk, w.dv)
 
 
-def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile=False, layers=None):
+def draw_layer_workload(wl, seed, shard_mode, world, rank):
+    from speculative_decoding_linear_gb300 import shard
+    w = wl.make_layer_workload(4, seed=seed)
+    return shard.shard_workload(w, world, rank) if shard_mode == "sequences" else w
+
+
+def layer_kernel_times(lys, gdnspec, torch, stream, steps, parity0):
+    """Average device time (us) of each of the layer step's five kernels over `steps` passes of the
+    rotation, from CUDA events the library records on the launching stream between the kernels
+    (gdn_layer_stage_events); calls are eager, so kernels of consecutive calls do not overlap."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(LAYER_KERNELS) + 1)]
+          for _ in range(steps * len(lys))]
+    i = 0
+    with torch.cuda.stream(stream):
+        for e in ev:                      # torch creates the CUDA event at its first record
+            for x in e:
+                x.record(stream)
+        for s in range(steps):
+            for ly in lys:
+                gdnspec.gdn_layer_stage_events(ev[i])
+                ly.call(gdnspec, (parity0 + s) % 2)
+                i += 1
+        gdnspec.gdn_layer_stage_events(None)
+        stream.synchronize()
+    assert gdnspec.gdn_last_error(stream) == 0
+    tot = np.zeros(len(LAYER_KERNELS))
+    for e in ev:
+        tot += [e[k].elapsed_time(e[k + 1]) for k in range(len(LAYER_KERNELS))]
+    return {k: float(t) * 1e3 / len(ev) for k, t in zip(LAYER_KERNELS, tot)}, (parity0 + steps) % 2
+
+
+def run_layer(steps, warmup, rank, world, device_index, torch, dist, profile=False, layers=None,
+              shard_mode="replicas"):
     from speculative_decoding_linear_gb300 import gdnspec
     from speculative_decoding_linear_gb300 import workloads as wl
 
     torch.cuda.set_device(device_index)
     device = torch.device("cuda", device_index)
     spec = wl.SPECS[4]
-    props = torch.cuda.get_device_properties(device_index)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 126 * 2 ** 20
-    first = LayerStep(wl.make_layer_workload(4, seed=1000 * (rank + 1) + 4), device, torch, gdnspec)
+    l2 = l2_size(torch, device_index)
+    seed_base = 1000 * (rank + 1) + 4 if shard_mode == "replicas" else 1004
+    first = LayerStep(draw_layer_workload(wl, seed_base, shard_mode, world, rank), device, torch, gdnspec)
     per_layer = first.nbytes()
     R = max(2, -(-4 * l2 // per_layer)) if layers is None else max(2, layers)
-    lys = [first] + [LayerStep(wl.make_layer_workload(4, seed=1000 * (rank + 1) + 4 + 7919 * r), device, torch,
+    lys = [first] + [LayerStep(draw_layer_workload(wl, seed_base + 7919 * r, shard_mode, world, rank), device, torch,
                                gdnspec) for r in range(1, R)]
     footprint = sum(ly.nbytes() for ly in lys)
     stream = torch.cuda.Stream(device=device)
@@ -499,49 +739,81 @@ def run_gpu_layer(steps, warmup, rank, world, device_index, torch, dist, profile
         assert gdnspec.gdn_last_error(stream) == 0
         sampler = ClockSampler(device_index)
         sampler.start()
-        t_soak = time.time()
-        i = 0
-        while not profile and time.time() - t_soak < 1.0:
-            graphs[i % 2].replay()
-            i += 1
-            if i % 4 == 0:
-                stream.synchronize()
-        stream.synchronize()
-        if world > 1:
-            dist.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for s_ in range(steps):
-            graphs[s_ % 2].replay()
-        e1.record(stream)
-        e1.synchronize()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        if not profile:
+            soak(graphs, stream, 1.0, 4)
+        ms_local = timed_steps(graphs, steps, stream, torch, dist, world)
         clocks = sampler.stop()
-        ms_local = e0.elapsed_time(e1)
         assert gdnspec.gdn_last_error(stream) == 0
-
+        dist_rec = None if profile else replay_distribution(graphs, max(100, steps), R, stream, torch)
+        # replays end on graph parity (n - 1) % 2; the next eager call takes the other parity
+        parity = 0 if dist_rec is None else max(100, steps) % 2
+        kt, parity = (None, parity) if profile else layer_kernel_times(lys, gdnspec, torch, stream,
+                                                                      max(3, min(steps, 10)), parity)
         seq = None if profile else run_sequential_baseline(lys[0], gdnspec, torch, stream, steps=3)
         model = None if profile else run_model_step(gdnspec, torch, stream, device, wl)
     ms = max_over_ranks(ms_local, dist, world, device)
+    cold = warm = None
+    if not profile:
+        ly0 = lys[0]
+        par = [parity]
 
-    e2e = None if profile else run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device)
+        def one():
+            ly0.call(gdnspec, par[0])
+            par[0] ^= 1
+        cold, warm = cold_and_warm(one, stream, torch, l2, reps=3, warm_reps=5)
+
+    e2e = None if profile else run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device, shard_mode)
     w0 = lys[0].w
-    t_layer_s = ms / 1e3 / (steps * R)
+    units = sum_over_ranks(w0.B * w0.N * R * steps, dist, world, device)
+    t_call_s = ms / 1e3 / (steps * R)
     flops = layer_flops(w0.B, w0.N, w0.H, w0.hidden, w0.dk, w0.dv)
-    peak, peak_kind = measured_tensor_peak()
-    achieved = flops / t_layer_s / 1e12
+    peaks = measured_peaks()
+    step_tensor = {"achieved": round(flops / t_call_s / 1e12, 1), "peak": peaks["bf16_sustained"],
+                   "unit": "TFLOP/s", "frac": round(flops / t_call_s / 1e12 / peaks["bf16_sustained"], 4),
+                   "algorithmic_flops_per_call": flops, "t_call_us": round(t_call_s * 1e6, 3),
+                   "what": "whole layer step: useful projection flops / step time (graph replays), against the "
+                           "measured sustained bf16 peak"}
+    roofline = {"bound": "tensor", "kernel": "gdn_layer_tree_step (whole step)", **step_tensor, "traffic": None}
+    if kt is not None:
+        L_total = float(np.mean([int(np.sum(ly.w.path >= 0)) for ly in lys]))
+        work = layer_kernel_work(w0.B, w0.N, w0.H, w0.hidden, w0.dk, w0.dv, L_total, w0.path.shape[1])
+        total = sum(kt.values())
+        per = []
+        for k in LAYER_KERNELS:
+            bound, amount, unit = work[k]
+            t = kt[k] * 1e-6
+            if bound == "hbm":
+                ach, peak, u = amount / t / 1e9, peaks["hbm"], "GB/s"
+                pk = peaks["kind"] + " hbm_gbs (copy)"
+            else:
+                ach, peak, u = amount / t / 1e12, peaks["bf16_sustained"], "TFLOP/s"
+                pk = peaks["kind"] + " bf16_tflops_sustained (cuBLAS, long loop)"
+            per.append({"kernel": LAYER_KERNEL_NAMES[k], "bound": bound, "t_us": round(kt[k], 2),
+                        "share": round(kt[k] / total, 4), "achieved": round(ach, 1), "peak": peak, "unit": u,
+                        "frac": round(ach / peak, 4), "peak_kind": pk,
+                        ("algorithmic_bytes" if bound == "hbm" else "algorithmic_flops"): amount,
+                        "traffic": ncu_traffic(spec.name, k)})
+        top = max(per, key=lambda r: r["t_us"])
+        roofline = {"bound": top["bound"], "achieved": top["achieved"], "peak": top["peak"], "unit": top["unit"],
+                    "frac": top["frac"], "traffic": top["traffic"], "traffic_note": NCU_TRAFFIC_NOTE,
+                    "peak_kind": top["peak_kind"], "kernel": top["kernel"] + " -- the step's dominant kernel",
+                    "t_kernel_us": top["t_us"],
+                    "t_kernel_from": "CUDA events recorded by the library between the step's kernels "
+                                     "(gdn_layer_stage_events), eager calls over the same rotation",
+                    "per_kernel": per, "step": step_tensor}
+    replays = None
+    if dist_rec is not None:
+        replays = dict(dist_rec)
+        replays["cold_single_call_us"] = None if cold is None else round(cold, 3)
+        replays["l2_warm_us_per_call"] = None if warm is None else round(warm, 3)
+        replays["what"] = ("median over graph replays of the %d-layer rotation; cold = one layer step after "
+                           "writing a 2x-L2 buffer; warm = one instance called back to back (its %.0f MB "
+                           "footprint exceeds the %.0f MB L2, so this is not L2-resident)"
+                           % (R, per_layer / 1e6, l2 / 1e6))
     return dict(
-        value=whole_job_rate(w0.B * w0.N * R * steps, world, ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
+        value=units / (ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
         spec=spec, B=w0.B, N=w0.N, H=w0.H, dk=w0.dk, dv=w0.dv, hidden=w0.hidden, chain=False, layer=True,
-        sequential=seq, model=model,
-        roofline={"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                  "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
-                  "kernel": "gdn_layer_tree_step (input/output projection GEMMs on tcgen05, conv, "
-                            "tree verify + commit, gate)",
-                  "algorithmic_flops_per_call": flops, "t_call_us": round(t_layer_s * 1e6, 3)},
+        sequential=seq, model=model, roofline=roofline, replays=replays,
         # GEMM, conv, tree verifier (one kernel at d_k = d_v = 256, else two), gate, GEMM
         gpu_launches=(5 if w0.dk == 256 and w0.dv == 256 else 6) * R * steps,
     )
@@ -592,27 +864,6 @@ def run_model_step(gdnspec, torch, stream, device, wl, n_layers=4, steps=5):
                     "every layer committing the previous step's accepted path" % n_layers}
 
 
-def run_prune_timing(gdnspec, torch, stream, device, wl, B, N, steps=50):
-    """Device time of one gdn_prune_tree call on B random trees of N nodes."""
-    rng = np.random.default_rng(77)
-    parent = torch.from_numpy(np.stack([wl.random_tree(rng, N, 8) for _ in range(B)])).to(device)
-    logp = torch.from_numpy((-rng.exponential(1.0, (B, N))).astype(np.float32)).to(device)
-    idx = torch.empty((B, N), dtype=torch.int32, device=device)
-    npar = torch.empty((B, N), dtype=torch.int32, device=device)
-    nk = torch.empty(B, dtype=torch.int32, device=device)
-    us = time_calls([lambda: gdnspec.gdn_prune_tree(parent, logp, 1.0, N // 2, idx, npar, nk)], torch, stream, steps)
-    assert gdnspec.gdn_last_error(stream) == 0
-    return {"us_per_call": round(us, 3), "B": B, "N": N, "tau": 1.0, "budget": N // 2}
-
-
-def measured_tensor_peak():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(p):
-        d = json.load(open(p))
-        return float(d["bf16_tflops_sustained"]), "measured bf16_tflops_sustained (cuBLAS, long loop)"
-    return 1700.0, "fallback"
-
-
 def pack_tensors(objs, names, torch, device):
     """Move the named tensors of every object into one device buffer (each view 256-byte aligned) and
     re-point the objects at the views; returns (device buffer, pinned host buffer with the same bytes)."""
@@ -633,7 +884,12 @@ def pack_tensors(objs, names, torch, device):
     return buf, buf.cpu().pin_memory()
 
 
-def run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device):
+def _e2e_rate(units_local, sec, world, dist, device):
+    units = sum_over_ranks(units_local, dist, world, device)
+    return units / sec
+
+
+def run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device, shard_mode="replicas"):
     """Layer step through the public API with every instance's X, parent_idx and accepted path copied
     in from pinned host memory (one transfer) and the layer outputs copied out (one transfer), every
     step."""
@@ -660,8 +916,8 @@ def run_e2e_layer(lys, steps, gdnspec, torch, stream, world, dist, device):
         t1 = time.perf_counter()
     sec = max_over_ranks(t1 - t0, dist, world, device)
     w = lys[0].w
-    return {"value": whole_job_rate(w.B * w.N * len(lys) * k, world, sec), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": 1e3 * sec / k}
+    return {"value": _e2e_rate(w.B * w.N * len(lys) * k, sec, world, dist, device), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": 1e3 * sec / k}
 
 
 def run_sequential_baseline(ly, gdnspec, torch, stream, steps=3):
@@ -706,7 +962,7 @@ def run_sequential_baseline(ly, gdnspec, torch, stream, steps=3):
     return res
 
 
-def run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device):
+def run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device, shard_mode="replicas"):
     """Same metric through the public API: every layer call made from the host each step, with all
     layers' draft inputs copied in from pinned host memory (one transfer) and their outputs copied
     out (one transfer) inside the timed region."""
@@ -734,7 +990,7 @@ def run_e2e(layers, steps, chain, gdnspec, torch, stream, world, dist, device):
         t1 = time.perf_counter()
     sec = max_over_ranks(t1 - t0, dist, world, device)
     w = layers[0].w
-    return {"value": whole_job_rate(w.B * w.N * len(layers) * k, world, sec), "unit": UNIT,
+    return {"value": _e2e_rate(w.B * w.N * len(layers) * k, sec, world, dist, device), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k, "ms_per_step": 1e3 * sec / k}
 
 
@@ -799,9 +1055,13 @@ def run_reference(args):
     if args.config == 4:
         w = wl.make_layer_workload(4, B=2)
         timer = oracle_full_layer_seconds
+        sample = ("one full-layer step of 2 of the 64 sequences of %s per step (numpy fp64 projections/conv/"
+                  "o_proj + path-walk recurrence + commit), %d threads" % (w.spec.name, cores))
     else:
         w = wl.make_workload(args.config)
         timer = oracle_layer_seconds
+        sample = ("one layer instance of %s per step (verify all nodes by path walks + commit), fp64, %d threads"
+                  % (w.spec.name, cores))
     for _ in range(max(args.warmup, 1)):
         timer(w, cores)
     sec = sum(timer(w, cores) for _ in range(args.steps))
@@ -811,39 +1071,60 @@ def run_reference(args):
             "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.spec.name, "B": w.spec.B, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "one layer instance of %s per step (verify all nodes by path "
-                                       "walks + commit), fp64, %d threads" % (w.spec.name, cores)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------------------
+def config_record(r, spec, world, shard_mode):
+    cfg = {"workload": spec.name, "B": r["B"], "N": r["N"], "H": r["H"], "dk": r["dk"], "dv": r["dv"],
+           "qkv": spec.dtype, "state": "f32",
+           "step": ("full GDN layer step: projections, ancestor-window conv, gates, tree verify with the "
+                    "pending commit (state + conv history) fused in, output gate, o_proj") if r.get("layer") else
+                   "per layer: pending commit fused into the next %s verify" % ("chain" if r["chain"] else "tree"),
+           "layers_rotated": r["R"], "footprint_bytes": r["footprint"], "l2_bytes": r["l2"],
+           "l2_policy": ("inputs larger than L2: %d-layer rotation, footprint >= 4x L2" % r["R"])
+           if r["footprint"] >= 4 * r["l2"] else "profiling rotation of %d layers (footprint below 4x L2)" % r["R"],
+           "parallelism": ("single GPU" if world == 1 else
+                           "replicas" if shard_mode == "replicas" else "sequences sharded across ranks")}
+    if r.get("layer"):
+        cfg["hidden"] = r["hidden"]
+    return cfg
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--shard", default="replicas", choices=["replicas", "sequences"],
+                    help="replicas: every rank its own workload (weak scaling); sequences: the batch's "
+                         "sequences split across ranks (strong scaling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="skip the verify+commit sub-record of the layer line")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
     ap.add_argument("--profile", action="store_true",
-                    help="for profiler runs: no clock soak, no e2e leg, no CPU baseline")
+                    help="for profiler runs: no clock soak, no e2e leg, no CPU baseline, no side records")
     ap.add_argument("--layers", type=int, default=None,
                     help="for profiler runs: rotate this many layers instead of >= 4x L2 of them")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rc = check_world(args, world)
+    if rc is not None:
+        sys.exit(rc)
 
     if args.impl == "reference":
         run_reference(args)
         return
 
     import torch
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -855,11 +1136,15 @@ def main():
         __graft_entry__.build()
     if world > 1:
         dist.barrier()
+    sub = None
     if args.config == 4:
-        r = run_gpu_layer(args.steps, args.warmup, rank, world, local, torch, dist, args.profile, args.layers)
+        r = run_layer(args.steps, args.warmup, rank, world, local, torch, dist, args.profile, args.layers, args.shard)
+        if not (args.profile or args.no_sub):
+            torch.cuda.empty_cache()
+            sub = run_tree(3, args.steps, args.warmup, rank, world, local, torch, dist, False, None, None, args.shard)
     else:
-        r = run_gpu(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
-                    args.batch, args.layers)
+        r = run_tree(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
+                     args.batch, args.layers, args.shard)
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or args.profile or world > 1 else cpu_baseline(args.config)
@@ -867,22 +1152,11 @@ def main():
         line = {
             "metric": METRIC, "value": round(r["value"], 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": {"workload": spec.name, "B": r["B"], "N": r["N"], "H": r["H"], "dk": r["dk"],
-                       "dv": r["dv"], "qkv": spec.dtype, "state": "f32",
-                       "step": ("full GDN layer step: projections, ancestor-window conv, gates, tree "
-                                "verify with the pending commit (state + conv history) fused in, output "
-                                "gate, o_proj") if r.get("layer") else
-                               "per layer: pending commit fused into the next %s verify"
-                               % ("chain" if r["chain"] else "tree"),
-                       "layers_rotated": r["R"], "footprint_bytes": r["footprint"], "l2_bytes": r["l2"],
-                       "l2_policy": ("inputs larger than L2: %d-layer rotation, footprint >= 4x L2" % r["R"])
-                       if r["footprint"] >= 4 * r["l2"] else
-                       "profiling rotation of %d layers (footprint below 4x L2)" % r["R"],
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "higher_is_better": True, "scaling": "strong" if args.shard == "sequences" and world > 1 else "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_record(r, spec, world, args.shard),
             "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
-            "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
+            "gpu_launches": r["gpu_launches"], "clocks": r["clocks"], "replays": r.get("replays"),
         }
         if r.get("baselines"):
             line["replay_baselines"] = r["baselines"]
@@ -893,11 +1167,19 @@ def main():
         if r.get("model"):
             line["model_step"] = r["model"]
         if r.get("layer"):
-            line["config"]["hidden"] = r["hidden"]
             seq = r["sequential"]
             if seq:
                 seq["tree_step_speedup"] = round(r["value"] / seq["value"], 2)
             line["sequential_decode"] = seq
+        if sub is not None:
+            rec = {"metric": METRIC, "value": round(sub["value"], 1), "unit": UNIT,
+                   "ms_per_step": round(sub["ms"], 4), "config": config_record(sub, sub["spec"], world, args.shard),
+                   "roofline": sub["roofline"], "replays": sub["replays"], "e2e": sub["e2e"],
+                   "gpu_launches": sub["gpu_launches"], "clocks": sub["clocks"]}
+            for key, name in (("baselines", "replay_baselines"), ("hybrid", "hybrid_verify"), ("prune", "prune_tree")):
+                if sub.get(key):
+                    rec[name] = sub[key]
+            line["tree_verify_commit"] = rec
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

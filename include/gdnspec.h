@@ -5,7 +5,7 @@
  * Source of the method: "Pith review of SpecLA: Efficient Speculative
  * Decoding for Linear-Attention Models" (pith.science 7ERME3HB) -- "Core
  * claim" and "What carries the argument" (tree-masked factorized verifier,
- * factor buffering, delayed state update fused into the next verification,
+ * factor buffering, the pending commit carried out by the next verification,
  * V-dimension tiling for chains) and the Referee Report's summary.  The
  * recurrence is the gated delta rule of "Gated Delta Networks: Improving
  * Mamba2 with Delta Rule", which that review cites:
@@ -66,8 +66,8 @@ extern "C" {
 
 /*
  * Factor buffer.  Verification writes, for every draft node, the compact
- * record the commit needs (review: "buffering the small per-token factors
- * produced during verification and applying only the accepted path"):
+ * record the commit needs (review, "Core claim": the verifier keeps a small
+ * record per draft token, and only the accepted tokens' records are applied):
  *
  *   delta  fp32  [B][H][N][d_v]   innovation delta_t = beta_t (v_t - alpha_t S_parent k_t)
  *   key    dtype [B][H][N][d_k]   k_t (same element type as the q/k/v inputs)
@@ -104,7 +104,7 @@ int gdn_tree_mask(const int32_t* parent_idx, int B, int N, uint64_t* mask, int32
 /*
  * Tree-masked factorized verification (review, "Core claim" / "What carries
  * the argument": O = Qhat S0^T - Attn (W S0^T) + Attn U from the masked UT
- * solve).  Scores every draft node from the same committed state in one pass.
+ * solve).  One pass gives the output of every draft node, all computed from S0.
  *   q, k       dtype [B][N][H][d_k]
  *   v          dtype [B][N][H][d_v]
  *   alpha,beta fp32  [B][N][H]      gate in (0, 1], write strength
@@ -129,10 +129,12 @@ int gdn_tree_verify(const void* q, const void* k, const void* v, int dtype, cons
  * counterpart; this is a property of this library's interface.)
  *   Same arguments, layouts and results as gdn_tree_verify.  The workspace
  *   lives in a fixed 32 MiB scratch array inside the library, held by every
- *   GPU that loads the library until the process exits.  B * H * (workspace
- *   record of one (sequence, head)) must fit in it -- at N = 64 that is up to
- *   992 (sequence, head) pairs, e.g. B = 124 with H = 8; larger requests
- *   return GDN_ERR_CAPACITY without launching anything.
+ *   GPU that loads the library until the process exits.  Shapes that run the
+ *   single-kernel tensor-core verifier (bf16 q/k with d_k = d_v = 256) need
+ *   no workspace and have no limit here.  For every other shape B * H *
+ *   (workspace record of one (sequence, head)) must fit in the array -- at
+ *   N = 64 that is up to 992 (sequence, head) pairs, e.g. B = 124 with H = 8;
+ *   larger requests return GDN_ERR_CAPACITY without launching anything.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
  *   stream capture.  The call allocates nothing.
@@ -148,8 +150,8 @@ int gdn_tree_verify_noalloc(const void* q, const void* k, const void* v, int dty
 
 /*
  * Chain verification with the state kept on chip and tiled along d_v
- * (review, "What carries the argument": "V-dimension tiling for the serial
- * chain path").  The draft is a linear chain: node t hangs under t-1 and
+ * (review, "What carries the argument": a serial chain kernel with the
+ * state cut into tiles along d_v).  The draft is a linear chain: node t hangs under t-1 and
  * node 0 under S0.  Same tensors and factor record as gdn_tree_verify
  * (the factor buffer's parent section receives -1, 0, 1, ..., N-2).
  */
@@ -159,8 +161,8 @@ int gdn_chain_verify(const void* q, const void* k, const void* v, int dtype, con
 
 /*
  * Accepted-path commit from buffered factors, without snapshots or replay
- * (review, Referee Report summary: "accepted-state recovery via buffered
- * per-token factors").
+ * (review, Referee Report summary: the state after the accepted tokens is
+ * rebuilt from the per-token records, with no snapshot and no replay).
  *   S0            fp32 [B][H][d_v][d_k]   state the factors were verified from
  *   factors       written by a verify call with the same B, N, H, d_k, d_v, dtype
  *   accepted_path int32 [B][Lmax]: root-first accepted nodes, padded with -1;
@@ -173,9 +175,9 @@ int gdn_commit(const float* S0, const void* factors, const int32_t* accepted_pat
                float* S_new, int B, int N, int H, int dk, int dv, int dtype, cudaStream_t stream);
 
 /*
- * Delayed state update fused into the next verification (review, "Core
- * claim": "applying only the accepted path inside the next verification
- * kernel").  In one pass over the state tiles:
+ * Delayed state update carried out by the next verification (review, "Core
+ * claim": the accepted path is applied to the state by the kernel that
+ * verifies the following draft).  In one pass over the state tiles:
  *   S <- commit(S, prev_factors, prev_path)   (written back once, in place)
  *   then the new tree is verified from the committed S, as gdn_tree_verify.
  *   S            fp32 [B][H][d_v][d_k], in: state before the commit, out: committed
@@ -200,7 +202,7 @@ int gdn_commit_chain_verify(float* S, const void* prev_factors, int N_prev,
 /*
  * Full GDN layer decode step over B draft trees ("Pith review of SpecLA",
  * Referee Report, major comment 1: one GDN layer, h_v heads of d_k = d_v,
- * causal depthwise convolution of kernel size 4, SiLU output gating; "Core
+ * a four-tap causal depthwise conv, SiLU gate on the output; "Core
  * claim": every node sees the recurrence along its own root-to-node path).
  * For every node t of every tree, in one call on `stream`:
  *   Y_t   = W_in x_t = [q~ | k~ | v~ | z | a | b]_t            (bf16 GEMM, fp32)
@@ -242,6 +244,20 @@ int gdn_layer_tree_step(const void* X, const void* W_in, const float* conv_w, co
                         int N_prev, const int32_t* prev_path, int Lmax, float* out, void* record,
                         void* workspace, int B, int N, int H, int hidden, int dk, int dv,
                         cudaStream_t stream);
+
+/*
+ * Per-kernel timing of gdn_layer_tree_step (a measurement hook; the pages have
+ * no counterpart).  events: host array of 6 cudaEvent_t handles created by the
+ * caller (with timing enabled) on the device the layer runs on; n = 6 turns the
+ * hook on, n = 0 (events ignored) turns it off.  While on, every
+ * gdn_layer_tree_step call records, on its stream, events[i] just before its
+ * kernel i (0 input GEMM, 1 conv, 2 tree verifier, 3 output gate, 4 output
+ * GEMM) and events[5] after the last one, so cudaEventElapsedTime(events[i],
+ * events[i + 1]) is kernel i's device time.  Process-wide; the caller keeps the
+ * events alive while the hook is on and does not turn it on during stream
+ * capture.  Other n, or a null handle, returns GDN_ERR_ARG.
+ */
+int gdn_layer_stage_events(void* const* events, int n);
 
 /*
  * L GDN layers back to back over the same draft trees (layer-major
@@ -290,7 +306,7 @@ int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, c
 /*
  * Chain-decomposed tree verification: serial within chains, parallel across
  * the chains that are ready ("Pith review of SpecLA", "What carries the
- * argument": V-dimension tiling for the serial chain path, next to the
+ * argument": a serial chain kernel with the state tiled along d_v, next to the
  * factorized tree form).  The tree is cut into chains (a chain starts at a
  * root or at a child of a node with two or more children and follows
  * only-children); chains whose parent chain is done run concurrently, each
@@ -391,6 +407,26 @@ int gdn_last_error(cudaStream_t stream);
 
 /* Static description of a status code. */
 const char* gdn_strerror(int code);
+
+/*
+ * Limit of every bounded device wait, in nanoseconds, for the current device
+ * (failure detection; the pages have no counterpart).  A kernel wait that has
+ * not completed after this long records GDN_ERR_TIMEOUT in the error word and
+ * the kernel winds down (its outstanding copies drained, tensor memory freed)
+ * instead of hanging.  Default 1 s; 1e3 <= ns <= 6e10, else GDN_ERR_ARG.  The
+ * value is written to device memory synchronously; set it between calls, not
+ * while kernels that wait are running.
+ */
+int gdn_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Self-test of that failure path: launches one thread that waits, through the
+ * kernels' own bounded wait, on an mbarrier nothing arrives on, with no copy
+ * or MMA outstanding.  After the wait limit it records GDN_ERR_TIMEOUT and
+ * returns, so gdn_last_error(stream) then reports GDN_ERR_TIMEOUT and the
+ * context remains usable.  Returns GDN_OK once launched.
+ */
+int gdn_selftest_stuck_wait(cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -1,8 +1,8 @@
 // gdn_chain.cu -- chain verification with the state resident on chip.
 //
-// Review of SpecLA (pith.science 7ERME3HB), "What carries the argument":
-// "V-dimension tiling for the serial chain path".  For a chain draft (node t
-// hangs under t-1) every row of S evolves independently:
+// Review of SpecLA (pith.science 7ERME3HB), "What carries the argument": a
+// serial chain with the state split into tiles along d_v.  For a chain draft
+// (node t hangs under t-1) every row of S evolves independently:
 //
 //     s = S_row . k_t,  u = S_row . q_t            (one pass over the row)
 //     delta_t = beta_t (v_t[row] - alpha_t s)

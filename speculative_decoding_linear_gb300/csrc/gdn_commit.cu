@@ -1,8 +1,9 @@
 // gdn_commit.cu -- accepted-path commit from buffered factors.
 //
-// Review of SpecLA (pith.science 7ERME3HB), Referee Report summary:
-// "accepted-state recovery via buffered per-token factors".  With the factor
-// record (delta, k, g) of every verified node, the state after accepting the
+// Review of SpecLA (pith.science 7ERME3HB), Referee Report summary: the state
+// after the accepted tokens is rebuilt from the small records kept per draft
+// node, with no snapshot and no replay.  With the factor record (delta, k, g)
+// of every verified node, the state after accepting the
 // root-first path ending at node a is a rank-L update of the committed state:
 //
 //     S_a = e^{g_a} S0 + sum_{j on path(a)} e^{g_a - g_j} delta_j k_j^T

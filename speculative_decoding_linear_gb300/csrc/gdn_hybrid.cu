@@ -2,7 +2,7 @@
 // parallel across the chains that are ready.
 //
 // Review of SpecLA (pith.science 7ERME3HB): "What carries the argument" names
-// V-dimension tiling for the serial chain path next to the factorized tree
+// serial chains with the state split along d_v, beside the factorized tree
 // form, and the Referee Report's Fig. 6 discussion contrasts them on deep,
 // narrow trees.  Here the tree is cut into chains: a chain starts at a root or
 // at a child of a node with two or more children, and follows only-children

@@ -16,12 +16,15 @@
 //      (the same kernels as gdn_commit_tree_verify, fp32 q/k/v)
 //   4. layer_gate_kernel  y = o * SiLU(z), split into bf16 hi + lo
 //   5. gemm_bf16_kernel   out = y W_o^T             (two bf16 terms of y)
+#include <mutex>
+
 #include "gdn_layer.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kConvThreads = 256;
+constexpr int kLayerStages = 5;   // input GEMM, conv, tree verifier, gate, output GEMM
 constexpr int kGateThreads = 256;
 
 struct ConvArgs {
@@ -390,6 +393,17 @@ bool disjoint(const void* a, size_t na, const void* b, size_t nb) {
     return !(x < y + nb && y < x + na);
 }
 
+// Timing hook (gdn_layer_stage_events): when set, gdn_layer_tree_step records
+// event i on its stream before kernel i and event 5 after the last kernel.
+std::mutex g_stage_mu;
+cudaEvent_t g_stage_ev[kLayerStages + 1];
+bool g_stage_on = false;
+
+void stage_mark(int i, cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_stage_mu);
+    if (g_stage_on) cudaEventRecord(g_stage_ev[i], s);
+}
+
 bool layer_shape_ok(int B, int N, int H, int hidden, int dk, int dv) {
     if (B < 1 || N < 1 || N > kMaxNodes || H < 1 || !dim_ok(dk) || !dim_ok(dv)) return false;
     if (hidden < 64 || hidden % 64 != 0 || hidden > 65536 || (H * dv) % 64 != 0) return false;
@@ -492,9 +506,11 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     float* Y = reinterpret_cast<float*>(rec + Ly.y_off);
     const long long M = (long long)B * N;
 
+    stage_mark(0, stream);
     cudaError_t e = launch_gemm_bf16(X, X_lo, X_lo ? 2 : 1, hidden, W_in, Y, Ly.ldy, (int)M, Ly.rows, hidden, err,
                                      stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
+    stage_mark(1, stream);
 
     ConvArgs ca;
     ca.Y = Y;
@@ -522,6 +538,7 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     ca.err = err;
     e = launch_conv(ca, stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
+    stage_mark(2, stream);
 
     VerifyArgs va;
     va.q = ca.q;
@@ -552,6 +569,7 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     va.tc = false;
     e = launch_tree_verify(va, GDN_DTYPE_F32, stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
+    stage_mark(3, stream);
 
     GateArgs gaa;
     gaa.o = va.out;
@@ -569,9 +587,12 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     if (blocks > 152 * 16) blocks = 152 * 16;
     e = launch_kernel(layer_gate_kernel, dim3((unsigned)blocks), dim3(kGateThreads), 0, stream, false, gaa);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
+    stage_mark(4, stream);
 
     e = launch_gemm_bf16(gaa.yhi, gaa.ylo, 2, H * dv, W_o, out, hidden, (int)M, hidden, H * dv, err, stream);
-    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    stage_mark(5, stream);
+    return GDN_OK;
 }
 
 }  // namespace
@@ -584,6 +605,17 @@ extern "C" int gdn_layer_tree_step(const void* X, const void* W_in, const float*
                                    cudaStream_t stream) {
     return layer_tree_step(X, nullptr, W_in, conv_w, W_o, parent_idx, S, conv_state, prev_record, N_prev, prev_path,
                            Lmax, out, record, workspace, B, N, H, hidden, dk, dv, stream);
+}
+
+extern "C" int gdn_layer_stage_events(void* const* events, int n) {
+    if (n != 0 && (n != kLayerStages + 1 || events == nullptr)) return GDN_ERR_ARG;
+    if (n != 0)
+        for (int i = 0; i <= kLayerStages; ++i)
+            if (events[i] == nullptr) return GDN_ERR_ARG;
+    std::lock_guard<std::mutex> lk(g_stage_mu);
+    for (int i = 0; n != 0 && i <= kLayerStages; ++i) g_stage_ev[i] = static_cast<cudaEvent_t>(events[i]);
+    g_stage_on = n != 0;
+    return GDN_OK;
 }
 
 extern "C" int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, const void* W_o,

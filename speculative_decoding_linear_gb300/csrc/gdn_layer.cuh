@@ -7,7 +7,7 @@
 
 namespace gdn {
 
-constexpr int kConvTaps = 4;      // causal depthwise convolution, kernel size 4
+constexpr int kConvTaps = 4;      // four-tap depthwise conv over each node's window
 
 // C[M x Nc] (fp32, row stride ldc elements) = sum_s A_s[M x K] B[Nc x K]^T with
 // bf16 row-major operands (K contiguous; A rows lda elements apart, B rows K).

@@ -45,6 +45,7 @@ SIGNATURES = {
                                  _I, _I, _I, _I, _I, _I, _P]),
     "gdn_layer_token_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                                   _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_layer_stage_events": (_I, [_P, _I]),
     "gdn_model_workspace_bytes": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
     "gdn_model_tree_step": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P,
                                  _I, _I, _I, _I, _I, _I, _P]),
@@ -54,6 +55,8 @@ SIGNATURES = {
     "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_linear_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_set_launch_overlap": (_I, [_I]),
+    "gdn_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
+    "gdn_selftest_stuck_wait": (_I, [_P]),
     "gdn_last_error": (_I, [_P]),
     "gdn_strerror": (ctypes.c_char_p, [_I]),
 }
@@ -265,6 +268,17 @@ def gdn_layer_token_step(X, W_in, conv_w, W_o, parent_idx, S0, conv_state, S_nod
            "gdn_layer_token_step")
 
 
+def gdn_layer_stage_events(events):
+    """Turn the layer step's per-kernel timing hook on with 6 torch.cuda.Event objects (timing
+    enabled, each recorded at least once so that its CUDA event exists), or off with None (see
+    include/gdnspec.h)."""
+    if events is None:
+        _check(lib().gdn_layer_stage_events(None, 0), "gdn_layer_stage_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event if hasattr(e, "cuda_event") else int(e) for e in events])
+    _check(lib().gdn_layer_stage_events(ctypes.cast(arr, ctypes.c_void_p), len(events)), "gdn_layer_stage_events")
+
+
 def gdn_model_workspace_bytes(L, B, N, H, hidden, dk, dv) -> int:
     out = ctypes.c_size_t(0)
     _check(lib().gdn_model_workspace_bytes(L, B, N, H, hidden, dk, dv, ctypes.byref(out)),
@@ -336,6 +350,16 @@ def gdn_linear_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, w
 def gdn_set_launch_overlap(enable: bool) -> bool:
     """Process-wide switch; returns the previous setting (see include/gdnspec.h)."""
     return bool(lib().gdn_set_launch_overlap(1 if enable else 0))
+
+
+def gdn_set_wait_limit_ns(ns: int):
+    """Limit of every bounded device wait on the current device (see include/gdnspec.h)."""
+    _check(lib().gdn_set_wait_limit_ns(int(ns)), "gdn_set_wait_limit_ns")
+
+
+def gdn_selftest_stuck_wait(stream=None):
+    """Launch a wait that nothing completes; gdn_last_error then reports GDN_ERR_TIMEOUT."""
+    _check(lib().gdn_selftest_stuck_wait(_stream(stream)), "gdn_selftest_stuck_wait")
 
 
 def gdn_last_error(stream=None) -> int:
