@@ -35,6 +35,7 @@ struct ConvArgs {
     const float* prevY;        // previous step's projections [B*N_prev][ldy], or nullptr
     int N_prev;
     const int32_t* prev_path;  // [B][Lmax] root first, -1 padded, or nullptr
+    const int32_t* prev_parent;   // [B][N_prev] parents of the previous tree (its factor record)
     int Lmax;
     const int32_t* parent;     // [B][N]
     float* q;                  // [B][N][H][dk]
@@ -98,7 +99,14 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
             const int p1 = lane + 32 < a.Lmax ? p[lane + 32] : -1;
             const unsigned n0 = __ballot_sync(0xffffffffu, p0 < 0), n1 = __ballot_sync(0xffffffffu, p1 < 0);
             L = n0 ? __ffs(n0) - 1 : (n1 ? 32 + __ffs(n1) - 1 : 64);
-            const bool bad = (lane < L && p0 >= a.N_prev) || (lane + 32 < L && p1 >= a.N_prev);
+            bool bad = (lane < L && p0 >= a.N_prev) || (lane + 32 < L && p1 >= a.N_prev);
+            // a root-first parent chain, as the verifier's fused commit requires: the same
+            // rejection leaves the conv history and the state uncommitted together
+            const int32_t* pp = a.prev_parent + (size_t)b * a.N_prev;
+            const int up0 = __shfl_up_sync(0xffffffffu, p0, 1), last0 = __shfl_sync(0xffffffffu, p0, 31);
+            const int up1 = __shfl_up_sync(0xffffffffu, p1, 1);
+            if (!bad && lane < L) bad = pp[p0] != (lane == 0 ? -1 : up0);
+            if (!bad && lane + 32 < L) bad = pp[p1] != (lane == 0 ? last0 : up1);
             if (__any_sync(0xffffffffu, bad)) {
                 if (lane == 0) set_error(a.err, GDN_ERR_PATH);
                 L = 0;
@@ -518,6 +526,10 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     ca.conv_w = conv_w;
     ca.conv_state = conv_state;
     ca.prevY = commit ? reinterpret_cast<const float*>(static_cast<const char*>(prev_record) + Lp.y_off) : nullptr;
+    ca.prev_parent = commit ? factors_view(const_cast<char*>(static_cast<const char*>(prev_record)) + Lp.fac_off, B,
+                                           N_prev, H, dk, dv, GDN_DTYPE_F32)
+                                  .parent
+                            : nullptr;
     ca.N_prev = N_prev;
     ca.prev_path = prev_path;
     ca.Lmax = Lmax;
@@ -557,8 +569,8 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     va.dk = dk;
     va.dv = dv;
     if (commit) {
-        Factors pf = factors_view(const_cast<char*>(static_cast<const char*>(prev_record)) + Lp.fac_off, B, N_prev,
-                                  H, dk, dv, GDN_DTYPE_F32);
+        const Factors pf = factors_view(const_cast<char*>(static_cast<const char*>(prev_record)) + Lp.fac_off, B,
+                                        N_prev, H, dk, dv, GDN_DTYPE_F32);
         va.commit = CommitSrc{pf.delta, pf.key, pf.g, pf.parent, N_prev, prev_path, Lmax};
     } else {
         va.commit = CommitSrc{nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0};
@@ -651,6 +663,7 @@ extern "C" int gdn_layer_token_step(const void* X, const void* W_in, const float
     ca.conv_w = conv_w;
     ca.conv_state = const_cast<float*>(conv_state);   // read only: no accepted path to commit
     ca.prevY = nullptr;
+    ca.prev_parent = nullptr;
     ca.N_prev = 0;
     ca.prev_path = nullptr;
     ca.Lmax = 0;

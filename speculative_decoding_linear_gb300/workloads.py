@@ -353,3 +353,37 @@ def make_layer_workload(cfg=4, seed: Optional[int] = None, B: Optional[int] = No
     S0 = (rng.standard_normal((B, H, dv, dk)) * spec.s0_std).astype(np.float32)
     path = draw_paths(rng, spec, parent)
     return LayerWorkload(spec, B, N, H, dk, dv, hid, X, W_in, conv_w, conv_state, W_o, parent, S0, path)
+
+
+# ---------------------------------------------------------------------------
+# gated linear attention (per-channel gates)
+# ---------------------------------------------------------------------------
+def make_gla_workload(cfg=3, seed: Optional[int] = None, B: Optional[int] = None, parent: Optional[np.ndarray] = None,
+                      **override) -> Workload:
+    """A tree workload whose gate alpha is per key channel, [B, N, H, dk] (every other input as
+    ``make_workload``).  Each gate channel is drawn like the scalar gates: alpha = exp(-softplus(U(-3, 1))).
+    ``parent`` ([B, N]) replaces the drawn trees (then paths go root -> a uniformly drawn node);
+    ``override`` replaces Spec fields (N, H, dk, dv, dtype, maxdepth).  Draw order: trees, q, k, v,
+    alpha pre-activations, beta pre-activations, S0, paths."""
+    base = SPECS[cfg] if isinstance(cfg, int) else cfg
+    spec = dataclasses.replace(base, name="gla_" + base.name, **({"B": B} if B is not None else {}), **override)
+    B = spec.B
+    rng = np.random.default_rng(spec.seed if seed is None else seed)
+    N, H, dk, dv = spec.N, spec.H, spec.dk, spec.dv
+    par = draw_trees(rng, spec, B).astype(np.int32) if parent is None else np.asarray(parent, np.int32)
+    q = _unit_rows(rng.standard_normal((B, N, H, dk)))
+    k = _unit_rows(rng.standard_normal((B, N, H, dk)))
+    v = rng.standard_normal((B, N, H, dv))
+    a_pre = rng.uniform(-3.0, 1.0, (B, N, H, dk))
+    b_pre = rng.uniform(-2.0, 2.0, (B, N, H))
+    alpha = np.exp(-np.logaddexp(0.0, a_pre)).astype(np.float32)
+    beta = (1.0 / (1.0 + np.exp(-b_pre))).astype(np.float32)
+    S0 = (rng.standard_normal((B, H, dv, dk)) * spec.s0_std).astype(np.float32)
+    if parent is None:
+        path = draw_paths(rng, spec, par)
+    else:
+        depth = np.stack([node_depths(par[b]) for b in range(B)])
+        lmax = int(depth.max()) + 1
+        path = np.stack([_pad_path(root_path(par[b], int(rng.integers(N))), lmax) for b in range(B)])
+    return Workload(spec, B, N, H, dk, dv, spec.dtype, _store(q, spec.dtype), _store(k, spec.dtype),
+                    _store(v, spec.dtype), alpha, beta, par, S0, path.astype(np.int32))

@@ -218,3 +218,27 @@ def test_model_step_layers_back_to_back(oracle_mod, shape):
         lays[l]["S0"], lays[l]["conv_state"] = S1, hist1
     _, h2 = layer.model_step(w2.widened("X"), lays, w2.parent, H, dk, dv)
     assert_close(out.cpu().numpy(), h2, "residual stream, second step")
+
+
+@pytest.mark.parametrize("shape", [SMALL[0], SMALL[3]])
+def test_invalid_prev_path_leaves_state_and_conv_history_uncommitted(shape):
+    """A previous accepted path that is not a root-first parent chain: the step reports
+    GDN_ERR_PATH and neither the recurrent state nor the conv history moves (the verifier's
+    commit and the conv kernel's history commit reject the same paths)."""
+    B, N, H, dk, dv, hid, md = shape
+    w = wl.make_layer_workload(4, seed=909, B=B, N=N, H=H, dk=dk, dv=dv, hidden=hid, maxdepth=md)
+    run = LayerRun(w)
+    run.step(w.X, w.parent)
+    bad = np.full((B, 3), -1, dtype=np.int32)
+    for b in range(B):                         # root, then a node that is not the root's child
+        kids = set(np.nonzero(w.parent[b] == 0)[0].tolist())
+        bad[b, :2] = [0, next(t for t in range(1, N) if t not in kids)]
+    S_before, hist_before = run.S.clone(), run.conv_state.clone()
+    rec = torch.empty(gdnspec.gdn_layer_record_bytes(B, N, H, hid, dk, dv), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(gdnspec.gdn_layer_workspace_bytes(B, N, H, hid, dk, dv), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, N, hid), dtype=torch.float32, device="cuda")
+    gdnspec.gdn_layer_tree_step(bf16(w.X), run.W_in, run.conv_w, run.W_o, torch.from_numpy(w.parent).cuda(), run.S,
+                                run.conv_state, run.recs[-1], N, torch.from_numpy(bad).cuda(), out, rec, ws, H, dk, dv)
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_PATH
+    assert torch.equal(run.S, S_before)
+    assert torch.equal(run.conv_state, hist_before)
