@@ -630,6 +630,84 @@ def run_prune_timing(gdnspec, torch, stream, device, wl, B, N, steps=50):
 
 
 # ---------------------------------------------------------------------------
+# gated linear attention (per-channel gates): verify and commit of its own record
+# ---------------------------------------------------------------------------
+def gla_bytes(B, N, H, dk, dv, esz, L_total, Lmax):
+    """Algorithmic bytes of one GLA verify and of one GLA commit call."""
+    verify = (B * H * dv * dk * 4                                   # read S0
+              + B * N * H * (2 * dk + dv) * esz + B * N * H * (dk + 1) * 4 + B * N * 4   # q k v, gates, beta, parents
+              + B * N * H * dv * 4                                   # o
+              + B * H * N * (dv * 4 + dk * esz + dk * 4) + B * N * 4)   # record: delta, key, g per channel, parent
+    commit = 2 * B * H * dv * dk * 4 + L_total * H * (dv * 4 + dk * esz + dk * 4) + B * Lmax * 4 + B * N * 4
+    return verify, commit
+
+
+def run_gla(steps, rank, world, device_index, torch, shard_mode, l2):
+    """gdn_gla_tree_verify and gdn_gla_commit on the 16 x 64-node, 8-head, d = 256 batch with per-channel gates,
+    each timed over a rotation of layer instances (footprint >= 4x L2) replayed as a CUDA graph."""
+    from speculative_decoding_linear_gb300 import gdnspec, shard
+    from speculative_decoding_linear_gb300 import workloads as wl
+    device = torch.device("cuda", device_index)
+
+    def draw(seed):
+        w = wl.make_gla_workload(3, seed=seed)
+        return shard.shard_workload(w, world, rank) if shard_mode == "sequences" else w
+
+    class G:
+        def __init__(self, w):
+            bf = lambda x: torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).to(device)
+            self.w = w
+            self.q, self.k, self.v = bf(w.q), bf(w.k), bf(w.v)
+            self.alpha = torch.from_numpy(w.alpha).to(device)
+            self.beta = torch.from_numpy(w.beta).to(device)
+            self.parent = torch.from_numpy(w.parent).to(device)
+            self.path = torch.from_numpy(w.path).to(device)
+            self.S = torch.from_numpy(w.S0).to(device)
+            self.S_new = torch.empty_like(self.S)
+            self.out = torch.empty((w.B, w.N, w.H, w.dv), dtype=torch.float32, device=device)
+            self.fac = torch.empty(gdnspec.gdn_gla_factors_bytes(w.B, w.N, w.H, w.dk, w.dv, w.dtype),
+                                   dtype=torch.uint8, device=device)
+            self.ws = torch.empty(gdnspec.gdn_gla_workspace_bytes(w.B, w.N, w.H, w.dk, w.dv), dtype=torch.uint8,
+                                  device=device)
+
+        def nbytes(self):
+            ts = [self.q, self.k, self.v, self.alpha, self.beta, self.parent, self.path, self.S, self.S_new, self.out,
+                  self.fac, self.ws]
+            return sum(t.numel() * t.element_size() for t in ts)
+
+    first = G(draw(2000 + rank))
+    R = max(2, -(-4 * l2 // first.nbytes()))
+    gs = [first] + [G(draw(2000 + rank + 7919 * r)) for r in range(1, R)]
+    stream = torch.cuda.Stream(device=device)
+    verify = [lambda g=g: gdnspec.gdn_gla_tree_verify(g.q, g.k, g.v, g.alpha, g.beta, g.parent, g.S, g.out, g.fac,
+                                                      g.ws) for g in gs]
+    commit = [lambda g=g: gdnspec.gdn_gla_commit(g.S, g.fac, g.path, g.S_new, g.w.N, g.w.dtype) for g in gs]
+    t_v = time_calls(verify, torch, stream, max(5, min(steps, 20)))
+    t_c = time_calls(commit, torch, stream, max(5, min(steps, 20)))
+    assert gdnspec.gdn_last_error(stream) == 0
+    w = gs[0].w
+    L_total = float(np.mean([int(np.sum(g.w.path >= 0)) for g in gs]))
+    vb, cb = gla_bytes(w.B, w.N, w.H, w.dk, w.dv, 2, L_total, w.path.shape[1])
+    peaks = measured_peaks()
+
+    def rl(nbytes, us, kernel):
+        ach = nbytes / (us * 1e-6) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm"], 4), "algorithmic_bytes_per_call": nbytes, "t_call_us": round(us, 3),
+                "kernel": kernel, "traffic": None, "peak_kind": peaks["kind"] + " hbm_gbs (copy)"}
+    units = (w.B * world if shard_mode == "replicas" else wl.SPECS[3].B) * w.N     # sequences of the whole job
+    res = {"workload": w.spec.name, "B": w.B, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv, "layers_rotated": R,
+           "verify": rl(vb, t_v, "gdn_gla_tree_verify (gla_prep_kernel + tree_contract_tc_kernel<1> in linear mode)"),
+           "commit": rl(cb, t_c, "gdn_gla_commit (gla_commit_kernel)"),
+           "nodes_per_s_verify_plus_commit": round(units / ((t_v + t_c) * 1e-6), 1),
+           "what": "per call, launch overlap off, CUDA-graph replays of the rotation; per-channel gates "
+                   "alpha = exp(-softplus(U(-3, 1))) per key channel"}
+    del gs
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------
 # full GDN layer decode step: projections, ancestor-window conv, gates, tree
 # verification with the pending commit fused in, output gate, o_proj
 # ---------------------------------------------------------------------------
@@ -1142,6 +1220,7 @@ def main():
         if not (args.profile or args.no_sub):
             torch.cuda.empty_cache()
             sub = run_tree(3, args.steps, args.warmup, rank, world, local, torch, dist, False, None, None, args.shard)
+            sub["gla"] = run_gla(args.steps, rank, world, local, torch, args.shard, sub["l2"])
     else:
         r = run_tree(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
                      args.batch, args.layers, args.shard)
@@ -1176,7 +1255,8 @@ def main():
                    "ms_per_step": round(sub["ms"], 4), "config": config_record(sub, sub["spec"], world, args.shard),
                    "roofline": sub["roofline"], "replays": sub["replays"], "e2e": sub["e2e"],
                    "gpu_launches": sub["gpu_launches"], "clocks": sub["clocks"]}
-            for key, name in (("baselines", "replay_baselines"), ("hybrid", "hybrid_verify"), ("prune", "prune_tree")):
+            for key, name in (("baselines", "replay_baselines"), ("hybrid", "hybrid_verify"), ("prune", "prune_tree"),
+                              ("gla", "gla_verify_commit")):
                 if sub.get(key):
                     rec[name] = sub[key]
             line["tree_verify_commit"] = rec

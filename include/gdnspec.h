@@ -382,6 +382,36 @@ int gdn_linear_tree_verify(const void* q, const void* k, const void* v, int dtyp
                            cudaStream_t stream);
 
 /*
+ * Gated linear attention (GLA: one gate per key channel, no delta-rule
+ * erasure) over a draft tree, with its own factor record and commit (review of
+ * SpecLA, editorial analysis: GLA is one of the recurrence families whose
+ * per-token records the same verify / commit runtime carries).  Along each
+ * node's root-to-node path from S0:
+ *     S_t = S_parent(t) diag(alpha_t) + beta_t v_t k_t^T,    o_t = S_t q_t,
+ * alpha_t in (0, 1]^{d_k}.  Tensors as gdn_tree_verify except
+ *   alpha      fp32 [B][N][H][d_k]   per-channel gates
+ * GLA factor record (gdn_gla_factors_bytes), sections 256-byte aligned:
+ *   delta  fp32  [B][H][N][d_v]   beta_t v_t
+ *   key    dtype [B][H][N][d_k]   k_t
+ *   g      fp32  [B][H][N][d_k]   sum of log alpha_j over path(t), root first
+ *   parent int32 [B][N]
+ * so that the state after accepting node a is
+ *   S_a = S0 diag(e^{g_a}) + sum_{j on path(a)} delta_j (k_j (.) e^{g_a - g_j})^T,
+ * which gdn_gla_commit evaluates (arguments as gdn_commit; an all -1 path row
+ * gives S_new = S0 bit-identical; an invalid path records GDN_ERR_PATH and
+ * leaves that sequence's S_new untouched).  The verifier's workspace has its
+ * own size, gdn_gla_workspace_bytes.  Invalid parent_idx -> GDN_ERR_TREE.
+ */
+int gdn_gla_factors_bytes(int B, int N, int H, int dk, int dv, int dtype, size_t* bytes);
+int gdn_gla_workspace_bytes(int B, int N, int H, int dk, int dv, size_t* bytes);
+int gdn_gla_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                        const float* beta, const int32_t* parent_idx, const float* S0, float* out,
+                        void* factors, void* workspace, int B, int N, int H, int dk, int dv,
+                        cudaStream_t stream);
+int gdn_gla_commit(const float* S0, const void* factors, const int32_t* accepted_path, int Lmax,
+                   float* S_new, int B, int N, int H, int dk, int dv, int dtype, cudaStream_t stream);
+
+/*
  * Launch overlap between consecutive calls (process-wide switch, default off;
  * returns the previous setting).  When on, the first kernel of every call is
  * launched as a programmatic dependent of the kernel before it on the stream:

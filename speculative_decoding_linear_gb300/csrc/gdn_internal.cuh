@@ -125,6 +125,9 @@ struct VerifyArgs {
     // decay-gated linear attention instead of the gated delta rule: S_t = alpha_t S_p +
     // beta_t v_t k_t^T (no erasure), i.e. A = 0, T = I and delta_t = beta_t v_t
     bool linear = false;
+    // the factor record's keys were written by the producer of q/k (the layer's conv
+    // kernel): the single-kernel verifier neither copies nor reads the fp32 keys
+    bool keys_done = false;
 };
 
 struct CommitArgs {
@@ -264,6 +267,9 @@ bool tc_uses_workspace(const VerifyArgs& a);
 // Whether launch_tree_verify(a, dtype, .) reads or writes a.ws at all.
 bool tree_verify_uses_workspace(const VerifyArgs& a, int dtype);
 cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s);
+// the contraction kernels alone, after a caller's own prologue (gdn_gla.cu)
+cudaError_t launch_tc_contract_only(const VerifyArgs& a, bool programmatic, cudaStream_t s);
+cudaError_t launch_tree_contract_simt_f32(const VerifyArgs& a, cudaStream_t s);
 
 }  // namespace gdn
 

@@ -448,6 +448,13 @@ cudaError_t launch_tree_contract_simt(const VerifyArgs& a, cudaStream_t s) {
     return launch_kernel(tree_contract_kernel<T>, grid, dim3(kCThreads), Ly.total, s, true, a);
 }
 
+// The SIMT contraction alone for fp32 q/k/v, after a prologue of the caller's
+// that has written the workspace records (it reads them, and q/k/v, only after
+// its programmatic wait).
+cudaError_t launch_tree_contract_simt_f32(const VerifyArgs& a, cudaStream_t s) {
+    return launch_tree_contract_simt<float>(a, s);
+}
+
 // Mirrors the dispatch of launch_tree_verify below: only the single-kernel
 // tensor-core verifier leaves the workspace untouched.
 bool tree_verify_uses_workspace(const VerifyArgs& a, int dtype) {

@@ -54,6 +54,10 @@ SIGNATURES = {
     "gdn_replay_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_linear_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_gla_factors_bytes": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
+    "gdn_gla_workspace_bytes": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
+    "gdn_gla_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_gla_commit": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gdn_set_launch_overlap": (_I, [_I]),
     "gdn_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
     "gdn_selftest_stuck_wait": (_I, [_P]),
@@ -347,6 +351,49 @@ def gdn_linear_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, w
                                         B, N, H, dk, dv, _stream(stream)), "gdn_linear_tree_verify")
 
 
+def gdn_gla_factors_bytes(B, N, H, dk, dv, dtype) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_gla_factors_bytes(B, N, H, dk, dv, dtype_code(dtype) if not isinstance(dtype, int) else dtype,
+                                       ctypes.byref(out)), "gdn_gla_factors_bytes")
+    return out.value
+
+
+def gdn_gla_workspace_bytes(B, N, H, dk, dv) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_gla_workspace_bytes(B, N, H, dk, dv, ctypes.byref(out)), "gdn_gla_workspace_bytes")
+    return out.value
+
+
+def gdn_gla_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, workspace, stream=None):
+    """Gated linear attention (per-channel gates alpha [B,N,H,dk]) over draft trees; see include/gdnspec.h."""
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_gla_tree_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha), _ptr(beta),
+                                     _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(factors), _ptr(workspace),
+                                     B, N, H, dk, dv, _stream(stream)), "gdn_gla_tree_verify")
+
+
+def gdn_gla_commit(S0, factors, accepted_path, S_new, N, dtype, stream=None):
+    """Accepted-path commit from a GLA factor record (see include/gdnspec.h)."""
+    B, H, dv, dk = S0.shape
+    _check(lib().gdn_gla_commit(_ptr(S0), _ptr(factors), _ptr(accepted_path), accepted_path.shape[1], _ptr(S_new),
+                                B, N, H, dk, dv, dtype_code(dtype), _stream(stream)), "gdn_gla_commit")
+
+
+def gla_factor_views(buf, B, N, H, dk, dv, dtype):
+    """(delta [B,H,N,dv] f32, key [B,H,N,dk], g [B,H,N,dk] f32, parent [B,N] i32) views of a GLA factor buffer."""
+    esz = 4 if dtype_code(dtype) == DTYPE_F32 else 2
+    BHN = B * H * N
+    o_key = _align(BHN * dv * 4)
+    o_g = _align(o_key + BHN * dk * esz)
+    o_par = _align(o_g + BHN * dk * 4)
+    kt = torch.float32 if esz == 4 else torch.bfloat16
+    delta = buf[: BHN * dv * 4].view(torch.float32).view(B, H, N, dv)
+    key = buf[o_key: o_key + BHN * dk * esz].view(kt).view(B, H, N, dk)
+    g = buf[o_g: o_g + BHN * dk * 4].view(torch.float32).view(B, H, N, dk)
+    par = buf[o_par: o_par + B * N * 4].view(torch.int32).view(B, N)
+    return delta, key, g, par
+
+
 def gdn_set_launch_overlap(enable: bool) -> bool:
     """Process-wide switch; returns the previous setting (see include/gdnspec.h)."""
     return bool(lib().gdn_set_launch_overlap(1 if enable else 0))
@@ -399,8 +446,10 @@ def layer_record_views(buf, B, N, H, hidden, dk, dv):
 
 
 def layer_workspace_views(buf, B, N, H, hidden, dk, dv):
-    """q, k [B,N,H,dk], v, o [B,N,H,dv], alpha, beta [B,N,H] fp32; the bf16 hi/lo terms of q and k;
-    y_hi, y_lo [B*N, H*dv] bf16."""
+    """q, k [B,N,H,dk], v, o [B,N,H,dv], alpha, beta [B,N,H] fp32; the bf16 hi/lo terms of q and k
+    (qhi, qlo, khi, klo [B,N,H,dk]); y_hi, y_lo [B*N, H*dv] bf16.  When the single-kernel verifier runs
+    (d_k = d_v = 256) the fp32 q and k rows are not written: q is carried by its hi/lo terms and the
+    keys go straight to the factor record."""
     BN = B * N
     sizes = [("q", BN * H * dk * 4), ("k", BN * H * dk * 4), ("v", BN * H * dv * 4), ("alpha", BN * H * 4),
              ("beta", BN * H * 4), ("o", BN * H * dv * 4), ("qhi", BN * H * dk * 2), ("khi", BN * H * dk * 2),
@@ -411,7 +460,9 @@ def layer_workspace_views(buf, B, N, H, hidden, dk, dv):
         out[name] = buf[off:off + n]
         off = _align(off + n)
     f32 = lambda x, *shape: x.view(torch.float32).view(*shape)
+    bf = lambda x: x.view(torch.bfloat16).view(B, N, H, dk)
     return dict(q=f32(out["q"], B, N, H, dk), k=f32(out["k"], B, N, H, dk), v=f32(out["v"], B, N, H, dv),
+                qhi=bf(out["qhi"]), qlo=bf(out["qlo"]), khi=bf(out["khi"]), klo=bf(out["klo"]),
                 alpha=f32(out["alpha"], B, N, H), beta=f32(out["beta"], B, N, H), o=f32(out["o"], B, N, H, dv),
                 yhi=out["yhi"].view(torch.bfloat16).view(BN, H * dv),
                 ylo=out["ylo"].view(torch.bfloat16).view(BN, H * dv))
