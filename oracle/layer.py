@@ -194,14 +194,6 @@ def sequential_chain(X, W_in, conv_w, conv_state, W_o, S0, H, dk, dv):
     return out, S, np.stack(buf)
 
 
-def round_bf16(x):
-    """Round to bf16 (nearest, ties to even) from the fp32 value, returned as fp64."""
-    f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
-    u = f.view(np.uint32).astype(np.uint64)
-    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
-    return r.astype(np.uint32).view(np.float32).astype(np.float64)
-
-
 def model_step(X, layers, parent, H, dk, dv, nthreads=None):
     """L layers on a residual stream: h_0 = X, h_(l+1) = h_l + out_l (fp64).  ``layers`` is a list of
     dicts with W_in, conv_w, conv_state, W_o, S0.  Returns (list of layer_step results, h_L)."""

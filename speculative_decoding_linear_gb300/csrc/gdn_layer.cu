@@ -38,8 +38,9 @@ struct ConvArgs {
     const int32_t* prev_parent;   // [B][N_prev] parents of the previous tree (its factor record)
     int Lmax;
     const int32_t* parent;     // [B][N]
-    float* q;                  // [B][N][H][dk]
-    float* k;
+    float* q;                  // [B][N][H][dk], or nullptr: not needed (tensor-core verifier)
+    float* k;                  // [B][N][H][dk], or nullptr: the keys go to key_rec instead
+    float* key_rec;            // [B][H][N][dk] keys of the factor record, or nullptr
     float* v;                  // [B][N][H][dv]
     __nv_bfloat16* qk_split[4];   // bf16 q_hi, k_hi, q_lo, k_lo [B][N][H][dk] (tensor-core verify)
     float* alpha;              // [B][N][H]
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
     __syncthreads();
     if (tr < npass) {
         float* dst = seg == 0 ? a.q : a.k;
+        float* krec = seg == 1 ? a.key_rec : nullptr;
         __nv_bfloat16* dhi = a.qk_split[seg];
         __nv_bfloat16* dlo = a.qk_split[2 + seg];
 #pragma unroll 2
@@ -245,7 +247,10 @@ __global__ void __launch_bounds__(kConvThreads) layer_conv_kernel(ConvArgs a) {
             y.y *= rn;
             y.z *= rn;
             y.w *= rn;
-            *reinterpret_cast<float4*>(dst + o) = y;
+            if (krec != nullptr)
+                *reinterpret_cast<float4*>(krec + (((size_t)b * H + h) * N + t) * dk + 4 * q4) = y;
+            else if (dst != nullptr)
+                *reinterpret_cast<float4*>(dst + o) = y;
             if (dhi != nullptr) {   // hi = bf16(y), lo = bf16(y - hi), two channels per conversion
                 const __nv_bfloat162 h01 = __floats2bfloat162_rn(y.x, y.y), h23 = __floats2bfloat162_rn(y.z, y.w);
                 const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
@@ -520,44 +525,12 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     stage_mark(1, stream);
 
-    ConvArgs ca;
-    ca.Y = Y;
-    ca.ldy = Ly.ldy;
-    ca.conv_w = conv_w;
-    ca.conv_state = conv_state;
-    ca.prevY = commit ? reinterpret_cast<const float*>(static_cast<const char*>(prev_record) + Lp.y_off) : nullptr;
-    ca.prev_parent = commit ? factors_view(const_cast<char*>(static_cast<const char*>(prev_record)) + Lp.fac_off, B,
-                                           N_prev, H, dk, dv, GDN_DTYPE_F32)
-                                  .parent
-                            : nullptr;
-    ca.N_prev = N_prev;
-    ca.prev_path = prev_path;
-    ca.Lmax = Lmax;
-    ca.parent = parent_idx;
-    ca.q = reinterpret_cast<float*>(ws + Ly.q_off);
-    ca.k = reinterpret_cast<float*>(ws + Ly.k_off);
-    ca.v = reinterpret_cast<float*>(ws + Ly.v_off);
-    ca.alpha = reinterpret_cast<float*>(ws + Ly.alpha_off);
-    ca.beta = reinterpret_cast<float*>(ws + Ly.beta_off);
-    ca.B = B;
-    ca.N = N;
-    ca.H = H;
-    ca.dk = dk;
-    ca.dv = dv;
-    for (int i = 0; i < 4; ++i) ca.qk_split[i] = reinterpret_cast<__nv_bfloat16*>(ws + Ly.split_off[i]);
-    ca.t0 = 0;
-    ca.t1 = N;
-    ca.err = err;
-    e = launch_conv(ca, stream);
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
-    stage_mark(2, stream);
-
     VerifyArgs va;
-    va.q = ca.q;
-    va.k = ca.k;
-    va.v = ca.v;
-    va.alpha = ca.alpha;
-    va.beta = ca.beta;
+    va.q = ws + Ly.q_off;
+    va.k = ws + Ly.k_off;
+    va.v = ws + Ly.v_off;
+    va.alpha = reinterpret_cast<float*>(ws + Ly.alpha_off);
+    va.beta = reinterpret_cast<float*>(ws + Ly.beta_off);
     va.parent = parent_idx;
     va.S = S;
     va.out = reinterpret_cast<float*>(ws + Ly.o_off);
@@ -575,10 +548,49 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     } else {
         va.commit = CommitSrc{nullptr, nullptr, nullptr, nullptr, 0, nullptr, 0};
     }
-    for (int i = 0; i < 4; ++i) va.split[i] = ca.qk_split[i];
+    for (int i = 0; i < 4; ++i) va.split[i] = ws + Ly.split_off[i];
     va.err = err;
     va.overlap = false;
     va.tc = false;
+    // When the single-kernel verifier runs it reads q and k only as their bf16 hi/lo
+    // terms, and the conv kernel writes the fp32 keys straight into the factor
+    // record; the fp32 q and k rows are then not written at all.
+    const bool direct = !tree_verify_uses_workspace(va, GDN_DTYPE_F32);
+    va.keys_done = direct;
+
+    ConvArgs ca;
+    ca.Y = Y;
+    ca.ldy = Ly.ldy;
+    ca.conv_w = conv_w;
+    ca.conv_state = conv_state;
+    ca.prevY = commit ? reinterpret_cast<const float*>(static_cast<const char*>(prev_record) + Lp.y_off) : nullptr;
+    ca.prev_parent = commit ? factors_view(const_cast<char*>(static_cast<const char*>(prev_record)) + Lp.fac_off, B,
+                                           N_prev, H, dk, dv, GDN_DTYPE_F32)
+                                  .parent
+                            : nullptr;
+    ca.N_prev = N_prev;
+    ca.prev_path = prev_path;
+    ca.Lmax = Lmax;
+    ca.parent = parent_idx;
+    ca.q = direct ? nullptr : reinterpret_cast<float*>(ws + Ly.q_off);
+    ca.k = direct ? nullptr : reinterpret_cast<float*>(ws + Ly.k_off);
+    ca.key_rec = direct ? static_cast<float*>(va.f.key) : nullptr;
+    ca.v = reinterpret_cast<float*>(ws + Ly.v_off);
+    ca.alpha = reinterpret_cast<float*>(ws + Ly.alpha_off);
+    ca.beta = reinterpret_cast<float*>(ws + Ly.beta_off);
+    ca.B = B;
+    ca.N = N;
+    ca.H = H;
+    ca.dk = dk;
+    ca.dv = dv;
+    for (int i = 0; i < 4; ++i) ca.qk_split[i] = reinterpret_cast<__nv_bfloat16*>(ws + Ly.split_off[i]);
+    ca.t0 = 0;
+    ca.t1 = N;
+    ca.err = err;
+    e = launch_conv(ca, stream);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    stage_mark(2, stream);
+
     e = launch_tree_verify(va, GDN_DTYPE_F32, stream);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     stage_mark(3, stream);
@@ -670,6 +682,7 @@ extern "C" int gdn_layer_token_step(const void* X, const void* W_in, const float
     ca.parent = parent_idx;
     ca.q = reinterpret_cast<float*>(ws + Ly.q_off);
     ca.k = reinterpret_cast<float*>(ws + Ly.k_off);
+    ca.key_rec = nullptr;
     ca.v = reinterpret_cast<float*>(ws + Ly.v_off);
     ca.alpha = reinterpret_cast<float*>(ws + Ly.alpha_off);
     ca.beta = reinterpret_cast<float*>(ws + Ly.beta_off);

@@ -737,13 +737,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 //   before the wait: one warp reads the pending commit's accepted path,
 //     parents and gates in one round trip and brings the path's key and delta
 //     rows in by bulk copies, while every thread has state slabs 0 and 1 in
-//     flight; then the state is streamed, the commit applied in registers and
-//     written back; slabs 0 and 1 become bf16 hi/lo operand stages (slabs 2
-//     and 3 are read back from L2 after the wait and take the stages over once
-//     slabs 0 and 1 are consumed);
+//     flight; those two slabs are committed in registers, written back and
+//     turned into bf16 hi/lo operand stages; slabs 2 and 3 are only brought
+//     into L2;
 //   after the wait: q/k slabs by TMA; per slab the Y MMAs of both tiles and
 //     the Gram MMA ([Q; K] K^T: M = 128 rows, N = 64 keys) on the same operand
-//     buffer; the node metadata meanwhile;
+//     buffer; slabs 2 and 3 are read from L2, committed and written back while
+//     the first MMAs run, and take the stages over once slabs 0 and 1 are
+//     consumed; the node metadata meanwhile;
 //   then warps 0-7 turn the Gram rows into the A and Attn tables, solve T,
 //     form P and the [T; P] operand, while warps 8-15 form R of both tiles
 //     from Y_K, v and the gates; one MMA group per tile gives [Delta | P R];
@@ -805,17 +806,11 @@ struct FusedLayout {
     }
 };
 
-// L2 cache policies: the state is read and written once per call, so its
-// lines go first (the call's inputs and the kernel stay resident); the two
-// slabs read back after the wait are kept.
+// L2 cache policy of the state stream: the state is read and written once per
+// call, so its lines go first (the call's inputs and the kernel stay resident).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
     return p;
 }
 
@@ -1007,7 +1002,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
         }
     }
-    const uint64_t pol_first = l2_policy_evict_first(), pol_last = l2_policy_evict_last();
+    const uint64_t pol_first = l2_policy_evict_first();
     float4 cur[8], nxt[8];             // slabs 0 and 1 in flight during the commit setup
     f_load_slab<kJ>(cur, a.S, srow0, rbase, 4 * c4, pol_first);
     f_load_slab<kJ>(nxt, a.S, srow0, rbase, kSlab + 4 * c4, pol_first);
@@ -1034,25 +1029,25 @@ __global__ void __launch_bounds__(kFThreads, 1)
         } else {
             prefetch_l2(static_cast<const KT*>(a.q) + rt * kDk, kDk * (int)sizeof(KT));
         }
-        prefetch_l2(static_cast<const KT*>(a.k) + rt * kDk, kDk * (int)sizeof(KT));
+        if (!a.keys_done) prefetch_l2(static_cast<const KT*>(a.k) + rt * kDk, kDk * (int)sizeof(KT));
         prefetch_l2(static_cast<const KT*>(a.v) + rt * kFRows, kFRows * (int)sizeof(KT));
         prefetch_line_l2(a.alpha + rt);
         prefetch_line_l2(a.beta + rt);
         prefetch_line_l2(a.parent + (size_t)b * N + tid);
     }
+    const float ega = *s_ega;
     if (ok) {
-        // slab by slab, the next one's loads in flight: commit, write back; slabs 0
-        // and 1 into the operand stages (2 and 3 are read back after the wait)
-        const float ega = *s_ega;
+        // slabs 0 and 1: commit, write back, into the operand stages.  Slabs 2 and 3
+        // only go to L2 here: they are committed and written back after the wait,
+        // while the first MMAs run, so that the state writes of all CTAs do not
+        // crowd into this phase, which every CTA of the call runs at the same time.
 #pragma unroll 1
-        for (int sl = 0; sl < kSlabs; ++sl) {
-            if (sl > 0 && sl + 1 < kSlabs)
-                f_load_slab<kJ>(nxt, a.S, srow0, rbase, (sl + 1) * kSlab + 4 * c4, pol_first);
+        for (int sl = 0; sl < 2; ++sl) {
             if (fused) {
                 f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, sl * kSlab + 4 * c4);
-                f_store_slab<kJ>(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, sl < 2 ? pol_first : pol_last);
+                f_store_slab<kJ>(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, pol_first);
             }
-            if (sl < 2) f_convert_slab<kJ>(cur, base + sl * kFAStage, rbase, c4);
+            f_convert_slab<kJ>(cur, base + sl * kFAStage, rbase, c4);
 #pragma unroll
             for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
         }
@@ -1064,7 +1059,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     griddep_wait();
     griddep_launch();
     if (ok) {
-        // this thread's part of the committed slabs 2 and 3, written above (L2)
+        // this thread's part of slabs 2 and 3 as they were before the commit (L2)
         f_load_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
         f_load_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
         if (warp == kFIssuerWarp && lane == 0) {
@@ -1095,6 +1090,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll 1
         for (int sl = 0; sl < kSlabs; ++sl) {
             if (sl >= 2) {
+                if (sl == 2 && fused && ok) {      // commit slabs 2 and 3 and write them back
+                    f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, 2 * kSlab + 4 * c4);
+                    f_store_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
+                    f_commit_slab<kJ>(nxt, ega, L, s_cd, s_key, row0 + rbase, 3 * kSlab + 4 * c4);
+                    f_store_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
+                }
                 ok = ok && mbar_wait(bars + 32 + 8 * (sl - 2), 0, a.err);
                 if (ok) f_convert_slab<kJ>(cur, base + (sl & 1) * kFAStage, rbase, c4);
 #pragma unroll
@@ -1174,7 +1175,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 constexpr int kVec = 16 / (int)sizeof(KT);
                 const KT* kin = static_cast<const KT*>(a.k);
                 KT* kout = static_cast<KT*>(a.f.key) + (size_t)bh * N * kDk;
-                for (int item = tid - 256; lead && item < N * (kDk / kVec); item += kFThreads - 256) {
+                for (int item = tid - 256; lead && !a.keys_done && item < N * (kDk / kVec); item += kFThreads - 256) {
                     const int t = item / (kDk / kVec), c = item % (kDk / kVec);
                     *reinterpret_cast<uint4*>(kout + (size_t)t * kDk + c * kVec) =
                         *reinterpret_cast<const uint4*>(kin + (((size_t)b * N + t) * H + h) * kDk + c * kVec);
@@ -1376,6 +1377,23 @@ cudaError_t launch_tree_tc_impl(const VerifyArgs& a, cudaStream_t s) {
     // always a programmatic dependent of the prologue kernel launched just before it
     return launch_kernel(tree_contract_tc_kernel<kSplit>, grid, dim3(kThreads), Ly.total, s, true, tq, tk, tql, tkl,
                          a);
+}
+
+// The contraction kernel alone (kSplit: fp32 q/k as bf16 hi/lo terms in a.split),
+// after a prologue of the caller's that has written the workspace records.  It
+// issues its q/k copies before its programmatic wait, so `programmatic` may be
+// true only when the q/k terms were written two or more launches earlier.
+cudaError_t launch_tc_contract_only(const VerifyArgs& a, bool programmatic, cudaStream_t s) {
+    static bool attr_c[64];
+    CUtensorMap tq, tk, tql, tkl;
+    if (!make_qk_map(&tq, a.split[0], a.B, a.N, a.H) || !make_qk_map(&tk, a.split[1], a.B, a.N, a.H) ||
+        !make_qk_map(&tql, a.split[2], a.B, a.N, a.H) || !make_qk_map(&tkl, a.split[3], a.B, a.N, a.H))
+        return cudaErrorInvalidValue;
+    const TcLayout Ly(a.commit.path ? a.commit.Lmax : 0, true);
+    cudaError_t e = ensure_smem(tree_contract_tc_kernel<true>, Ly.total, attr_c);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(tree_contract_tc_kernel<true>, dim3(a.B * a.H, a.dv / kTileV), dim3(kThreads), Ly.total,
+                         s, programmatic, tq, tk, tql, tkl, a);
 }
 
 // d_v = 256 with the layout within the shared-memory limit: the single-kernel path.

@@ -174,13 +174,6 @@ def test_two_steps_equal_sequential_decode(layer):
         np.testing.assert_allclose(r2["out"][b], out[len(acc):], rtol=0, atol=1e-12)
 
 
-def test_round_bf16_matches_the_generators_rounding(layer):
-    rng = np.random.default_rng(3)
-    x = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-8, 8, 4000),
-                        [0.0, -0.0, 1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8)]])
-    np.testing.assert_array_equal(layer.round_bf16(x), wl.bf16_bits_to_f64(wl.f32_to_bf16_bits(x.astype(np.float32))))
-
-
 def test_model_step_of_one_layer_is_the_layer_step(layer):
     w = small(21)
     r, x = run(layer, w)
