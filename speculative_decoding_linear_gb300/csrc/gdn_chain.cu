@@ -404,27 +404,7 @@ cudaError_t launch_chain_t(const VerifyArgs& a, cudaStream_t s) {
 // lane's 32 columns are interleaved with its group's (4 at a time) so that the
 // shared-memory reads of a group cover contiguous bytes; the four row groups of
 // a warp read the same k/q words (broadcast), widened to fp32 in registers.
-// Packed fp32 pairs (two independent round-to-nearest operations per instruction,
-// the same results as two fmaf / products).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    unsigned long long ra, rb, rc, rd;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-    float2 d;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-    return d;
-}
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-    unsigned long long ra, rb, rd;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
-    float2 d;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-    return d;
-}
+// Packed fp32 pairs: ffma2 / fmul2 (gdn_internal.cuh).
 
 constexpr int kG8Rows = 16;            // state rows per CTA
 constexpr int kG8Cols = 32;            // state columns per lane (8 groups of 4)

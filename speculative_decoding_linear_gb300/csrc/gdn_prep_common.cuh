@@ -152,6 +152,22 @@ __device__ __forceinline__ void gram_row(int t, int m, const uint8_t* plist, con
     }
 }
 
+// gram_row's entries i = part, part + nparts, ... of row t's path: several threads
+// share one node's row.
+__device__ __forceinline__ void gram_row_part(int t, int part, int nparts, int m, const uint8_t* plist,
+                                              const float* qk, const float* kk, int ld, const float* g,
+                                              const float* beta, float* sA, float* sAt, bool delta_rule = true) {
+    const uint8_t* p = plist + t * 64;
+    const float gt = g[t], bt = beta[t];
+#pragma unroll 1
+    for (int i = part; i <= m; i += nparts) {
+        const int j = p[i];
+        const float gam = expf(gt - g[j]);
+        sAt[t * ld + j] = gam * qk[j];
+        if (j != t) sA[t * ld + j] = delta_rule ? bt * gam * kk[j] : 0.f;
+    }
+}
+
 // solve_rows with the path held in registers: q_0 = t, q_1 = parent, ..., q_m
 // = root.  Row t of T: x_0 = 1, x_i = -sum_{j < i} x_j A[q_j, q_i]; row t of
 // P: P[t, q_i] = sum_{j <= i} Attn[t, q_j] T[q_j, q_i].  Fully unrolled for

@@ -765,7 +765,7 @@ struct FusedLayout {
     // stages and nB q/k buffers during Y, then R (both tiles), the A / Attn / T
     // tables and the [T; P] operand.
     int nB, bsz, ops, R, A, At, T, op;
-    int cd, key, vs, nodes, coef, par, la, g, beta, eg, depth, anc, plist, bars, misc, total;
+    int vs, cd, key, nodes, coef, par, la, g, beta, eg, depth, anc, plist, bars, misc, total;
     __host__ __device__ FusedLayout(int N, int Lcap, bool split) {
         bsz = (split ? 2 : 1) * kBufBytes;
         build(N, Lcap, split, 2);
@@ -787,9 +787,9 @@ struct FusedLayout {
             return;
         }
         o = ops;
+        vs = take(split ? 0 : N * kFRows * 2);      // bf16 v rows [t][256], copied after the wait
         cd = take(Lcap * kFRows * 4);
         key = take(Lcap * kDk * (split ? 4 : 2));
-        vs = take(split ? 0 : N * kFRows * 2);      // bf16 v rows [t][256], copied after the wait
         nodes = take(kMaxPath * 4);
         coef = take(kMaxPath * 4);
         par = take(kMaxNodes * 4);
@@ -801,7 +801,7 @@ struct FusedLayout {
         anc = take(kMaxNodes * 8);
         plist = take(kMaxNodes * 64);
         bars = take(16 * 8);
-        misc = take(16);
+        misc = take(32);
         total = o + 1024;   // slack for aligning the base to 1024 bytes
     }
 };
@@ -814,54 +814,59 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
-// Rows rbase + 32 j (j = 0 .. J-1, J = 4 per 128-row tile) of a CTA's state
-// slab: j < 4 lie in its tile 0, j >= 4 in its tile 1.
-template <int J>
+// Rows rbase + kRS j (j = 0 .. J-1) of a CTA's state slab.  With the default
+// kRS = 32 and J = 4 per 128-row tile, j < 4 lie in its tile 0, j >= 4 in tile 1.
+template <int J, int kRS = 32>
 __device__ __forceinline__ void f_load_slab(float4 (&x)[8], const float* S, size_t srow0, int rbase, int col,
                                             uint64_t pol) {
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const float* p = S + srow0 + (size_t)(rbase + 32 * j) * kDk + col;
+        const float* p = S + srow0 + (size_t)(rbase + kRS * j) * kDk + col;
         asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;\n"
                      : "=f"(x[j].x), "=f"(x[j].y), "=f"(x[j].z), "=f"(x[j].w)
                      : "l"(p), "l"(pol));
     }
 }
-template <int J>
+template <int J, int kRS = 32>
 __device__ __forceinline__ void f_store_slab(const float4 (&x)[8], float* S, size_t srow0, int rbase, int col,
                                              uint64_t pol) {
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        float* p = S + srow0 + (size_t)(rbase + 32 * j) * kDk + col;
+        float* p = S + srow0 + (size_t)(rbase + kRS * j) * kDk + col;
         asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;\n" ::"l"(p), "f"(x[j].x),
                      "f"(x[j].y), "f"(x[j].z), "f"(x[j].w), "l"(pol)
                      : "memory");
     }
 }
-// Same arithmetic order per element as commit_slab (and gdn_commit).  s_cd rows
-// are the (sequence, head)'s 256 state rows; cd_row0 is this thread's first.
-template <int J, typename KT>
+// Same arithmetic order per element as commit_slab (and gdn_commit), in packed
+// fp32 pairs (each lane one correctly rounded product or fma, so the bits are
+// those of the scalar form).  s_cd rows are the (sequence, head)'s 256 state
+// rows; cd_row0 is this thread's first.
+template <int J, typename KT, int kRS = 32>
 __device__ __forceinline__ void f_commit_slab(float4 (&x)[8], float ega, int L, const float* s_cd,
                                               const KT* s_key, int cd_row0, int col) {
+    const float2 e2 = make_float2(ega, ega);
+    float2 lo[J], hi[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        x[j].x *= ega;
-        x[j].y *= ega;
-        x[j].z *= ega;
-        x[j].w *= ega;
+        lo[j] = fmul2(make_float2(x[j].x, x[j].y), e2);
+        hi[j] = fmul2(make_float2(x[j].z, x[j].w), e2);
     }
+#pragma unroll 1
     for (int i = 0; i < L; ++i) {
         const float4 kq = ld4<KT>(s_key, (size_t)i * kDk + col);
+        const float2 k01 = make_float2(kq.x, kq.y), k23 = make_float2(kq.z, kq.w);
         const float* cdi = s_cd + i * kFRows + cd_row0;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
-            const float w = cdi[32 * j];
-            x[j].x = fmaf(w, kq.x, x[j].x);
-            x[j].y = fmaf(w, kq.y, x[j].y);
-            x[j].z = fmaf(w, kq.z, x[j].z);
-            x[j].w = fmaf(w, kq.w, x[j].w);
+            const float w = cdi[kRS * j];
+            const float2 w2 = make_float2(w, w);
+            lo[j] = ffma2(w2, k01, lo[j]);
+            hi[j] = ffma2(w2, k23, hi[j]);
         }
     }
+#pragma unroll
+    for (int j = 0; j < J; ++j) x[j] = make_float4(lo[j].x, lo[j].y, hi[j].x, hi[j].y);
 }
 // hi/lo split into one A stage ([tile 0 hi, tile 0 lo, tile 1 hi, tile 1 lo]).
 template <int J>
@@ -951,9 +956,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
     int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 4);    // path length, or -1: skip the CTA
     float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 8);
+    int* s_vcopy = reinterpret_cast<int*>(base + Ly.misc + 12);  // the v-row copies were issued
+    int* s_qkmask = reinterpret_cast<int*>(base + Ly.misc + 16); // bit s: the q/k copy of slab s was issued
     const uint32_t stage0 = base_s, stage1 = base_s + kFAStage, bbase = base_s + 2 * kFAStage;
     const int nB = Ly.nB;
     auto bbuf = [&](int s) { return bbase + (nB == 2 ? (uint32_t)((s & 1) * Ly.bsz) : 0u); };
+    const uint32_t vrows_s = base_s + Ly.vs;
 
     if (fused && warp == 2 && lane < 6) {   // the pending commit's path, parent and g rows, first of all
         const int r = lane >> 1, half = lane & 1;
@@ -969,6 +977,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         fence_proxy_async_smem();
         *s_flag = 0;
         *s_ega = 1.f;
+        *s_vcopy = 0;
+        *s_qkmask = 0;
     }
     if (warp == 1) tmem_alloc(smem_u32(s_tmem), kFTmemCols);
     tc_fence_before();
@@ -1006,6 +1016,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float4 cur[8], nxt[8];             // slabs 0 and 1 in flight during the commit setup
     f_load_slab<kJ>(cur, a.S, srow0, rbase, 4 * c4, pol_first);
     f_load_slab<kJ>(nxt, a.S, srow0, rbase, kSlab + 4 * c4, pol_first);
+    // slabs 2 and 3 into L2 meanwhile: they are read only after the wait, and the
+    // setup leaves the memory system idle for a few microseconds
+    if (tid < 128 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * kDk + 2 * kSlab, 2 * kSlab * 4);
     bool landed = true;
     if (fused) {
         __syncthreads();
@@ -1019,9 +1032,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     landed = __syncthreads_and(landed);
     const int L = fused ? *s_flag : 0;
     bool ok = L >= 0 && landed;
-    // slabs 2 and 3 and this call's inputs into L2 only now: requests issued
-    // earlier queue ahead of the commit setup's loads and delay the stream
-    if (tid < 128 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * kDk + 2 * kSlab, 2 * kSlab * 4);
+    // this call's inputs into L2 only now: requests issued earlier queue ahead of
+    // the commit setup's loads
     if (tid < N) {                    // this call's inputs into L2; read only after the wait
         const size_t rt = ((size_t)b * N + tid) * H + h;
         if (kSplit) {
@@ -1065,12 +1077,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (warp == kFIssuerWarp && lane == 0) {
             issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(0), 0, h, b * N, bars);
             if (nB == 2) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
+            *s_qkmask = nB == 2 ? 0x3 : 0x1;
         }
         if (!kSplit && warp == kFIssuerWarp + 1) {   // this (sequence, head)'s v rows, one node per lane
-            if (lane == 0) mbar_expect_tx(bar_v, (uint32_t)(N * kFRows * 2));
+            if (lane == 0) {
+                mbar_expect_tx(bar_v, (uint32_t)(N * kFRows * 2));
+                *s_vcopy = 1;
+            }
             __syncwarp();
             for (int t = lane; t < N; t += 32)
-                bulk_copy_g2s(base_s + Ly.vs + t * kFRows * 2,
+                bulk_copy_g2s(vrows_s + t * kFRows * 2,
                               static_cast<const KT*>(a.v) + (((size_t)b * N + t) * H + h) * kFRows, kFRows * 2, bar_v);
         }
         // parents and gates: loads issued now, used once the Y MMAs are under way
@@ -1090,11 +1106,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll 1
         for (int sl = 0; sl < kSlabs; ++sl) {
             if (sl >= 2) {
-                if (sl == 2 && fused && ok) {      // commit slabs 2 and 3 and write them back
-                    f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, 2 * kSlab + 4 * c4);
-                    f_store_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
-                    f_commit_slab<kJ>(nxt, ega, L, s_cd, s_key, row0 + rbase, 3 * kSlab + 4 * c4);
-                    f_store_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
+                if (fused && ok) {                 // commit slab sl and write it back
+                    f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, sl * kSlab + 4 * c4);
+                    f_store_slab<kJ>(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, pol_first);
                 }
                 ok = ok && mbar_wait(bars + 32 + 8 * (sl - 2), 0, a.err);
                 if (ok) f_convert_slab<kJ>(cur, base + (sl & 1) * kFAStage, rbase, c4);
@@ -1114,7 +1128,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     const int sn = sl + nB;                             // next copy into bbuf(sl)
                     if (sn < kSlabs) {
                         l = l && mbar_wait(bars + 32 + 8 * sl, 0, a.err);
-                        if (l) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(sn), sn, h, b * N, bars + 8 * sn);
+                        if (l) {
+                            issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(sn), sn, h, b * N, bars + 8 * sn);
+                            *s_qkmask |= 1 << sn;
+                        }
                     }
                 }
                 __syncwarp();
@@ -1145,14 +1162,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
         // ---- 4. warps 0-7: tables, T, P and the [T; P] operand; warps 8-15: R ----
         if (ok) {
-            if (warp < 4) {
+            if (warp < 8) {
                 // raw Gram rows into the tables, in place of the entries gram_row turns into
-                // A and Attn: TMEM lane r < 64 holds q_r . k_j, lane 64 + r holds k_r . k_j
+                // A and Attn: TMEM lane r < 64 holds q_r . k_j, lane 64 + r holds k_r . k_j;
+                // warps w and w + 4 read the same lanes, columns 0..31 and 32..63
                 const int t = tid & 63;
-                float* row = (tid < 64 ? sAt : sA) + t * ld;
-                const uint32_t t_lane = tmem + ((uint32_t)(32 * warp) << 16) + 256;
+                float* row = ((tid & 127) < 64 ? sAt : sA) + t * ld;
+                const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256;
+                const int cend = min(N, 32 * (warp >> 2) + 32);
 #pragma unroll 1
-                for (int c = 0; c < N; c += 8) {
+                for (int c = 32 * (warp >> 2); c < cend; c += 8) {
                     float gr[8];
                     tmem_ld8(t_lane + c, gr);
                     if (t < N) {
@@ -1164,21 +1183,32 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             if (tid < 256) {
                 prep::group_sync(256);
-                if (tid < N)
-                    prep::gram_row(tid, sdepth[tid], plist, sAt + tid * ld, sA + tid * ld, ld, sg, sbeta, sA, sAt,
-                                   !a.linear);
+                if ((tid >> 2) < N)          // four threads per node, path entries strided by four
+                    prep::gram_row_part(tid >> 2, tid & 3, 4, sdepth[tid >> 2], plist, sAt + (tid >> 2) * ld,
+                                        sA + (tid >> 2) * ld, ld, sg, sbeta, sA, sAt, !a.linear);
                 prep::group_sync(256);
                 prep::solve_rows_fast<9>(tid, N, ld, sdepth, plist, sA, sAt, sT, 256);
                 prep::write_operand(tid, 256, N, ld, anc, sA, sT, base + Ly.op);
             } else {
-                // keys into the factor record
-                constexpr int kVec = 16 / (int)sizeof(KT);
+                // keys into the factor record, four 16-byte loads in flight per thread
+                constexpr int kVec = 16 / (int)sizeof(KT), kRow = kDk / kVec, kBatch = 4;
                 const KT* kin = static_cast<const KT*>(a.k);
                 KT* kout = static_cast<KT*>(a.f.key) + (size_t)bh * N * kDk;
-                for (int item = tid - 256; lead && !a.keys_done && item < N * (kDk / kVec); item += kFThreads - 256) {
-                    const int t = item / (kDk / kVec), c = item % (kDk / kVec);
-                    *reinterpret_cast<uint4*>(kout + (size_t)t * kDk + c * kVec) =
-                        *reinterpret_cast<const uint4*>(kin + (((size_t)b * N + t) * H + h) * kDk + c * kVec);
+                const int items = lead && !a.keys_done ? N * kRow : 0;
+#pragma unroll 1
+                for (int i0 = tid - 256; i0 < items; i0 += kBatch * (kFThreads - 256)) {
+                    uint4 x[kBatch];
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int item = i0 + u * (kFThreads - 256), t = item / kRow, c = item % kRow;
+                        if (item < items)
+                            x[u] = *reinterpret_cast<const uint4*>(kin + (((size_t)b * N + t) * H + h) * kDk + c * kVec);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int item = i0 + u * (kFThreads - 256), t = item / kRow, c = item % kRow;
+                        if (item < items) *reinterpret_cast<uint4*>(kout + (size_t)t * kDk + c * kVec) = x[u];
+                    }
                 }
                 // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) of tile u as bf16
                 // hi + lo rows of the second MMA's A operand (row v, 64 columns t).  kT = 2:
@@ -1233,7 +1263,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     }
                 } else {
                     // bf16 v rows staged in shared memory
-                    const KT* vsm = reinterpret_cast<const KT*>(base + Ly.vs) + row0 + 128 * u + v;
+                    const KT* vsm = reinterpret_cast<const KT*>(base + (vrows_s - base_s)) + row0 + 128 * u + v;
                     const bool vok = mbar_wait(bar_v, 0, a.err);
 #pragma unroll 1
                     for (int t0 = tbeg; t0 < tend; t0 += 8) {
@@ -1299,8 +1329,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
     }
 
-    // ---- teardown: the v copies have landed; TMEM is always released ----
-    if (!kSplit && L >= 0 && landed && tid == 0) mbar_wait(bar_v, 0, a.err);
+    // ---- teardown: every copy into shared memory has landed; TMEM is always released ----
+    if (tid == 0) {
+        if (!kSplit && *s_vcopy) mbar_wait(bar_v, 0, a.err);
+        for (int s = 0; s < kSlabs; ++s)      // done already unless a wait gave up on the way
+            if ((*s_qkmask >> s) & 1) mbar_wait(bars + 8 * s, 0, a.err);
+    }
     if (!landed && tid == 0) mbar_wait(bar_c, 0, a.err);    // the commit copies, before the CTA's memory goes
     tc_fence_before();
     __syncthreads();
