@@ -114,13 +114,13 @@ def layer_kernel_work(B, N, H, hidden, dk, dv, L_total, Lmax):
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel from one ncu
 # capture, keyed by (workload, kernel), with the hash of the kernel sources it was taken on: a changed
 # kernel reports null.  How each figure was taken is in profiles/.
+_TREE_SRC = ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh", "gdn_internal.cuh")
 NCU_TRAFFIC = {
-    ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.276e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
-                                               "4369be9a62c19566"),
-    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (
-        2.615e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh", "gdn_internal.cuh"), "1ca8894d6f526df8"),
-    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (
-        47.74e6, ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh", "gdn_internal.cuh"), "1ca8894d6f526df8"),
+    ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.274e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
+                                               "b67ec3376243f1fc"),
+    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.615e6, _TREE_SRC, "1ca8894d6f526df8"),
+    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (48.49e6, _TREE_SRC, "c5f08b699625db92"),
+    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (386.2e6, _TREE_SRC + ("gdn_layer.cu",), "cfe72fafbfc44491"),
 }
 NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
                     "start; writes still held in L2 when the kernel ends are not counted)")
@@ -405,7 +405,7 @@ def l2_size(torch, device_index):
 
 
 def run_tree(cfg, steps, warmup, rank, world, device_index, torch, dist, profile=False, batch=None, layers=None,
-             shard_mode="replicas", extras=True):
+             shard_mode="replicas", extras=True, side=True):
     """Commit + verify calls of workload `cfg` over a rotation of layer instances."""
     from speculative_decoding_linear_gb300 import gdnspec
     from speculative_decoding_linear_gb300 import workloads as wl
@@ -474,9 +474,9 @@ def run_tree(cfg, steps, warmup, rank, world, device_index, torch, dist, profile
         prev = gdnspec.gdn_set_launch_overlap(False)
         cold, warm = cold_and_warm(one, stream, torch, l2)
         gdnspec.gdn_set_launch_overlap(prev)
-    e2e = None if profile or not extras else run_e2e(lys, steps, chain, gdnspec, torch, stream, world, dist, device,
-                                                    shard_mode)
-    more = extras and not profile and not chain
+    e2e = None if profile or not (extras and side) else run_e2e(lys, steps, chain, gdnspec, torch, stream, world,
+                                                               dist, device, shard_mode)
+    more = extras and side and not profile and not chain
     baselines = run_replay_baselines(lys, gdnspec, torch, stream, max(5, min(steps, 20))) if more else None
     hybrid = run_hybrid_comparison(lys, gdnspec, torch, stream, max(5, min(steps, 20)), device, wl) if more else None
     prune = run_prune_timing(gdnspec, torch, stream, device, wl, B=B, N=N) if more else None
@@ -1214,13 +1214,17 @@ def main():
         __graft_entry__.build()
     if world > 1:
         dist.barrier()
-    sub = None
+    sub = small = None
     if args.config == 4:
         r = run_layer(args.steps, args.warmup, rank, world, local, torch, dist, args.profile, args.layers, args.shard)
         if not (args.profile or args.no_sub):
             torch.cuda.empty_cache()
             sub = run_tree(3, args.steps, args.warmup, rank, world, local, torch, dist, False, None, None, args.shard)
             sub["gla"] = run_gla(args.steps, rank, world, local, torch, args.shard, sub["l2"])
+            torch.cuda.empty_cache()
+            # the single-sequence workloads: the 8-token chain and the 32-node tree
+            small = {c: run_tree(c, args.steps, args.warmup, rank, world, local, torch, dist, False, None, None,
+                                 "replicas", True, False) for c in (1, 2)}
     else:
         r = run_tree(args.config, args.steps, args.warmup, rank, world, local, torch, dist, args.profile,
                      args.batch, args.layers, args.shard)
@@ -1260,6 +1264,10 @@ def main():
                 if sub.get(key):
                     rec[name] = sub[key]
             line["tree_verify_commit"] = rec
+            line["single_sequence"] = {
+                s["spec"].name: {"value": round(s["value"], 1), "unit": UNIT, "ms_per_step": round(s["ms"], 4),
+                                 "layers_rotated": s["R"], "roofline": s["roofline"], "replays": s["replays"],
+                                 "gpu_launches": s["gpu_launches"]} for s in small.values()}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
