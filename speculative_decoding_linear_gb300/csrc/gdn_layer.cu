@@ -1,8 +1,9 @@
 // gdn_layer.cu -- one full GDN layer decode step over B draft trees.
 //
 // SpecLA review (pith.science 7ERME3HB), "Referee Report" major comment 1:
-// one GDN layer (hidden 2048, h_v = 8 heads of d_k = d_v = 256) with a causal
-// depthwise convolution of kernel size 4 and SiLU output gating; "Core claim":
+// the benchmarked unit is one GDN layer -- hidden 2048, 8 heads of 256, a
+// four-tap depthwise conv in front of the recurrence and a SiLU gate on its
+// output; "Core claim":
 // every draft node sees the recurrence along its own root-to-node path only,
 // so the convolution window of node t is (great-grandparent, grandparent,
 // parent, t), with the committed convolution history standing in above a root.

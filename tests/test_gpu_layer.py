@@ -82,6 +82,8 @@ def compare(w, r, out, Y, fac, views, parent):
     np.testing.assert_allclose(views["alpha"].cpu().numpy(), r["alpha"], rtol=2e-5, atol=1e-6)
     np.testing.assert_allclose(views["beta"].cpu().numpy(), r["beta"], rtol=2e-5, atol=1e-6)
     assert_close(views["o"].cpu().numpy(), r["o"], "o")
+    y = (views["yhi"].float() + views["ylo"].float()).cpu().numpy().reshape(B, N, H * dv)
+    assert_close(y, r["y"], "gated output y (hi + lo)")
     assert_close(delta.cpu().numpy(), r["delta"], "delta")
     assert np.array_equal(par.cpu().numpy(), parent)
     return assert_close(out.cpu().numpy(), r["out"], "layer output")
