@@ -522,6 +522,8 @@ def run_replay_baselines(layers, gdnspec, torch, stream, steps):
     prev = gdnspec.gdn_set_launch_overlap(False)
     scratch = [torch.empty_like(ly.S) for ly in layers]
     w0 = layers[0].w
+    # every node's state, for the snapshot baseline (one buffer shared by the rotation)
+    S_nodes = torch.empty((w0.N, w0.B, w0.H, w0.dv, w0.dk), dtype=torch.float32, device=layers[0].S.device)
 
     def variant(name):
         def call(ly, sc):
@@ -532,6 +534,10 @@ def run_replay_baselines(layers, gdnspec, torch, stream, steps):
                 gdnspec.gdn_replay_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out)
             elif name == "factor_commit":
                 gdnspec.gdn_commit(ly.S, ly.fac[0], ly.path, sc, w.N, w.dtype)
+            elif name == "snapshot_verify":
+                gdnspec.gdn_snapshot_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out, S_nodes)
+            elif name == "snapshot_commit":
+                gdnspec.gdn_snapshot_commit(S_nodes, ly.S, ly.parent, ly.path, sc)
             else:
                 gdnspec.gdn_replay_commit(ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.path, sc)
         with torch.cuda.stream(stream):
@@ -556,15 +562,19 @@ def run_replay_baselines(layers, gdnspec, torch, stream, steps):
     with torch.cuda.stream(stream):
         for ly in layers:                 # the factor record the commits read
             gdnspec.gdn_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out, ly.fac[0], ly.ws)
-    us = {n: variant(n) for n in ("tree_verify", "replay_verify", "factor_commit", "replay_commit")}
+    us = {n: variant(n) for n in ("tree_verify", "replay_verify", "factor_commit", "replay_commit",
+                                  "snapshot_verify", "snapshot_commit")}
     gdnspec.gdn_set_launch_overlap(prev)
-    del scratch
+    del scratch, S_nodes
     return {"us_per_call": {k: round(v, 3) for k, v in us.items()},
             "replay_verify_over_tree_verify": round(us["replay_verify"] / us["tree_verify"], 2),
             "replay_commit_over_factor_commit": round(us["replay_commit"] / us["factor_commit"], 2),
+            "snapshot_verify_over_tree_verify": round(us["snapshot_verify"] / us["tree_verify"], 2),
+            "snapshot_commit_over_factor_commit": round(us["snapshot_commit"] / us["factor_commit"], 2),
             "what": "per layer call, %s, same rotation of %d layers; replay = every root-to-leaf path "
-                    "(verify) or the accepted tokens (commit) run token by token from S0"
-                    % (w0.spec.name, len(layers))}
+                    "(verify) or the accepted tokens (commit) run token by token from S0; snapshot = every "
+                    "node's state built from its parent's and stored (verify, one launch per node index), "
+                    "then the accepted node's state copied (commit)" % (w0.spec.name, len(layers))}
 
 
 # ---------------------------------------------------------------------------

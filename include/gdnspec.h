@@ -367,6 +367,30 @@ int gdn_replay_commit(const void* k, const void* v, int dtype, const float* alph
                       float* S_new, int B, int N, int H, int dk, int dv, cudaStream_t stream);
 
 /*
+ * Snapshot baseline of state management ("Pith review of SpecLA", Figure 11:
+ * the factor-buffer commit against keeping every draft node's state and
+ * against replaying the accepted tokens).  Same tensors as gdn_tree_verify;
+ * fp32 state throughout.
+ *
+ * gdn_snapshot_tree_verify: every node's state S_t = alpha_t S_p + delta_t k_t^T,
+ * delta_t = beta_t (v_t - alpha_t S_p k_t), is built from its parent's stored state
+ * (S0 above a root) and stored, node by node in index order; o_t = S_t q_t.
+ *   S_nodes  fp32 [N][B][H][d_v][d_k], written (N times the state)
+ * Invalid parent_idx -> GDN_ERR_TREE in the error word.
+ *
+ * gdn_snapshot_commit: S_new = S_nodes[a] for the last node a of the accepted
+ * path (int32 [B][Lmax], root first, -1 padded, checked against parent_idx);
+ * S_new = S0 for an empty path.  S_new may equal S0.  Invalid path ->
+ * GDN_ERR_PATH in the error word, that sequence's S_new untouched.
+ */
+int gdn_snapshot_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
+                             const float* beta, const int32_t* parent_idx, const float* S0, float* out,
+                             float* S_nodes, int B, int N, int H, int dk, int dv, cudaStream_t stream);
+int gdn_snapshot_commit(const float* S_nodes, const float* S0, const int32_t* parent_idx,
+                        const int32_t* accepted_path, int Lmax, float* S_new, int B, int N, int H, int dk,
+                        int dv, cudaStream_t stream);
+
+/*
  * Tree verification of decay-gated linear attention (Mamba-2 / RetNet-style:
  * S_t = alpha_t S_parent(t) + beta_t v_t k_t^T, o_t = S_t q_t, no delta-rule
  * erasure) through the same kernels and factor record: the review of SpecLA

@@ -33,7 +33,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kGThreads = 256;
+constexpr int kGThreads = 1024;
 constexpr int kGcThreads = 256;
 constexpr int kGcRows = 16;      // state rows per commit CTA
 
@@ -142,42 +142,43 @@ __global__ void __launch_bounds__(kGThreads) gla_prep_kernel(GlaArgs a) {
             cp_async16((r < N ? sq + t * dk : sk + t * dk) + cc * (16 / (int)sizeof(T)), src + cc * (16 / (int)sizeof(T)));
         }
     }
-    for (int c = tid; c < dk; c += kGThreads) {
-        const float* al = a.alpha + ((size_t)b * N * H + h) * dk + c;
-#pragma unroll 8
-        for (int t = 0; t < N; ++t) sg[t * dk + c] = logf(al[(size_t)t * H * dk]);
+#pragma unroll 4
+    for (int i = tid; i < N * dk; i += kGThreads) {
+        const int t = i / dk, c = i - t * dk;
+        sg[i] = logf(a.alpha[(((size_t)b * N + t) * H + h) * dk + c]);
     }
     cp_async_wait_all();
     __syncthreads();
 
-    // Thread c owns key channel c: g_t[c] = g_parent(t)[c] + log alpha_t[c] in node
-    // order (parents come first, and were written by this same thread); then the
-    // record's g and key copy and qhat_t[c] = q_t[c] e^{g_t[c]}.
-    __nv_bfloat16* qh = static_cast<__nv_bfloat16*>(a.qhat);
-    __nv_bfloat16* ql = qh + (size_t)a.B * N * H * dk;
+    // Thread c < d_k owns key channel c: g_t[c] = g_parent(t)[c] + log alpha_t[c] in
+    // node order (parents come first, and were written by this same thread).
     for (int c = tid; c < dk; c += kGThreads) {
 #pragma unroll 1
         for (int t = 1; t < N; ++t) {
             const int p = par[t];
             if (p >= 0) sg[t * dk + c] += sg[p * dk + c];
         }
-#pragma unroll 4
-        for (int t = 0; t < N; ++t) {
-            const size_t src = (((size_t)b * N + t) * H + h) * dk + c;
-            const size_t dst = ((size_t)bh * N + t) * dk + c;
-            const float gt = sg[t * dk + c];
-            a.g[dst] = gt;
-            const T kv = kStage ? sk[t * dk + c] : k[src];
-            const T qv = kStage ? sq[t * dk + c] : q[src];
-            static_cast<T*>(a.key)[dst] = kv;
-            const float x = ld_elem<T>(&qv, 0) * expf(gt);
-            if (kTc) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-                qh[src] = hi;
-                ql[src] = __float2bfloat16_rn(x - __bfloat162float(hi));
-            } else {
-                static_cast<float*>(a.qhat)[src] = x;
-            }
+    }
+    __syncthreads();
+    // the record's g and key copy and qhat_t[c] = q_t[c] e^{g_t[c]}, every (node, channel)
+    __nv_bfloat16* qh = static_cast<__nv_bfloat16*>(a.qhat);
+    __nv_bfloat16* ql = qh + (size_t)a.B * N * H * dk;
+    for (int i = tid; i < N * dk; i += kGThreads) {
+        const int t = i / dk, c = i - t * dk;
+        const size_t src = (((size_t)b * N + t) * H + h) * dk + c;
+        const size_t dst = ((size_t)bh * N + t) * dk + c;
+        const float gt = sg[i];
+        a.g[dst] = gt;
+        const T kv = kStage ? sk[i] : k[src];
+        const T qv = kStage ? sq[i] : q[src];
+        static_cast<T*>(a.key)[dst] = kv;
+        const float x = ld_elem<T>(&qv, 0) * expf(gt);
+        if (kTc) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+            qh[src] = hi;
+            ql[src] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        } else {
+            static_cast<float*>(a.qhat)[src] = x;
         }
     }
     if (a.v32 != nullptr)
@@ -241,28 +242,6 @@ struct GlaCommitArgs {
     int* err;
 };
 
-// Accepted-path check by one full warp: the -1 padded path row must be a
-// root-first parent chain of the previous tree.  Returns L, or -1 if invalid;
-// fills s_nodes[0 .. L).
-__device__ int gla_path_setup(const int32_t* row, int Lmax, const int32_t* par, int N, int* s_nodes) {
-    const int lane = threadIdx.x & 31;
-    int n[2];
-#pragma unroll
-    for (int s = 0; s < 2; ++s) n[s] = lane + 32 * s < Lmax ? row[lane + 32 * s] : -1;
-    const unsigned long long nn = (unsigned long long)__ballot_sync(0xffffffffu, n[0] >= 0) |
-                                  ((unsigned long long)__ballot_sync(0xffffffffu, n[1] >= 0) << 32);
-    const int L = (~nn == 0ull) ? 64 : __ffsll((long long)~nn) - 1;
-    bool bad = n[0] < -1 || n[1] < -1 || n[0] >= N || n[1] >= N || nn != (L == 64 ? ~0ull : (1ull << L) - 1ull);
-    const int up0 = __shfl_up_sync(0xffffffffu, n[0], 1), up1 = __shfl_up_sync(0xffffffffu, n[1], 1);
-    const int last0 = __shfl_sync(0xffffffffu, n[0], 31);
-    if (!bad && lane < L) bad = par[n[0]] != (lane == 0 ? -1 : up0);
-    if (!bad && lane + 32 < L) bad = par[n[1]] != (lane == 0 ? last0 : up1);
-    if (__any_sync(0xffffffffu, bad)) return -1;
-    if (lane < L) s_nodes[lane] = n[0];
-    if (lane + 32 < L) s_nodes[lane + 32] = n[1];
-    return L;
-}
-
 // Dynamic shared memory of the commit: e^{g_a} [dk], w [Lmax][dk], delta [Lmax][16].
 inline size_t gla_commit_smem(int Lmax, int dk) { return ((size_t)dk + (size_t)Lmax * dk + (size_t)Lmax * kGcRows) * 4; }
 
@@ -279,7 +258,7 @@ __global__ void __launch_bounds__(kGcThreads) gla_commit_kernel(GlaCommitArgs a)
     griddep_wait();
     griddep_launch();
     if (tid < 32) {
-        const int L = gla_path_setup(a.path + (size_t)b * a.Lmax, a.Lmax, a.parent + (size_t)b * N, N, s_nodes);
+        const int L = path_chain_setup(a.path + (size_t)b * a.Lmax, a.Lmax, a.parent + (size_t)b * N, N, s_nodes);
         if (tid == 0) {
             s_L = L;
             if (L < 0 && blockIdx.y == 0 && bh % a.H == 0) set_error(a.err, GDN_ERR_PATH);

@@ -204,6 +204,28 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// Accepted-path check by one full warp: the -1 padded path row must be a
+// root-first parent chain of the tree with parents `par` (N entries).  Returns L,
+// or -1 if invalid; fills s_nodes[0 .. L).
+__device__ inline int path_chain_setup(const int32_t* row, int Lmax, const int32_t* par, int N, int* s_nodes) {
+    const int lane = threadIdx.x & 31;
+    int n[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) n[s] = lane + 32 * s < Lmax ? row[lane + 32 * s] : -1;
+    const unsigned long long nn = (unsigned long long)__ballot_sync(0xffffffffu, n[0] >= 0) |
+                                  ((unsigned long long)__ballot_sync(0xffffffffu, n[1] >= 0) << 32);
+    const int L = (~nn == 0ull) ? 64 : __ffsll((long long)~nn) - 1;
+    bool bad = n[0] < -1 || n[1] < -1 || n[0] >= N || n[1] >= N || nn != (L == 64 ? ~0ull : (1ull << L) - 1ull);
+    const int up0 = __shfl_up_sync(0xffffffffu, n[0], 1), up1 = __shfl_up_sync(0xffffffffu, n[1], 1);
+    const int last0 = __shfl_sync(0xffffffffu, n[0], 31);
+    if (!bad && lane < L) bad = par[n[0]] != (lane == 0 ? -1 : up0);
+    if (!bad && lane + 32 < L) bad = par[n[1]] != (lane == 0 ? last0 : up1);
+    if (__any_sync(0xffffffffu, bad)) return -1;
+    if (lane < L) s_nodes[lane] = n[0];
+    if (lane + 32 < L) s_nodes[lane + 32] = n[1];
+    return L;
+}
+
 // Accepted-path setup, executed by ONE full warp.  Validates the -1 padded,
 // root-first path row against the previous tree's parents and fills
 //   s_nodes[i]  accepted node i (root first), i < L

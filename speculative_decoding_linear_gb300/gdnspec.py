@@ -53,6 +53,8 @@ SIGNATURES = {
     "gdn_hybrid_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_snapshot_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_snapshot_commit": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_linear_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_gla_factors_bytes": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
     "gdn_gla_workspace_bytes": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_S)]),
@@ -341,6 +343,23 @@ def gdn_replay_commit(k, v, alpha, beta, parent_idx, S0, accepted_path, S_new, s
     _check(lib().gdn_replay_commit(_ptr(k), _ptr(v), dtype_code(k.dtype), _ptr(alpha), _ptr(beta), _ptr(parent_idx),
                                    _ptr(S0), _ptr(accepted_path), accepted_path.shape[1], _ptr(S_new), B, N, H, dk,
                                    dv, _stream(stream)), "gdn_replay_commit")
+
+
+def gdn_snapshot_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, S_nodes, stream=None):
+    """Baseline: build and store every draft node's state, node by node (see include/gdnspec.h);
+    S_nodes is [N, B, H, dv, dk] fp32."""
+    B, N, H, dk, dv = _dims(q, v)
+    _check(lib().gdn_snapshot_tree_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha), _ptr(beta),
+                                          _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(S_nodes), B, N, H, dk, dv,
+                                          _stream(stream)), "gdn_snapshot_tree_verify")
+
+
+def gdn_snapshot_commit(S_nodes, S0, parent_idx, accepted_path, S_new, stream=None):
+    """Baseline: the accepted node's stored state becomes the committed state (see include/gdnspec.h)."""
+    N, B, H, dv, dk = S_nodes.shape
+    _check(lib().gdn_snapshot_commit(_ptr(S_nodes), _ptr(S0), _ptr(parent_idx), _ptr(accepted_path),
+                                     accepted_path.shape[1], _ptr(S_new), B, N, H, dk, dv, _stream(stream)),
+           "gdn_snapshot_commit")
 
 
 def gdn_linear_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, workspace, stream=None):
