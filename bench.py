@@ -609,11 +609,13 @@ def run_hybrid_comparison(layers, gdnspec, torch, stream, steps, device, wl):
     res = {}
     narrow = [Layer(wl.custom_workload(w0.B, w0.N, w0.H, w0.dk, w0.dv, wl.narrow_tree(w0.N, 4, 8), seed=9000 + r),
                     device, torch, gdnspec) for r in range(len(layers))]
+    hws_bytes = gdnspec.gdn_hybrid_workspace_bytes(w0.B, w0.N, w0.H, w0.dk, w0.dv)
+    hws = torch.empty(hws_bytes, dtype=torch.uint8, device=device) if hws_bytes else None   # calls in stream order
     for name, lys in (("bench_trees", layers), ("narrow_trees", narrow)):
         tree = [lambda ly=ly: gdnspec.gdn_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S, ly.out,
                                                       ly.fac[0], ly.ws) for ly in lys]
         hyb = [lambda ly=ly: gdnspec.gdn_hybrid_tree_verify(ly.q, ly.k, ly.v, ly.alpha, ly.beta, ly.parent, ly.S,
-                                                            ly.out, ly.fac[0]) for ly in lys]
+                                                            ly.out, ly.fac[0], hws) for ly in lys]
         t_tree = time_calls(tree, torch, stream, steps)
         t_hyb = time_calls(hyb, torch, stream, steps)
         rc = gdnspec.gdn_last_error(stream)

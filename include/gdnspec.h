@@ -57,8 +57,8 @@ extern "C" {
 #define GDN_ERR_TIMEOUT (-4)  /* a bounded device wait ran out (device-detected) */
 #define GDN_ERR_CUDA (-5)     /* a CUDA runtime call or launch failed */
 #define GDN_ERR_DEVICE (-6)   /* current device is not sm_103 */
-#define GDN_ERR_CAPACITY (-7) /* request larger than a fixed on-device capacity: gdn_tree_verify_noalloc's
-                                 scratch, gdn_hybrid_tree_verify's branch-state slots */
+#define GDN_ERR_CAPACITY (-7) /* request larger than a fixed on-device capacity (gdn_tree_verify_noalloc's
+                                 scratch array) */
 
 /* ---- q/k/v element types ------------------------------------------------ */
 #define GDN_DTYPE_BF16 0
@@ -311,15 +311,23 @@ int gdn_layer_token_step(const void* X, const void* W_in, const float* conv_w, c
  * root or at a child of a node with two or more children and follows
  * only-children); chains whose parent chain is done run concurrently, each
  * token by token on state rows held in registers; a chain ending at a
- * branching node keeps its state rows on chip for the chains below.  Same
+ * branching node leaves its state rows in a slot for the chains below.  Same
  * tensors, outputs and factor record as gdn_tree_verify (so gdn_commit applies
- * to its factors), no workspace.  Suited to deep, narrow trees.  At most 8
- * branching nodes (nodes with two or more children) per tree: more records
- * GDN_ERR_CAPACITY in the error word and writes nothing.
+ * to its factors).  Suited to deep, narrow trees.  Any valid tree runs: the
+ * first 8 live branch states per tree are kept on chip, the rest spill to the
+ * workspace.
+ *   workspace  gdn_hybrid_workspace_bytes(B,N,H,dk,dv) bytes of device
+ *              scratch, 16-byte aligned, not overlapping out or factors; may
+ *              be NULL when that size is 0 (N <= 18).  Sized for the most
+ *              branching nodes an N-node tree can have, (N - 1) / 2.
+ * Returns GDN_ERR_ARG for bad shapes, pointers or overlaps (nothing launched);
+ * an invalid parent_idx records GDN_ERR_TREE in the error word.
  */
+int gdn_hybrid_workspace_bytes(int B, int N, int H, int dk, int dv, size_t* bytes);
+
 int gdn_hybrid_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
                            const float* beta, const int32_t* parent_idx, const float* S0, float* out,
-                           void* factors, int B, int N, int H, int dk, int dv, cudaStream_t stream);
+                           void* factors, void* workspace, int B, int N, int H, int dk, int dv, cudaStream_t stream);
 
 /*
  * Confidence-guided pruning of B draft trees before verification ("Pith review

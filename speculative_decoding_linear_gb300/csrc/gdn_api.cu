@@ -267,8 +267,7 @@ const char* gdn_strerror(int code) {
         case GDN_ERR_CUDA: return "CUDA runtime error";
         case GDN_ERR_DEVICE: return "current device is not an sm_103 GPU";
         case GDN_ERR_CAPACITY:
-            return "request exceeds a fixed on-device capacity (gdn_tree_verify_noalloc's scratch array, "
-                   "gdn_hybrid_tree_verify's branch-state slots)";
+            return "request exceeds a fixed on-device capacity (gdn_tree_verify_noalloc's scratch array)";
         default: return "unknown status";
     }
 }

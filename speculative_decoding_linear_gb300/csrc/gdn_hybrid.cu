@@ -13,15 +13,18 @@
 //     delta_t = beta_t (v_t - alpha_t S k_t),  S <- alpha_t S + delta_t k_t^T,
 //     o_t = S q_t,
 //
-// and a chain that ends at a branching node leaves its state rows in shared
-// memory for the chains below it.  Every node is computed once, as in the
-// tree verifier, and the factor record (delta, k, g, parent) is the same, so
+// and a chain that ends at a branching node leaves its state rows in a slot
+// for the chains below it.  Every node is computed once, as in the tree
+// verifier, and the factor record (delta, k, g, parent) is the same, so
 // gdn_commit applies to it unchanged.
 //
 // One CTA owns kRows rows of one (sequence, head) state; its warps take the
-// chains of one level of the chain tree at a time.  At most kMaxBranch
-// branching nodes per tree (their state rows live in shared memory); more
-// records GDN_ERR_CAPACITY and writes nothing.
+// chains of one level of the chain tree at a time.  A branch state is live
+// from the level whose chain writes it to the end of the next level, whose
+// chains start from it, so slots are reused level by level, lowest free slot
+// first.  The first kSmemSlots slots are in shared memory; the rest spill to
+// the caller's workspace, sized for the most branching nodes an N-node tree
+// can have, (N - 1) / 2, so every valid tree runs.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -30,16 +33,25 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kRows = 8;             // state rows per CTA; every warp holds all of them for its chain
 constexpr int kEPL = kMaxDim / 32;   // state columns per lane
-constexpr int kMaxBranch = 8;
+constexpr int kSmemSlots = 8;        // branch-state slots in shared memory (two CTAs per SM at d_k = 256)
 constexpr int kChunk = 8;            // chain tokens staged per warp at a time
 
-// dynamic smem: branch-state slots [kMaxBranch][kRows][dk] fp32, then per warp
+// a node with >= 2 children uses >= 2 of the N - 1 possible child links, so an
+// N-node forest has at most (N - 1) / 2 branching nodes
+__host__ __device__ inline int spill_slots(int N) { return max(0, (N - 1) / 2 - kSmemSlots); }
+
+// dynamic smem: branch-state slots [kSmemSlots][kRows][dk] fp32, then per warp
 // a token chunk [kChunk][k | q][dk] of the input type
 struct HybridSmem {
     int branch, tok, total;
     __host__ __device__ HybridSmem(int dk, int esz)
-        : branch(0), tok(kMaxBranch * kRows * dk * 4), total(tok + kWarps * kChunk * 2 * dk * esz) {}
+        : branch(0), tok(kSmemSlots * kRows * dk * 4), total(tok + kWarps * kChunk * 2 * dk * esz) {}
 };
+
+// workspace: per CTA (bh, blockIdx.y) spill_slots(N) slots of [kRows][dk] fp32
+size_t hybrid_ws_bytes(int B, int N, int H, int dk, int dv) {
+    return (size_t)B * H * ((dv + kRows - 1) / kRows) * spill_slots(N) * kRows * dk * sizeof(float);
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
@@ -84,9 +96,6 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
                 s_only[p] = t;
             }
         }
-        int nb = 0;
-        for (int t = 0; t < N && !fail; ++t) s_slot[t] = s_nch[t] >= 2 ? nb++ : -1;
-        if (!fail && nb > kMaxBranch) fail = GDN_ERR_CAPACITY;
         int nc = 0, off = 0, nlev = 0;
         if (!fail) {
             for (int t = 0; t < N; ++t) {
@@ -110,6 +119,29 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
             int fill[kMaxNodes + 1];
             for (int l = 0; l <= nlev; ++l) fill[l] = s_loff[l];
             for (int c = 0; c < nc; ++c) s_order[fill[s_clevel[c]]++] = c;
+            // slots of the branch states: those written at level l are read at level l + 1, so
+            // they are taken while the level l - 1 ones are still held and freed after level l + 1
+            const int nslots = kSmemSlots + spill_slots(N);
+            unsigned long long busy = 0ull;
+            for (int t = 0; t < N; ++t) s_slot[t] = -1;
+            for (int l = 0; l < nlev && !fail; ++l) {
+                for (int ci = s_loff[l]; ci < s_loff[l + 1]; ++ci) {
+                    const int u = s_nodes[s_coff[s_order[ci] + 1] - 1];
+                    if (s_nch[u] < 2) continue;
+                    const int sl = __ffsll((long long)~busy) - 1;
+                    if (sl < 0 || sl >= nslots) {             // cannot happen for a valid tree
+                        fail = GDN_ERR_CAPACITY;
+                        break;
+                    }
+                    busy |= 1ull << sl;
+                    s_slot[u] = sl;
+                }
+                if (l >= 1)
+                    for (int ci = s_loff[l - 1]; ci < s_loff[l]; ++ci) {
+                        const int u = s_nodes[s_coff[s_order[ci] + 1] - 1];
+                        if (s_slot[u] >= 0) busy &= ~(1ull << s_slot[u]);
+                    }
+            }
         }
         s_nc = nc;
         s_nlev = nlev;
@@ -124,6 +156,12 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
     const T* vg = static_cast<const T*>(a.v);
     T* tok = reinterpret_cast<T*>(smem + Ls.tok) + (size_t)warp * kChunk * 2 * dk;
     const int rowb = dk * (int)sizeof(T);
+    // slot i: shared memory below kSmemSlots, else this CTA's part of the workspace
+    float* const spill = reinterpret_cast<float*>(a.ws) +
+                         ((size_t)bh * gridDim.y + blockIdx.y) * spill_slots(N) * kRows * dk;
+    auto slot_rows = [&](int i) -> float* {
+        return i < kSmemSlots ? s_branch + (size_t)i * kRows * dk : spill + (size_t)(i - kSmemSlots) * kRows * dk;
+    };
 
     for (int lvl = 0; lvl < s_nlev; ++lvl) {
         for (int ci = s_loff[lvl] + warp; ci < s_loff[lvl + 1]; ci += kWarps) {
@@ -142,7 +180,7 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
                     }
                 }
             } else {
-                const float* st = s_branch + (size_t)s_slot[p] * kRows * dk;
+                const float* st = slot_rows(s_slot[p]);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r)
 #pragma unroll
@@ -231,7 +269,7 @@ __global__ void __launch_bounds__(kWarps * 32) hybrid_kernel(VerifyArgs a) {
             }
             const int last = s_nodes[s_coff[c + 1] - 1];
             if (s_slot[last] >= 0) {                  // branching node: rows for the chains below
-                float* st = s_branch + (size_t)s_slot[last] * kRows * dk;
+                float* st = slot_rows(s_slot[last]);
 #pragma unroll
                 for (int r = 0; r < kRows; ++r)
 #pragma unroll
@@ -278,9 +316,19 @@ cudaError_t launch_hybrid_t(const VerifyArgs& a, cudaStream_t s) {
 
 using namespace gdn;
 
+extern "C" int gdn_hybrid_workspace_bytes(int B, int N, int H, int dk, int dv, size_t* bytes) {
+    auto dim_ok = [](int d) { return d >= 16 && d <= kMaxDim && d % 16 == 0; };
+    if (bytes == nullptr || B < 1 || H < 1 || N < 1 || N > kMaxNodes || !dim_ok(dk) || !dim_ok(dv) ||
+        (long long)B * H > 0x7fffffffLL)
+        return GDN_ERR_ARG;
+    *bytes = hybrid_ws_bytes(B, N, H, dk, dv);
+    return GDN_OK;
+}
+
 extern "C" int gdn_hybrid_tree_verify(const void* q, const void* k, const void* v, int dtype, const float* alpha,
                                       const float* beta, const int32_t* parent_idx, const float* S0, float* out,
-                                      void* factors, int B, int N, int H, int dk, int dv, cudaStream_t stream) {
+                                      void* factors, void* workspace, int B, int N, int H, int dk, int dv,
+                                      cudaStream_t stream) {
     auto ok16 = [](const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     auto dim_ok = [](int d) { return d >= 16 && d <= kMaxDim && d % 16 == 0; };
     if (B < 1 || H < 1 || N < 1 || N > kMaxNodes || !dim_ok(dk) || !dim_ok(dv) || (long long)B * H > 0x7fffffffLL)
@@ -289,11 +337,15 @@ extern "C" int gdn_hybrid_tree_verify(const void* q, const void* k, const void* 
     if (!ok16(q) || !ok16(k) || !ok16(v) || !ok16(alpha) || !ok16(beta) || !ok16(parent_idx) || !ok16(S0) ||
         !ok16(out) || !ok16(factors))
         return GDN_ERR_ARG;
+    const size_t wbytes = hybrid_ws_bytes(B, N, H, dk, dv);
+    if (wbytes > 0 && !ok16(workspace)) return GDN_ERR_ARG;
     const size_t fbytes = factor_layout(B, N, H, dk, dv, dtype).total;
     const size_t obytes = (size_t)B * N * H * dv * 4;
     const char* o = reinterpret_cast<const char*>(out);
     const char* f = static_cast<const char*>(factors);
+    const char* w = static_cast<const char*>(workspace);
     if (o < f + fbytes && f < o + obytes) return GDN_ERR_ARG;
+    if (wbytes > 0 && ((o < w + wbytes && w < o + obytes) || (f < w + wbytes && w < f + fbytes))) return GDN_ERR_ARG;
     int st = GDN_OK;
     int* err = current_error_word(&st);
     if (err == nullptr) return st;
@@ -307,7 +359,7 @@ extern "C" int gdn_hybrid_tree_verify(const void* q, const void* k, const void* 
     a.S = const_cast<float*>(S0);
     a.out = out;
     a.f = factors_view(factors, B, N, H, dk, dv, dtype);
-    a.ws = nullptr;
+    a.ws = wbytes > 0 ? static_cast<char*>(workspace) : nullptr;
     a.B = B;
     a.N = N;
     a.H = H;

@@ -50,7 +50,8 @@ SIGNATURES = {
     "gdn_model_tree_step": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _P,
                                  _I, _I, _I, _I, _I, _I, _P]),
     "gdn_prune_tree": (_I, [_P, _P, ctypes.c_float, _I, _P, _P, _P, _I, _I, _P]),
-    "gdn_hybrid_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "gdn_hybrid_workspace_bytes": (_I, [_I, _I, _I, _I, _I, _P]),
+    "gdn_hybrid_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_replay_commit": (_I, [_P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P]),
     "gdn_snapshot_tree_verify": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -320,12 +321,19 @@ def gdn_prune_tree(parent_idx, logp, tau, budget, new_index, new_parent, n_kept,
                                 _ptr(new_parent), _ptr(n_kept), B, N, _stream(stream)), "gdn_prune_tree")
 
 
-def gdn_hybrid_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, stream=None):
+def gdn_hybrid_workspace_bytes(B, N, H, dk, dv) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().gdn_hybrid_workspace_bytes(B, N, H, dk, dv, ctypes.byref(out)), "gdn_hybrid_workspace_bytes")
+    return out.value
+
+
+def gdn_hybrid_tree_verify(q, k, v, alpha, beta, parent_idx, S0, out, factors, workspace, stream=None):
     """Chain-decomposed tree verification (see include/gdnspec.h); same outputs and factor record as
-    gdn_tree_verify, no workspace."""
+    gdn_tree_verify.  workspace: gdn_hybrid_workspace_bytes(...) bytes (None when that is 0)."""
     B, N, H, dk, dv = _dims(q, v)
     _check(lib().gdn_hybrid_tree_verify(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), _ptr(alpha), _ptr(beta),
-                                        _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(factors), B, N, H, dk, dv,
+                                        _ptr(parent_idx), _ptr(S0), _ptr(out), _ptr(factors),
+                                        _ptr(workspace), B, N, H, dk, dv,
                                         _stream(stream)), "gdn_hybrid_tree_verify")
 
 

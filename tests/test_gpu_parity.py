@@ -4,6 +4,8 @@ Indices and masks are compared bit for bit; floating-point outputs, buffered
 innovations and committed states within max|err| <= 2e-3 x RMS of the oracle
 (fp32 state, bf16 inputs).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -427,7 +429,18 @@ def test_replay_commit_rejects_bad_path():
 # ---------------------------------------------------------------------------
 # chain-decomposed (hybrid) verification
 # ---------------------------------------------------------------------------
+def _random_trees(B, N, depth, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([wl.random_tree(rng, N, depth) for _ in range(B)])
+
+
+def _wide_two_level():
+    """A root with 21 children, each with two leaf children: 22 branching nodes, all live at once."""
+    return np.array([-1] + [0] * 21 + [1 + i // 2 for i in range(42)], dtype=np.int32)
+
+
 def _hybrid_cases():
+    full_binary = np.array([-1] + [(t - 1) // 2 for t in range(1, 63)], dtype=np.int32)   # 31 branching nodes
     return [
         ("tiny_binary7", lambda: wl.make_workload(0)),
         ("chain8", lambda: wl.make_workload(1)),
@@ -437,7 +450,18 @@ def _hybrid_cases():
         ("narrow_b3_n37_f32", lambda: wl.custom_workload(3, 37, 2, 64, 128, wl.narrow_tree(37, 3, 5), seed=62,
                                                          dtype=wl.F32)),
         ("forest_b2", lambda: wl.custom_workload(2, 16, 4, 256, 256, np.full(16, -1, np.int32), seed=63)),
+        # more branch states than the on-chip slots: the rest go through the workspace
+        ("full_binary63", lambda: wl.custom_workload(1, 63, 2, 64, 64, full_binary, seed=64)),
+        ("wide_two_level_n64", lambda: wl.custom_workload(2, 64, 2, 256, 256, _wide_two_level(), seed=65)),
+        ("random_depth8_n64", lambda: wl.custom_workload(4, 64, 4, 256, 256, _random_trees(4, 64, 8, 66), seed=66)),
+        ("random_depth4_n50_f32", lambda: wl.custom_workload(3, 50, 2, 128, 64, _random_trees(3, 50, 4, 67),
+                                                             seed=67, dtype=wl.F32)),
     ]
+
+
+def hybrid_workspace(w):
+    n = gdnspec.gdn_hybrid_workspace_bytes(w.B, w.N, w.H, w.dk, w.dv)
+    return torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
 
 
 @pytest.mark.parametrize("name,make", _hybrid_cases())
@@ -445,9 +469,13 @@ def test_hybrid_verify_matches_oracle(oracle_mod, name, make):
     w = make()
     d = dev_inputs(w)
     out, fac, _ = alloc_outputs(w)
-    gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out, fac)
-    assert gdnspec.gdn_last_error() == 0
-    check_verify(w, out, fac, oracle_mod)
+    ws = hybrid_workspace(w)
+    for _ in range(2):                                   # the second call reuses the workspace's slots
+        out.fill_(float("nan"))
+        gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out,
+                                       fac, ws)
+        assert gdnspec.gdn_last_error() == 0
+        check_verify(w, out, fac, oracle_mod)
     # its factor record commits like the tree verifier's
     S_new = torch.empty_like(d["S0"])
     gdnspec.gdn_commit(d["S0"], fac, d["path"], S_new, w.N, w.dtype)
@@ -457,13 +485,45 @@ def test_hybrid_verify_matches_oracle(oracle_mod, name, make):
     assert_close(S_new.cpu().numpy(), S_ref, "commit of hybrid factors")
 
 
-def test_hybrid_rejects_too_many_branching_nodes():
-    full_binary = np.array([-1] + [(t - 1) // 2 for t in range(1, 63)], dtype=np.int32)   # 31 branching nodes
-    w = wl.custom_workload(1, 63, 2, 64, 64, full_binary, seed=64)
+def test_hybrid_full_batch_sampled_sequences(oracle_mod):
+    """The batched tree workload (16 x 64-node random trees of depth <= 8, 8 heads, d = 256, bf16): every
+    sequence's record against the tree verifier's, three sequences against the oracle."""
+    w = wl.make_workload(3)
+    d = dev_inputs(w)
+    out, fac, ws = alloc_outputs(w)
+    gdnspec.gdn_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out, fac, ws)
+    out_h, fac_h, _ = alloc_outputs(w)
+    gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out_h,
+                                   fac_h, hybrid_workspace(w))
+    assert gdnspec.gdn_last_error() == 0
+    assert_close(out_h.cpu().numpy(), out.cpu().numpy(), "hybrid vs tree verifier out")
+    dt, _, _, _ = gdnspec.factor_views(fac, w.B, w.N, w.H, w.dk, w.dv, w.dtype)
+    dh, _, _, _ = gdnspec.factor_views(fac_h, w.B, w.N, w.H, w.dk, w.dv, w.dtype)
+    assert_close(dh.cpu().numpy(), dt.cpu().numpy(), "hybrid vs tree verifier delta")
+    seqs = [0, 9, 15]
+    sub = dataclasses.replace(w, B=len(seqs), q=w.q[seqs], k=w.k[seqs], v=w.v[seqs], alpha=w.alpha[seqs],
+                              beta=w.beta[seqs], parent=w.parent[seqs], S0=w.S0[seqs], path=w.path[seqs])
+    x = oracle_inputs(sub)
+    o_ref, d_ref, _ = oracle_mod.tree_verify(**x)
+    assert_close(out_h.cpu().numpy()[seqs], o_ref, "hybrid out, sampled sequences")
+    assert_close(dh.cpu().numpy()[seqs], d_ref, "hybrid delta, sampled sequences")
+
+
+def test_hybrid_argument_and_tree_errors():
+    w = wl.custom_workload(2, 40, 2, 64, 64, _random_trees(2, 40, 5, 68), seed=68)
     d = dev_inputs(w)
     out, fac, _ = alloc_outputs(w)
-    gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out, fac)
-    assert gdnspec.gdn_last_error() == gdnspec.ERR_CAPACITY
+    assert gdnspec.gdn_hybrid_workspace_bytes(w.B, 18, w.H, w.dk, w.dv) == 0
+    assert gdnspec.gdn_hybrid_workspace_bytes(w.B, 19, w.H, w.dk, w.dv) > 0
+    with pytest.raises(gdnspec.GdnError) as e:            # this size needs a workspace: nothing launched
+        gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["parent"], d["S0"], out,
+                                       fac, None)
+    assert e.value.code == gdnspec.ERR_ARG
+    bad = d["parent"].clone()
+    bad[1, 7] = 30                                        # parent after the node
+    gdnspec.gdn_hybrid_tree_verify(d["q"], d["k"], d["v"], d["alpha"], d["beta"], bad, d["S0"], out, fac,
+                                   hybrid_workspace(w))
+    assert gdnspec.gdn_last_error() == gdnspec.ERR_TREE
 
 
 # ---------------------------------------------------------------------------
