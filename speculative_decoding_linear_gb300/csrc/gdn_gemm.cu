@@ -10,7 +10,13 @@
 //               instruction, fp32 accumulators in TMEM, two accumulator
 //               buffers (2 x 256 columns) so a tile's epilogue overlaps the
 //               next tile's main loop
-//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes, fp32 stores
+//   warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes; each 32 x 32
+//               fp32 chunk goes through a swizzled shared-memory buffer (two
+//               per warp) and out by a TMA tensor store, whole 128-byte lines,
+//               tails clipped by the copy engine.  Row-per-lane global stores
+//               instead cost 32 L1 transactions per instruction, wrote every
+//               sector in two halves and held the L1 unit at ~70 % busy,
+//               delaying the operand fills that the MMAs wait on.
 // An fp32 left operand enters as two bf16 terms (hi + lo) accumulated into
 // the same TMEM tile, which keeps its relative error near 2^-16.
 #include <cuda.h>
@@ -38,8 +44,32 @@ struct GemmGeom {
     static constexpr uint32_t kBarOff = kStages * kStageBytes;
     static constexpr uint32_t kAccCols = BN;                  // per accumulator buffer (two buffers)
     static constexpr uint32_t kIdesc = idesc_bf16(kBM, BN);
-    static constexpr uint32_t kSmem = kBarOff + 256 + 1024;   // barriers, TMEM holder, 1 KiB alignment slack
+    // epilogue staging: per epilogue warp two 32 x 32 fp32 buffers (4 KiB each, 1 KiB aligned)
+    static constexpr uint32_t kEpiOff = (kBarOff + 256 + 1023u) & ~1023u;
+    static constexpr uint32_t kSmem = kEpiOff + 4 * 2 * 4096 + 1024;   // + 1 KiB alignment slack
+    static_assert(kSmem <= 227 * 1024, "shared memory");
 };
+
+// 32 x 32 fp32 box from shared memory (128-byte swizzle) to the tensor at
+// (c0 = column, c1 = row); the parts outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// at most N of this thread's committed bulk groups still reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
+}
+// all of this thread's bulk groups complete (writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
 
 struct GemmArgs {
     float* C;
@@ -79,7 +109,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 template <int NA, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                     const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
+                     GemmArgs g) {
     using G = GemmGeom<NA, BN>;
     constexpr uint32_t kAccCols = G::kAccCols;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -183,37 +214,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         const int qtr = warp & 3;                  // TMEM lanes 32 qtr .. 32 qtr + 31
-        int lt = 0;
+        const uint32_t ebuf = base + G::kEpiOff + (uint32_t)qtr * 8192u;
+        int lt = 0, nchunk = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
             const int buf = lt & 1;
             if (!wait_or_abort(accf0 + 8u * buf, ((uint32_t)lt >> 1) & 1u, g.err, abort_flag)) break;
             tc_fence_after();
             const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * BN;
-            const int row = m0 + 32 * qtr + lane;
+            const int r0 = m0 + 32 * qtr;          // this warp's first row
             const uint32_t t = tmem + buf * kAccCols + ((uint32_t)(32 * qtr) << 16);
-            float* crow = g.C + (size_t)row * g.ldc;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 const int col = n0 + 32 * c;
                 if (col >= g.Nc) break;            // warp-uniform
                 float v[32];
                 tmem_ld32(t + 32 * c, v);
-                if (row < g.M) {
-                    if (col + 32 <= g.Nc) {
+                if (r0 >= g.M) continue;           // rows past the end: nothing to store
+                // the buffer's previous store (two chunks ago) has read it
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                const uint32_t sb = ebuf + (uint32_t)(nchunk & 1) * 4096u, row = sb + (uint32_t)lane * 128u;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(crow + col + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (col + i < g.Nc) crow[col + i] = v[i];
-                    }
+                for (int j = 0; j < 8; ++j)        // 16-byte chunk j of row `lane` at j ^ (lane mod 8)
+                    st_shared_v4(row + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                 v[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmC, sb, col, r0);
+                    bulk_commit_group();
                 }
+                ++nchunk;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8u * buf);
         }
+        if (lane == 0) bulk_wait_all();            // the stores are done before the CTA leaves
+        __syncwarp();
     }
     griddep_launch();
     tc_fence_before();
@@ -252,6 +290,20 @@ bool make_operand_map(CUtensorMap* m, const void* ptr, long long rows, int K, lo
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major fp32 [rows][cols] output with a row stride of ld elements; 32 x 32
+// boxes, 128-byte swizzle (the epilogue's staging layout).
+bool make_output_map(CUtensorMap* m, float* ptr, long long rows, int cols, long long ld) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_2d();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {32u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int n[64];
     int dev = 0;
@@ -265,8 +317,8 @@ int sm_count() {
 }
 
 template <int NA, int BN>
-cudaError_t launch_tiles(const CUtensorMap& ta0, const CUtensorMap& ta1, const CUtensorMap& tb, const GemmArgs& g,
-                         cudaStream_t s) {
+cudaError_t launch_tiles(const CUtensorMap& ta0, const CUtensorMap& ta1, const CUtensorMap& tb, const CUtensorMap& tc,
+                         const GemmArgs& g, cudaStream_t s) {
     using G = GemmGeom<NA, BN>;
     static bool attr[64];
     cudaError_t e = ensure_smem(gemm_bf16_kernel<NA, BN>, G::kSmem, attr);
@@ -274,24 +326,27 @@ cudaError_t launch_tiles(const CUtensorMap& ta0, const CUtensorMap& ta1, const C
     const int ntiles = ((g.M + kBM - 1) / kBM) * ((g.Nc + BN - 1) / BN);
     const int grid = ntiles < sm_count() ? ntiles : sm_count();
     return launch_kernel(gemm_bf16_kernel<NA, BN>, dim3(grid), dim3(kGemmThreads), G::kSmem, s, false, ta0, ta1, tb,
-                         g);
+                         tc, g);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_bf16(const void* A0, const void* A1, int nA, long long lda, const void* B, float* C,
                              long long ldc, int M, int Nc, int K, int* err, cudaStream_t s) {
-    if (M < 1 || Nc < 1 || K < kBK || K % kBK != 0 || (nA != 1 && nA != 2) || lda < K || lda % 8 != 0)
+    if (M < 1 || Nc < 1 || K < kBK || K % kBK != 0 || (nA != 1 && nA != 2) || lda < K || lda % 8 != 0 ||
+        ldc < Nc || ldc % 4 != 0 || (reinterpret_cast<uintptr_t>(C) & 15u) != 0)
         return cudaErrorInvalidValue;
     const bool wide = (long long)((M + kBM - 1) / kBM) * ((Nc + 255) / 256) >= sm_count() / 2;
-    CUtensorMap ta0, ta1, tb;
-    if (!make_operand_map(&ta0, A0, M, K, lda, kBM) || !make_operand_map(&tb, B, Nc, K, K, wide ? 256 : 64))
+    CUtensorMap ta0, ta1, tb, tc;
+    if (!make_operand_map(&ta0, A0, M, K, lda, kBM) || !make_operand_map(&tb, B, Nc, K, K, wide ? 256 : 64) ||
+        !make_output_map(&tc, C, M, Nc, ldc))
         return cudaErrorInvalidValue;
     if (nA == 2 && !make_operand_map(&ta1, A1, M, K, lda, kBM)) return cudaErrorInvalidValue;
     if (nA == 1) ta1 = ta0;
     const GemmArgs g{C, ldc, M, Nc, K, err};
-    if (nA == 1) return wide ? launch_tiles<1, 256>(ta0, ta1, tb, g, s) : launch_tiles<1, 64>(ta0, ta1, tb, g, s);
-    return wide ? launch_tiles<2, 256>(ta0, ta1, tb, g, s) : launch_tiles<2, 64>(ta0, ta1, tb, g, s);
+    if (nA == 1)
+        return wide ? launch_tiles<1, 256>(ta0, ta1, tb, tc, g, s) : launch_tiles<1, 64>(ta0, ta1, tb, tc, g, s);
+    return wide ? launch_tiles<2, 256>(ta0, ta1, tb, tc, g, s) : launch_tiles<2, 64>(ta0, ta1, tb, tc, g, s);
 }
 
 }  // namespace gdn
