@@ -1016,9 +1016,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float4 cur[8], nxt[8];             // slabs 0 and 1 in flight during the commit setup
     f_load_slab<kJ>(cur, a.S, srow0, rbase, 4 * c4, pol_first);
     f_load_slab<kJ>(nxt, a.S, srow0, rbase, kSlab + 4 * c4, pol_first);
-    // slabs 2 and 3 into L2 meanwhile: they are read only after the wait, and the
-    // setup leaves the memory system idle for a few microseconds
-    if (tid < 128 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * kDk + 2 * kSlab, 2 * kSlab * 4);
     bool landed = true;
     if (fused) {
         __syncthreads();
@@ -1030,6 +1027,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
     }
     landed = __syncthreads_and(landed);
+    if (tid < 128 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * kDk + 2 * kSlab, 2 * kSlab * 4);
     const int L = fused ? *s_flag : 0;
     bool ok = L >= 0 && landed;
     // this call's inputs into L2 only now: requests issued earlier queue ahead of
