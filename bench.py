@@ -115,12 +115,15 @@ def layer_kernel_work(B, N, H, hidden, dk, dv, L_total, Lmax):
 # capture, keyed by (workload, kernel), with the hash of the kernel sources it was taken on: a changed
 # kernel reports null.  How each figure was taken is in profiles/.
 _TREE_SRC = ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh", "gdn_internal.cuh")
+_GEMM_SRC = ("gdn_gemm.cu", "gdn_tc_ptx.cuh", "gdn_internal.cuh")
 NCU_TRAFFIC = {
     ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.274e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
-                                               "b67ec3376243f1fc"),
-    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.615e6, _TREE_SRC, "1ca8894d6f526df8"),
-    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (48.49e6, _TREE_SRC, "c5f08b699625db92"),
-    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (386.2e6, _TREE_SRC + ("gdn_layer.cu",), "cfe72fafbfc44491"),
+                                               "c4e29e52ec7029ec"),
+    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.619e6, _TREE_SRC, "ed228747f1a09981"),
+    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (48.39e6, _TREE_SRC, "ed228747f1a09981"),
+    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (386.2e6, _TREE_SRC + ("gdn_layer.cu",), "b46ded500ccfdf16"),
+    ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (136.06e6, _GEMM_SRC, "b8e73642ca01a2f5"),
+    ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (45.15e6, _GEMM_SRC, "b8e73642ca01a2f5"),
 }
 NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
                     "start; writes still held in L2 when the kernel ends are not counted)")
