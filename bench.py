@@ -119,9 +119,9 @@ _GEMM_SRC = ("gdn_gemm.cu", "gdn_tc_ptx.cuh", "gdn_internal.cuh")
 NCU_TRAFFIC = {
     ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.274e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
                                                "c4e29e52ec7029ec"),
-    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.619e6, _TREE_SRC, "ed228747f1a09981"),
-    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (48.39e6, _TREE_SRC, "ed228747f1a09981"),
-    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (386.2e6, _TREE_SRC + ("gdn_layer.cu",), "b46ded500ccfdf16"),
+    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.618e6, _TREE_SRC, "448e3936832dcc81"),
+    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (48.53e6, _TREE_SRC, "448e3936832dcc81"),
+    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (385.5e6, _TREE_SRC + ("gdn_layer.cu",), "7753087d228d97f9"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (136.06e6, _GEMM_SRC, "b8e73642ca01a2f5"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (45.15e6, _GEMM_SRC, "b8e73642ca01a2f5"),
 }

@@ -1030,21 +1030,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (tid < 128 * kT) bulk_prefetch_l2(a.S + srow0 + (size_t)tid * kDk + 2 * kSlab, 2 * kSlab * 4);
     const int L = fused ? *s_flag : 0;
     bool ok = L >= 0 && landed;
-    // this call's inputs into L2 only now: requests issued earlier queue ahead of
-    // the commit setup's loads
-    if (tid < N) {                    // this call's inputs into L2; read only after the wait
-        const size_t rt = ((size_t)b * N + tid) * H + h;
-        if (kSplit) {
-            for (int i = 0; i < 4; ++i) prefetch_l2(static_cast<const __nv_bfloat16*>(a.split[i]) + rt * kDk, kDk * 2);
-        } else {
-            prefetch_l2(static_cast<const KT*>(a.q) + rt * kDk, kDk * (int)sizeof(KT));
-        }
-        if (!a.keys_done) prefetch_l2(static_cast<const KT*>(a.k) + rt * kDk, kDk * (int)sizeof(KT));
-        prefetch_l2(static_cast<const KT*>(a.v) + rt * kFRows, kFRows * (int)sizeof(KT));
-        prefetch_line_l2(a.alpha + rt);
-        prefetch_line_l2(a.beta + rt);
-        prefetch_line_l2(a.parent + (size_t)b * N + tid);
-    }
+    // This call's q/k/v rows are not prefetched into L2 before the wait: with all CTAs
+    // streaming their state, the prefetch cost more than the copies after the wait gained.
     const float ega = *s_ega;
     if (ok) {
         // slabs 0 and 1: commit, write back, into the operand stages.  Slabs 2 and 3
