@@ -1173,6 +1173,21 @@ def cpu_baseline(cfg, budget_s=10.0):
                       "by path walks + commit), fp64, %d threads" % (n, w.spec.name, w.B * w.N, w.H, cores)}
 
 
+def reference_config(cfg, wl):
+    """The workload keys of the GPU arm's `config` (config_record), for the full workload; the reference
+    times a bounded sample of it, described in its cpu_baseline.sample."""
+    spec = wl.SPECS[cfg]
+    layer = cfg == 4
+    out = {"workload": spec.name, "B": spec.B, "N": spec.N, "H": spec.H, "dk": spec.dk, "dv": spec.dv,
+           "qkv": spec.dtype, "state": "f32",
+           "step": ("full GDN layer step: projections, ancestor-window conv, gates, tree verify with the "
+                    "pending commit (state + conv history) fused in, output gate, o_proj") if layer else
+                   "per layer: pending commit fused into the next %s verify" % ("chain" if cfg == 1 else "tree")}
+    if layer:
+        out["hidden"] = spec.hidden
+    return out
+
+
 def run_reference(args):
     """Reference arm: the oracle as it stands, timed on the host cores (rank 0 only)."""
     from speculative_decoding_linear_gb300 import workloads as wl
@@ -1200,7 +1215,7 @@ def run_reference(args):
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.spec.name, "B": w.spec.B, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv},
+            "config": reference_config(args.config, wl),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
