@@ -116,6 +116,8 @@ def layer_kernel_work(B, N, H, hidden, dk, dv, L_total, Lmax):
 # kernel reports null.  How each figure was taken is in profiles/.
 _TREE_SRC = ("gdn_tree_tc.cu", "gdn_prep_common.cuh", "gdn_tc_ptx.cuh", "gdn_internal.cuh")
 _GEMM_SRC = ("gdn_gemm.cu", "gdn_tc_ptx.cuh", "gdn_internal.cuh")
+_GLA_VERIFY_SRC = ("gdn_gla.cu",) + _TREE_SRC
+_GLA_COMMIT_SRC = ("gdn_gla.cu", "gdn_internal.cuh")
 NCU_TRAFFIC = {
     ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.274e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
                                                "c4e29e52ec7029ec"),
@@ -124,6 +126,8 @@ NCU_TRAFFIC = {
     ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (385.5e6, _TREE_SRC + ("gdn_layer.cu",), "7753087d228d97f9"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (136.06e6, _GEMM_SRC, "b8e73642ca01a2f5"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (45.15e6, _GEMM_SRC, "b8e73642ca01a2f5"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (76.67e6, _GLA_VERIFY_SRC, "b3ba5acc3720367b"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.29e6, _GLA_COMMIT_SRC, "7b54a687c4878090"),
 }
 NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
                     "start; writes still held in L2 when the kernel ends are not counted)")
@@ -705,15 +709,17 @@ def run_gla(steps, rank, world, device_index, torch, shard_mode, l2):
     vb, cb = gla_bytes(w.B, w.N, w.H, w.dk, w.dv, 2, L_total, w.path.shape[1])
     peaks = measured_peaks()
 
-    def rl(nbytes, us, kernel):
+    def rl(nbytes, us, kernel, key):
         ach = nbytes / (us * 1e-6) / 1e9
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm"], 4), "algorithmic_bytes_per_call": nbytes, "t_call_us": round(us, 3),
-                "kernel": kernel, "traffic": None, "peak_kind": peaks["kind"] + " hbm_gbs (copy)"}
+                "kernel": kernel, "traffic": ncu_traffic(w.spec.name, key), "traffic_note": NCU_TRAFFIC_NOTE,
+                "peak_kind": peaks["kind"] + " hbm_gbs (copy)"}
     units = (w.B * world if shard_mode == "replicas" else wl.SPECS[3].B) * w.N     # sequences of the whole job
     res = {"workload": w.spec.name, "B": w.B, "N": w.N, "H": w.H, "dk": w.dk, "dv": w.dv, "layers_rotated": R,
-           "verify": rl(vb, t_v, "gdn_gla_tree_verify (gla_prep_kernel + tree_contract_tc_kernel<1> in linear mode)"),
-           "commit": rl(cb, t_c, "gdn_gla_commit (gla_commit_kernel)"),
+           "verify": rl(vb, t_v, "gdn_gla_tree_verify (gla_prep_kernel + tree_contract_tc_kernel<1> in linear mode)",
+                        "gla_verify"),
+           "commit": rl(cb, t_c, "gdn_gla_commit (gla_commit_kernel)", "gla_commit"),
            "nodes_per_s_verify_plus_commit": round(units / ((t_v + t_c) * 1e-6), 1),
            "what": "per call, launch overlap off, CUDA-graph replays of the rotation; per-channel gates "
                    "alpha = exp(-softplus(U(-3, 1))) per key channel"}
@@ -1251,6 +1257,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub", action="store_true", help="skip the verify+commit sub-record of the layer line")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
+    ap.add_argument("--gla-only", action="store_true",
+                    help="for profiler runs: only the per-channel-gate (GLA) verify and commit record")
     ap.add_argument("--profile", action="store_true",
                     help="for profiler runs: no clock soak, no e2e leg, no CPU baseline, no side records")
     ap.add_argument("--layers", type=int, default=None,
@@ -1281,6 +1289,11 @@ def main():
         __graft_entry__.build()
     if world > 1:
         dist.barrier()
+    if args.gla_only:
+        rec = run_gla(args.steps, rank, world, local, torch, args.shard, l2_size(torch, local))
+        if rank == 0:
+            print(json.dumps(rec), flush=True)
+        return
     sub = small = None
     if args.config == 4:
         r = run_layer(args.steps, args.warmup, rank, world, local, torch, dist, args.profile, args.layers, args.shard)
