@@ -59,7 +59,7 @@ LAYER_KERNELS = ("gemm_in", "conv", "tree_verify", "gate", "gemm_out")
 LAYER_KERNEL_NAMES = {
     "gemm_in": "gemm_bf16_kernel<1,256> (input projection)",
     "conv": "layer_conv_kernel (ancestor-window conv, norms, gates)",
-    "tree_verify": "tree_fused_tc_kernel<1,2> (tree verify + pending commit)",
+    "tree_verify": "tree_fused_tc_kernel<1,2> (+ <1,1> for the pairs past whole waves; tree verify + pending commit)",
     "gate": "layer_gate_kernel (o * SiLU(z))",
     "gemm_out": "gemm_bf16_kernel<2,256> (output projection, two bf16 terms)",
 }
@@ -496,6 +496,7 @@ def run_tree(cfg, steps, warmup, rank, world, device_index, torch, dist, profile
     achieved = per_call / t_call_s / 1e9
     fused_tree = not chain and dk == 256 and dv == 256
     kernel = "chain_g8_kernel" if chain else "tree_fused_tc_kernel" if fused_tree else "tree_contract_tc_kernel"
+    launches = 1 if chain else verifier_launches(lys[0].w, torch, device_index)
     replays = None
     if dist_rec is not None:
         replays = dict(dist_rec)
@@ -511,10 +512,11 @@ def run_tree(cfg, steps, warmup, rank, world, device_index, torch, dist, profile
         roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
                   "frac": round(achieved / peaks["hbm"], 4), "traffic": ncu_traffic(spec.name, kernel),
                   "traffic_note": NCU_TRAFFIC_NOTE, "peak_kind": peaks["kind"] + " hbm_gbs (copy)",
-                  "kernel": "gdn_commit_%s_verify (%s, one launch per call)" % ("chain" if chain else "tree", kernel),
+                  "kernel": "gdn_commit_%s_verify (%s, %d launch%s per call)"
+                            % ("chain" if chain else "tree", kernel, launches, "" if launches == 1 else "es"),
                   "algorithmic_bytes_per_call": per_call, "t_call_us": round(t_call_s * 1e6, 3),
                   "t_call_from": "CUDA events around the timed graph replays / calls (launch overlap on)"},
-        gpu_launches=(1 if (chain or fused_tree) else 2) * R * steps, baselines=baselines, hybrid=hybrid, prune=prune,
+        gpu_launches=launches * R * steps, baselines=baselines, hybrid=hybrid, prune=prune,
     )
 
 
@@ -776,7 +778,8 @@ def draw_layer_workload(wl, seed, shard_mode, world, rank):
 
 
 def layer_kernel_times(lys, gdnspec, torch, stream, steps, parity0):
-    """Average device time (us) of each of the layer step's five kernels over `steps` passes of the
+    """Average device time (us) of each of the layer step's five stages (the verifier one or two launches)
+    over `steps` passes of the
     rotation, from CUDA events the library records on the launching stream between the kernels
     (gdn_layer_stage_events); calls are eager, so kernels of consecutive calls do not overlap."""
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(LAYER_KERNELS) + 1)]
@@ -913,9 +916,21 @@ def run_layer(steps, warmup, rank, world, device_index, torch, dist, profile=Fal
         value=units / (ms / 1e3), ms=ms / steps, R=R, footprint=footprint, l2=l2, clocks=clocks, e2e=e2e,
         spec=spec, B=w0.B, N=w0.N, H=w0.H, dk=w0.dk, dv=w0.dv, hidden=w0.hidden, chain=False, layer=True,
         sequential=seq, model=model, roofline=roofline, replays=replays,
-        # GEMM, conv, tree verifier (one kernel at d_k = d_v = 256, else two), gate, GEMM
-        gpu_launches=(5 if w0.dk == 256 and w0.dv == 256 else 6) * R * steps,
+        # GEMM, conv, tree verifier, gate, GEMM
+        gpu_launches=(4 + verifier_launches(w0, torch, device_index)) * R * steps,
     )
+
+
+def verifier_launches(w, torch, device_index):
+    """Kernels of one tree verification: one at d_k = d_v = 256 (a second launch when the (sequence,
+    head) pairs fill whole waves of the SMs plus a remainder that fits one wave as two CTAs per pair),
+    else the prologue and the contraction."""
+    if not (w.dk == 256 and w.dv == 256):
+        return 2
+    sms = torch.cuda.get_device_properties(device_index).multi_processor_count
+    pairs = w.B * w.H
+    rest = pairs % sms
+    return 2 if pairs > sms // 2 and 0 < rest and 2 * rest <= sms else 1
 
 
 def run_model_step(gdnspec, torch, stream, device, wl, n_layers=4, steps=5):

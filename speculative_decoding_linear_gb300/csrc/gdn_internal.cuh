@@ -128,6 +128,9 @@ struct VerifyArgs {
     // the factor record's keys were written by the producer of q/k (the layer's conv
     // kernel): the single-kernel verifier neither copies nor reads the fp32 keys
     bool keys_done = false;
+    // first (sequence, head) of the launch: the single-kernel verifier may cover the B*H pairs
+    // in two launches (whole waves of one CTA per pair, then the rest as two CTAs per pair)
+    int bh_base = 0;
 };
 
 struct CommitArgs {

@@ -929,7 +929,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int N = a.N, H = a.H, ld = N + 1;
     const FusedLayout Ly(N, fused ? a.commit.Lmax : 0, kSplit);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int bh = a.bh_base + (int)blockIdx.x, b = bh / H, h = bh % H;
     const int row0 = kT == 1 ? 128 * (int)blockIdx.y : 0;    // the CTA's first state row
     const bool lead = row0 == 0;                            // writes the per-(b, h) factor parts
     constexpr int kJ = 4 * kT;                              // state rows per thread and slab
@@ -1425,7 +1425,7 @@ bool fused_eligible(const VerifyArgs& a, bool split) {
 bool tc_uses_workspace(const VerifyArgs& a) { return !fused_eligible(a, a.split[0] != nullptr); }
 
 template <bool kSplit, int kT>
-cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s) {
+cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s, int npairs = -1, bool programmatic = false) {
     static bool attr[64];
     CUtensorMap tq, tk, tql, tkl;
     const void* qh = kSplit ? a.split[0] : a.q;
@@ -1441,8 +1441,9 @@ cudaError_t launch_tree_fused_impl(const VerifyArgs& a, cudaStream_t s) {
     const FusedLayout L(a.N, a.commit.path ? a.commit.Lmax : 0, kSplit);
     cudaError_t e = ensure_smem(tree_fused_tc_kernel<kSplit, kT>, L.total, attr);
     if (e != cudaSuccess) return e;
-    return launch_kernel(tree_fused_tc_kernel<kSplit, kT>, dim3(a.B * a.H, 2 / kT), dim3(kFThreads), L.total, s,
-                         a.overlap, tq, tk, tql, tkl, a);
+    const int n = npairs < 0 ? a.B * a.H : npairs;
+    return launch_kernel(tree_fused_tc_kernel<kSplit, kT>, dim3(n, 2 / kT), dim3(kFThreads), L.total, s,
+                         a.overlap || programmatic, tq, tk, tql, tkl, a);
 }
 
 // bf16 q/k (or fp32 q/k with their bf16 hi/lo terms in `split`) with the
@@ -1456,9 +1457,24 @@ cudaError_t launch_tree_tc(const VerifyArgs& a, cudaStream_t s) {
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return cudaErrorInvalidValue;
-        if (2LL * a.B * a.H <= sms)
+        const long long pairs = (long long)a.B * a.H;
+        if (2 * pairs <= sms)
             return split ? launch_tree_fused_impl<true, 1>(a, s) : launch_tree_fused_impl<false, 1>(a, s);
-        return split ? launch_tree_fused_impl<true, 2>(a, s) : launch_tree_fused_impl<false, 2>(a, s);
+        // Whole waves of one CTA per pair, then -- when the rest fit one wave as two CTAs per
+        // pair -- the rest as a second launch of half-tile CTAs, a programmatic dependent of the
+        // first: it covers other pairs, and what it touches before its wait (its pairs' state and
+        // the previous factors) the first launch does not.  The last wave then holds shorter CTAs
+        // than a partial wave of whole-pair ones.
+        const long long full = pairs / sms * sms, rest = pairs - full;
+        if (rest == 0 || 2 * rest > sms)
+            return split ? launch_tree_fused_impl<true, 2>(a, s) : launch_tree_fused_impl<false, 2>(a, s);
+        cudaError_t e = split ? launch_tree_fused_impl<true, 2>(a, s, (int)full)
+                              : launch_tree_fused_impl<false, 2>(a, s, (int)full);
+        if (e != cudaSuccess) return e;
+        VerifyArgs r = a;
+        r.bh_base = (int)full;
+        return split ? launch_tree_fused_impl<true, 1>(r, s, (int)rest, true)
+                     : launch_tree_fused_impl<false, 1>(r, s, (int)rest, true);
     }
     return split ? launch_tree_tc_impl<true>(a, s) : launch_tree_tc_impl<false>(a, s);
 }

@@ -211,6 +211,33 @@ def test_fused_commit_tree_verify(oracle_mod, cfg):
     check_verify(w2, out2, fac2, oracle_mod)
 
 
+def test_split_launch_verify_and_fused_commit(oracle_mod):
+    """More (sequence, head) pairs than SMs with a remainder that fits one wave as two CTAs per pair:
+    the single-kernel verifier covers whole waves in one launch and the rest in a second launch of
+    half-tile CTAs.  22 sequences x 8 heads = 176 pairs (on 152 SMs: 152 + 24 x 2)."""
+    rng = np.random.default_rng(808)
+    B, N, H = 22, 40, 8
+    parent = np.stack([wl.random_tree(rng, N, 8) for _ in range(B)])
+    w1 = wl.custom_workload(B, N, H, 256, 256, parent, seed=808)
+    d1, out1, fac1 = run_tree_verify(w1)
+    check_verify(w1, out1, fac1, oracle_mod)
+    w2 = _second_tree(w1, seed=809)
+    d2 = dev_inputs(w2)
+    S = d1["S0"].clone()
+    out2, fac2, ws2 = alloc_outputs(w2)
+    gdnspec.gdn_commit_tree_verify(S, fac1, w1.N, d1["path"], d2["q"], d2["k"], d2["v"], d2["alpha"],
+                                   d2["beta"], d2["parent"], out2, fac2, ws2)
+    assert gdnspec.gdn_last_error() == 0
+    S_unf = torch.empty_like(S)
+    gdnspec.gdn_commit(d1["S0"], fac1, d1["path"], S_unf, w1.N, w1.dtype)
+    assert torch.equal(S, S_unf)
+    x1 = oracle_inputs(w1)
+    S_ref = oracle_mod.commit(x1["k"], x1["v"], x1["alpha"], x1["beta"], w1.parent, x1["S0"], w1.path)
+    assert_close(S.cpu().numpy(), S_ref, "committed S")
+    w2.S0 = S.cpu().numpy()
+    check_verify(w2, out2, fac2, oracle_mod)
+
+
 @pytest.mark.parametrize("cfg", [1, "b2"])
 def test_fused_commit_chain_verify(oracle_mod, cfg):
     w1 = wl.make_workload(1) if cfg == 1 else wl.custom_workload(2, 8, 3, 64, 128, wl.chain_tree(8), seed=8)
