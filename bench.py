@@ -120,14 +120,16 @@ _GLA_VERIFY_SRC = ("gdn_gla.cu",) + _TREE_SRC
 _GLA_COMMIT_SRC = ("gdn_gla.cu", "gdn_internal.cuh")
 NCU_TRAFFIC = {
     ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.274e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
-                                               "c4e29e52ec7029ec"),
-    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.618e6, _TREE_SRC, "448e3936832dcc81"),
-    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (48.53e6, _TREE_SRC, "448e3936832dcc81"),
-    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (385.5e6, _TREE_SRC + ("gdn_layer.cu",), "7753087d228d97f9"),
-    ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (136.06e6, _GEMM_SRC, "b8e73642ca01a2f5"),
-    ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (45.15e6, _GEMM_SRC, "b8e73642ca01a2f5"),
-    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (76.67e6, _GLA_VERIFY_SRC, "b3ba5acc3720367b"),
-    ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.29e6, _GLA_COMMIT_SRC, "7b54a687c4878090"),
+                                               "10502adcdbd91ed8"),
+    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.618e6, _TREE_SRC, "ebdcd71771e0062c"),
+    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (47.80e6, _TREE_SRC, "ebdcd71771e0062c"),
+    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (357.9e6, _TREE_SRC + ("gdn_layer.cu",), "9329da3db41bc70e"),
+    ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (134.6e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
+    ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (43.08e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
+    ("layer_tree64_depth8_b64_hid2048", "conv"): (190.1e6, ("gdn_layer.cu", "gdn_layer.cuh", "gdn_internal.cuh"),
+                                                  "1db5df1f1d68dff0"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.78e6, _GLA_VERIFY_SRC, "9f9d81b7453dbbde"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.31e6, _GLA_COMMIT_SRC, "8231be4c7a297db5"),
 }
 NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
                     "start; writes still held in L2 when the kernel ends are not counted)")
