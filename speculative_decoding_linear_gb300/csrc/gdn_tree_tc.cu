@@ -806,6 +806,16 @@ struct FusedLayout {
     }
 };
 
+// Named barrier `id` of `count` threads: arrive without waiting (the arrival
+// orders this thread's earlier shared-memory writes before the barrier completes),
+// or wait for it to complete.
+__device__ __forceinline__ void named_barrier_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
 // L2 cache policy of the state stream: the state is read and written once per
 // call, so its lines go first (the call's inputs and the kernel stay resident).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -958,9 +968,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 8);
     int* s_vcopy = reinterpret_cast<int*>(base + Ly.misc + 12);  // the v-row copies were issued
     int* s_qkmask = reinterpret_cast<int*>(base + Ly.misc + 16); // bit s: the q/k copy of slab s was issued
+    int* s_fail = reinterpret_cast<int*>(base + Ly.misc + 20);   // a worker's wait gave up in a slab step
     const uint32_t stage0 = base_s, stage1 = base_s + kFAStage, bbase = base_s + 2 * kFAStage;
     const int nB = Ly.nB;
     auto bbuf = [&](int s) { return bbase + (nB == 2 ? (uint32_t)((s & 1) * Ly.bsz) : 0u); };
+    // After the wait the issuer warp holds no state rows: the J elements of each of its
+    // threads in slabs 2 and 3 are taken by threads 256 .. 256 + 32 J - 1 (warps 8-15),
+    // one each, so that the issuer's MMA issue and its waits never hold up the stage
+    // that the next slab's barrier waits for.
+    const bool helper = tid >= 256 && tid < 256 + 32 * kJ;
+    const int hx = tid - 256, hw = hx & 31, hj = hx >> 5;              // issuer lane, element
+    const int h_rb = (32 * kFIssuerWarp + hw) >> 4, h_c4 = hw & 15;     // its rbase and column quad
+    const int h_row = h_rb + 32 * hj;                                   // the element's state row
     const uint32_t vrows_s = base_s + Ly.vs;
 
     if (fused && warp == 2 && lane < 6) {   // the pending commit's path, parent and g rows, first of all
@@ -979,6 +998,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         *s_ega = 1.f;
         *s_vcopy = 0;
         *s_qkmask = 0;
+        *s_fail = 0;
     }
     if (warp == 1) tmem_alloc(smem_u32(s_tmem), kFTmemCols);
     tc_fence_before();
@@ -1055,10 +1075,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
     // ---- 2. this call's inputs ----
     griddep_wait();
     griddep_launch();
+    float4 ecur[8], enxt[8];           // a helper's element of the issuer's rows in slabs 2 and 3 ([0] only)
     if (ok) {
         // this thread's part of slabs 2 and 3 as they were before the commit (L2)
-        f_load_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
-        f_load_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
+        if (warp != kFIssuerWarp) {
+            f_load_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
+            f_load_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
+        }
+        if (helper) {
+            f_load_slab<1>(ecur, a.S, srow0, h_row, 2 * kSlab + 4 * h_c4, pol_first);
+            f_load_slab<1>(enxt, a.S, srow0, h_row, 3 * kSlab + 4 * h_c4, pol_first);
+        }
         if (warp == kFIssuerWarp && lane == 0) {
             issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(0), 0, h, b * N, bars);
             if (nB == 2) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
@@ -1085,22 +1112,39 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
 
         // ---- 3. Y of both tiles and the Gram, slab by slab.  Slab s: (s >= 2) its
-        // state part into the stage slab s - 2 has freed; lane 0 of the issuer warp
-        // issues its MMAs once its q/k copy has landed, then the copy into the q/k
-        // buffer that the MMAs of slab s + 1 - nB free ----
+        // state part into the stage slab s - 2 has freed, after which the workers
+        // arrive at named barrier s and go on; lane 0 of the issuer warp waits there,
+        // issues the slab's MMAs once its q/k copy has landed, then the copy into the
+        // q/k buffer that the MMAs of slab s + 1 - nB free ----
 #pragma unroll 1
         for (int sl = 0; sl < kSlabs; ++sl) {
             if (sl >= 2) {
-                if (fused && ok) {                 // commit slab sl and write it back
-                    f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, sl * kSlab + 4 * c4);
-                    f_store_slab<kJ>(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, pol_first);
-                }
-                ok = ok && mbar_wait(bars + 32 + 8 * (sl - 2), 0, a.err);
-                if (ok) f_convert_slab<kJ>(cur, base + (sl & 1) * kFAStage, rbase, c4);
+                unsigned char* stage = base + (sl & 1) * kFAStage;
+                if (warp != kFIssuerWarp) {
+                    if (fused && ok) {             // commit slab sl and write it back
+                        f_commit_slab<kJ>(cur, ega, L, s_cd, s_key, row0 + rbase, sl * kSlab + 4 * c4);
+                        f_store_slab<kJ>(cur, a.S, srow0, rbase, sl * kSlab + 4 * c4, pol_first);
+                        if (helper) {
+                            f_commit_slab<1>(ecur, ega, L, s_cd, s_key, row0 + h_row, sl * kSlab + 4 * h_c4);
+                            f_store_slab<1>(ecur, a.S, srow0, h_row, sl * kSlab + 4 * h_c4, pol_first);
+                        }
+                    }
+                    ok = ok && mbar_wait(bars + 32 + 8 * (sl - 2), 0, a.err);
+                    if (ok) {
+                        f_convert_slab<kJ>(cur, stage, rbase, c4);
+                        if (helper)
+                            f_convert_slab<1>(ecur, stage + (hj >> 2) * 2 * kBufBytes, h_rb + 32 * (hj & 3), h_c4);
+                    }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
-                fence_proxy_async_smem();
-                ok = __syncthreads_and(ok);
+                    for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+                    ecur[0] = enxt[0];
+                    fence_proxy_async_smem();
+                    if (!ok) *s_fail = 1;
+                    named_barrier_arrive(sl, kFThreads);
+                } else {
+                    named_barrier_sync(sl, kFThreads);
+                    ok = ok && *s_fail == 0;
+                }
             }
             if (ok && warp == kFIssuerWarp) {
                 if (lane == 0) {
