@@ -1166,6 +1166,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 __syncwarp();
             }
         }
+        // fp32 v rows (read in place by R) into L2 while the last slab's MMAs and the tables run
+        if (kSplit && ok && tid < N)
+            bulk_prefetch_l2(static_cast<const KT*>(a.v) + (((size_t)b * N + tid) * H + h) * kFRows + row0,
+                             (uint32_t)(128 * kT * sizeof(KT)));
         // node metadata while the last slab's MMAs run
         bool bad = false;
         if (tid < N) {
@@ -1219,26 +1223,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 prep::solve_rows_fast<9>(tid, N, ld, sdepth, plist, sA, sAt, sT, 256);
                 prep::write_operand(tid, 256, N, ld, anc, sA, sT, base + Ly.op);
             } else {
-                // keys into the factor record, four 16-byte loads in flight per thread
-                constexpr int kVec = 16 / (int)sizeof(KT), kRow = kDk / kVec, kBatch = 4;
-                const KT* kin = static_cast<const KT*>(a.k);
-                KT* kout = static_cast<KT*>(a.f.key) + (size_t)bh * N * kDk;
-                const int items = lead && !a.keys_done ? N * kRow : 0;
-#pragma unroll 1
-                for (int i0 = tid - 256; i0 < items; i0 += kBatch * (kFThreads - 256)) {
-                    uint4 x[kBatch];
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        const int item = i0 + u * (kFThreads - 256), t = item / kRow, c = item % kRow;
-                        if (item < items)
-                            x[u] = *reinterpret_cast<const uint4*>(kin + (((size_t)b * N + t) * H + h) * kDk + c * kVec);
-                    }
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        const int item = i0 + u * (kFThreads - 256), t = item / kRow, c = item % kRow;
-                        if (item < items) *reinterpret_cast<uint4*>(kout + (size_t)t * kDk + c * kVec) = x[u];
-                    }
-                }
                 // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) of tile u as bf16
                 // hi + lo rows of the second MMA's A operand (row v, 64 columns t).  kT = 2:
                 // warps 8-11 tile 0, 12-15 tile 1; kT = 1: they split the nodes of tile 0.
@@ -1308,6 +1292,30 @@ __global__ void __launch_bounds__(kFThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
+
+        // keys into the factor record (warps 8-15, while the second MMA runs)
+        if (ok && tid >= 256) {
+            // four 16-byte loads in flight per thread
+            constexpr int kVec = 16 / (int)sizeof(KT), kRow = kDk / kVec, kBatch = 4;
+            const KT* kin = static_cast<const KT*>(a.k);
+            KT* kout = static_cast<KT*>(a.f.key) + (size_t)bh * N * kDk;
+            const int items = lead && !a.keys_done ? N * kRow : 0;
+#pragma unroll 1
+            for (int i0 = tid - 256; i0 < items; i0 += kBatch * (kFThreads - 256)) {
+                uint4 x[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int item = i0 + u * (kFThreads - 256), t = item / kRow, c = item % kRow;
+                    if (item < items)
+                        x[u] = *reinterpret_cast<const uint4*>(kin + (((size_t)b * N + t) * H + h) * kDk + c * kVec);
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    const int item = i0 + u * (kFThreads - 256), t = item / kRow, c = item % kRow;
+                    if (item < items) *reinterpret_cast<uint4*>(kout + (size_t)t * kDk + c * kVec) = x[u];
+                }
+            }
+        }
 
         // ---- 5. [Delta | P R] = R [T; P]^T per tile: three bf16 terms (hi.hi, hi.lo, lo.hi) ----
         if (ok && warp == kFIssuerWarp) {
