@@ -223,7 +223,9 @@ __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const in
     }
     group_sync(group);
     if (fast) {
-        float at[kRegDepth];
+        // every entry of the row first, then the stores: a store to sA between them would
+        // keep the next entry's sT loads (which the compiler must assume may alias it) behind it
+        float at[kRegDepth], pr[kRegDepth];
 #pragma unroll
         for (int j = 0; j < kRegDepth; ++j) at[j] = j <= m ? sAt[t * ld + q[j]] : 0.f;
 #pragma unroll
@@ -234,8 +236,11 @@ __device__ __forceinline__ void solve_rows_fast(int tid, int N, int ld, const in
                 s0 = fmaf(at[j], sT[q[j] * ld + q[i]], s0);
                 if (j + 1 <= i) s1 = fmaf(at[j + 1], sT[q[j + 1] * ld + q[i]], s1);
             }
-            if (i <= m) sA[t * ld + q[i]] = s0 + s1;
+            pr[i] = s0 + s1;
         }
+#pragma unroll
+        for (int i = 0; i < kRegDepth; ++i)
+            if (i <= m) sA[t * ld + q[i]] = pr[i];
     } else if (tid < N) {
         const uint8_t* p = plist + t * 64;
 #pragma unroll 1

@@ -1202,14 +1202,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const int t = tid & 63;
                 float* row = ((tid & 127) < 64 ? sAt : sA) + t * ld;
                 const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256;
-                const int cend = min(N, 32 * (warp >> 2) + 32);
-#pragma unroll 1
-                for (int c = 32 * (warp >> 2); c < cend; c += 8) {
-                    float gr[8];
-                    tmem_ld8(t_lane + c, gr);
+                const int c = 32 * (warp >> 2);
+                if (c < N) {                         // one 32-column load (a single wait)
+                    float gr[32];
+                    tmem_ld32(t_lane + c, gr);
                     if (t < N) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
+                        for (int i = 0; i < 32; ++i)
                             if (c + i < N) row[c + i] = gr[i];
                     }
                 }
@@ -1265,12 +1264,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             vt[i] = 32 * c + i < N ? vin[(size_t)(32 * c + i) * H * kFRows] : 0.f;
+                        float yk32[32];
+                        tmem_ld32(t_lane + 32 * c, yk32);
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
                             float yk[8], v8[8];
-                            tmem_ld8(t_lane + 32 * c + 8 * q8, yk);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) v8[i] = vt[8 * q8 + i];
+                            for (int i = 0; i < 8; ++i) {
+                                yk[i] = yk32[8 * q8 + i];
+                                v8[i] = vt[8 * q8 + i];
+                            }
                             r_chunk(32 * c + 8 * q8, yk, v8);
                         }
                     }
@@ -1279,12 +1282,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     const KT* vsm = reinterpret_cast<const KT*>(base + (vrows_s - base_s)) + row0 + 128 * u + v;
                     const bool vok = mbar_wait(bar_v, 0, a.err);
 #pragma unroll 1
-                    for (int t0 = tbeg; t0 < tend; t0 += 8) {
-                        float yk[8], v8[8];
-                        tmem_ld8(t_lane + t0, yk);
+                    for (int c0 = tbeg; c0 < tend; c0 += 32) {      // 32 nodes per TMEM load
+                        float yk32[32];
+                        tmem_ld32(t_lane + c0, yk32);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) v8[i] = t0 + i < N && vok ? to_f32(vsm[(t0 + i) * kFRows]) : 0.f;
-                        r_chunk(t0, yk, v8);
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const int t0 = c0 + 8 * q8;
+                            float yk[8], v8[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                yk[i] = yk32[8 * q8 + i];
+                                v8[i] = t0 + i < N && vok ? to_f32(vsm[(t0 + i) * kFRows]) : 0.f;
+                            }
+                            r_chunk(t0, yk, v8);
+                        }
                     }
                 }
             }
@@ -1353,12 +1364,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
             float* dst = is_o ? a.out + ((size_t)b * N * H + h) * kFRows + row : a.f.delta + (size_t)bh * N * kFRows + row;
             const size_t dstep = is_o ? (size_t)H * kFRows : (size_t)kFRows;
 #pragma unroll 1
-            for (int t0 = tbeg; t0 < tend; t0 += 8) {
-                float x[8], yq[8];
-                tmem_ld8(src + t0, x);
-                if (is_o) tmem_ld8(t_lane + 128 * u + t0, yq);
+            for (int t0 = tbeg; t0 < tend; t0 += 32) {           // 32 nodes per TMEM load
+                float x[32], yq[32];
+                tmem_ld32(src + t0, x);
+                if (is_o) tmem_ld32(t_lane + 128 * u + t0, yq);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     const int t = t0 + i;
                     if (t < tend) dst[(size_t)t * dstep] = is_o ? fmaf(seg[t], yq[i], x[i]) : x[i];
                 }
