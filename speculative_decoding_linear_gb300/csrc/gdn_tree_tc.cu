@@ -963,6 +963,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t bar_e = bars + 64;                         // bars + 8 s: slab s copied; + 32 + 8 s: its MMAs done
     const uint32_t bar_v = bars + 72;                         // v rows landed (bf16 inputs)
     const uint32_t bar_c = bars + 80;                         // the commit's key and delta rows landed
+    const uint32_t bar_e2 = bars + 88;                        // the second MMA of tile 1 done (kT = 2)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(base + Ly.misc);
     int* s_flag = reinterpret_cast<int*>(base + Ly.misc + 4);    // path length, or -1: skip the CTA
     float* s_ega = reinterpret_cast<float*>(base + Ly.misc + 8);
@@ -991,7 +992,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (128 * half < bytes) prefetch_line_l2(row + 128 * half);
     }
     if (tid == 0) {
-        for (int i = 0; i < 11; ++i) mbar_init(bars + 8 * i, 1);
+        for (int i = 0; i < 12; ++i) mbar_init(bars + 8 * i, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         fence_proxy_async_smem();
         *s_flag = 0;
@@ -1345,12 +1346,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     mma_bf16(d, ahi, blo, kIdesc, 1u);
                     mma_bf16(d, alo, bhi, kIdesc, 1u);
                 }
+                mma_commit(u == 0 ? bar_e : bar_e2);   // tile 0's stores start while tile 1's MMAs run
             }
-            mma_commit(bar_e);
             }
             __syncwarp();
         }
-        if (ok) ok = mbar_wait(bar_e, 0, a.err);
+        if (ok) ok = mbar_wait(kT == 2 && warp >= 8 ? bar_e2 : bar_e, 0, a.err);
         tc_fence_after();
         if (ok) {
             // kT = 2: warps 0-3 / 8-11 Delta of tile 0 / 1, warps 4-7 / 12-15 O of tile 0 / 1;
