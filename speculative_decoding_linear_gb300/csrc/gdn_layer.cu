@@ -24,7 +24,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kConvThreads = 256;
+constexpr int kConvThreads = 384;   // 12 warps: three blocks (their staged rows) per SM; 256 and 512 measured slower
 constexpr int kLayerStages = 5;   // input GEMM, conv, tree verifier, gate, output GEMM
 constexpr int kGateThreads = 256;
 
