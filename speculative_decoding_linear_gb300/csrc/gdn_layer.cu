@@ -609,7 +609,7 @@ int layer_tree_step(const void* X, const void* X_lo, const void* W_in, const flo
     gaa.width = H * dv;
     const long long work = M * (H * dv / 4);
     long long blocks = (work + kGateThreads - 1) / kGateThreads;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks > 152 * 32) blocks = 152 * 32;   // 152 x 8 and 152 x 16 measured 21.8 and 21.4 us against 20.3
     e = launch_kernel(layer_gate_kernel, dim3((unsigned)blocks), dim3(kGateThreads), 0, stream, false, gaa);
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     stage_mark(4, stream);
