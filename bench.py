@@ -123,11 +123,11 @@ NCU_TRAFFIC = {
                                                "10502adcdbd91ed8"),
     ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.634e6, _TREE_SRC, "64426eb42ac6d51a"),
     ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (47.87e6, _TREE_SRC, "64426eb42ac6d51a"),
-    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (358.7e6, _TREE_SRC + ("gdn_layer.cu",), "eef3c02a999f2cce"),
+    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (357.3e6, _TREE_SRC + ("gdn_layer.cu",), "d0a46fd57693ad35"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (134.6e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (43.08e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
-    ("layer_tree64_depth8_b64_hid2048", "conv"): (190.1e6, ("gdn_layer.cu", "gdn_layer.cuh", "gdn_internal.cuh"),
-                                                  "1db5df1f1d68dff0"),
+    ("layer_tree64_depth8_b64_hid2048", "conv"): (188.2e6, ("gdn_layer.cu", "gdn_layer.cuh", "gdn_internal.cuh"),
+                                                  "066e72e5baf0efbc"),
     ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.80e6, _GLA_VERIFY_SRC, "4acbbc59a18a2450"),
     ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.31e6, _GLA_COMMIT_SRC, "8231be4c7a297db5"),
 }
