@@ -742,13 +742,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 //     into L2;
 //   after the wait: q/k slabs by TMA; per slab the Y MMAs of both tiles and
 //     the Gram MMA ([Q; K] K^T: M = 128 rows, N = 64 keys) on the same operand
-//     buffer; slabs 2 and 3 are read from L2, committed and written back while
-//     the first MMAs run, and take the stages over once slabs 0 and 1 are
-//     consumed; the node metadata meanwhile;
+//     buffer, issued by lane 0 of warp 4; slabs 2 and 3 are read from L2,
+//     committed and written back while the first MMAs run, and take the stages
+//     over once slabs 0 and 1 are consumed -- by the other fifteen warps (warps
+//     8-15 take warp 4's share), which arrive at a named barrier per slab that
+//     only the issuer waits on; the node metadata meanwhile;
 //   then warps 0-7 turn the Gram rows into the A and Attn tables, solve T,
 //     form P and the [T; P] operand, while warps 8-15 form R of both tiles
-//     from Y_K, v and the gates; one MMA group per tile gives [Delta | P R];
-//     every warp stores Delta or O rows.
+//     from Y_K, v and the gates; one MMA group per tile gives [Delta | P R]
+//     (committed per tile); warps 8-15 copy the keys into the factor record
+//     while it runs; every warp stores Delta or O rows.
 // TMEM, 512 columns: Y of tile u in 128u .. 128u+127 ([Y_Q | Y_K]); the Gram
 // in 256 .. 319 until it is read; [Delta | P R] of tile u in 256+128u .. +127.
 constexpr int kFThreads = 512;
