@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kGThreads) gla_prep_kernel(GlaArgs a) {
     __shared__ uint8_t plist[kMaxNodes * 64];
     __shared__ float la0[kMaxNodes], g0[kMaxNodes];   // node_meta's scalar-gate slots (zero gates)
     __shared__ uint16_t pairs[kMaxNodes * kMaxNodes];
-    __shared__ int s_bad;
+    __shared__ int s_bad, s_maxd;
     const int N = a.N, H = a.H, dk = a.dk, dv = a.dv, ld = N + 1;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -113,7 +113,10 @@ __global__ void __launch_bounds__(kGThreads) gla_prep_kernel(GlaArgs a) {
     griddep_wait();
     griddep_launch();     // the contraction only streams the state before its own wait
 
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) {
+        s_bad = 0;
+        s_maxd = 0;
+    }
     __syncthreads();
     if (tid < N) {
         const int p = a.parent[(size_t)b * N + tid];
@@ -130,6 +133,7 @@ __global__ void __launch_bounds__(kGThreads) gla_prep_kernel(GlaArgs a) {
         return;
     }
     prep::node_meta(tid, N, par, la0, anc, depth, g0, plist);
+    if (tid < N) atomicMax(&s_maxd, depth[tid]);
     __syncthreads();
 
     // The tree's q and k rows into shared memory (bf16 inputs) by async copies, and
@@ -146,43 +150,73 @@ __global__ void __launch_bounds__(kGThreads) gla_prep_kernel(GlaArgs a) {
             cp_async16((r < N ? sq + t * dk : sk + t * dk) + cc * (16 / (int)sizeof(T)), src + cc * (16 / (int)sizeof(T)));
         }
     }
-#pragma unroll 4
-    for (int i = tid; i < N * dk; i += kGThreads) {
-        const int t = i / dk, c = i - t * dk;
-        sg[i] = logf(a.alpha[(((size_t)b * N + t) * H + h) * dk + c]);
+    const int dk4 = dk / 4;                                  // d_k is a multiple of 16
+    for (int i = tid; i < N * dk4; i += kGThreads) {         // four channels per load, all in flight
+        const int t = i / dk4, c = 4 * (i - t * dk4);
+        const float4 al = *reinterpret_cast<const float4*>(a.alpha + (((size_t)b * N + t) * H + h) * dk + c);
+        *reinterpret_cast<float4*>(sg + t * dk + c) = make_float4(logf(al.x), logf(al.y), logf(al.z), logf(al.w));
     }
     cp_async_wait_all();
     __syncthreads();
 
-    // Thread c < d_k owns key channel c: g_t[c] = g_parent(t)[c] + log alpha_t[c] in
-    // node order (parents come first, and were written by this same thread).
-    for (int c = tid; c < dk; c += kGThreads) {
-#pragma unroll 1
-        for (int t = 1; t < N; ++t) {
-            const int p = par[t];
-            if (p >= 0) sg[t * dk + c] += sg[p * dk + c];
-        }
+    // g_t[c] = g_parent(t)[c] + log alpha_t[c], one tree level at a time (a node's parent
+    // is one level up, so it is final when the node's level is reached)
+    float4* sg4 = reinterpret_cast<float4*>(sg);
+    constexpr int kItems = kMaxNodes * (kMaxDim / 4) / kGThreads;   // (node, channel quad) items per thread
+    int it_i[kItems], it_p[kItems], it_d[kItems];                  // item, its parent's item, its depth
+#pragma unroll
+    for (int e = 0; e < kItems; ++e) {
+        const int i = tid + e * kGThreads, t = i / dk4;
+        const bool in = i < N * dk4;
+        it_i[e] = i;
+        it_d[e] = in ? depth[t] : -1;
+        it_p[e] = in && par[t] >= 0 ? par[t] * dk4 + (i - t * dk4) : 0;
     }
-    __syncthreads();
+#pragma unroll 1
+    for (int lvl = 1; lvl <= s_maxd; ++lvl) {
+#pragma unroll
+        for (int e = 0; e < kItems; ++e) {
+            if (it_d[e] == lvl) {
+                float4 x = sg4[it_i[e]];
+                const float4 pg = sg4[it_p[e]];
+                x.x += pg.x;
+                x.y += pg.y;
+                x.z += pg.z;
+                x.w += pg.w;
+                sg4[it_i[e]] = x;
+            }
+        }
+        __syncthreads();
+    }
     // the record's g and key copy and qhat_t[c] = q_t[c] e^{g_t[c]}, every (node, channel)
     __nv_bfloat16* qh = static_cast<__nv_bfloat16*>(a.qhat);
     __nv_bfloat16* ql = qh + (size_t)a.B * N * H * dk;
-    for (int i = tid; i < N * dk; i += kGThreads) {
-        const int t = i / dk, c = i - t * dk;
+    for (int i = tid; i < N * dk4; i += kGThreads) {         // four channels per thread and store
+        const int t = i / dk4, c = 4 * (i - t * dk4);
         const size_t src = (((size_t)b * N + t) * H + h) * dk + c;
         const size_t dst = ((size_t)bh * N + t) * dk + c;
-        const float gt = sg[i];
-        a.g[dst] = gt;
-        const T kv = kStage ? sk[i] : k[src];
-        const T qv = kStage ? sq[i] : q[src];
-        static_cast<T*>(a.key)[dst] = kv;
-        const float x = ld_elem<T>(&qv, 0) * exp2f(gt * kLog2e);
-        if (kTc) {
-            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-            qh[src] = hi;
-            ql[src] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        const float4 gt = sg4[t * dk4 + c / 4];
+        *reinterpret_cast<float4*>(a.g + dst) = gt;
+        const T* kp = kStage ? sk + t * dk + c : k + src;
+        const T* qp = kStage ? sq + t * dk + c : q + src;
+        if constexpr (sizeof(T) == 2)
+            *reinterpret_cast<uint2*>(static_cast<T*>(a.key) + dst) = *reinterpret_cast<const uint2*>(kp);
+        else
+            *reinterpret_cast<float4*>(static_cast<T*>(a.key) + dst) = *reinterpret_cast<const float4*>(kp);
+        const float4 qv = ld4<T>(qp, 0);
+        const float x[4] = {qv.x * exp2f(gt.x * kLog2e), qv.y * exp2f(gt.y * kLog2e), qv.z * exp2f(gt.z * kLog2e),
+                            qv.w * exp2f(gt.w * kLog2e)};
+        if (kTc) {   // hi = bf16(x), lo = bf16(x - hi), two channels per conversion
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(x[0], x[1]), h23 = __floats2bfloat162_rn(x[2], x[3]);
+            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+            const __nv_bfloat162 l01 = __floats2bfloat162_rn(x[0] - f01.x, x[1] - f01.y);
+            const __nv_bfloat162 l23 = __floats2bfloat162_rn(x[2] - f23.x, x[3] - f23.y);
+            *reinterpret_cast<uint2*>(qh + src) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+            *reinterpret_cast<uint2*>(ql + src) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
         } else {
-            static_cast<float*>(a.qhat)[src] = x;
+            *reinterpret_cast<float4*>(static_cast<float*>(a.qhat) + src) = make_float4(x[0], x[1], x[2], x[3]);
         }
     }
     if (a.v32 != nullptr)
@@ -197,21 +231,34 @@ __global__ void __launch_bounds__(kGThreads) gla_prep_kernel(GlaArgs a) {
     // Attn[t, j] = sum_c q_t[c] k_j[c] e^{g_t[c] - g_j[c]} on the inclusive mask; T = I there
     prep::pair_list(tid, N, depth, anc, off, pairs);
     const int npairs = off[N];
+    // Each warp takes a contiguous run of the (node-major) pair list, so that it keeps its
+    // lanes' q_t and g_t channels in registers while t stays the same.
+    const int per_warp = (npairs + kGThreads / 32 - 1) / (kGThreads / 32);
+    const int pend = min(npairs, (warp + 1) * per_warp);
+    int cur_t = -1;
+    float qr[kMaxDim / 32], gr[kMaxDim / 32];             // channel lane + 32 i of q_t and g_t
 #pragma unroll 1
-    for (int pi = warp; pi < npairs; pi += kGThreads / 32) {
+    for (int pi = warp * per_warp; pi < pend; ++pi) {
         const int t = pairs[pi] >> 8, j = pairs[pi] & 255;
-        const T* qt = kStage ? sq + t * dk : q + (((size_t)b * N + t) * H + h) * dk;
+        if (t != cur_t) {
+            cur_t = t;
+            const T* qt = kStage ? sq + t * dk : q + (((size_t)b * N + t) * H + h) * dk;
+            const float* gt = sg + t * dk;
+#pragma unroll
+            for (int i = 0; i < kMaxDim / 32; ++i) {
+                const int c = lane + 32 * i;
+                qr[i] = c < dk ? ld_elem<T>(qt, c) : 0.f;
+                gr[i] = c < dk ? gt[c] : 0.f;
+            }
+        }
         const T* kj = kStage ? sk + j * dk : k + (((size_t)b * N + j) * H + h) * dk;
-        const float* gt = sg + t * dk;
         const float* gj = sg + j * dk;
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int i = 0; i < kMaxDim / 32; i += 2) {           // d_k <= 256: at most 8 channels per lane
             const int c0 = lane + 32 * i, c1 = c0 + 32;
-            if (c0 < dk)
-                s0 = fmaf(ld_elem<T>(qt, c0) * ld_elem<T>(kj, c0), exp2f((gt[c0] - gj[c0]) * kLog2e), s0);
-            if (c1 < dk)
-                s1 = fmaf(ld_elem<T>(qt, c1) * ld_elem<T>(kj, c1), exp2f((gt[c1] - gj[c1]) * kLog2e), s1);
+            if (c0 < dk) s0 = fmaf(qr[i] * ld_elem<T>(kj, c0), exp2f((gr[i] - gj[c0]) * kLog2e), s0);
+            if (c1 < dk) s1 = fmaf(qr[i + 1] * ld_elem<T>(kj, c1), exp2f((gr[i + 1] - gj[c1]) * kLog2e), s1);
         }
         const float s = warp_sum(s0 + s1);
         if (lane == 0) {
