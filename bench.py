@@ -128,8 +128,8 @@ NCU_TRAFFIC = {
     ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (43.08e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
     ("layer_tree64_depth8_b64_hid2048", "conv"): (188.2e6, ("gdn_layer.cu", "gdn_layer.cuh", "gdn_internal.cuh"),
                                                   "066e72e5baf0efbc"),
-    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.80e6, _GLA_VERIFY_SRC, "de2b787704116949"),
-    ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.31e6, _GLA_COMMIT_SRC, "8231be4c7a297db5"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.77e6, _GLA_VERIFY_SRC, "caeaab162aab62a1"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.29e6, _GLA_COMMIT_SRC, "e2c276b3adf2e905"),
 }
 NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
                     "start; writes still held in L2 when the kernel ends are not counted)")
