@@ -121,14 +121,14 @@ _GLA_COMMIT_SRC = ("gdn_gla.cu", "gdn_internal.cuh")
 NCU_TRAFFIC = {
     ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.274e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
                                                "10502adcdbd91ed8"),
-    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.634e6, _TREE_SRC, "4dbdabca491f281a"),
-    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (47.87e6, _TREE_SRC, "4dbdabca491f281a"),
-    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (357.3e6, _TREE_SRC + ("gdn_layer.cu",), "2778e7792b4d1f58"),
+    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.634e6, _TREE_SRC, "8eefd5dd93c63ecd"),
+    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (47.84e6, _TREE_SRC, "8eefd5dd93c63ecd"),
+    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (358.6e6, _TREE_SRC + ("gdn_layer.cu",), "cd77c6ef65279efd"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (134.6e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (43.08e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
     ("layer_tree64_depth8_b64_hid2048", "conv"): (188.2e6, ("gdn_layer.cu", "gdn_layer.cuh", "gdn_internal.cuh"),
                                                   "066e72e5baf0efbc"),
-    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.77e6, _GLA_VERIFY_SRC, "caeaab162aab62a1"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.80e6, _GLA_VERIFY_SRC, "7eed09a7aa8835f9"),
     ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.29e6, _GLA_COMMIT_SRC, "e2c276b3adf2e905"),
 }
 NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
