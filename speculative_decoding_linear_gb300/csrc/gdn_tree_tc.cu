@@ -1082,16 +1082,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float4 ecur[8], enxt[8];           // a helper's element of the issuer's rows in slabs 2 and 3 ([0] only)
     if (ok) {
         // this thread's part of slabs 2 and 3 as they were before the commit (L2)
-        // fp32 inputs (the layer step): both slabs at once; bf16 inputs: slab 3's loads only once the
-        // thread has committed slab 2, so that they do not compete with slab 2's (faster there)
-        if (warp != kFIssuerWarp) {
-            f_load_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
-            if (kSplit) f_load_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
-        }
-        if (helper) {
-            f_load_slab<1>(ecur, a.S, srow0, h_row, 2 * kSlab + 4 * h_c4, pol_first);
-            if (kSplit) f_load_slab<1>(enxt, a.S, srow0, h_row, 3 * kSlab + 4 * h_c4, pol_first);
-        }
+        // (slab 3's loads only once the thread has committed slab 2, so that they do not compete
+        // with slab 2's)
+        if (warp != kFIssuerWarp) f_load_slab<kJ>(cur, a.S, srow0, rbase, 2 * kSlab + 4 * c4, pol_first);
+        if (helper) f_load_slab<1>(ecur, a.S, srow0, h_row, 2 * kSlab + 4 * h_c4, pol_first);
         if (warp == kFIssuerWarp && lane == 0) {
             issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(0), 0, h, b * N, bars);
             if (nB == 2) issue_qk_tma<kSplit>(&tmQ, &tmK, &tmQl, &tmKl, bbuf(1), 1, h, b * N, bars + 8);
@@ -1135,7 +1129,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                             f_store_slab<1>(ecur, a.S, srow0, h_row, sl * kSlab + 4 * h_c4, pol_first);
                         }
                     }
-                    if (!kSplit && sl == 2) {      // bf16 inputs: slab 3 only now, behind slab 2's loads
+                    if (sl == 2) {                 // slab 3 only now, behind slab 2's loads
                         f_load_slab<kJ>(nxt, a.S, srow0, rbase, 3 * kSlab + 4 * c4, pol_first);
                         if (helper) f_load_slab<1>(enxt, a.S, srow0, h_row, 3 * kSlab + 4 * h_c4, pol_first);
                     }
