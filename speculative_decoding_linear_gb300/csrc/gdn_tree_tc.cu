@@ -768,7 +768,7 @@ struct FusedLayout {
     // stages and nB q/k buffers during Y, then R (both tiles), the A / Attn / T
     // tables and the [T; P] operand.
     int nB, bsz, ops, R, A, At, T, op;
-    int vs, cd, key, nodes, coef, par, la, g, beta, eg, depth, anc, plist, bars, misc, total;
+    int vs, cd, key, nodes, coef, par, la, g, beta, eg, bk, depth, anc, plist, bars, misc, total;
     __host__ __device__ FusedLayout(int N, int Lcap, bool split) {
         bsz = (split ? 2 : 1) * kBufBytes;
         build(N, Lcap, split, 2);
@@ -800,6 +800,7 @@ struct FusedLayout {
         g = take(kMaxNodes * 4);
         beta = take(kMaxNodes * 4);
         eg = take(kMaxNodes * 4);
+        bk = take(kMaxNodes * 8);
         depth = take(kMaxNodes * 4);
         anc = take(kMaxNodes * 8);
         plist = take(kMaxNodes * 64);
@@ -956,6 +957,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     float* sg = reinterpret_cast<float*>(base + Ly.g);
     float* sbeta = reinterpret_cast<float*>(base + Ly.beta);
     float* seg = reinterpret_cast<float*>(base + Ly.eg);
+    float2* sbk = reinterpret_cast<float2*>(base + Ly.bk);       // (beta_t, beta_t e^{g_t}) for R, 0 past N
     int* sdepth = reinterpret_cast<int*>(base + Ly.depth);
     uint64_t* anc = reinterpret_cast<uint64_t*>(base + Ly.anc);
     uint8_t* plist = reinterpret_cast<uint8_t*>(base + Ly.plist);
@@ -1182,12 +1184,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
             la[tid] = logf(al_in);
             sbeta[tid] = be_in;
         }
+        if (tid >= N && tid < kMaxNodes) sbk[tid] = make_float2(0.f, 0.f);
         bad = __syncthreads_or(bad);
         if (bad) {
             if (tid == 0) set_error(a.err, GDN_ERR_TREE);
         } else if (tid < N) {
             prep::node_meta(tid, N, par, la, anc, sdepth, sg, plist);
             seg[tid] = expf(sg[tid]);
+            sbk[tid] = make_float2(sbeta[tid], a.linear ? 0.f : sbeta[tid] * seg[tid]);
             if (lead) {
                 a.f.g[(size_t)bh * N + tid] = sg[tid];
                 if (h == 0) a.f.parent[(size_t)b * N + tid] = par[tid];
@@ -1243,9 +1247,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                         float r[2];
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
-                            const int t = t0 + 2 * e + q;
-                            const float ek = a.linear ? 0.f : seg[t] * yk[2 * e + q];
-                            r[q] = t < N ? sbeta[t] * (vt[2 * e + q] - ek) : 0.f;
+                            const float2 c = sbk[t0 + 2 * e + q];   // zeros past N, where v is 0 too
+                            r[q] = fmaf(-c.y, yk[2 * e + q], c.x * vt[2 * e + q]);
                         }
                         const __nv_bfloat162 hh = __floats2bfloat162_rn(r[0], r[1]);
                         const float2 hf = __bfloat1622float2(hh);
