@@ -747,9 +747,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 //     over once slabs 0 and 1 are consumed -- by the other fifteen warps (warps
 //     8-15 take warp 4's share), which arrive at a named barrier per slab that
 //     only the issuer waits on; the node metadata meanwhile;
-//   then warps 0-7 turn the Gram rows into the A and Attn tables, solve T,
-//     form P and the [T; P] operand, while warps 8-15 form R of both tiles
-//     from Y_K, v and the gates; one MMA group per tile gives [Delta | P R]
+//   then warps 0-7 turn the Gram rows into the A and Attn tables and solve T
+//     and P, while warps 8-15 form R of both tiles from Y_K, v and the gates;
+//     all sixteen warps then write the [T; P] operand; one MMA group per tile gives [Delta | P R]
 //     (committed per tile); warps 8-15 copy the keys into the factor record
 //     while it runs; every warp stores Delta or O rows.
 // TMEM, 512 columns: Y of tile u in 128u .. 128u+127 ([Y_Q | Y_K]); the Gram
@@ -1228,7 +1228,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
                                         sA + (tid >> 2) * ld, ld, sg, sbeta, sA, sAt, !a.linear);
                 prep::group_sync(256);
                 prep::solve_rows_fast<9>(tid, N, ld, sdepth, plist, sA, sAt, sT, 256);
-                prep::write_operand(tid, 256, N, ld, anc, sA, sT, base + Ly.op);
+                // T and P are in place: warps 8-15, done with R by now, take half of the operand
+                named_barrier_arrive(5, kFThreads);
+                prep::write_operand(tid, kFThreads, N, ld, anc, sA, sT, base + Ly.op);
             } else {
                 // R[v, t] = beta_t (v_t[v] - e^{g_t} Y_K[v, t]) (0 for t >= N) of tile u as bf16
                 // hi + lo rows of the second MMA's A operand (row v, 64 columns t).  kT = 2:
@@ -1305,6 +1307,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                         }
                     }
                 }
+                named_barrier_sync(5, kFThreads);     // the tables' T and P rows
+                prep::write_operand(tid, kFThreads, N, ld, anc, sA, sT, base + Ly.op);
             }
         }
         fence_proxy_async_smem();
