@@ -1364,25 +1364,48 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (ok) ok = mbar_wait(kT == 2 && warp >= 8 ? bar_e2 : bar_e, 0, a.err);
         tc_fence_after();
         if (ok) {
-            // kT = 2: warps 0-3 / 8-11 Delta of tile 0 / 1, warps 4-7 / 12-15 O of tile 0 / 1;
-            // kT = 1: the same split of tile 0 by nodes 0..31 (warps 0-7) and 32..63 (8-15)
-            const int u = kT == 2 ? warp >> 3 : 0;
-            const int tbeg = kT == 2 ? 0 : 32 * (warp >> 3), tend = kT == 2 ? N : min(N, tbeg + 32);
-            const int row = row0 + 128 * u + 32 * (warp & 3) + lane;
-            const bool is_o = ((warp >> 2) & 1) != 0;
-            const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-            const uint32_t src = t_lane + 256 + 128 * u + (is_o ? kNodeRows : 0);   // T R or P R
-            float* dst = is_o ? a.out + ((size_t)b * N * H + h) * kFRows + row : a.f.delta + (size_t)bh * N * kFRows + row;
-            const size_t dstep = is_o ? (size_t)H * kFRows : (size_t)kFRows;
-#pragma unroll 1
-            for (int t0 = tbeg; t0 < tend; t0 += 32) {           // 32 nodes per TMEM load
-                float x[32], yq[32];
-                tmem_ld32(src + t0, x);
-                if (is_o) tmem_ld32(t_lane + 128 * u + t0, yq);
+            if constexpr (kT == 2) {
+                // warp w: tile w >> 3, nodes 32 ((w >> 2) & 1) .. +31, first their Delta rows, then
+                // their O rows, so that every warp carries the same share of reads and stores
+                const int u = warp >> 3, t0 = 32 * ((warp >> 2) & 1);
+                const int row = 128 * u + 32 * (warp & 3) + lane;
+                const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+                if (t0 < N) {
+                    const int tend = min(N, t0 + 32);
+                    {
+                        float x[32];
+                        tmem_ld32(t_lane + 256 + 128 * u + t0, x);            // T R
+                        float* dst = a.f.delta + (size_t)bh * N * kFRows + row;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int t = t0 + i;
-                    if (t < tend) dst[(size_t)t * dstep] = is_o ? fmaf(seg[t], yq[i], x[i]) : x[i];
+                        for (int i = 0; i < 32; ++i)
+                            if (t0 + i < tend) dst[(size_t)(t0 + i) * kFRows] = x[i];
+                    }
+                    float x[32], yq[32];
+                    tmem_ld32(t_lane + 256 + 128 * u + kNodeRows + t0, x);   // P R
+                    tmem_ld32(t_lane + 128 * u + t0, yq);                    // Y_Q
+                    float* dst = a.out + ((size_t)b * N * H + h) * kFRows + row;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (t0 + i < tend) dst[(size_t)(t0 + i) * H * kFRows] = fmaf(seg[t0 + i], yq[i], x[i]);
+                }
+            } else {
+                // kT = 1: warps 0-3 / 8-11 Delta of nodes 0..31 / 32..63, warps 4-7 / 12-15 O
+                const int tbeg = 32 * (warp >> 3), tend = min(N, tbeg + 32);
+                const int row = row0 + 32 * (warp & 3) + lane;
+                const bool is_o = ((warp >> 2) & 1) != 0;
+                const uint32_t t_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+                const uint32_t src = t_lane + 256 + (is_o ? kNodeRows : 0);   // T R or P R
+                float* dst = is_o ? a.out + ((size_t)b * N * H + h) * kFRows + row : a.f.delta + (size_t)bh * N * kFRows + row;
+                const size_t dstep = is_o ? (size_t)H * kFRows : (size_t)kFRows;
+                if (tbeg < tend) {                                  // one chunk of 32 nodes
+                    float x[32], yq[32];
+                    tmem_ld32(src + tbeg, x);
+                    if (is_o) tmem_ld32(t_lane + tbeg, yq);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = tbeg + i;
+                        if (t < tend) dst[(size_t)t * dstep] = is_o ? fmaf(seg[t], yq[i], x[i]) : x[i];
+                    }
                 }
             }
         }
