@@ -121,14 +121,14 @@ _GLA_COMMIT_SRC = ("gdn_gla.cu", "gdn_internal.cuh")
 NCU_TRAFFIC = {
     ("chain8_b1_h8_d256", "chain_g8_kernel"): (2.274e6, ("gdn_chain.cu", "gdn_internal.cuh", "gdn_tc_ptx.cuh"),
                                                "10502adcdbd91ed8"),
-    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.632e6, _TREE_SRC, "f36666ce9d02e145"),
-    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (47.83e6, _TREE_SRC, "f36666ce9d02e145"),
-    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (358.6e6, _TREE_SRC + ("gdn_layer.cu",), "60b3cfe7168f2724"),
+    ("tree32_depth6_b1_h8_d256", "tree_fused_tc_kernel"): (2.627e6, _TREE_SRC, "91888a95b7896ca6"),
+    ("tree64_depth8_b16_h8_d256", "tree_fused_tc_kernel"): (47.81e6, _TREE_SRC, "91888a95b7896ca6"),
+    ("layer_tree64_depth8_b64_hid2048", "tree_verify"): (358.8e6, _TREE_SRC + ("gdn_layer.cu",), "ac989d0002dee1a9"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_in"): (134.6e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
     ("layer_tree64_depth8_b64_hid2048", "gemm_out"): (43.08e6, _GEMM_SRC, "e61b6b4b2b2a32d8"),
     ("layer_tree64_depth8_b64_hid2048", "conv"): (188.2e6, ("gdn_layer.cu", "gdn_layer.cuh", "gdn_internal.cuh"),
                                                   "066e72e5baf0efbc"),
-    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.79e6, _GLA_VERIFY_SRC, "161ab7b7112f1932"),
+    ("gla_tree64_depth8_b16_h8_d256", "gla_verify"): (75.80e6, _GLA_VERIFY_SRC, "5cb5e2ac463bfd31"),
     ("gla_tree64_depth8_b16_h8_d256", "gla_commit"): (35.29e6, _GLA_COMMIT_SRC, "e2c276b3adf2e905"),
 }
 NCU_TRAFFIC_NOTE = ("dram read + write bytes per launch from a serialised ncu capture (cold L2 at kernel "
